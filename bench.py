@@ -1,0 +1,477 @@
+#!/usr/bin/env python
+"""SSD forward benchmark on GB300: prints ONE JSON line.
+
+Default workload: the Mamba-2 2.7B-layer-shaped SSD forward (batch 4,
+seqlen 4096, 80 heads, headdim 64, dstate 128, 1 group, chunk 256, bf16
+x/B/C, f32 dt/A/D, zero initial state, final state returned).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (the
+units -- batch rows and heads -- are independent; no collective on the data
+path), so scaling is weak and `value` counts the tokens of all ranks.
+
+A step is one whole SSD forward (every stage) over one batch of synthetic
+input resident in HBM.  Each timed step is bracketed by CUDA events on the
+launching stream; L2 is flushed (512 MB write) before every timed step,
+outside the events.  The step calls the same C-ABI stage entry points that
+ssd_fwd dispatches to, with an event between stages, so the dominant
+kernel's own duration is measured live for the roofline object.  `e2e`
+times the public ssd_fwd call with host (pinned) inputs copied in and the
+result copied out inside the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from state_space_sequence_cumsum_gb300.inputs import (EXTREME_256K, LAYER_2P7B, LONG_S256_G8,  # noqa: E402
+                                                      PAGES_EXAMPLE, TINY_FP32, Shape,
+                                                      make_inputs, sweep_shape)
+
+METRIC = "SSD forward tokens/sec on 1 GB300 and % of roofline (H=80,P=64,S=128)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# name -> (shape, dtype, init, want chunk states)
+WORKLOADS = {
+    "mamba2-2.7b-layer-B4-L4096-H80-P64-S128-T256": (LAYER_2P7B, torch.bfloat16, "zero", False),
+    "tiny-fp32-B1-L256-H2-P16-S16-T64": (TINY_FP32, torch.float32, "zero", False),
+    "long-B2-L32768-H64-P64-S256-G8-T256": (LONG_S256_G8, torch.bfloat16, "randn", False),
+    "extreme-B1-L262144-H32-P64-S512-T128-states": (EXTREME_256K, torch.bfloat16, "zero", True),
+    "pages-example-B4-L16384-H8-P64-S128-T128": (PAGES_EXAMPLE, torch.bfloat16, "zero", False),
+}
+for _L in (1024, 4096, 16384, 65536, 262144, 4095):
+    for _S in (64, 128, 256, 512):
+        _sh = sweep_shape(_L, _S, 128)
+        WORKLOADS[f"sweep-B{_sh.batch}-L{_L}-H64-P64-S{_S}-T128"] = (_sh, torch.bfloat16, "zero",
+                                                                     False)
+DEFAULT = "mamba2-2.7b-layer-B4-L4096-H80-P64-S128-T256"
+
+
+# ------------------------------------------------------------------ accounting
+
+def elem_bytes(dtype):
+    return 2 if dtype == torch.bfloat16 else 4
+
+
+def compulsory_bytes(s: Shape, dtype, init: str, want_states: bool) -> int:
+    """Bytes the forward must move at least once: read x, B, C, dt, A, D (and
+    init), write y and the final state (and chunk states when requested)."""
+    e = elem_bytes(dtype)
+    n = 2 * s.batch * s.seqlen * s.nheads * s.headdim * e          # x read, y written
+    n += 2 * s.batch * s.seqlen * s.ngroups * s.dstate * e          # B, C
+    n += s.batch * s.seqlen * s.nheads * 4 + 2 * s.nheads * 4       # dt, A, D
+    st = s.batch * s.nheads * s.headdim * s.dstate * 4
+    n += st                                                          # final state
+    if init == "randn":
+        n += st
+    if want_states:
+        n += st * s.nchunks
+    return n
+
+
+def algorithmic_flops(s: Shape) -> int:
+    """Per (batch, chunk of Tc tokens): per head 4 Tc S P (C h^T and the state
+    jump) + P Tc (Tc + 1) (causal scores x X); per group S Tc (Tc + 1) (causal CB^T)."""
+    total = 0
+    for c in range(s.nchunks):
+        tc = min(s.chunk_size, s.seqlen - c * s.chunk_size)
+        per_head = 4 * tc * s.dstate * s.headdim + s.headdim * tc * (tc + 1)
+        per_group = s.dstate * tc * (tc + 1)
+        total += s.batch * (s.nheads * per_head + s.ngroups * per_group)
+    return total
+
+
+def kernel_bytes(kernel: str, s: Shape, dtype, init: str, want_states: bool) -> int:
+    """Algorithmic bytes one launch of `kernel` must move (each operand once)."""
+    e = elem_bytes(dtype)
+    blh = s.batch * s.seqlen * s.nheads
+    xb = blh * s.headdim * e
+    bb = s.batch * s.seqlen * s.ngroups * s.dstate * e
+    st = s.batch * s.nheads * s.headdim * s.dstate * 4
+    states = st * s.nchunks
+    init_b = st if init == "randn" else 0
+    if kernel == "chunk_cumsum":
+        return blh * 4 + blh * 8 + s.nheads * 4
+    if kernel == "state_pass":
+        return xb + bb + 2 * blh * 4 + init_b + states + st
+    if kernel == "chunk_out":
+        return xb + 2 * bb + 2 * blh * 4 + states + s.nheads * 4 + xb
+    if kernel == "state_out":  # fused stages 2+3
+        return (xb + 2 * bb + 2 * blh * 4 + s.nheads * 4 + init_b + xb + st +
+                (states if want_states else 0))
+    raise KeyError(kernel)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None if absent or if the kernel's source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d[kernel][workload]
+        if ent["source_digest"] != source_digest(ent["sources"]):
+            return None
+        return int(ent["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_sample(inp, s: Shape, pairs: int, threads: int):
+    """Run the float64 oracle on the first `pairs` (batch, head) pairs for the
+    full sequence; return (seconds, head-tokens processed)."""
+    import oracle
+    H = s.nheads
+    hpg = H // s.ngroups
+    done, t = 0, 0.0
+    b = 0
+    while done < pairs and b < s.batch:
+        k = min(H, pairs - done)
+        heads = list(range(k))
+        groups = sorted({h // hpg for h in heads})
+        heads = [h for g in groups for h in range(g * hpg, (g + 1) * hpg)][:max(k, hpg)]
+        idx, gidx = torch.tensor(heads), torch.tensor(groups)
+        x = inp["x"][b:b + 1, :, idx]
+        dt = inp["dt"][b:b + 1, :, idx]
+        Bm, Cm = inp["B"][b:b + 1, :, gidx], inp["C"][b:b + 1, :, gidx]
+        init = None if inp["init"] is None else inp["init"][b:b + 1, idx]
+        args = [oracle._f64(v) for v in (x, dt, inp["A"][idx], Bm, Cm, inp["D"][idx])]
+        init = oracle._f64(init)
+        t0 = time.perf_counter()
+        oracle.fwd(*args, s.chunk_size, init=init, nthreads=threads)
+        t += time.perf_counter() - t0
+        done += len(heads)
+        b += 1
+    return t, done * s.seqlen
+
+
+def cpu_baseline(inp, s: Shape, budget_s: float = 15.0):
+    import oracle
+    oracle.build()
+    threads = oracle.cpu_cores()
+    pairs = max(1, min(threads, s.batch * s.nheads))
+    t, head_tokens = oracle_sample(inp, s, pairs, threads)
+    # grow the sample toward ~budget_s of CPU work
+    while t < budget_s / 4 and pairs < s.batch * s.nheads:
+        pairs = min(s.batch * s.nheads, pairs * 4)
+        t, head_tokens = oracle_sample(inp, s, pairs, threads)
+    tokens = head_tokens / s.nheads  # a token is all heads of one position
+    return {"value": tokens / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": (f"float64 recurrence over {head_tokens // s.seqlen} (batch, head) pairs "
+                       f"x {s.seqlen} tokens = {tokens:.0f} full-width tokens in {t:.2f} s")}
+
+
+# ------------------------------------------------------------------ our arm
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_ours(args):
+    import state_space_sequence_cumsum_gb300 as ssd
+    from state_space_sequence_cumsum_gb300 import _lib
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    shape, dtype, init, want_states = WORKLOADS[args.workload]
+    T = shape.chunk_size
+    inp = make_inputs(shape, dtype=dtype, init=init, seed=rank)
+    lib = _lib.load()
+
+    g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    y = torch.empty_like(g["x"])
+    fin = torch.empty((shape.batch, shape.nheads, shape.headdim, shape.dstate), device=dev)
+    states = (torch.empty((shape.batch, shape.nheads, shape.nchunks, shape.headdim,
+                           shape.dstate), device=dev) if want_states else None)
+    wsp = ssd.Workspace()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    plan = ssd.ssd_fwd_plan(g["x"], g["B"], T, want_states=want_states)
+
+    def step(events=None):
+        return ssd.ssd_fwd_staged(plan, g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"],
+                                  g["init"], y, fin, states, wsp, events=events)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = ssd.ssd_stream_status()
+    if st != 0:
+        raise RuntimeError(f"kernel status {st} during warm-up")
+
+    nk = len(plan["kernels"])
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    launches0 = lib.ssd_launch_count()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            step(events=ev[k])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if ws > 1:
+        torch.distributed.barrier()
+    launches = lib.ssd_launch_count() - launches0
+    per_kernel = [[ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)]
+                  for i in range(nk)]
+    step_ms = [sum(per_kernel[i][k] for i in range(nk)) for k in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = shape.tokens
+    value = ws * tokens / (ms / 1e3)
+
+    # dominant kernel and its roofline
+    means = [statistics.mean(v) for v in per_kernel]
+    dom = int(np.argmax(means))
+    kname = plan["kernels"][dom]
+    peaks, peak_src = load_peaks()
+    kb = kernel_bytes(kname, shape, dtype, init, want_states)
+    achieved = kb / (means[dom] / 1e3) / 1e9
+    traffic = profiled_traffic(kname, args.workload)
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic, "algorithmic_bytes": kb, "kernel_ms": round(means[dom], 5),
+                "peak_source": peak_src}
+    # whole-step roofline: max(compulsory bytes / HBM, algorithmic flops / bf16 peak)
+    cb = compulsory_bytes(shape, dtype, init, want_states)
+    fl = algorithmic_flops(shape)
+    t_roof = max(cb / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+    step_roof = {"compulsory_bytes": cb, "algorithmic_flops": fl,
+                 "t_roof_us": round(t_roof * 1e6, 2), "frac": round(t_roof / (ms / 1e3), 4),
+                 "bound": "hbm" if cb / peaks["hbm_gbs"] >= fl / (peaks["bf16_tflops"] * 1e3)
+                 else "tensor"}
+
+    # e2e: public ssd_fwd call, pinned host inputs in, y + final out, per step
+    host_in = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    fin_host = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+    d2h = y_host.numel() * y_host.element_size() + fin_host.numel() * fin_host.element_size()
+
+    def e2e_step():
+        for k, v in host_in.items():
+            if v is not None:
+                g[k].copy_(v, non_blocking=True)
+        ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=T,
+                    initial_state=g["init"], y=y, final_state=fin, chunk_states=states,
+                    return_chunk_states=want_states, workspace=wsp)
+        y_host.copy_(y, non_blocking=True)
+        fin_host.copy_(fin, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_ms = []
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e_ms.append(a.elapsed_time(b))
+    e_ms_mean = statistics.mean(e_ms)
+    if ws > 1:
+        t = torch.tensor([e_ms_mean], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e_ms_mean = float(t.item())
+    st = ssd.ssd_stream_status()
+    if st != 0:
+        raise RuntimeError(f"kernel status {st} in the timed region")
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": shape.batch, "seqlen": shape.seqlen,
+                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+                   "ngroups": shape.ngroups, "chunk_size": T, "init": init,
+                   "chunk_states": want_states, "parallelism": f"replicas{ws}",
+                   "l2": "flushed before every timed step (512 MB write, outside the events)",
+                   "path": plan["path"]},
+        "roofline": roofline, "step_roofline": step_roof,
+        "per_kernel_ms": {n: round(m, 5) for n, m in zip(plan["kernels"], means)},
+        "wall_s_timed_loop": round(t_wall, 4),
+        "e2e": {"value": round(ws * tokens / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e_ms_mean, 4)},
+        "gpu_launches": int(launches),
+    }
+    clocks = clk.summary()
+    if clocks:
+        line["clocks"] = clocks
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, shape)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, on a bounded sample per step."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    shape, dtype, init, want_states = WORKLOADS[args.workload]
+    inp = make_inputs(shape, dtype=dtype, init=init, seed=0)
+    threads = oracle.cpu_cores()
+    pairs = max(1, min(threads, shape.batch * shape.nheads))
+    for _ in range(max(1, args.warmup)):
+        oracle_sample(inp, shape, pairs, threads)
+    times, toks = [], 0
+    for _ in range(args.steps):
+        t, ht = oracle_sample(inp, shape, pairs, threads)
+        times.append(t)
+        toks = ht / shape.nheads
+    sec = statistics.mean(times)
+    value = toks / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(1, args.warmup),
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": shape.batch, "seqlen": shape.seqlen,
+                   "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
+                   "ngroups": shape.ngroups, "chunk_size": shape.chunk_size},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": (f"each step: float64 recurrence over {pairs} (batch, head) "
+                                    f"pairs x {shape.seqlen} tokens ({toks:.0f} full-width "
+                                    "tokens)")},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

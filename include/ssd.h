@@ -1,0 +1,165 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 chunked SSD forward library.
+ *
+ * The operation is the chunked state-space-duality (SSD) forward pass of
+ * "Accelerating Mamba-2 forward-pass kernels with CUDA Tile (cuTile)"
+ * (dbyun.net/article/14364).  For every batch row b and head h, with
+ * g = h / (nheads / ngroups) the head's B/C group:
+ *
+ *     h_t = exp(A[h] dt_t) h_{t-1} + dt_t x_t B_t^T        (state, headdim x dstate)
+ *     y_t = h_t C_t + D[h] x_t                              (section "Mamba-2 架构")
+ *
+ * computed chunk by chunk (chunk_size T tokens) in three stages: the
+ * within-chunk log2 cumsum G (section "Kernel 1"), the chunk-to-chunk state
+ * pass (section "Kernel 2: fwd_pass_state") and the fused chunk output
+ * (section "Kernel 3: compute_out").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers: all tensor pointers are DEVICE pointers owned by the caller.
+ *   The library never allocates, frees or retains them beyond the call.
+ *   Every tensor is contiguous, row-major, 16-byte aligned.
+ * Layouts (B = batch, L = seqlen, H = nheads, P = headdim, S = dstate,
+ *   G = ngroups, nc = ceil(L / T)):
+ *     x, y            [B, L, H, P]   dtype of the call (bf16 or f32)
+ *     Bm, Cm          [B, L, G, S]   dtype of the call
+ *     dt              [B, L, H]      f32, already activated (softplus etc. is
+ *                                    the caller's job)
+ *     A, D            [H]            f32 (A < 0 for a decaying state)
+ *     G_cum, dt_t     [B, H, L]      f32, token-contiguous (the layout the
+ *                                    pages move decay_cumsum and dt to)
+ *     init_state, final_state  [B, H, P, S]      f32
+ *     chunk_states    [B, H, nc, P, S]          f32; chunk_states[:,:,c] is
+ *                                    the state before token c*T, so
+ *                                    chunk_states[:,:,0] == init_state
+ * Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Every call is asynchronous and stream-ordered.
+ * Errors: every call validates its arguments on the host BEFORE launching
+ *   anything and returns a status; nothing aborts, throws or prints.  A
+ *   failed launch returns SSD_ERR_CUDA.  Errors raised inside a kernel (a
+ *   bounded wait that ran out) are recorded in a per-device status word that
+ *   ssd_stream_status() reads.
+ * Threads: calls are thread-safe; the only shared host state is a
+ *   mutex-guarded cache of TMA descriptors and tuning choices.
+ * Supported sizes: 1 <= P <= 256, 1 <= S <= 512, 1 <= T <= 256, H % G == 0,
+ *   L >= 0 (L == 0 copies init_state to final_state and launches nothing
+ *   else).  The tensor-core path serves bf16 with P in {32, 64, 128},
+ *   S % 64 == 0 and T in {64, 128, 256}; other shapes and all f32 calls run
+ *   the f32-arithmetic CUDA-core kernels.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,  /* null pointer, bad size or inconsistent dims */
+    SSD_ERR_UNSUPPORTED = 2,  /* sizes outside the supported ranges above */
+    SSD_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned */
+    SSD_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    SSD_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
+    SSD_ERR_WORKSPACE = 6     /* workspace pointer missing or too small */
+} ssd_status_t;
+
+typedef enum {
+    SSD_BF16 = 0,  /* x, Bm, Cm, y are bf16; arithmetic accumulates in f32 */
+    SSD_F32 = 1    /* x, Bm, Cm, y are f32; all arithmetic is f32 */
+} ssd_dtype_t;
+
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups;
+} ssd_dims_t;
+
+/*
+ * Stage 1 -- within-chunk cumulative decay (section "Kernel 1").
+ *   G_cum[b,h,t] = log2(e) * sum_{t' = c*T}^{t} A[h] * dt[b,t',h],  c = t / T.
+ * The sum restarts at every chunk boundary.  G is kept in log2 units so the
+ * later stages use exp2.  dt_t (may be NULL) receives dt transposed to
+ * [B, H, L].
+ */
+ssd_status_t ssd_chunk_cumsum(const float *dt, const float *A, float *G_cum, float *dt_t,
+                              ssd_dims_t dims, int chunk_size, void *stream);
+
+/*
+ * Stage 2 -- chunk-to-chunk state pass (section "Kernel 2: fwd_pass_state").
+ * For c = 0 .. nc-1, per (b, h):
+ *     chunk_states[b,h,c] = h
+ *     h <- exp2(G_last) h + X_c^T (B_c * dt_c * exp2(G_last - G_c))      ([P,S])
+ * where G_last is G at the chunk's last VALID token (a ragged last chunk
+ * uses its own last token, not a zero-padded one).  h starts at init_state
+ * (NULL = zeros).  final_state (may be NULL) receives h after the last chunk.
+ * chunk_states may be NULL when only the final state is wanted.
+ */
+ssd_status_t ssd_state_pass(const void *x, const void *Bm, const float *dt_t, const float *G_cum,
+                            const float *init_state, float *chunk_states, float *final_state,
+                            ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, void *stream);
+
+/*
+ * Stage 3 -- chunk output (section "Kernel 3: compute_out").  Per (b, c, h):
+ *     Y = exp2(G) * (C_c h_c^T) + (exp2(G_i - G_j) * (C_c B_c^T) * M) (dt * X_c) + D[h] X_c
+ * with M the inclusive causal mask (i >= j) and h_c = chunk_states[b,h,c].
+ * The T x T score matrix never leaves the chip.  Masked entries are zero,
+ * never inf or NaN.
+ */
+ssd_status_t ssd_chunk_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
+                           const float *G_cum, const float *chunk_states, const float *D, void *y,
+                           ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, void *stream);
+
+/*
+ * Bytes of device workspace ssd_fwd needs for these arguments (the G_cum,
+ * dt_t and, when the caller does not want them, the chunk states the
+ * three-stage path keeps between stages, plus the chain buffers of the fused
+ * path).  chunk_size 0 means "let the library choose", as in ssd_fwd.
+ * Returns 0 for invalid arguments.
+ */
+size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
+                              int want_chunk_states);
+
+/*
+ * Whole forward pass: stage 1 -> 2 -> 3 on one stream, or the fused
+ * single-pass kernel (state carried on chip / in L2 between chunks) when the
+ * shape allows it.  y receives the output; final_state and chunk_states are
+ * optional outputs (NULL = not wanted); init_state may be NULL (zeros).
+ * chunk_size 0 lets the library choose among {64, 128, 256}.
+ * workspace must hold ssd_fwd_workspace_size(dims, dtype, chunk_size,
+ * chunk_states != NULL) bytes, 256-byte aligned; its contents on entry do
+ * not matter.
+ */
+ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void *Bm,
+                     const void *Cm, const float *D, const float *init_state, void *y,
+                     float *final_state, float *chunk_states, ssd_dims_t dims,
+                     ssd_dtype_t dtype, int chunk_size, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/* Chunk size ssd_fwd uses for chunk_size == 0 with these dims and dtype. */
+int ssd_fwd_chosen_chunk_size(ssd_dims_t dims, ssd_dtype_t dtype);
+
+/*
+ * Number of kernel launches this library has issued in this process (all
+ * devices, all threads).  Diagnostic: a call rejected by validation leaves it
+ * unchanged; the benchmark reports launches per step from it.
+ */
+uint64_t ssd_launch_count(void);
+
+/* Static, human-readable name of a status. */
+const char *ssd_status_string(ssd_status_t status);
+
+/*
+ * Synchronizes `stream`, then reads and clears the calling thread's current
+ * device's kernel status word.  Returns SSD_ERR_TIMEOUT if any kernel since
+ * the last read gave up a bounded wait, SSD_ERR_CUDA if the stream reports
+ * an error, else SSD_OK.
+ */
+ssd_status_t ssd_stream_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_GB300_H */

@@ -1,0 +1,308 @@
+// C ABI of the SSD forward library: argument validation, workspace layout,
+// stage orchestration and the kernel status word.  See include/ssd.h for the
+// contract of every entry point.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+
+// Kernel-side error word.  Kernels OR bit 0 into it when a bounded wait runs
+// out; ssd_stream_status() reads and clears it.
+__device__ unsigned int g_ssd_status_word;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void note_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int *g_status_addr[kMaxDevices];
+}  // namespace
+
+unsigned int *device_status_word()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ssd_status_word) != cudaSuccess)
+            return nullptr;
+        g_status_addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return g_status_addr[dev];
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates dims and chunk size; fills g.  T == 0 is accepted only when
+// allow_auto (ssd_fwd), and then g.T stays 0 for the caller to choose.
+ssd_status_t make_geom(const ssd_dims_t &d, int T, bool allow_auto, Geom *g)
+{
+    if (d.batch < 1 || d.seqlen < 0 || d.nheads < 1 || d.headdim < 1 || d.dstate < 1 ||
+        d.ngroups < 1)
+        return SSD_ERR_INVALID_ARG;
+    if (d.nheads % d.ngroups != 0)
+        return SSD_ERR_INVALID_ARG;
+    if (T < 0 || (T == 0 && !allow_auto))
+        return SSD_ERR_INVALID_ARG;
+    if (T > 256 || d.headdim > 256 || d.dstate > 512 || d.batch > 65535 ||
+        d.batch * d.nheads > 65535LL * 64 || d.seqlen > (1LL << 40))
+        return SSD_ERR_UNSUPPORTED;
+    // keep every element count far from int64 overflow
+    const double elems = (double)d.batch * (double)d.seqlen * (double)d.nheads * (double)d.headdim;
+    const double st = (double)d.batch * d.nheads * d.headdim * d.dstate *
+                      (double)((d.seqlen + (T ? T : 64) - 1) / (T ? T : 64) + 1);
+    if (elems > 4e15 || st > 4e15)
+        return SSD_ERR_UNSUPPORTED;
+    g->B = d.batch;
+    g->L = d.seqlen;
+    g->H = d.nheads;
+    g->P = d.headdim;
+    g->S = d.dstate;
+    g->G = d.ngroups;
+    g->T = T;
+    g->nc = T ? (d.seqlen + T - 1) / T : 0;
+    g->hpg = (int)(d.nheads / d.ngroups);
+    return SSD_OK;
+}
+
+// A required pointer may be NULL only when the tensor it names is empty.
+ssd_status_t need(const void *p, bool nonempty)
+{
+    if (!p)
+        return nonempty ? SSD_ERR_INVALID_ARG : SSD_OK;
+    return aligned16(p) ? SSD_OK : SSD_ERR_ALIGNMENT;
+}
+
+ssd_status_t opt(const void *p) { return (!p || aligned16(p)) ? SSD_OK : SSD_ERR_ALIGNMENT; }
+
+#define SSD_TRY(expr)                                  \
+    do {                                               \
+        ssd_status_t _s = (expr);                      \
+        if (_s != SSD_OK)                              \
+            return _s;                                 \
+    } while (0)
+
+ssd_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int choose_chunk_size(const Geom &g, ssd_dtype_t t)
+{
+    (void)t;
+    // Longer chunks amortise the serial carry; short sequences do not need them.
+    if (g.L <= 64)
+        return 64;
+    return 128;
+}
+
+struct Workspace {
+    float *Gc, *dtT, *states;
+    size_t bytes;
+};
+
+Workspace layout(const Geom &g, bool caller_states, char *base)
+{
+    const size_t bhl = (size_t)(g.B * g.H * g.L) * sizeof(float);
+    size_t off = 0;
+    Workspace w{};
+    w.Gc = reinterpret_cast<float *>(base + off);
+    off = round_up(off + bhl, 256);
+    w.dtT = reinterpret_cast<float *>(base + off);
+    off = round_up(off + bhl, 256);
+    w.states = nullptr;
+    if (!caller_states) {
+        w.states = reinterpret_cast<float *>(base + off);
+        off = round_up(off + (size_t)(g.B * g.H * g.nc * g.P * g.S) * sizeof(float), 256);
+    }
+    w.bytes = off;
+    if (!base)
+        w.Gc = w.dtT = w.states = nullptr;
+    return w;
+}
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+uint64_t ssd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *ssd_status_string(ssd_status_t s)
+{
+    switch (s) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_ARG: return "invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "unsupported size";
+    case SSD_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case SSD_ERR_CUDA: return "CUDA error";
+    case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+    case SSD_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+ssd_status_t ssd_chunk_cumsum(const float *dt, const float *A, float *G_cum, float *dt_t,
+                              ssd_dims_t dims, int chunk_size, void *stream)
+{
+    Geom g;
+    SSD_TRY(make_geom(dims, chunk_size, false, &g));
+    const bool ne = g.L > 0;
+    SSD_TRY(need(dt, ne));
+    SSD_TRY(need(A, true));
+    SSD_TRY(need(G_cum, ne));
+    SSD_TRY(opt(dt_t));
+    return cuda_status(launch_chunk_cumsum(dt, A, G_cum, dt_t, g, (cudaStream_t)stream));
+}
+
+ssd_status_t ssd_state_pass(const void *x, const void *Bm, const float *dt_t, const float *G_cum,
+                            const float *init_state, float *chunk_states, float *final_state,
+                            ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, void *stream)
+{
+    Geom g;
+    SSD_TRY(make_geom(dims, chunk_size, false, &g));
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return SSD_ERR_INVALID_ARG;
+    const bool ne = g.L > 0;
+    SSD_TRY(need(x, ne));
+    SSD_TRY(need(Bm, ne));
+    SSD_TRY(need(dt_t, ne));
+    SSD_TRY(need(G_cum, ne));
+    SSD_TRY(opt(init_state));
+    SSD_TRY(opt(chunk_states));
+    SSD_TRY(opt(final_state));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (g.L == 0) {
+        if (!final_state)
+            return SSD_OK;
+        const size_t bytes = (size_t)(g.B * g.H * g.P * g.S) * sizeof(float);
+        return cuda_status(init_state
+                               ? cudaMemcpyAsync(final_state, init_state, bytes,
+                                                 cudaMemcpyDeviceToDevice, st)
+                               : cudaMemsetAsync(final_state, 0, bytes, st));
+    }
+    return cuda_status(launch_state_pass_simt(x, Bm, dt_t, G_cum, init_state, chunk_states,
+                                              final_state, g, dtype == SSD_BF16, st));
+}
+
+ssd_status_t ssd_chunk_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
+                           const float *G_cum, const float *chunk_states, const float *D, void *y,
+                           ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, void *stream)
+{
+    Geom g;
+    SSD_TRY(make_geom(dims, chunk_size, false, &g));
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return SSD_ERR_INVALID_ARG;
+    const bool ne = g.L > 0;
+    SSD_TRY(need(x, ne));
+    SSD_TRY(need(Bm, ne));
+    SSD_TRY(need(Cm, ne));
+    SSD_TRY(need(dt_t, ne));
+    SSD_TRY(need(G_cum, ne));
+    SSD_TRY(need(chunk_states, ne));
+    SSD_TRY(need(D, true));
+    SSD_TRY(need(y, ne));
+    if (!ne)
+        return SSD_OK;
+    return cuda_status(launch_chunk_out_simt(x, Bm, Cm, dt_t, G_cum, chunk_states, D, y, g,
+                                             dtype == SSD_BF16, (cudaStream_t)stream));
+}
+
+int ssd_fwd_chosen_chunk_size(ssd_dims_t dims, ssd_dtype_t dtype)
+{
+    Geom g;
+    if (make_geom(dims, 0, true, &g) != SSD_OK)
+        return 0;
+    return choose_chunk_size(g, dtype);
+}
+
+size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
+                              int want_chunk_states)
+{
+    Geom g;
+    if (make_geom(dims, chunk_size, true, &g) != SSD_OK)
+        return 0;
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return 0;
+    if (g.T == 0) {
+        g.T = choose_chunk_size(g, dtype);
+        g.nc = (g.L + g.T - 1) / g.T;
+    }
+    const size_t b = layout(g, want_chunk_states != 0, nullptr).bytes;
+    return b ? b : 256;
+}
+
+ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void *Bm,
+                     const void *Cm, const float *D, const float *init_state, void *y,
+                     float *final_state, float *chunk_states, ssd_dims_t dims,
+                     ssd_dtype_t dtype, int chunk_size, void *workspace, size_t workspace_bytes,
+                     void *stream)
+{
+    Geom g;
+    SSD_TRY(make_geom(dims, chunk_size, true, &g));
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return SSD_ERR_INVALID_ARG;
+    if (g.T == 0) {
+        g.T = choose_chunk_size(g, dtype);
+        g.nc = (g.L + g.T - 1) / g.T;
+    }
+    const bool ne = g.L > 0;
+    SSD_TRY(need(x, ne));
+    SSD_TRY(need(dt, ne));
+    SSD_TRY(need(A, true));
+    SSD_TRY(need(Bm, ne));
+    SSD_TRY(need(Cm, ne));
+    SSD_TRY(need(D, true));
+    SSD_TRY(need(y, ne));
+    SSD_TRY(opt(init_state));
+    SSD_TRY(opt(final_state));
+    SSD_TRY(opt(chunk_states));
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!ne)
+        return ssd_state_pass(x, Bm, nullptr, nullptr, init_state, chunk_states, final_state,
+                              dims, dtype, g.T, stream);
+
+    const Workspace need_ws = layout(g, chunk_states != nullptr, nullptr);
+    if (!workspace || workspace_bytes < need_ws.bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return SSD_ERR_WORKSPACE;
+    const Workspace w = layout(g, chunk_states != nullptr, static_cast<char *>(workspace));
+    float *states = chunk_states ? chunk_states : w.states;
+    const bool bf16 = dtype == SSD_BF16;
+
+    SSD_TRY(cuda_status(launch_chunk_cumsum(dt, A, w.Gc, w.dtT, g, st)));
+    SSD_TRY(cuda_status(
+        launch_state_pass_simt(x, Bm, w.dtT, w.Gc, init_state, states, final_state, g, bf16, st)));
+    return cuda_status(
+        launch_chunk_out_simt(x, Bm, Cm, w.dtT, w.Gc, states, D, y, g, bf16, st));
+}
+
+ssd_status_t ssd_stream_status(void *stream)
+{
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    unsigned int *w = device_status_word();
+    if (!w)
+        return SSD_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (v && cudaMemset(w, 0, sizeof(v)) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    return (v & 1u) ? SSD_ERR_TIMEOUT : SSD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,41 @@
+// Host-side declarations shared by the library's translation units.
+// Not part of the public ABI (include/ssd.h is).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ssd.h"
+
+namespace ssd {
+
+// Problem geometry after validation.  hpg = heads per B/C group.
+struct Geom {
+    int64_t B, L, H, P, S, G;
+    int T;
+    int64_t nc;
+    int hpg;
+};
+
+// Kernel-side error word (bit 0: a bounded wait ran out).  Returns its
+// device address for the current device, or nullptr on failure.
+unsigned int *device_status_word();
+
+// Counts kernel launches (ssd_launch_count); every launcher calls it once per
+// kernel it enqueues.
+void note_launch(unsigned n = 1);
+
+// Stage launchers (one translation unit each).
+cudaError_t launch_chunk_cumsum(const float *dt, const float *A, float *Gc, float *dtT,
+                                const Geom &g, cudaStream_t st);
+
+// CUDA-core kernels with f32 arithmetic; serve every shape and both dtypes.
+cudaError_t launch_state_pass_simt(const void *x, const void *Bm, const float *dtT,
+                                   const float *Gc, const float *init, float *states,
+                                   float *final_state, const Geom &g, bool bf16,
+                                   cudaStream_t st);
+cudaError_t launch_chunk_out_simt(const void *x, const void *Bm, const void *Cm,
+                                  const float *dtT, const float *Gc, const float *states,
+                                  const float *D, void *y, const Geom &g, bool bf16,
+                                  cudaStream_t st);
+
+}  // namespace ssd

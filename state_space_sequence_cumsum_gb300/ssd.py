@@ -1,0 +1,218 @@
+"""Tensor-level binding of the C ABI (same names as ``include/ssd.h``).
+
+PyTorch only allocates outputs/workspace and supplies the current CUDA
+stream; every arithmetic step runs in the library's kernels.  Inputs must be
+contiguous CUDA tensors on one device: x, B, C in bf16 or f32 (one dtype),
+dt, A, D and states in f32.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import SsdError, check, dims as _dims
+
+__all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_fwd", "ssd_fwd_plan",
+           "ssd_fwd_staged",
+           "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_stream_status",
+           "ssd_status_string", "SsdError", "Workspace"]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return _lib.SSD_BF16
+    if t.dtype == torch.float32:
+        return _lib.SSD_F32
+    raise TypeError(f"x/B/C must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("SSD tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("SSD tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def _f32(t, name):
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    return t
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _geom(x, B):
+    b, L, H, P = x.shape
+    if B.dim() != 4 or B.shape[0] != b or B.shape[1] != L:
+        raise ValueError("B/C must be [batch, seqlen, ngroups, dstate]")
+    return _dims(b, L, H, P, B.shape[3], B.shape[2])
+
+
+def ssd_status_string(status: int) -> str:
+    return _lib.status_string(status)
+
+
+def ssd_chunk_cumsum(dt, A, chunk_size, G_cum=None, dt_t=None, want_dt_t=True, stream=None):
+    """Stage 1.  Returns (G_cum [B,H,L] f32, dt_t [B,H,L] f32 or None)."""
+    _f32(dt, "dt"), _f32(A, "A")
+    b, L, H = dt.shape
+    if G_cum is None:
+        G_cum = torch.empty((b, H, L), device=dt.device, dtype=torch.float32)
+    if dt_t is None and want_dt_t:
+        dt_t = torch.empty((b, H, L), device=dt.device, dtype=torch.float32)
+    d = _dims(b, L, H, 1, 1, 1)
+    check(_lib.load().ssd_chunk_cumsum(_ptr(dt), _ptr(A), _ptr(G_cum), _ptr(dt_t), d,
+                                       int(chunk_size), _stream(stream)), "ssd_chunk_cumsum")
+    return G_cum, dt_t
+
+
+def ssd_state_pass(x, B, dt_t, G_cum, chunk_size, init_state=None, chunk_states=True,
+                   final_state=True, stream=None):
+    """Stage 2.  chunk_states / final_state: True = allocate, None/False = skip,
+    or a preallocated f32 tensor.  Returns (chunk_states, final_state)."""
+    d = _geom(x, B)
+    nc = (d.seqlen + chunk_size - 1) // chunk_size
+    dev = x.device
+    if chunk_states is True:
+        chunk_states = torch.empty((d.batch, d.nheads, nc, d.headdim, d.dstate), device=dev,
+                                   dtype=torch.float32)
+    if final_state is True:
+        final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate), device=dev,
+                                  dtype=torch.float32)
+    chunk_states = chunk_states if isinstance(chunk_states, torch.Tensor) else None
+    final_state = final_state if isinstance(final_state, torch.Tensor) else None
+    _f32(init_state, "init_state")
+    check(_lib.load().ssd_state_pass(_ptr(x), _ptr(B), _ptr(dt_t), _ptr(G_cum),
+                                     _ptr(init_state), _ptr(chunk_states), _ptr(final_state), d,
+                                     _dtype_code(x), int(chunk_size), _stream(stream)),
+          "ssd_state_pass")
+    return chunk_states, final_state
+
+
+def ssd_chunk_out(x, B, C, dt_t, G_cum, chunk_states, D, chunk_size, y=None, stream=None):
+    """Stage 3.  Returns y [B,L,H,P] in x's dtype."""
+    d = _geom(x, B)
+    if y is None:
+        y = torch.empty_like(x)
+    check(_lib.load().ssd_chunk_out(_ptr(x), _ptr(B), _ptr(C), _ptr(dt_t), _ptr(G_cum),
+                                    _ptr(chunk_states), _ptr(_f32(D, "D")), _ptr(y), d,
+                                    _dtype_code(x), int(chunk_size), _stream(stream)),
+          "ssd_chunk_out")
+    return y
+
+
+def ssd_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, dtype, chunk_size,
+                           want_chunk_states) -> int:
+    code = _lib.SSD_BF16 if dtype == torch.bfloat16 else _lib.SSD_F32
+    return int(_lib.load().ssd_fwd_workspace_size(
+        _dims(batch, seqlen, nheads, headdim, dstate, ngroups), code, int(chunk_size),
+        int(bool(want_chunk_states))))
+
+
+def ssd_fwd_chosen_chunk_size(batch, seqlen, nheads, headdim, dstate, ngroups, dtype) -> int:
+    code = _lib.SSD_BF16 if dtype == torch.bfloat16 else _lib.SSD_F32
+    return int(_lib.load().ssd_fwd_chosen_chunk_size(
+        _dims(batch, seqlen, nheads, headdim, dstate, ngroups), code))
+
+
+class Workspace:
+    """Reusable device workspace for ssd_fwd (grown on demand, 256-byte aligned)
+    plus named buffers for the stage-by-stage form of the same pass."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+        self.named = {}
+
+    def get(self, nbytes: int, device) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != device:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        return self.buf
+
+    def tensor(self, name, shape, dtype, device) -> torch.Tensor:
+        t = self.named.get(name)
+        if t is None or tuple(t.shape) != tuple(shape) or t.dtype != dtype or t.device != device:
+            t = torch.empty(shape, dtype=dtype, device=device)
+            self.named[name] = t
+        return t
+
+
+def ssd_fwd(x, dt, A, B, C, D, chunk_size=0, initial_state=None, return_final_state=True,
+            return_chunk_states=False, y=None, final_state=None, chunk_states=None,
+            workspace: Workspace | None = None, stream=None):
+    """Whole SSD forward.  Returns (y, final_state or None, chunk_states or None)."""
+    d = _geom(x, B)
+    for t, n in ((dt, "dt"), (A, "A"), (D, "D"), (initial_state, "initial_state")):
+        _f32(t, n)
+    code = _dtype_code(x)
+    lib = _lib.load()
+    T = int(chunk_size) or int(lib.ssd_fwd_chosen_chunk_size(d, code))
+    if T <= 0:
+        raise SsdError(_lib.SSD_ERR_INVALID_ARG, "ssd_fwd")
+    nc = (d.seqlen + T - 1) // T
+    dev = x.device
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate), device=dev,
+                                  dtype=torch.float32)
+    if chunk_states is None and return_chunk_states:
+        chunk_states = torch.empty((d.batch, d.nheads, nc, d.headdim, d.dstate), device=dev,
+                                   dtype=torch.float32)
+    nbytes = int(lib.ssd_fwd_workspace_size(d, code, T, int(chunk_states is not None)))
+    ws = (workspace or Workspace()).get(nbytes, dev)
+    check(lib.ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                      _ptr(initial_state), _ptr(y), _ptr(final_state), _ptr(chunk_states), d,
+                      code, T, _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream)), "ssd_fwd")
+    return y, final_state, chunk_states
+
+
+def ssd_fwd_plan(x, B, chunk_size, want_states=False) -> dict:
+    """The C-ABI stage calls ssd_fwd makes for these arguments, in order."""
+    return {"path": "three-stage", "chunk_size": int(chunk_size),
+            "kernels": ["chunk_cumsum", "state_pass", "chunk_out"]}
+
+
+def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk_states,
+                   workspace: Workspace, events=None, stream=None):
+    """ssd_fwd as its individual stage calls (same kernels, same order), with an
+    optional CUDA event recorded before the first and after every stage on the
+    launching stream.  Used to time each kernel inside a whole pass."""
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    b, L, H, P = x.shape
+    Sd = B.shape[3]
+    T = plan["chunk_size"]
+    dev = x.device
+    Gc = workspace.tensor("G_cum", (b, H, L), torch.float32, dev)
+    dtT = workspace.tensor("dt_t", (b, H, L), torch.float32, dev)
+    nc = (L + T - 1) // T
+    states = chunk_states
+    if states is None:
+        states = workspace.tensor("chunk_states", (b, H, nc, P, Sd), torch.float32, dev)
+
+    def mark(i):
+        if events is not None:
+            events[i].record(s)
+
+    mark(0)
+    ssd_chunk_cumsum(dt, A, T, G_cum=Gc, dt_t=dtT, stream=s)
+    mark(1)
+    ssd_state_pass(x, B, dtT, Gc, T, init_state=initial_state, chunk_states=states,
+                   final_state=final_state if final_state is not None else False, stream=s)
+    mark(2)
+    ssd_chunk_out(x, B, C, dtT, Gc, states, D, T, y=y, stream=s)
+    mark(3)
+    return y, final_state, chunk_states
+
+
+def ssd_stream_status(stream=None) -> int:
+    """Synchronize the stream and read/clear the kernels' status word."""
+    return int(_lib.load().ssd_stream_status(_stream(stream)))

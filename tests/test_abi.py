@@ -1,0 +1,110 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/ssd.h, and rejects each class of invalid argument on the
+host with the documented status before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_sequence_cumsum_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.ssd_status_string(code)
+    assert b"timed out" in lib.ssd_status_string(_lib.SSD_ERR_TIMEOUT)
+
+
+FAKE = ctypes.c_void_p(0x10000)       # aligned, never dereferenced (validation fails first)
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def cumsum(lib, d, T, dt=FAKE, A=FAKE, G=FAKE, dtT=None):
+    return lib.ssd_chunk_cumsum(dt, A, G, dtT, d, T, None)
+
+
+@pytest.mark.parametrize("dims,T,expect", [
+    ((0, 16, 2, 8, 8, 1), 16, _lib.SSD_ERR_INVALID_ARG),      # batch 0
+    ((1, -1, 2, 8, 8, 1), 16, _lib.SSD_ERR_INVALID_ARG),      # negative seqlen
+    ((1, 16, 3, 8, 8, 2), 16, _lib.SSD_ERR_INVALID_ARG),      # H % G != 0
+    ((1, 16, 2, 8, 8, 1), 0, _lib.SSD_ERR_INVALID_ARG),       # stages need T > 0
+    ((1, 16, 2, 8, 8, 1), 257, _lib.SSD_ERR_UNSUPPORTED),     # T > 256
+    ((1, 16, 2, 300, 8, 1), 16, _lib.SSD_ERR_UNSUPPORTED),    # P > 256
+    ((1, 16, 2, 8, 600, 1), 16, _lib.SSD_ERR_UNSUPPORTED),    # S > 512
+    ((70000, 16, 2, 8, 8, 1), 16, _lib.SSD_ERR_UNSUPPORTED),  # batch beyond grid
+])
+def test_invalid_dims(lib, dims, T, expect):
+    d = _lib.dims(*dims)
+    assert lib.ssd_state_pass(FAKE, FAKE, FAKE, FAKE, None, None, None, d, 0, T, None) == expect
+    assert lib.ssd_chunk_out(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, d, 0, T,
+                             None) == expect
+
+
+def test_null_and_misaligned_pointers(lib):
+    before = lib.ssd_launch_count()
+    d = _lib.dims(1, 32, 2, 8, 8, 1)
+    assert cumsum(lib, d, 16, dt=None) == _lib.SSD_ERR_INVALID_ARG
+    assert cumsum(lib, d, 16, A=None) == _lib.SSD_ERR_INVALID_ARG
+    assert cumsum(lib, d, 16, G=MISALIGNED) == _lib.SSD_ERR_ALIGNMENT
+    assert cumsum(lib, d, 16, dtT=MISALIGNED) == _lib.SSD_ERR_ALIGNMENT
+    assert lib.ssd_chunk_out(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, d, 0, 16,
+                             None) == _lib.SSD_ERR_INVALID_ARG  # chunk_states required
+    assert lib.ssd_state_pass(FAKE, FAKE, FAKE, FAKE, MISALIGNED, None, None, d, 0, 16,
+                              None) == _lib.SSD_ERR_ALIGNMENT
+    assert lib.ssd_launch_count() == before  # rejected calls launch nothing
+
+
+def test_bad_dtype(lib):
+    d = _lib.dims(1, 32, 2, 8, 8, 1)
+    assert lib.ssd_state_pass(FAKE, FAKE, FAKE, FAKE, None, None, None, d, 7, 16,
+                              None) == _lib.SSD_ERR_INVALID_ARG
+
+
+def test_fwd_workspace_checks(lib):
+    d = _lib.dims(2, 300, 4, 16, 32, 2)
+    need = lib.ssd_fwd_workspace_size(d, 0, 64, 0)
+    assert need > 0 and need % 256 == 0
+    args = [FAKE] * 6 + [None, FAKE, None, None, d, 0, 64]
+    assert lib.ssd_fwd(*args, None, need, None) == _lib.SSD_ERR_WORKSPACE
+    assert lib.ssd_fwd(*args, FAKE, need - 256, None) == _lib.SSD_ERR_WORKSPACE
+    assert lib.ssd_fwd(*args, ctypes.c_void_p(0x10010), need, None) == _lib.SSD_ERR_WORKSPACE
+
+
+def test_workspace_size_grows_with_problem(lib):
+    small = lib.ssd_fwd_workspace_size(_lib.dims(1, 1024, 8, 64, 128, 1), 0, 128, 0)
+    big = lib.ssd_fwd_workspace_size(_lib.dims(1, 4096, 8, 64, 128, 1), 0, 128, 0)
+    assert big > small > 0
+    assert lib.ssd_fwd_workspace_size(_lib.dims(0, 1, 1, 1, 1, 1), 0, 64, 0) == 0
+    # asking for caller-owned chunk states never needs more workspace
+    d = _lib.dims(1, 4096, 8, 64, 128, 1)
+    assert lib.ssd_fwd_workspace_size(d, 0, 128, 1) <= lib.ssd_fwd_workspace_size(d, 0, 128, 0)
+
+
+def test_auto_chunk_size_is_supported(lib):
+    for L in (1, 64, 1000, 4096, 262144):
+        T = lib.ssd_fwd_chosen_chunk_size(_lib.dims(1, L, 8, 64, 128, 1), 0)
+        assert T in (64, 128, 256)

@@ -1,0 +1,121 @@
+"""GPU parity of ssd_fwd (through the C ABI) against the float64 oracle.
+
+Sizes here finish in seconds on the oracle yet span several tiles and a
+ragged tail; edge cases cover empty, single-token, sub-chunk and
+chunk-plus-one sequences, grouped B/C, an initial state, every supported
+chunk size and the f32 path.  The full-size workloads are in
+test_parity_full.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity_util import TOL, assert_parity, case_inputs, oracle_run, to_gpu
+import state_space_sequence_cumsum_gb300 as ssd
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd(inp, T, want_states=True):
+    g = to_gpu(inp)
+    y, fin, st = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=T,
+                             initial_state=g["init"], return_final_state=True,
+                             return_chunk_states=want_states)
+    assert ssd.ssd_stream_status() == 0
+    return y, fin, st
+
+
+def check_case(B, L, H, P, S, G, T, dtype, init="zero", seed=0, want_states=True):
+    inp = case_inputs(B, L, H, P, S, G, T, dtype=dtype, init=init, seed=seed)
+    y, fin, st = run_fwd(inp, T, want_states)
+    ref = oracle_run(inp, T, want_states=want_states)
+    assert_parity(y, ref["y"], dtype, "y")
+    assert_parity(fin, ref["final_state"], dtype, "final_state")
+    if want_states:
+        assert_parity(st, ref["chunk_states"], dtype, "chunk_states")
+
+
+def test_tiny_fp32_config():
+    """batch 1, L 256, 2 heads, P 16, S 16, chunk 64, f32, zero init."""
+    check_case(1, 256, 2, 16, 16, 1, 64, torch.float32)
+
+
+@pytest.mark.parametrize("T", [64, 128, 256])
+def test_bf16_chunk_sizes(T):
+    check_case(2, 3 * T + 17, 4, 64, 128, 1, T, torch.bfloat16, init="randn", seed=T)
+
+
+@pytest.mark.parametrize("P,S", [(32, 64), (64, 256), (128, 128), (64, 512), (16, 16)])
+def test_bf16_head_and_state_sizes(P, S):
+    check_case(1, 700, 4, P, S, 2, 128, torch.bfloat16, init="randn", seed=P + S)
+
+
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 129])
+def test_edge_lengths(L):
+    check_case(2, L, 4, 64, 128, 1, 64, torch.bfloat16, init="randn", seed=L)
+
+
+def test_empty_sequence_copies_init():
+    inp = case_inputs(2, 0, 4, 64, 128, 1, 64, init="randn", seed=5)
+    y, fin, st = run_fwd(inp, 64)
+    assert y.numel() == 0 and st.shape[2] == 0
+    assert torch.equal(fin.cpu(), inp["init"])
+
+
+def test_grouped_heads_share_B_and_C():
+    check_case(2, 515, 8, 64, 128, 4, 128, torch.bfloat16, init="randn", seed=9)
+
+
+def test_fp32_path_several_tiles():
+    check_case(2, 333, 3, 64, 96, 3, 64, torch.float32, init="randn", seed=11)
+
+
+def test_auto_chunk_size_and_no_states():
+    inp = case_inputs(1, 1000, 4, 64, 128, 1, 64, seed=13)
+    g = to_gpu(inp)
+    y, fin, st = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=0)
+    assert st is None
+    T = ssd.ssd_fwd_chosen_chunk_size(1, 1000, 4, 64, 128, 1, torch.bfloat16)
+    ref = oracle_run(inp, T)
+    assert_parity(y, ref["y"], torch.bfloat16, "y")
+    assert_parity(fin, ref["final_state"], torch.bfloat16, "final")
+
+
+def test_two_halves_with_carried_state_equal_one_run():
+    """final_state of call 1 fed as init of call 2 reproduces the single run
+    (section "Kernel 2": the final state is the next call's init_state)."""
+    inp = case_inputs(2, 1024, 4, 64, 128, 1, 128, init="randn", seed=17)
+    g = to_gpu(inp)
+    y_full, f_full, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], 128,
+                                    initial_state=g["init"])
+    cut = 384
+    a = {k: (v[:, :cut].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in g.items()}
+    b = {k: (v[:, cut:].contiguous() if k in ("x", "dt", "B", "C") else v) for k, v in g.items()}
+    y1, f1, _ = ssd.ssd_fwd(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], 128,
+                            initial_state=a["init"])
+    y2, f2, _ = ssd.ssd_fwd(b["x"], b["dt"], b["A"], b["B"], b["C"], b["D"], 128,
+                            initial_state=f1)
+    ref = oracle_run(inp, 128)
+    assert_parity(torch.cat([y1, y2], dim=1), ref["y"], torch.bfloat16, "split y")
+    assert_parity(f2, ref["final_state"], torch.bfloat16, "split final")
+    assert_parity(y_full, ref["y"], torch.bfloat16, "full y")
+
+
+def test_final_state_independent_of_chunk_size():
+    inp = case_inputs(1, 777, 4, 64, 128, 1, 64, init="randn", seed=19)
+    g = to_gpu(inp)
+    finals = []
+    for T in (64, 128, 256):
+        _, f, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], T,
+                              initial_state=g["init"])
+        finals.append(f)
+    ref = oracle_run(inp, 64)["final_state"]
+    for f in finals:
+        assert_parity(f, ref, torch.bfloat16, "final")
+
+
+def test_repeat_calls_are_deterministic():
+    inp = case_inputs(1, 600, 4, 64, 128, 1, 128, seed=23)
+    y1, f1, _ = run_fwd(inp, 128, False)
+    y2, f2, _ = run_fwd(inp, 128, False)
+    assert torch.equal(y1, y2) and torch.equal(f1, f2)
