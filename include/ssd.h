@@ -43,9 +43,11 @@
  *   mutex-guarded cache of TMA descriptors and tuning choices.
  * Supported sizes: 1 <= P <= 256, 1 <= S <= 512, 1 <= T <= 256, H % G == 0,
  *   L >= 0 (L == 0 copies init_state to final_state and launches nothing
- *   else).  The tensor-core path serves bf16 with P in {32, 64, 128},
- *   S % 64 == 0 and T in {64, 128, 256}; other shapes and all f32 calls run
- *   the f32-arithmetic CUDA-core kernels.
+ *   else).  The tensor-core (tcgen05) kernels serve bf16 with T a multiple
+ *   of 128: the state pass for P in {64, 128} and S % 64 == 0; the chunk
+ *   output and the fused pass for (P, S) in {64} x {64, 128, 256} and
+ *   {128} x {64, 128}.  Other shapes and all f32 calls run f32-arithmetic
+ *   CUDA-core kernels.
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H
@@ -110,6 +112,29 @@ ssd_status_t ssd_state_pass(const void *x, const void *Bm, const float *dt_t, co
 ssd_status_t ssd_chunk_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
                            const float *G_cum, const float *chunk_states, const float *D, void *y,
                            ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, void *stream);
+
+/*
+ * Stages 2 and 3 fused (bf16 tensor-core path): walks every (batch, head)
+ * sequence once, carrying the state on chip from tile to tile, and writes y,
+ * the final state (may be NULL) and, if chunk_states is not NULL, every
+ * chunk's start state.  Arithmetic is that of ssd_state_pass followed by
+ * ssd_chunk_out.  G_cum and dt_t are stage 1's outputs.  Returns
+ * SSD_ERR_UNSUPPORTED for f32 calls and for shapes outside the tensor-core
+ * path (see "Supported sizes"); use the two separate stages there.
+ */
+ssd_status_t ssd_state_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
+                           const float *G_cum, const float *D, const float *init_state, void *y,
+                           float *final_state, float *chunk_states, ssd_dims_t dims,
+                           ssd_dtype_t dtype, int chunk_size, void *stream);
+
+/* Which kernels ssd_fwd runs for these arguments (chunk_size 0 = auto). */
+typedef enum {
+    SSD_PATH_INVALID = -1,
+    SSD_PATH_STAGED_CUDA_CORES = 0,   /* cumsum -> state_pass -> chunk_out, f32 CUDA cores */
+    SSD_PATH_STAGED_TENSOR_CORES = 1, /* cumsum -> state_pass -> chunk_out, tcgen05 */
+    SSD_PATH_FUSED_TENSOR_CORES = 2   /* cumsum -> state_out (fused), tcgen05 */
+} ssd_path_t;
+ssd_path_t ssd_fwd_path(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, int want_chunk_states);
 
 /*
  * Bytes of device workspace ssd_fwd needs for these arguments (the G_cum,

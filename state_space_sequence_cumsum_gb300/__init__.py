@@ -6,7 +6,7 @@ load the library; the first call does, and raises if the library cannot be
 built or loaded (there is no CPU fallback).
 """
 from .ssd import (SsdError, Workspace, ssd_chunk_cumsum, ssd_chunk_out, ssd_fwd,  # noqa: F401
-                  ssd_fwd_chosen_chunk_size, ssd_fwd_plan, ssd_fwd_staged, ssd_fwd_workspace_size,
-                  ssd_state_pass,
+                  ssd_fwd_chosen_chunk_size, ssd_fwd_path, ssd_fwd_plan, ssd_fwd_staged,
+                  ssd_fwd_workspace_size, ssd_state_out, ssd_state_pass,
                   ssd_status_string, ssd_stream_status)
 from ._build import build  # noqa: F401

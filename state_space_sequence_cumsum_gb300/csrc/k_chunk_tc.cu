@@ -1,0 +1,661 @@
+// Stage 3 (chunk output) and the fused single-pass forward on tensor cores,
+// bf16 inputs.
+//
+// "Accelerating Mamba-2 forward-pass kernels with CUDA Tile (cuTile)",
+// section "Kernel 3: compute_out", per (batch, chunk, head):
+//     Y = exp2(G) * (C h_c^T) + (exp2(G_i - G_j) * (C B^T) * M)(dt * X) + D X
+// and section "Kernel 2: fwd_pass_state" for the state jump
+//     h <- exp2(G_last) h + X^T (B * dt * exp2(G_last - G)).
+//
+// One kernel, two modes:
+//   OUT   -- a work item is (batch, chunk, head); h_c comes from chunk_states.
+//   FUSED -- a work item is (batch, head) over the whole sequence; the state
+//            is carried on chip from tile to tile, so chunk states never go
+//            through HBM unless the caller asks for them.
+// Tokens are processed in 128-token tiles (the tcgen05 M and K extent).  A
+// chunk of 256 tokens is two tiles: the second tile's starting state is the
+// first tile's state jump applied to h_c, and its G is taken relative to the
+// token before it, which is the same arithmetic regrouped
+// (exp2(G_i - G_j) = exp2(G_i - G_m) exp2(G_m - G_j) with both factors <= 1).
+//
+// Per tile (all contractions are tcgen05.mma kind::f16, f32 accumulate in TMEM):
+//   CB  = C B^T                 M 128 (i) x N 128 (j), K = S     [TMEM cols 0..127]
+//   scores_ij = CB_ij exp2(g_i - g_j) dt_j for j <= i (masked entries are set
+//               to zero without evaluating the exponent), bf16 into shared memory
+//   Y1  = scores X              N = P, K = 128                   [TMEM]
+//   Y2  = C H^T, H = bf16(h_c)  N = P, K = S                     [TMEM]
+//   y   = Y1 + exp2(g_i) Y2 + D x      (f32 epilogue, bf16 store)
+//   and, when a later tile needs the state: h <- exp2(g_L) h + B^T X_hat with
+//   X_hat = dt exp2(g_L - g) X split into bf16 hi + lo (two MMA passes); the
+//   state h^T [S, P] is an f32 TMEM accumulator.
+//
+// Roles: warps 0-3 are the compute warpgroup (thread i owns tile row i, i.e.
+// TMEM lane i); warp 4 lane 0 issues TMA loads into a STAGES-deep ring
+// (B, C and x tiles, 128-byte swizzle); warp 5 lane 0 issues the MMAs.  The
+// CTA is persistent over work items.  Every wait is bounded; a timeout sets
+// the kernel status word and the role leaves its loop.
+#include "common.cuh"
+#include "ssd_internal.h"
+#include "tc05.cuh"
+
+namespace ssd {
+namespace {
+using namespace tc;
+
+constexpr int kTile = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kRegion = 128 * 128;
+
+template <int P, int S, int STAGES>
+struct CoLayout {
+    static constexpr int kSReg = S / 64;       // 64-wide dstate regions of B / C
+    static constexpr int kPReg = P / 64;       // 64-wide headdim regions of x
+    static constexpr int kSBlk = (S + 127) / 128;  // 128-row blocks of the state
+    static constexpr uint32_t kB = kSReg * kRegion;
+    static constexpr uint32_t kX = kPReg * kRegion;
+    static constexpr uint32_t kStage = 2 * kB + kX;        // B, C, x
+    static constexpr uint32_t off_scores = STAGES * kStage;  // 2 regions (keys 0-63, 64-127)
+    static constexpr uint32_t kScores = 2 * kRegion;
+    // X_hat (hi, then lo) starts on the scores buffer, which is free once the
+    // scores MMA has completed; what does not fit extends past it
+    static constexpr uint32_t off_xh = off_scores;
+    static constexpr uint32_t off_h = off_scores + (2 * kX > kScores ? 2 * kX : kScores);
+    static constexpr uint32_t kHRegion = P * 128;          // P rows x 128 bytes
+    static constexpr uint32_t kH = kSReg * kHRegion;
+    static constexpr uint32_t off_g = off_h + kH;          // g[2][128], dt[2][128] (f32)
+    static constexpr uint32_t bytes = off_g + 4 * 128 * 4;
+    // TMEM columns
+    static constexpr uint32_t t_cb = 0, t_y1 = 128, t_y2 = 128 + P, t_st = 128 + 2 * P;
+    static constexpr uint32_t cols_used = t_st + kSBlk * P;
+    static constexpr uint32_t kTmemCols = cols_used <= 256 ? 256 : 512;
+    static_assert(cols_used <= 512, "TMEM budget");
+    // dynamic bytes + alignment pad + static barriers within the 227 KB opt-in limit
+    static_assert(bytes + 1024 + 256 <= 232448, "shared memory budget");
+};
+
+enum Mode { kModeOut = 0, kModeFused = 1 };
+
+struct Params {
+    const float *dtT, *Gc, *D;
+    const float *h_src;   // OUT: chunk_states; FUSED: init_state (may be null)
+    float *states_out;    // FUSED: chunk_states to emit (may be null)
+    float *final_state;   // FUSED: may be null
+    __nv_bfloat16 *y;
+    Geom g;
+    int64_t n_items;
+    int64_t n_tiles;      // tiles per sequence
+    int tiles_per_chunk;
+    unsigned int *status;
+};
+
+struct TileInfo {
+    int64_t b, h, tau;
+    int n;
+    bool first, do_state, last;
+    int64_t item_chunk;  // OUT mode: chunk of the item
+};
+
+template <int MODE>
+struct Items {
+    const Params &p;
+    __device__ Items(const Params &pp) : p(pp) {}
+    // decode work item -> (b, h, tile range)
+    __device__ void decode(int64_t item, int64_t &b, int64_t &h, int64_t &t0, int64_t &t1,
+                           int64_t &chunk) const
+    {
+        if (MODE == kModeOut) {
+            // consecutive items share (b, chunk) so their B/C tiles hit in L2
+            h = item % p.g.H;
+            const int64_t bc = item / p.g.H;
+            chunk = bc % p.g.nc;
+            b = bc / p.g.nc;
+            t0 = chunk * p.tiles_per_chunk;
+            t1 = min64(t0 + p.tiles_per_chunk, p.n_tiles);
+        } else {
+            h = item % p.g.H;
+            b = item / p.g.H;
+            t0 = 0;
+            t1 = p.n_tiles;
+            chunk = 0;
+        }
+    }
+};
+
+__device__ __forceinline__ void tma4(void *dst, const void *tmap, uint64_t *bar, int c0, int c1,
+                                     int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// K-major operand (rows x K, 64 K-elements per 128-byte row, regions of
+// `rows` rows per 64 K): descriptor for the 16-wide K step ks.
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, uint32_t region_bytes, int ks)
+{
+    return smem_desc(base + (ks >> 2) * region_bytes + (ks & 3) * 32, 16, 1024);
+}
+// MN-major operand (128 K-rows of 64 M/N elements per region): K step ks.
+__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int ks)
+{
+    return smem_desc(base + ks * 2048, kRegion, 1024);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+template <int P, int S, int STAGES, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                const __grid_constant__ CUtensorMap tm_c, const Params prm)
+{
+    using Lay = CoLayout<P, S, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES];
+    __shared__ uint64_t bar_cb, bar_scores, bar_y1, bar_h, bar_y2, bar_xh, bar_ds, bar_g;
+    __shared__ uint32_t tmem_slot;
+
+    const Geom &g = prm.g;
+    const Items<MODE> items(prm);
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1 + 128);
+        }
+        mbar_init(&bar_cb, 1);
+        mbar_init(&bar_scores, 128);
+        mbar_init(&bar_y1, 1);
+        mbar_init(&bar_h, 128);
+        mbar_init(&bar_y2, 1);
+        mbar_init(&bar_xh, 128);
+        mbar_init(&bar_ds, 1);
+        mbar_init(&bar_g, 128);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, Lay::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    // Every role walks the same (item, tile) sequence.
+    auto tile_at = [&](int64_t item, int64_t t, int64_t t0, int64_t t1, int64_t b, int64_t h,
+                       int64_t chunk) {
+        TileInfo ti;
+        ti.b = b;
+        ti.h = h;
+        ti.tau = t * kTile;
+        ti.n = (int)min64(kTile, g.L - ti.tau);
+        ti.first = t == t0;
+        ti.last = t + 1 == t1;
+        ti.do_state = !ti.last || (MODE == kModeFused && prm.final_state != nullptr);
+        ti.item_chunk = chunk;
+        (void)item;
+        return ti;
+    };
+
+    if (warp == 4) {
+        // ---------------- TMA producer
+        if ((tid & 31) == 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_b);
+            prefetch_tmap(&tm_c);
+            int64_t it = 0;
+            bool ok = true;
+            for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                int64_t b, h, t0, t1, chunk;
+                items.decode(item, b, h, t0, t1, chunk);
+                const int64_t grp = h / g.hpg;
+                for (int64_t t = t0; t < t1; ++t, ++it) {
+                    const int s = (int)(it % STAGES);
+                    if (it >= STAGES &&
+                        !mbar_wait(&bar_empty[s], (uint32_t)(((it / STAGES) - 1) & 1))) {
+                        atomicOr(prm.status, 1u);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = smem + s * Lay::kStage;
+                    mbar_arrive_expect_tx(&bar_full[s], Lay::kStage);
+                    const int tok = (int)(t * kTile);
+                    for (int r = 0; r < Lay::kSReg; ++r) {
+                        tma4(st + r * kRegion, &tm_b, &bar_full[s], r * 64, (int)grp, tok, (int)b);
+                        tma4(st + Lay::kB + r * kRegion, &tm_c, &bar_full[s], r * 64, (int)grp,
+                             tok, (int)b);
+                    }
+                    for (int r = 0; r < Lay::kPReg; ++r)
+                        tma4(st + 2 * Lay::kB + r * kRegion, &tm_x, &bar_full[s], r * 64, (int)h,
+                             tok, (int)b);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer
+        if ((tid & 31) == 0) {
+            const uint32_t id_cb = idesc_bf16(128, 128, false, false);
+            const uint32_t id_y1 = idesc_bf16(128, P, false, true);
+            const uint32_t id_y2 = idesc_bf16(128, P, false, false);
+            const uint32_t id_ds = idesc_bf16(128, P, true, true);
+            const uint32_t s_scores = smem_u32(smem + Lay::off_scores);
+            const uint32_t s_xh = smem_u32(smem + Lay::off_xh);
+            const uint32_t s_h = smem_u32(smem + Lay::off_h);
+            int64_t it = 0, n_state = 0;
+            bool ok = true;
+            for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                int64_t b, h, t0, t1, chunk;
+                items.decode(item, b, h, t0, t1, chunk);
+                for (int64_t t = t0; t < t1; ++t, ++it) {
+                    const TileInfo ti = tile_at(item, t, t0, t1, b, h, chunk);
+                    const int s = (int)(it % STAGES);
+                    const uint32_t sb = smem_u32(smem + s * Lay::kStage);
+                    const uint32_t sc = sb + Lay::kB;
+                    const uint32_t sx = sb + 2 * Lay::kB;
+                    const uint32_t par = (uint32_t)(it & 1);
+                    if (!mbar_wait(&bar_full[s], (uint32_t)((it / STAGES) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < S / 16; ++ks)
+                        mma_ss(tmem + Lay::t_cb, desc_k(sc, kRegion, ks), desc_k(sb, kRegion, ks),
+                               id_cb, ks > 0);
+                    mma_commit(&bar_cb);
+                    if (!mbar_wait(&bar_scores, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < kTile / 16; ++ks)
+                        mma_ss(tmem + Lay::t_y1, desc_k(s_scores, kRegion, ks), desc_mn(sx, ks),
+                               id_y1, ks > 0);
+                    mma_commit(&bar_y1);
+                    if (!mbar_wait(&bar_h, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < S / 16; ++ks)
+                        mma_ss(tmem + Lay::t_y2, desc_k(sc, kRegion, ks),
+                               desc_k(s_h, Lay::kHRegion, ks), id_y2, ks > 0);
+                    mma_commit(&bar_y2);
+                    if (ti.do_state) {
+                        if (!mbar_wait(&bar_xh, (uint32_t)(n_state & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int mb = 0; mb < Lay::kSBlk; ++mb)
+#pragma unroll
+                            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                                for (int ks = 0; ks < kTile / 16; ++ks)
+                                    mma_ss(tmem + Lay::t_st + mb * P,
+                                           desc_mn(sb + 2 * mb * kRegion, ks),
+                                           desc_mn(s_xh + part * Lay::kX, ks), id_ds, 1u);
+                        mma_commit(&bar_ds);
+                        ++n_state;
+                    }
+                    mma_commit(&bar_empty[s]);
+                }
+            }
+            if (!ok)
+                atomicOr(prm.status, 1u);
+        }
+    } else {
+        // ---------------- compute warpgroup: thread i = tile row i = TMEM lane i
+        const int i = tid;
+        const uint32_t lane = tmem_at(tmem, (uint32_t)(warp * 32), 0);
+        float *sg_all = reinterpret_cast<float *>(smem + Lay::off_g);
+        uint8_t *s_scores = smem + Lay::off_scores;
+        uint8_t *s_xh = smem + Lay::off_xh;
+        uint8_t *s_h = smem + Lay::off_h;
+        int64_t it = 0, n_state = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+            int64_t b, h, t0, t1, chunk;
+            items.decode(item, b, h, t0, t1, chunk);
+            const int64_t bh = b * g.H + h;
+            const float *grow = prm.Gc + bh * g.L;
+            const float *drow = prm.dtT + bh * g.L;
+            const float Dh = prm.D[h];
+            for (int64_t t = t0; t < t1; ++t, ++it) {
+                const TileInfo ti = tile_at(item, t, t0, t1, b, h, chunk);
+                const int s = (int)(it % STAGES);
+                const uint8_t *sx = smem + s * Lay::kStage + 2 * Lay::kB;
+                const uint32_t par = (uint32_t)(it & 1);
+                const int64_t tau = ti.tau;
+                const int n = ti.n;
+                const float base = (tau % g.T == 0) ? 0.f : grow[tau - 1];
+                const float gL = grow[tau + n - 1] - base;
+                const float gi = i < n ? grow[tau + i] - base : 0.f;
+                const float dti = i < n ? drow[tau + i] : 0.f;
+                // per-tile g / dt table, double-buffered by tile parity; the
+                // bounded mbarrier makes all 128 rows visible before use
+                float *sg = sg_all + (it & 1) * 256;
+                float *sdt = sg + 128;
+                sg[i] = gi;
+                sdt[i] = dti;
+                mbar_arrive(&bar_g);
+                if (!mbar_wait(&bar_g, par)) {
+                    ok = false;
+                    break;
+                }
+
+                // ---- scores = CB * exp2(g_i - g_j) * dt_j, causal, bf16 (K-major rows i)
+                if (!mbar_wait(&bar_cb, par)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int wmax = warp * 32 + 31;
+#pragma unroll 1
+                for (int j0 = 0; j0 < kTile; j0 += 16) {
+                    uint32_t pk[8];
+                    if (j0 <= wmax) {  // warp-uniform: tcgen05.ld is warp-collective
+                        uint32_t r[16];
+                        tmem_ld16(lane + Lay::t_cb + j0, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            float v[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int j = j0 + 2 * q + e;
+                                v[e] = (j <= i && j < n)
+                                           ? __uint_as_float(r[2 * q + e]) * exp2f(gi - sg[j]) * sdt[j]
+                                           : 0.f;
+                            }
+                            pk[q] = pack_bf16x2(v[0], v[1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            pk[q] = 0u;
+                    }
+                    uint8_t *rbase = s_scores + (j0 >> 6) * kRegion;
+                    const int c0 = (j0 & 63) >> 3;
+                    *reinterpret_cast<uint4 *>(rbase + sw128_offset(i, c0)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4 *>(rbase + sw128_offset(i, c0 + 1)) =
+                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bar_scores);
+
+                // ---- H = bf16(h at tile start) into K-major [p][s]; state bookkeeping
+                const float decay = exp2f(gL);
+                const bool emit = MODE == kModeFused && prm.states_out && (tau % g.T == 0);
+#pragma unroll 1
+                for (int mb = 0; mb < Lay::kSBlk; ++mb) {
+                    const int sidx = mb * 128 + i;
+                    const bool s_ok = sidx < S;
+                    const uint32_t acc = lane + Lay::t_st + mb * P;
+                    const float *src = nullptr;
+                    if (ti.first) {
+                        if (MODE == kModeOut)
+                            src = prm.h_src + ((bh * g.nc + ti.item_chunk) * g.P) * g.S;
+                        else if (prm.h_src)
+                            src = prm.h_src + bh * g.P * g.S;
+                    }
+                    float *emit_dst =
+                        emit ? prm.states_out + ((bh * g.nc + tau / g.T) * g.P) * g.S : nullptr;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < P; c0 += 16) {
+                        uint32_t r[16];
+                        if (ti.first) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                r[j] = __float_as_uint((src && s_ok) ? src[(int64_t)(c0 + j) * S + sidx]
+                                                                     : 0.f);
+                        } else {
+                            tmem_ld16(acc + c0, r);
+                            tmem_ld_wait();
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float v = __uint_as_float(r[j]);
+                            if (emit_dst && s_ok)
+                                emit_dst[(int64_t)(c0 + j) * S + sidx] = v;
+                            if (s_ok) {
+                                const int p = c0 + j;
+                                uint8_t *hb = s_h + (sidx >> 6) * Lay::kHRegion;
+                                const int cs = sidx & 63;
+                                *reinterpret_cast<__nv_bfloat16 *>(
+                                    hb + sw128_offset(p, cs >> 3) + (cs & 7) * 2) =
+                                    __float2bfloat16_rn(v);
+                            }
+                            r[j] = __float_as_uint(v * decay);
+                        }
+                        if (ti.do_state)
+                            tmem_st16(acc + c0, r);
+                    }
+                }
+                if (ti.do_state)
+                    tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bar_h);
+
+                // ---- X_hat = dt exp2(g_L - g) x (hi / lo) for the state jump
+                if (ti.do_state) {
+                    if (!mbar_wait(&bar_y1, par)) {  // X_hat may overwrite the scores
+                        ok = false;
+                        break;
+                    }
+                    const float w = i < n ? dti * exp2f(gL - gi) : 0.f;
+#pragma unroll
+                    for (int r = 0; r < Lay::kPReg; ++r) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint32_t off = r * kRegion + sw128_offset(i, c);
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
+                            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float a = bf_lo(vv[q]) * w, bb = bf_hi(vv[q]) * w;
+                                hi[q] = pack_bf16x2(a, bb);
+                                lo[q] = pack_bf16x2(a - bf_lo(hi[q]), bb - bf_hi(hi[q]));
+                            }
+                            *reinterpret_cast<uint4 *>(s_xh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *reinterpret_cast<uint4 *>(s_xh + Lay::kX + off) =
+                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&bar_xh);
+                }
+
+                // ---- epilogue: y = Y1 + exp2(g_i) Y2 + D x
+                if (!mbar_wait(&bar_y2, par)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float eg = exp2f(gi);
+                __nv_bfloat16 *yrow = prm.y + ((b * g.L + tau + i) * g.H + h) * g.P;
+#pragma unroll 1
+                for (int c0 = 0; c0 < P; c0 += 16) {
+                    uint32_t r1[16], r2[16];
+                    tmem_ld16(lane + Lay::t_y1 + c0, r1);
+                    tmem_ld16(lane + Lay::t_y2 + c0, r2);
+                    tmem_ld_wait();
+                    // x row i, headdim c0..c0+15: two 16-byte chunks of the swizzled tile
+                    const uint8_t *xr = sx + (c0 >> 6) * kRegion;
+                    const int cc = (c0 & 63) >> 3;
+                    const uint4 xa = *reinterpret_cast<const uint4 *>(xr + sw128_offset(i, cc));
+                    const uint4 xb = *reinterpret_cast<const uint4 *>(xr + sw128_offset(i, cc + 1));
+                    const uint32_t xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float a = __uint_as_float(r1[2 * q]) +
+                                        eg * __uint_as_float(r2[2 * q]) + Dh * bf_lo(xv[q]);
+                        const float bb = __uint_as_float(r1[2 * q + 1]) +
+                                         eg * __uint_as_float(r2[2 * q + 1]) + Dh * bf_hi(xv[q]);
+                        o[q] = pack_bf16x2(a, bb);
+                    }
+                    if (i < n) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + c0);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bar_empty[s]);
+
+                // ---- the state jump must land before the next tile reads h
+                if (ti.do_state) {
+                    if (!mbar_wait(&bar_ds, (uint32_t)(n_state & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    ++n_state;
+                    if (ti.last && MODE == kModeFused && prm.final_state) {
+#pragma unroll 1
+                        for (int mb = 0; mb < Lay::kSBlk; ++mb) {
+                            const int sidx = mb * 128 + i;
+#pragma unroll 1
+                            for (int c0 = 0; c0 < P; c0 += 16) {
+                                uint32_t r[16];
+                                tmem_ld16(lane + Lay::t_st + mb * P + c0, r);
+                                tmem_ld_wait();
+                                if (sidx < S) {
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j)
+                                        prm.final_state[(bh * g.P + c0 + j) * g.S + sidx] =
+                                            __uint_as_float(r[j]);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (!ok)
+            atomicOr(prm.status, 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
+int sm_count()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0)
+            n = 1;
+    }
+    return n;
+}
+
+template <int P, int S, int STAGES, int MODE>
+cudaError_t launch_cfg(const CUtensorMap &tx, const CUtensorMap &tb, const CUtensorMap &tcm,
+                       const Params &prm, cudaStream_t st)
+{
+    using Lay = CoLayout<P, S, STAGES>;
+    const size_t smem = Lay::bytes + 1024;
+    auto k = chunk_tc_kernel<P, S, STAGES, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t grid = min64(prm.n_items, (int64_t)sm_count());
+    k<<<(unsigned)grid, kThreads, smem, st>>>(tx, tb, tcm, prm);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtensorMap &tcm,
+                     const Params &prm, cudaStream_t st)
+{
+    const Geom &g = prm.g;
+    if (g.P == 64 && g.S == 64)
+        return launch_cfg<64, 64, 2, MODE>(tx, tb, tcm, prm, st);
+    if (g.P == 64 && g.S == 128)
+        return launch_cfg<64, 128, 2, MODE>(tx, tb, tcm, prm, st);
+    if (g.P == 64 && g.S == 256)
+        return launch_cfg<64, 256, 1, MODE>(tx, tb, tcm, prm, st);
+    if (g.P == 128 && g.S == 64)
+        return launch_cfg<128, 64, 1, MODE>(tx, tb, tcm, prm, st);
+    if (g.P == 128 && g.S == 128)
+        return launch_cfg<128, 128, 1, MODE>(tx, tb, tcm, prm, st);
+    return cudaErrorNotSupported;
+}
+
+cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const float *dtT,
+                const float *Gc, const float *D, const float *h_src, float *states_out,
+                float *final_state, void *y, const Geom &g, cudaStream_t st)
+{
+    if (!chunk_tc_supported(g))
+        return cudaErrorNotSupported;
+    Params prm{};
+    prm.dtT = dtT;
+    prm.Gc = Gc;
+    prm.D = D;
+    prm.h_src = h_src;
+    prm.states_out = states_out;
+    prm.final_state = final_state;
+    prm.y = static_cast<__nv_bfloat16 *>(y);
+    prm.g = g;
+    prm.n_tiles = (g.L + kTile - 1) / kTile;
+    prm.tiles_per_chunk = g.T / kTile;
+    prm.n_items = mode == kModeOut ? g.B * g.nc * g.H : g.B * g.H;
+    prm.status = device_status_word();
+    if (!prm.status)
+        return cudaErrorUnknown;
+    CUtensorMap tx, tb, tcm;
+    if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g) ||
+        !make_tmap_tokens_groups(&tcm, Cm, g))
+        return cudaErrorInvalidValue;
+    return mode == kModeOut ? dispatch<kModeOut>(tx, tb, tcm, prm, st)
+                            : dispatch<kModeFused>(tx, tb, tcm, prm, st);
+}
+
+}  // namespace
+
+bool chunk_tc_supported(const Geom &g)
+{
+    const bool shape = (g.P == 64 && (g.S == 64 || g.S == 128 || g.S == 256)) ||
+                       (g.P == 128 && (g.S == 64 || g.S == 128));
+    return shape && g.T % kTile == 0 && g.L > 0 && g.L < (1LL << 31) && g.H <= 65535 &&
+           g.G <= 65535 && g.B <= 65535;
+}
+
+cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                                const float *Gc, const float *states, const float *D, void *y,
+                                const Geom &g, cudaStream_t st)
+{
+    return run(kModeOut, x, Bm, Cm, dtT, Gc, D, states, nullptr, nullptr, y, g, st);
+}
+
+cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                            const float *Gc, const float *D, const float *init, float *states,
+                            float *final_state, void *y, const Geom &g, cudaStream_t st)
+{
+    return run(kModeFused, x, Bm, Cm, dtT, Gc, D, init, states, final_state, y, g, st);
+}
+
+}  // namespace ssd

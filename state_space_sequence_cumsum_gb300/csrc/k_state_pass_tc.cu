@@ -1,0 +1,301 @@
+// Stage 2 on tensor cores: the chunk-to-chunk state pass for bf16 inputs.
+//
+// "Accelerating Mamba-2 forward-pass kernels with CUDA Tile (cuTile)",
+// section "Kernel 2: fwd_pass_state": per (batch, head) the state h [P, S] is
+// carried serially across chunks; at every chunk start it is stored, then
+//     h <- exp2(G_last) h + X^T (B * dt * exp2(G_last - G))
+// as one tensor-core contraction over the chunk's tokens.
+//
+// GB300 mapping
+//   * CTA = (128-wide dstate slice sigma, batch*head).  The state slice
+//     h^T [128 s, P] is the tcgen05 accumulator itself and stays in TMEM for
+//     the whole sequence (lane = s, column = p); each step scales it by
+//     exp2(G_last) in place and the MMA accumulates the jump onto it.
+//   * Tokens are walked in 128-token tiles (the MMA K extent).  For
+//     chunk_size 256 a chunk is two tiles; the decay of the first tile is
+//     G at its last token, of the second G_last - G at the first tile's last
+//     token, so the product of the two steps is the chunk's exp2(G_last).
+//   * x [128 t, P] and B [128 t, 128 s] tiles arrive by TMA (128-byte
+//     swizzle) into a 3-stage ring; both are token-major, so the contraction
+//     over tokens uses MN-major operands: A = B^T (M = s), B = X_hat (N = p).
+//   * The pages scale B by dt * exp2(G_last - G) (b_dt_d); here the same
+//     per-token weight w_t is applied to x instead (X_hat = w * X, P < S so
+//     fewer elements), written back to shared memory in the swizzled layout.
+//     w_t <= dt_t because G is non-increasing, so nothing can overflow.
+//   * X_hat is split into two bf16 operands, hi = bf16(w x) and
+//     lo = bf16(w x - hi), and both are contracted (two MMA passes): the jump
+//     then carries ~16 mantissa bits instead of bf16's 8, so the carried
+//     state does not accumulate bf16 rounding of the weighted inputs.
+//   * Roles: warps 0-3 (one thread per token row / state row) build X_hat,
+//     store chunk states and rescale the accumulator; one thread of warp 4
+//     issues TMA loads and MMAs.  Every mbarrier wait is bounded; a timeout
+//     sets the kernel status word and the CTA leaves its loop.
+#include "common.cuh"
+#include "ssd_internal.h"
+#include "tc05.cuh"
+
+namespace ssd {
+namespace {
+using namespace tc;
+
+constexpr int kTile = 128;
+constexpr int kThreads = 160;
+constexpr uint32_t kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region
+
+template <int P>
+struct SpLayout {
+    static constexpr int kStages = P <= 64 ? 3 : 2;
+    static constexpr int kXRegions = P / 64;
+    static constexpr uint32_t kX = kXRegions * kRegion;
+    static constexpr uint32_t kB = 2 * kRegion;
+    static constexpr uint32_t kStage = kX + kB;
+    static constexpr uint32_t off_xh = kStages * kStage;  // X_hat hi, then lo
+    static constexpr uint32_t bytes = off_xh + 2 * kX;
+    static constexpr uint32_t kTmemCols = P < 32 ? 32 : P;
+    static_assert(bytes + 1024 + 256 <= 232448, "shared memory budget");
+};
+
+// (w * a pair of bf16) as hi = bf16(value) and lo = bf16(value - hi), packed.
+__device__ __forceinline__ void split_scaled(uint32_t v, float w, uint32_t &hi, uint32_t &lo)
+{
+    const float a = __uint_as_float(v << 16) * w;
+    const float b = __uint_as_float(v & 0xffff0000u) * w;
+    hi = pack_bf16x2(a, b);
+    const float ah = __uint_as_float(hi << 16), bh = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16x2(a - ah, b - bh);
+}
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_t *bar, int c0,
+                                            int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+template <int P>
+__global__ void __launch_bounds__(kThreads, 1)
+state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ dtT,
+                     const float *__restrict__ Gc, const float *__restrict__ init,
+                     float *__restrict__ states, float *__restrict__ final_state, Geom g,
+                     unsigned int *status)
+{
+    using Lay = SpLayout<P>;
+    constexpr int kStages = Lay::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_ready, bar_mma;
+    __shared__ uint32_t tmem_slot;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int sigma = blockIdx.x;
+    const int64_t bh = blockIdx.y, b = bh / g.H, h = bh % g.H, grp = h / g.hpg;
+    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 128);
+        }
+        mbar_init(&bar_ready, 128);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, Lay::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (tid == 128) {
+        // ---------------- TMA producer + MMA issuer (one thread)
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_b);
+        auto issue = [&](int64_t i) {
+            const int s = (int)(i % kStages);
+            uint8_t *stage = smem + s * Lay::kStage;
+            mbar_arrive_expect_tx(&bar_full[s], Lay::kStage);
+            const int tok = (int)(i * kTile);
+            for (int r = 0; r < Lay::kXRegions; ++r)
+                tma_load_4d(stage + r * kRegion, &tm_x, &bar_full[s], r * 64, (int)h, tok, (int)b);
+            for (int r = 0; r < 2; ++r)
+                tma_load_4d(stage + Lay::kX + r * kRegion, &tm_b, &bar_full[s],
+                            sigma * 128 + r * 64, (int)grp, tok, (int)b);
+        };
+        for (int64_t i = 0; i < kStages && i < n_tiles; ++i)
+            issue(i);
+        const uint32_t idesc = idesc_bf16(128, P, true, true);
+        const uint32_t xh = smem_u32(smem + Lay::off_xh);
+        for (int64_t i = 0; i < n_tiles; ++i) {
+            const int s = (int)(i % kStages);
+            if (!mbar_wait(&bar_ready, (uint32_t)(i & 1))) {
+                atomicOr(status, 1u);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + s * Lay::kStage + Lay::kX);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)  // X_hat hi, then lo
+#pragma unroll
+                for (int ks = 0; ks < kTile / 16; ++ks)
+                    mma_ss(tmem, smem_desc(a0 + ks * 2048, kRegion, 1024),
+                           smem_desc(xh + part * Lay::kX + ks * 2048, kRegion, 1024), idesc, 1u);
+            mma_commit(&bar_mma);
+            if (i + kStages < n_tiles) {
+                const uint32_t par = (uint32_t)((i / kStages) & 1);
+                if (!mbar_wait(&bar_empty[s], par) || !mbar_wait(&bar_mma, (uint32_t)(i & 1))) {
+                    atomicOr(status, 1u);
+                    break;
+                }
+                issue(i + kStages);
+            }
+        }
+    } else if (tid < 128) {
+        // ---------------- compute threads: token row `tid`, state row s = sigma*128 + tid
+        const int row = tid;
+        const int64_t s_idx = (int64_t)sigma * 128 + row;
+        const bool s_ok = s_idx < g.S;
+        const uint32_t lane_base = tmem_at(tmem, (uint32_t)(warp * 32), 0);
+#pragma unroll
+        for (int c0 = 0; c0 < P; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                r[j] = __float_as_uint((init && s_ok) ? init[(bh * g.P + c0 + j) * g.S + s_idx]
+                                                      : 0.f);
+            tmem_st16(lane_base + c0, r);
+        }
+        tmem_st_wait();
+
+        const float *grow = Gc + bh * g.L;
+        const float *drow = dtT + bh * g.L;
+        uint8_t *sxh = smem + Lay::off_xh;
+        for (int64_t i = 0; i < n_tiles; ++i) {
+            const int s = (int)(i % kStages);
+            const int64_t tau = i * kTile;
+            const int n = (int)min64(kTile, g.L - tau);
+            // tile-local log2 decay: G restarts at chunk starts, so a tile in
+            // the middle of a chunk subtracts G at the token before it
+            const float base = (tau % g.T == 0) ? 0.f : grow[tau - 1];
+            const float gL = grow[tau + n - 1] - base;
+            const float w = row < n ? drow[tau + row] * exp2f(gL - (grow[tau + row] - base)) : 0.f;
+            const float decay = exp2f(gL);
+
+            if (!mbar_wait(&bar_full[s], (uint32_t)((i / kStages) & 1))) {
+                atomicOr(status, 1u);
+                break;
+            }
+            const uint8_t *sx = smem + s * Lay::kStage;
+#pragma unroll
+            for (int r = 0; r < Lay::kXRegions; ++r) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t off = r * kRegion + sw128_offset(row, c);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
+                    uint4 hi, lo;
+                    split_scaled(v.x, w, hi.x, lo.x);
+                    split_scaled(v.y, w, hi.y, lo.y);
+                    split_scaled(v.z, w, hi.z, lo.z);
+                    split_scaled(v.w, w, hi.w, lo.w);
+                    *reinterpret_cast<uint4 *>(sxh + off) = hi;
+                    *reinterpret_cast<uint4 *>(sxh + Lay::kX + off) = lo;
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bar_empty[s]);
+
+            // chunk start: store h (the state before this chunk), then decay it
+            const bool emit = states && s_ok && (tau % g.T == 0);
+            float *dst = emit ? states + ((bh * g.nc + tau / g.T) * g.P) * g.S + s_idx : nullptr;
+#pragma unroll
+            for (int c0 = 0; c0 < P; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + c0, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float v = __uint_as_float(r[j]);
+                    if (emit)
+                        dst[(int64_t)(c0 + j) * g.S] = v;
+                    r[j] = __float_as_uint(v * decay);
+                }
+                tmem_st16(lane_base + c0, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_ready);
+            if (!mbar_wait(&bar_mma, (uint32_t)(i & 1))) {
+                atomicOr(status, 1u);
+                break;
+            }
+            tc_fence_after();
+        }
+        if (final_state && s_ok) {
+#pragma unroll
+            for (int c0 = 0; c0 < P; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(lane_base + c0, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    final_state[(bh * g.P + c0 + j) * g.S + s_idx] = __uint_as_float(r[j]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
+template <int P>
+cudaError_t launch_p(const CUtensorMap &tx, const CUtensorMap &tb, const float *dtT,
+                     const float *Gc, const float *init, float *states, float *final_state,
+                     const Geom &g, unsigned int *status, cudaStream_t st)
+{
+    const size_t smem = SpLayout<P>::bytes + 1024;
+    auto k = state_pass_tc_kernel<P>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    dim3 grid((unsigned)((g.S + 127) / 128), (unsigned)(g.B * g.H));
+    k<<<grid, kThreads, smem, st>>>(tx, tb, dtT, Gc, init, states, final_state, g, status);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool state_pass_tc_supported(const Geom &g)
+{
+    return (g.P == 64 || g.P == 128) && g.S % 64 == 0 && g.T % kTile == 0 && g.L > 0 &&
+           g.H <= 65535 && g.G <= 65535 && g.L < (1LL << 31) && g.B * g.H <= 65535;
+}
+
+cudaError_t launch_state_pass_tc(const void *x, const void *Bm, const float *dtT,
+                                 const float *Gc, const float *init, float *states,
+                                 float *final_state, const Geom &g, cudaStream_t st)
+{
+    if (!state_pass_tc_supported(g))
+        return cudaErrorNotSupported;
+    unsigned int *status = device_status_word();
+    if (!status)
+        return cudaErrorUnknown;
+    CUtensorMap tx, tb;
+    if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g))
+        return cudaErrorInvalidValue;
+    if (g.P == 64)
+        return launch_p<64>(tx, tb, dtT, Gc, init, states, final_state, g, status, st);
+    return launch_p<128>(tx, tb, dtT, Gc, init, states, final_state, g, status, st);
+}
+
+}  // namespace ssd

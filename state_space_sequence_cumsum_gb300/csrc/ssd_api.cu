@@ -2,6 +2,8 @@
 // stage orchestration and the kernel status word.  See include/ssd.h for the
 // contract of every entry point.
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -97,13 +99,48 @@ ssd_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Stage 3 dispatch: tcgen05 kernel for bf16 shapes it serves, else CUDA cores.
+cudaError_t run_chunk_out(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                          const float *Gc, const float *states, const float *D, void *y,
+                          const Geom &g, bool bf16, cudaStream_t st)
+{
+    if (bf16 && chunk_tc_supported(g))
+        return launch_chunk_out_tc(x, Bm, Cm, dtT, Gc, states, D, y, g, st);
+    return launch_chunk_out_simt(x, Bm, Cm, dtT, Gc, states, D, y, g, bf16, st);
+}
+
+// ssd_fwd's choice of kernels.  SSD_FWD_PATH=staged|fused overrides the
+// default for the tensor-core shapes (a debugging / measurement switch).
+ssd_path_t choose_path(const Geom &g, ssd_dtype_t t, bool want_states)
+{
+    (void)want_states;
+    if (t != SSD_BF16 || !chunk_tc_supported(g))
+        return (t == SSD_BF16 && state_pass_tc_supported(g)) ? SSD_PATH_STAGED_TENSOR_CORES
+                                                             : SSD_PATH_STAGED_CUDA_CORES;
+    const char *env = getenv("SSD_FWD_PATH");
+    if (env && strcmp(env, "staged") == 0)
+        return SSD_PATH_STAGED_TENSOR_CORES;
+    return SSD_PATH_FUSED_TENSOR_CORES;
+}
+
+// Stage 2 dispatch: tcgen05 kernel for bf16 shapes it serves, else CUDA cores.
+cudaError_t run_state_pass(const void *x, const void *Bm, const float *dtT, const float *Gc,
+                           const float *init, float *states, float *final_state, const Geom &g,
+                           bool bf16, cudaStream_t st)
+{
+    if (bf16 && state_pass_tc_supported(g))
+        return launch_state_pass_tc(x, Bm, dtT, Gc, init, states, final_state, g, st);
+    return launch_state_pass_simt(x, Bm, dtT, Gc, init, states, final_state, g, bf16, st);
+}
+
 int choose_chunk_size(const Geom &g, ssd_dtype_t t)
 {
-    (void)t;
-    // Longer chunks amortise the serial carry; short sequences do not need them.
-    if (g.L <= 64)
-        return 64;
-    return 128;
+    // bf16: the tensor-core kernels walk 128-token tiles; 128 keeps the chunk
+    // states (when requested) as fine as the tiles.  f32: short chunks keep
+    // the CUDA-core score tile small.
+    if (t == SSD_BF16)
+        return 128;
+    return g.L <= 64 ? 64 : 128;
 }
 
 struct Workspace {
@@ -193,8 +230,8 @@ ssd_status_t ssd_state_pass(const void *x, const void *Bm, const float *dt_t, co
                                                  cudaMemcpyDeviceToDevice, st)
                                : cudaMemsetAsync(final_state, 0, bytes, st));
     }
-    return cuda_status(launch_state_pass_simt(x, Bm, dt_t, G_cum, init_state, chunk_states,
-                                              final_state, g, dtype == SSD_BF16, st));
+    return cuda_status(run_state_pass(x, Bm, dt_t, G_cum, init_state, chunk_states, final_state,
+                                      g, dtype == SSD_BF16, st));
 }
 
 ssd_status_t ssd_chunk_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
@@ -216,8 +253,50 @@ ssd_status_t ssd_chunk_out(const void *x, const void *Bm, const void *Cm, const 
     SSD_TRY(need(y, ne));
     if (!ne)
         return SSD_OK;
-    return cuda_status(launch_chunk_out_simt(x, Bm, Cm, dt_t, G_cum, chunk_states, D, y, g,
-                                             dtype == SSD_BF16, (cudaStream_t)stream));
+    return cuda_status(run_chunk_out(x, Bm, Cm, dt_t, G_cum, chunk_states, D, y, g,
+                                     dtype == SSD_BF16, (cudaStream_t)stream));
+}
+
+ssd_status_t ssd_state_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
+                           const float *G_cum, const float *D, const float *init_state, void *y,
+                           float *final_state, float *chunk_states, ssd_dims_t dims,
+                           ssd_dtype_t dtype, int chunk_size, void *stream)
+{
+    Geom g;
+    SSD_TRY(make_geom(dims, chunk_size, false, &g));
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return SSD_ERR_INVALID_ARG;
+    const bool ne = g.L > 0;
+    SSD_TRY(need(x, ne));
+    SSD_TRY(need(Bm, ne));
+    SSD_TRY(need(Cm, ne));
+    SSD_TRY(need(dt_t, ne));
+    SSD_TRY(need(G_cum, ne));
+    SSD_TRY(need(D, true));
+    SSD_TRY(need(y, ne));
+    SSD_TRY(opt(init_state));
+    SSD_TRY(opt(final_state));
+    SSD_TRY(opt(chunk_states));
+    if (!ne)
+        return ssd_state_pass(x, Bm, dt_t, G_cum, init_state, chunk_states, final_state, dims,
+                              dtype, chunk_size, stream);
+    if (dtype != SSD_BF16 || !chunk_tc_supported(g))
+        return SSD_ERR_UNSUPPORTED;
+    return cuda_status(launch_fused_tc(x, Bm, Cm, dt_t, G_cum, D, init_state, chunk_states,
+                                       final_state, y, g, (cudaStream_t)stream));
+}
+
+ssd_path_t ssd_fwd_path(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, int want_chunk_states)
+{
+    Geom g;
+    if (make_geom(dims, chunk_size, true, &g) != SSD_OK ||
+        (dtype != SSD_BF16 && dtype != SSD_F32))
+        return SSD_PATH_INVALID;
+    if (g.T == 0) {
+        g.T = choose_chunk_size(g, dtype);
+        g.nc = (g.L + g.T - 1) / g.T;
+    }
+    return choose_path(g, dtype, want_chunk_states != 0);
 }
 
 int ssd_fwd_chosen_chunk_size(ssd_dims_t dims, ssd_dtype_t dtype)
@@ -240,7 +319,8 @@ size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size
         g.T = choose_chunk_size(g, dtype);
         g.nc = (g.L + g.T - 1) / g.T;
     }
-    const size_t b = layout(g, want_chunk_states != 0, nullptr).bytes;
+    const bool fused = choose_path(g, dtype, want_chunk_states != 0) == SSD_PATH_FUSED_TENSOR_CORES;
+    const size_t b = layout(g, want_chunk_states != 0 || fused, nullptr).bytes;
     return b ? b : 256;
 }
 
@@ -274,19 +354,22 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
         return ssd_state_pass(x, Bm, nullptr, nullptr, init_state, chunk_states, final_state,
                               dims, dtype, g.T, stream);
 
-    const Workspace need_ws = layout(g, chunk_states != nullptr, nullptr);
+    const bool fused = choose_path(g, dtype, chunk_states != nullptr) == SSD_PATH_FUSED_TENSOR_CORES;
+    const Workspace need_ws = layout(g, chunk_states != nullptr || fused, nullptr);
     if (!workspace || workspace_bytes < need_ws.bytes ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return SSD_ERR_WORKSPACE;
-    const Workspace w = layout(g, chunk_states != nullptr, static_cast<char *>(workspace));
+    const Workspace w = layout(g, chunk_states != nullptr || fused, static_cast<char *>(workspace));
     float *states = chunk_states ? chunk_states : w.states;
     const bool bf16 = dtype == SSD_BF16;
 
     SSD_TRY(cuda_status(launch_chunk_cumsum(dt, A, w.Gc, w.dtT, g, st)));
+    if (fused)
+        return cuda_status(launch_fused_tc(x, Bm, Cm, w.dtT, w.Gc, D, init_state, chunk_states,
+                                           final_state, y, g, st));
     SSD_TRY(cuda_status(
-        launch_state_pass_simt(x, Bm, w.dtT, w.Gc, init_state, states, final_state, g, bf16, st)));
-    return cuda_status(
-        launch_chunk_out_simt(x, Bm, Cm, w.dtT, w.Gc, states, D, y, g, bf16, st));
+        run_state_pass(x, Bm, w.dtT, w.Gc, init_state, states, final_state, g, bf16, st)));
+    return cuda_status(run_chunk_out(x, Bm, Cm, w.dtT, w.Gc, states, D, y, g, bf16, st));
 }
 
 ssd_status_t ssd_stream_status(void *stream)

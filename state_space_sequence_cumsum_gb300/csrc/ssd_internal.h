@@ -2,6 +2,7 @@
 // Not part of the public ABI (include/ssd.h is).
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/ssd.h"
@@ -37,5 +38,27 @@ cudaError_t launch_chunk_out_simt(const void *x, const void *Bm, const void *Cm,
                                   const float *dtT, const float *Gc, const float *states,
                                   const float *D, void *y, const Geom &g, bool bf16,
                                   cudaStream_t st);
+
+// TMA tensor maps (bf16, 128-byte swizzle, zero fill out of bounds).
+bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                    const uint64_t *strides_bytes, const uint32_t *box);
+bool make_tmap_tokens_heads(CUtensorMap *map, const void *base, const Geom &g);
+bool make_tmap_tokens_groups(CUtensorMap *map, const void *base, const Geom &g);
+
+// Tensor-core (tcgen05) state pass; bf16 inputs.  Returns cudaErrorNotSupported
+// for shapes it does not serve (the caller then uses the CUDA-core kernel).
+bool state_pass_tc_supported(const Geom &g);
+cudaError_t launch_state_pass_tc(const void *x, const void *Bm, const float *dtT,
+                                 const float *Gc, const float *init, float *states,
+                                 float *final_state, const Geom &g, cudaStream_t st);
+
+// Tensor-core chunk output (stage 3) and fused single-pass forward (bf16).
+bool chunk_tc_supported(const Geom &g);
+cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                                const float *Gc, const float *states, const float *D, void *y,
+                                const Geom &g, cudaStream_t st);
+cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                            const float *Gc, const float *D, const float *init, float *states,
+                            float *final_state, void *y, const Geom &g, cudaStream_t st);
 
 }  // namespace ssd

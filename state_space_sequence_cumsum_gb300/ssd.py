@@ -14,8 +14,8 @@ import torch
 from . import _lib
 from ._lib import SsdError, check, dims as _dims
 
-__all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_fwd", "ssd_fwd_plan",
-           "ssd_fwd_staged",
+__all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out", "ssd_fwd",
+           "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd_staged",
            "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_stream_status",
            "ssd_status_string", "SsdError", "Workspace"]
 
@@ -175,10 +175,42 @@ def ssd_fwd(x, dt, A, B, C, D, chunk_size=0, initial_state=None, return_final_st
     return y, final_state, chunk_states
 
 
+def ssd_state_out(x, B, C, dt_t, G_cum, D, chunk_size, initial_state=None, y=None,
+                  final_state=True, chunk_states=None, stream=None):
+    """Fused stages 2+3 (tensor-core path).  Returns (y, final_state, chunk_states)."""
+    d = _geom(x, B)
+    nc = (d.seqlen + chunk_size - 1) // chunk_size
+    dev = x.device
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is True:
+        final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate), device=dev,
+                                  dtype=torch.float32)
+    if chunk_states is True:
+        chunk_states = torch.empty((d.batch, d.nheads, nc, d.headdim, d.dstate), device=dev,
+                                   dtype=torch.float32)
+    final_state = final_state if isinstance(final_state, torch.Tensor) else None
+    chunk_states = chunk_states if isinstance(chunk_states, torch.Tensor) else None
+    check(_lib.load().ssd_state_out(_ptr(x), _ptr(B), _ptr(C), _ptr(dt_t), _ptr(G_cum),
+                                    _ptr(_f32(D, "D")), _ptr(_f32(initial_state, "init")), _ptr(y),
+                                    _ptr(final_state), _ptr(chunk_states), d, _dtype_code(x),
+                                    int(chunk_size), _stream(stream)), "ssd_state_out")
+    return y, final_state, chunk_states
+
+
+def ssd_fwd_path(x, B, chunk_size=0, want_states=False) -> str:
+    """Name of the kernel path ssd_fwd takes for these arguments."""
+    d = _geom(x, B)
+    code = _lib.load().ssd_fwd_path(d, _dtype_code(x), int(chunk_size), int(bool(want_states)))
+    return _lib.PATH_NAMES.get(code, "invalid")
+
+
 def ssd_fwd_plan(x, B, chunk_size, want_states=False) -> dict:
     """The C-ABI stage calls ssd_fwd makes for these arguments, in order."""
-    return {"path": "three-stage", "chunk_size": int(chunk_size),
-            "kernels": ["chunk_cumsum", "state_pass", "chunk_out"]}
+    path = ssd_fwd_path(x, B, chunk_size, want_states)
+    kernels = (["chunk_cumsum", "state_out"] if path == "fused-tensor-cores"
+               else ["chunk_cumsum", "state_pass", "chunk_out"])
+    return {"path": path, "chunk_size": int(chunk_size), "kernels": kernels}
 
 
 def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk_states,
@@ -195,7 +227,7 @@ def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk
     dtT = workspace.tensor("dt_t", (b, H, L), torch.float32, dev)
     nc = (L + T - 1) // T
     states = chunk_states
-    if states is None:
+    if states is None and plan["kernels"][1] != "state_out":
         states = workspace.tensor("chunk_states", (b, H, nc, P, Sd), torch.float32, dev)
 
     def mark(i):
@@ -205,6 +237,12 @@ def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk
     mark(0)
     ssd_chunk_cumsum(dt, A, T, G_cum=Gc, dt_t=dtT, stream=s)
     mark(1)
+    if plan["kernels"][1] == "state_out":
+        ssd_state_out(x, B, C, dtT, Gc, D, T, initial_state=initial_state, y=y,
+                      final_state=final_state if final_state is not None else False,
+                      chunk_states=chunk_states, stream=s)
+        mark(2)
+        return y, final_state, chunk_states
     ssd_state_pass(x, B, dtT, Gc, T, init_state=initial_state, chunk_states=states,
                    final_state=final_state if final_state is not None else False, stream=s)
     mark(2)

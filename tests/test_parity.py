@@ -55,6 +55,38 @@ def test_edge_lengths(L):
     check_case(2, L, 4, 64, 128, 1, 64, torch.bfloat16, init="randn", seed=L)
 
 
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 255, 257])
+def test_edge_lengths_tensor_core_tiles(L):
+    check_case(2, L, 4, 64, 128, 1, 128, torch.bfloat16, init="randn", seed=L)
+    check_case(1, L, 2, 64, 128, 1, 256, torch.bfloat16, init="randn", seed=L + 1)
+
+
+@pytest.mark.parametrize("T", [128, 256])
+def test_staged_tensor_core_path_matches_oracle(T, monkeypatch):
+    """SSD_FWD_PATH=staged forces cumsum -> tcgen05 state pass -> tcgen05 chunk out."""
+    monkeypatch.setenv("SSD_FWD_PATH", "staged")
+    inp = case_inputs(2, 3 * T + 5, 4, 64, 128, 2, T, init="randn", seed=31)
+    g = to_gpu(inp)
+    assert ssd.ssd_fwd_path(g["x"], g["B"], T) == "staged-tensor-cores"
+    check_case(2, 3 * T + 5, 4, 64, 128, 2, T, torch.bfloat16, init="randn", seed=31)
+
+
+def test_fused_and_staged_paths_agree(monkeypatch):
+    inp = case_inputs(1, 1000, 8, 64, 128, 1, 256, init="randn", seed=37)
+    g = to_gpu(inp)
+    assert ssd.ssd_fwd_path(g["x"], g["B"], 256) == "fused-tensor-cores"
+    y_f, f_f, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], 256,
+                              initial_state=g["init"])
+    monkeypatch.setenv("SSD_FWD_PATH", "staged")
+    y_s, f_s, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], 256,
+                              initial_state=g["init"])
+    ref = oracle_run(inp, 256)
+    assert_parity(y_f, ref["y"], torch.bfloat16, "fused y")
+    assert_parity(y_s, ref["y"], torch.bfloat16, "staged y")
+    assert_parity(f_f, ref["final_state"], torch.bfloat16, "fused final")
+    assert_parity(f_s, ref["final_state"], torch.bfloat16, "staged final")
+
+
 def test_empty_sequence_copies_init():
     inp = case_inputs(2, 0, 4, 64, 128, 1, 64, init="randn", seed=5)
     y, fin, st = run_fwd(inp, 64)

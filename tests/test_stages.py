@@ -34,7 +34,11 @@ def test_chunk_cumsum(L, H, T):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("B,L,H,P,S,G,T", [(2, 520, 4, 64, 128, 1, 128),
                                            (1, 700, 6, 32, 64, 3, 256),
-                                           (1, 257, 2, 16, 16, 1, 64)])
+                                           (1, 257, 2, 16, 16, 1, 64),
+                                           (1, 300, 2, 128, 192, 1, 256),   # ragged dstate slice
+                                           (2, 1000, 4, 64, 64, 2, 256),    # half-empty slice
+                                           (1, 129, 3, 64, 256, 3, 128),    # tile + 1 token
+                                           (1, 4095, 2, 64, 128, 1, 256)])  # ragged, many tiles
 def test_state_pass(dtype, B, L, H, P, S, G, T):
     inp = case_inputs(B, L, H, P, S, G, T, dtype=dtype, init="randn", seed=L + P)
     g = to_gpu(inp)
@@ -49,7 +53,12 @@ def test_state_pass(dtype, B, L, H, P, S, G, T):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("B,L,H,P,S,G,T", [(2, 520, 4, 64, 128, 1, 128),
                                            (1, 700, 6, 32, 64, 3, 256),
-                                           (1, 100, 2, 128, 256, 2, 64)])
+                                           (1, 100, 2, 128, 256, 2, 64),
+                                           (1, 600, 4, 64, 128, 2, 256),   # two tiles per chunk
+                                           (2, 333, 2, 128, 128, 1, 256),
+                                           (1, 260, 4, 64, 256, 1, 128),
+                                           (1, 390, 2, 64, 64, 2, 256),
+                                           (1, 200, 2, 128, 64, 1, 128)])
 def test_chunk_out_from_oracle_states(dtype, B, L, H, P, S, G, T):
     inp = case_inputs(B, L, H, P, S, G, T, dtype=dtype, init="randn", seed=L + S)
     g = to_gpu(inp)
@@ -68,3 +77,28 @@ def test_state_pass_without_outputs_is_a_noop():
                                  final_state=None)
     assert st is None and fin is None
     assert ssd.ssd_stream_status() == 0
+
+
+@pytest.mark.parametrize("B,L,H,P,S,G,T", [(2, 700, 4, 64, 128, 2, 256),
+                                           (1, 513, 2, 128, 128, 1, 128),
+                                           (1, 300, 4, 64, 256, 4, 128)])
+def test_fused_state_out_with_chunk_states(B, L, H, P, S, G, T):
+    """Fused stages 2+3 through ssd_state_out: y, final and every chunk state."""
+    inp = case_inputs(B, L, H, P, S, G, T, init="randn", seed=L + S)
+    g = to_gpu(inp)
+    Gc, dtT = ssd.ssd_chunk_cumsum(g["dt"], g["A"], T)
+    y, fin, st = ssd.ssd_state_out(g["x"], g["B"], g["C"], dtT, Gc, g["D"], T,
+                                   initial_state=g["init"], chunk_states=True)
+    assert ssd.ssd_stream_status() == 0
+    ref = oracle_run(inp, T, want_states=True)
+    assert_parity(y, ref["y"], torch.bfloat16, "y")
+    assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
+    assert_parity(st, ref["chunk_states"], torch.bfloat16, "chunk_states")
+
+
+def test_state_out_rejects_f32():
+    inp = case_inputs(1, 64, 2, 64, 64, 1, 128, dtype=torch.float32)
+    g = to_gpu(inp)
+    Gc, dtT = ssd.ssd_chunk_cumsum(g["dt"], g["A"], 128)
+    with pytest.raises(ssd.SsdError):
+        ssd.ssd_state_out(g["x"], g["B"], g["C"], dtT, Gc, g["D"], 128)
