@@ -162,6 +162,34 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
                      ssd_dtype_t dtype, int chunk_size, void *workspace, size_t workspace_bytes,
                      void *stream);
 
+/*
+ * ssd_fwd without a workspace argument, for callers that cannot allocate
+ * device memory (code running inside an allocator or memory-pool callback, a
+ * host framework that owns all device allocations, a latency-critical loop
+ * that must not pay for an allocation's implicit synchronisation).  The
+ * pages describe no counterpart; this is a convenience of this library.
+ *
+ * The workspace is a fixed scratch array inside the library: 160 MiB
+ * (167772160 bytes) per device, reserved on a device when the library's code
+ * for this entry point is first loaded there and kept until the process
+ * exits.  A call whose ssd_fwd_workspace_size(...) exceeds it returns
+ * SSD_ERR_UNSUPPORTED before launching anything (roughly: the fused path
+ * needs 8 bytes per batch x head x token; the staged paths also hold the
+ * chunk states when chunk_states is NULL).  Inputs, outputs and their
+ * conventions are exactly those of ssd_fwd, and nothing is allocated.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before capturing
+ * a stream into a CUDA graph.  Every call on a device shares the same array
+ * and it keeps the previous call's contents (no region needs to start at
+ * zero), so calls whose kernels may overlap on the GPU -- concurrent streams,
+ * or several host threads -- race on it: serialize them.
+ */
+ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, const void *Bm,
+                             const void *Cm, const float *D, const float *init_state, void *y,
+                             float *final_state, float *chunk_states, ssd_dims_t dims,
+                             ssd_dtype_t dtype, int chunk_size, void *stream);
+
 /* Chunk size ssd_fwd uses for chunk_size == 0 with these dims and dtype. */
 int ssd_fwd_chosen_chunk_size(ssd_dims_t dims, ssd_dtype_t dtype);
 
