@@ -43,28 +43,29 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;
-constexpr int kThreads = 192;
+constexpr int kComputeThreads = 256;  // two warpgroups
+constexpr int kThreads = kComputeThreads + 64;
 constexpr uint32_t kRegion = 128 * 128;
+// A tile takes the factorized decay when |g_first - g_last| <= kNarrow
+// (log2 units): then exp2(g_i - g_L) <= 2^64 and dt exp2(g_L - g_j) >= dt 2^-64,
+// both comfortably inside the normal f32 / bf16 range.
+constexpr float kNarrow = 64.f;
 
 template <int P, int S, int STAGES>
 struct CoLayout {
-    static constexpr int kSReg = S / 64;       // 64-wide dstate regions of B / C
-    static constexpr int kPReg = P / 64;       // 64-wide headdim regions of x
+    static constexpr int kSReg = S / 64;           // 64-wide dstate regions of B / C
+    static constexpr int kPReg = P / 64;           // 64-wide headdim regions of x
     static constexpr int kSBlk = (S + 127) / 128;  // 128-row blocks of the state
     static constexpr uint32_t kB = kSReg * kRegion;
     static constexpr uint32_t kX = kPReg * kRegion;
-    static constexpr uint32_t kStage = 2 * kB + kX;        // B, C, x
-    static constexpr uint32_t off_scores = STAGES * kStage;  // 2 regions (keys 0-63, 64-127)
-    static constexpr uint32_t kScores = 2 * kRegion;
-    // X_hat (hi, then lo) starts on the scores buffer, which is free once the
-    // scores MMA has completed; what does not fit extends past it
-    static constexpr uint32_t off_xh = off_scores;
-    static constexpr uint32_t off_h = off_scores + (2 * kX > kScores ? 2 * kX : kScores);
-    static constexpr uint32_t kHRegion = P * 128;          // P rows x 128 bytes
+    static constexpr uint32_t kStage = 2 * kB + kX;  // B, C, x
+    static constexpr uint32_t off_xh = STAGES * kStage;  // X_hat hi, then lo
+    static constexpr uint32_t off_h = off_xh + 2 * kX;
+    static constexpr uint32_t kHRegion = P * 128;  // P rows x 128 bytes
     static constexpr uint32_t kH = kSReg * kHRegion;
-    static constexpr uint32_t off_g = off_h + kH;          // g[2][128], dt[2][128] (f32)
-    static constexpr uint32_t bytes = off_g + 4 * 128 * 4;
-    // TMEM columns
+    static constexpr uint32_t off_g = off_h + kH;  // [2 tiles][g 128 | dt 128] f32
+    static constexpr uint32_t bytes = off_g + 2 * 256 * 4;
+    // TMEM columns: CB (f32) is converted in place to the bf16 score operand
     static constexpr uint32_t t_cb = 0, t_y1 = 128, t_y2 = 128 + P, t_st = 128 + 2 * P;
     static constexpr uint32_t cols_used = t_st + kSBlk * P;
     static constexpr uint32_t kTmemCols = cols_used <= 256 ? 256 : 512;
@@ -83,43 +84,53 @@ struct Params {
     __nv_bfloat16 *y;
     Geom g;
     int64_t n_items;
-    int64_t n_tiles;      // tiles per sequence
+    int64_t n_tiles;  // tiles per sequence
     int tiles_per_chunk;
     unsigned int *status;
 };
 
-struct TileInfo {
-    int64_t b, h, tau;
+template <int MODE>
+__device__ __forceinline__ void decode_item(const Params &p, int64_t item, int64_t &b, int64_t &h,
+                                            int64_t &t0, int64_t &t1, int64_t &chunk)
+{
+    if (MODE == kModeOut) {
+        // consecutive items share (b, chunk) so their B/C tiles hit in L2
+        h = item % p.g.H;
+        const int64_t bc = item / p.g.H;
+        chunk = bc % p.g.nc;
+        b = bc / p.g.nc;
+        t0 = chunk * p.tiles_per_chunk;
+        t1 = min64(t0 + p.tiles_per_chunk, p.n_tiles);
+    } else {
+        h = item % p.g.H;
+        b = item / p.g.H;
+        t0 = 0;
+        t1 = p.n_tiles;
+        chunk = 0;
+    }
+}
+
+// Per-tile scalars every role derives identically from G.
+struct TileScalars {
+    float base, g0, gL;
     int n;
-    bool first, do_state, last;
-    int64_t item_chunk;  // OUT mode: chunk of the item
+    bool narrow;
 };
 
-template <int MODE>
-struct Items {
-    const Params &p;
-    __device__ Items(const Params &pp) : p(pp) {}
-    // decode work item -> (b, h, tile range)
-    __device__ void decode(int64_t item, int64_t &b, int64_t &h, int64_t &t0, int64_t &t1,
-                           int64_t &chunk) const
-    {
-        if (MODE == kModeOut) {
-            // consecutive items share (b, chunk) so their B/C tiles hit in L2
-            h = item % p.g.H;
-            const int64_t bc = item / p.g.H;
-            chunk = bc % p.g.nc;
-            b = bc / p.g.nc;
-            t0 = chunk * p.tiles_per_chunk;
-            t1 = min64(t0 + p.tiles_per_chunk, p.n_tiles);
-        } else {
-            h = item % p.g.H;
-            b = item / p.g.H;
-            t0 = 0;
-            t1 = p.n_tiles;
-            chunk = 0;
-        }
-    }
-};
+__device__ __forceinline__ TileScalars tile_scalars(const float *grow, int64_t tau, int64_t L,
+                                                    int T)
+{
+    TileScalars t;
+    t.n = (int)min64(kTile, L - tau);
+    // G restarts at chunk starts; a tile inside a chunk is relative to the
+    // token before it
+    t.base = (tau % T == 0) ? 0.f : grow[tau - 1];
+    t.g0 = grow[tau] - t.base;
+    t.gL = grow[tau + t.n - 1] - t.base;
+    const float range = t.g0 - t.gL;
+    t.narrow = range <= kNarrow && range >= -kNarrow;
+    return t;
+}
 
 __device__ __forceinline__ void tma4(void *dst, const void *tmap, uint64_t *bar, int c0, int c1,
                                      int c2, int c3)
@@ -131,8 +142,8 @@ __device__ __forceinline__ void tma4(void *dst, const void *tmap, uint64_t *bar,
         : "memory");
 }
 
-// K-major operand (rows x K, 64 K-elements per 128-byte row, regions of
-// `rows` rows per 64 K): descriptor for the 16-wide K step ks.
+// K-major operand (rows x K, 64 K-elements per 128-byte row, one region per
+// 64 K): descriptor for the 16-wide K step ks.
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, uint32_t region_bytes, int ks)
 {
     return smem_desc(base + (ks >> 2) * region_bytes + (ks & 3) * 32, 16, 1024);
@@ -156,26 +167,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES];
-    __shared__ uint64_t bar_cb, bar_scores, bar_y1, bar_h, bar_y2, bar_xh, bar_ds, bar_g;
+    __shared__ uint64_t bar_cb, bar_cbread, bar_scores, bar_xh, bar_y1, bar_h, bar_y2, bar_ds,
+        bar_g;
     __shared__ uint32_t tmem_slot;
 
     const Geom &g = prm.g;
-    const Items<MODE> items(prm);
     const int tid = threadIdx.x, warp = tid >> 5;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1 + 128);
+            mbar_init(&bar_empty[s], 1 + kComputeThreads);
         }
         mbar_init(&bar_cb, 1);
-        mbar_init(&bar_scores, 128);
+        mbar_init(&bar_cbread, kComputeThreads);
+        mbar_init(&bar_scores, kComputeThreads);
+        mbar_init(&bar_xh, kComputeThreads);
         mbar_init(&bar_y1, 1);
-        mbar_init(&bar_h, 128);
+        mbar_init(&bar_h, kComputeThreads);
         mbar_init(&bar_y2, 1);
-        mbar_init(&bar_xh, 128);
         mbar_init(&bar_ds, 1);
-        mbar_init(&bar_g, 128);
+        mbar_init(&bar_g, kComputeThreads);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -186,24 +198,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    const bool want_final = MODE == kModeFused && prm.final_state != nullptr;
 
-    // Every role walks the same (item, tile) sequence.
-    auto tile_at = [&](int64_t item, int64_t t, int64_t t0, int64_t t1, int64_t b, int64_t h,
-                       int64_t chunk) {
-        TileInfo ti;
-        ti.b = b;
-        ti.h = h;
-        ti.tau = t * kTile;
-        ti.n = (int)min64(kTile, g.L - ti.tau);
-        ti.first = t == t0;
-        ti.last = t + 1 == t1;
-        ti.do_state = !ti.last || (MODE == kModeFused && prm.final_state != nullptr);
-        ti.item_chunk = chunk;
-        (void)item;
-        return ti;
-    };
-
-    if (warp == 4) {
+    if (warp == 8) {
         // ---------------- TMA producer
         if ((tid & 31) == 0) {
             prefetch_tmap(&tm_x);
@@ -213,7 +210,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             bool ok = true;
             for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
                 int64_t b, h, t0, t1, chunk;
-                items.decode(item, b, h, t0, t1, chunk);
+                decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
                 const int64_t grp = h / g.hpg;
                 for (int64_t t = t0; t < t1; ++t, ++it) {
                     const int s = (int)(it % STAGES);
@@ -237,23 +234,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ---------------- MMA issuer
         if ((tid & 31) == 0) {
             const uint32_t id_cb = idesc_bf16(128, 128, false, false);
-            const uint32_t id_y1 = idesc_bf16(128, P, false, true);
+            const uint32_t id_y1 = idesc_bf16(128, P, false, true);  // A (scores) from TMEM
             const uint32_t id_y2 = idesc_bf16(128, P, false, false);
             const uint32_t id_ds = idesc_bf16(128, P, true, true);
-            const uint32_t s_scores = smem_u32(smem + Lay::off_scores);
             const uint32_t s_xh = smem_u32(smem + Lay::off_xh);
             const uint32_t s_h = smem_u32(smem + Lay::off_h);
             int64_t it = 0, n_state = 0;
             bool ok = true;
             for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
                 int64_t b, h, t0, t1, chunk;
-                items.decode(item, b, h, t0, t1, chunk);
+                decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
+                const float *grow = prm.Gc + (b * g.H + h) * g.L;
                 for (int64_t t = t0; t < t1; ++t, ++it) {
-                    const TileInfo ti = tile_at(item, t, t0, t1, b, h, chunk);
+                    const TileScalars ts = tile_scalars(grow, t * kTile, g.L, g.T);
+                    const bool last = t + 1 == t1;
+                    const bool do_state = !last || want_final;
                     const int s = (int)(it % STAGES);
                     const uint32_t sb = smem_u32(smem + s * Lay::kStage);
                     const uint32_t sc = sb + Lay::kB;
@@ -263,21 +262,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         ok = false;
                         break;
                     }
+                    // CB reuses the previous tile's score columns: wait for its last MMAs
+                    if (it > 0 && !mbar_wait(&bar_y2, (uint32_t)((it - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < S / 16; ++ks)
                         mma_ss(tmem + Lay::t_cb, desc_k(sc, kRegion, ks), desc_k(sb, kRegion, ks),
                                id_cb, ks > 0);
                     mma_commit(&bar_cb);
-                    if (!mbar_wait(&bar_scores, par)) {
+                    if (!mbar_wait(&bar_scores, par) || !mbar_wait(&bar_xh, par)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t y1b = ts.narrow ? s_xh : sx;  // X_hat or raw x
 #pragma unroll
                     for (int ks = 0; ks < kTile / 16; ++ks)
-                        mma_ss(tmem + Lay::t_y1, desc_k(s_scores, kRegion, ks), desc_mn(sx, ks),
-                               id_y1, ks > 0);
+                        mma_ts(tmem + Lay::t_y1, tmem + Lay::t_cb + ks * 8, desc_mn(y1b, ks), id_y1,
+                               ks > 0);
                     mma_commit(&bar_y1);
                     if (!mbar_wait(&bar_h, par)) {
                         ok = false;
@@ -289,12 +294,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         mma_ss(tmem + Lay::t_y2, desc_k(sc, kRegion, ks),
                                desc_k(s_h, Lay::kHRegion, ks), id_y2, ks > 0);
                     mma_commit(&bar_y2);
-                    if (ti.do_state) {
-                        if (!mbar_wait(&bar_xh, (uint32_t)(n_state & 1))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                    if (do_state) {
 #pragma unroll
                         for (int mb = 0; mb < Lay::kSBlk; ++mb)
 #pragma unroll
@@ -314,108 +314,169 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 atomicOr(prm.status, 1u);
         }
     } else {
-        // ---------------- compute warpgroup: thread i = tile row i = TMEM lane i
-        const int i = tid;
-        const uint32_t lane = tmem_at(tmem, (uint32_t)(warp * 32), 0);
-        float *sg_all = reinterpret_cast<float *>(smem + Lay::off_g);
-        uint8_t *s_scores = smem + Lay::off_scores;
+        // ---------------- two compute warpgroups.  Thread (wg, q, lane) owns
+        // tile row / TMEM lane i = 32 q + lane; warpgroup wg owns half of the
+        // columns of every per-tile step.
+        const int wg = warp >> 2, q = warp & 3;
+        const int i = q * 32 + (tid & 31);
+        const uint32_t lane = tmem_at(tmem, (uint32_t)(q * 32), 0);
+        float *gtab_all = reinterpret_cast<float *>(smem + Lay::off_g);
         uint8_t *s_xh = smem + Lay::off_xh;
         uint8_t *s_h = smem + Lay::off_h;
+        constexpr int kPHalf = P / 2;
         int64_t it = 0, n_state = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
             int64_t b, h, t0, t1, chunk;
-            items.decode(item, b, h, t0, t1, chunk);
+            decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
             const int64_t bh = b * g.H + h;
             const float *grow = prm.Gc + bh * g.L;
             const float *drow = prm.dtT + bh * g.L;
             const float Dh = prm.D[h];
             for (int64_t t = t0; t < t1; ++t, ++it) {
-                const TileInfo ti = tile_at(item, t, t0, t1, b, h, chunk);
+                const int64_t tau = t * kTile;
+                const TileScalars ts = tile_scalars(grow, tau, g.L, g.T);
+                const bool first = t == t0, last = t + 1 == t1;
+                const bool do_state = !last || want_final;
+                const int n = ts.n;
                 const int s = (int)(it % STAGES);
                 const uint8_t *sx = smem + s * Lay::kStage + 2 * Lay::kB;
                 const uint32_t par = (uint32_t)(it & 1);
-                const int64_t tau = ti.tau;
-                const int n = ti.n;
-                const float base = (tau % g.T == 0) ? 0.f : grow[tau - 1];
-                const float gL = grow[tau + n - 1] - base;
-                const float gi = i < n ? grow[tau + i] - base : 0.f;
+                const float gi = i < n ? grow[tau + i] - ts.base : 0.f;
                 const float dti = i < n ? drow[tau + i] : 0.f;
-                // per-tile g / dt table, double-buffered by tile parity; the
-                // bounded mbarrier makes all 128 rows visible before use
-                float *sg = sg_all + (it & 1) * 256;
-                float *sdt = sg + 128;
-                sg[i] = gi;
-                sdt[i] = dti;
+
+                // ---- per-tile g / dt table (double-buffered by tile parity)
+                float *gtab = gtab_all + (it & 1) * 256;
+                if (wg == 0)
+                    gtab[i] = gi;
+                else
+                    gtab[128 + i] = dti;
                 mbar_arrive(&bar_g);
-                if (!mbar_wait(&bar_g, par)) {
+                if (!mbar_wait(&bar_g, par) || !mbar_wait(&bar_full[s], (uint32_t)((it / STAGES) & 1))) {
                     ok = false;
                     break;
                 }
 
-                // ---- scores = CB * exp2(g_i - g_j) * dt_j, causal, bf16 (K-major rows i)
+                // ---- X_hat = dt exp2(g_L - g) x as bf16 hi (+ lo for the state jump)
+                if (ts.narrow || do_state) {
+                    const float w = i < n ? dti * ex2_approx(ts.gL - gi) : 0.f;
+#pragma unroll
+                    for (int r = 0; r < Lay::kPReg; ++r) {
+#pragma unroll
+                        for (int c = wg * 4; c < wg * 4 + 4; ++c) {
+                            const uint32_t off = r * kRegion + sw128_offset(i, c);
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
+                            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float a = bf_lo(vv[e]) * w, bb = bf_hi(vv[e]) * w;
+                                hi[e] = pack_bf16x2(a, bb);
+                                lo[e] = pack_bf16x2(a - bf_lo(hi[e]), bb - bf_hi(hi[e]));
+                            }
+                            *reinterpret_cast<uint4 *>(s_xh + off) =
+                                make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            if (do_state)
+                                *reinterpret_cast<uint4 *>(s_xh + Lay::kX + off) =
+                                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                mbar_arrive(&bar_xh);
+
+                // ---- scores, in place over CB (f32 -> bf16 A operand in TMEM)
                 if (!mbar_wait(&bar_cb, par)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int wmax = warp * 32 + 31;
-#pragma unroll 1
-                for (int j0 = 0; j0 < kTile; j0 += 16) {
+                const int row_max = q * 32 + 31;  // warp-uniform bound for the collective ld/st
+                uint32_t cbv[4][16];
+#pragma unroll
+                for (int gq = 0; gq < 4; ++gq) {
+                    const int j0 = wg * 64 + gq * 16;
+                    if (j0 <= row_max)
+                        tmem_ld16(lane + Lay::t_cb + j0, cbv[gq]);
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&bar_cbread);  // every CB value is in registers before any write
+                if (!mbar_wait(&bar_cbread, par)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int gq = 0; gq < 4; ++gq) {
+                    const int j0 = wg * 64 + gq * 16;
                     uint32_t pk[8];
-                    if (j0 <= wmax) {  // warp-uniform: tcgen05.ld is warp-collective
-                        uint32_t r[16];
-                        tmem_ld16(lane + Lay::t_cb + j0, r);
-                        tmem_ld_wait();
+                    if (j0 <= row_max) {
+                        if (ts.narrow) {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            float v[2];
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int j = j0 + 2 * q + e;
-                                v[e] = (j <= i && j < n)
-                                           ? __uint_as_float(r[2 * q + e]) * exp2f(gi - sg[j]) * sdt[j]
-                                           : 0.f;
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = j0 + 2 * e;
+                                const float a = (j <= i && j < n) ? __uint_as_float(cbv[gq][2 * e]) : 0.f;
+                                const float bb =
+                                    (j + 1 <= i && j + 1 < n) ? __uint_as_float(cbv[gq][2 * e + 1]) : 0.f;
+                                pk[e] = pack_bf16x2(a, bb);
                             }
-                            pk[q] = pack_bf16x2(v[0], v[1]);
+                        } else {
+                            const float4 *g4 = reinterpret_cast<const float4 *>(gtab + j0);
+                            const float4 *d4 = reinterpret_cast<const float4 *>(gtab + 128 + j0);
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                const float4 gg = g4[v4], dd = d4[v4];
+                                const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
+                                const float dj[4] = {dd.x, dd.y, dd.z, dd.w};
+                                float val[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int j = j0 + 4 * v4 + e;
+                                    val[e] = (j <= i && j < n)
+                                                 ? __uint_as_float(cbv[gq][4 * v4 + e]) *
+                                                       ex2_approx(gi - gj[e]) * dj[e]
+                                                 : 0.f;
+                                }
+                                pk[2 * v4] = pack_bf16x2(val[0], val[1]);
+                                pk[2 * v4 + 1] = pack_bf16x2(val[2], val[3]);
+                            }
                         }
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            pk[q] = 0u;
+                        for (int e = 0; e < 8; ++e)
+                            pk[e] = 0u;
                     }
-                    uint8_t *rbase = s_scores + (j0 >> 6) * kRegion;
-                    const int c0 = (j0 & 63) >> 3;
-                    *reinterpret_cast<uint4 *>(rbase + sw128_offset(i, c0)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(rbase + sw128_offset(i, c0 + 1)) =
-                        make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    tmem_st8(lane + Lay::t_cb + j0 / 2, pk);
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bar_scores);
 
-                // ---- H = bf16(h at tile start) into K-major [p][s]; state bookkeeping
-                const float decay = exp2f(gL);
+                // ---- H = bf16(hscale * h) into K-major [p][s]; emit and decay the state
+                const float decay = ex2_approx(ts.gL);
+                const float hscale = ts.narrow ? decay : 1.f;
                 const bool emit = MODE == kModeFused && prm.states_out && (tau % g.T == 0);
-#pragma unroll 1
+#pragma unroll
                 for (int mb = 0; mb < Lay::kSBlk; ++mb) {
                     const int sidx = mb * 128 + i;
                     const bool s_ok = sidx < S;
                     const uint32_t acc = lane + Lay::t_st + mb * P;
                     const float *src = nullptr;
-                    if (ti.first) {
+                    if (first) {
                         if (MODE == kModeOut)
-                            src = prm.h_src + ((bh * g.nc + ti.item_chunk) * g.P) * g.S;
+                            src = prm.h_src + ((bh * g.nc + chunk) * g.P) * g.S;
                         else if (prm.h_src)
                             src = prm.h_src + bh * g.P * g.S;
                     }
                     float *emit_dst =
                         emit ? prm.states_out + ((bh * g.nc + tau / g.T) * g.P) * g.S : nullptr;
-#pragma unroll 1
-                    for (int c0 = 0; c0 < P; c0 += 16) {
+                    uint8_t *hb = s_h + (sidx >> 6) * Lay::kHRegion;
+                    const int cs = sidx & 63;
+#pragma unroll
+                    for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
                         uint32_t r[16];
-                        if (ti.first) {
+                        if (first) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
                                 r[j] = __float_as_uint((src && s_ok) ? src[(int64_t)(c0 + j) * S + sidx]
@@ -427,74 +488,40 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const float v = __uint_as_float(r[j]);
-                            if (emit_dst && s_ok)
-                                emit_dst[(int64_t)(c0 + j) * S + sidx] = v;
                             if (s_ok) {
-                                const int p = c0 + j;
-                                uint8_t *hb = s_h + (sidx >> 6) * Lay::kHRegion;
-                                const int cs = sidx & 63;
+                                if (emit_dst)
+                                    emit_dst[(int64_t)(c0 + j) * S + sidx] = v;
                                 *reinterpret_cast<__nv_bfloat16 *>(
-                                    hb + sw128_offset(p, cs >> 3) + (cs & 7) * 2) =
-                                    __float2bfloat16_rn(v);
+                                    hb + sw128_offset(c0 + j, cs >> 3) + (cs & 7) * 2) =
+                                    __float2bfloat16_rn(v * hscale);
                             }
                             r[j] = __float_as_uint(v * decay);
                         }
-                        if (ti.do_state)
+                        if (do_state)
                             tmem_st16(acc + c0, r);
                     }
                 }
-                if (ti.do_state)
+                if (do_state)
                     tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(&bar_h);
 
-                // ---- X_hat = dt exp2(g_L - g) x (hi / lo) for the state jump
-                if (ti.do_state) {
-                    if (!mbar_wait(&bar_y1, par)) {  // X_hat may overwrite the scores
-                        ok = false;
-                        break;
-                    }
-                    const float w = i < n ? dti * exp2f(gL - gi) : 0.f;
-#pragma unroll
-                    for (int r = 0; r < Lay::kPReg; ++r) {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint32_t off = r * kRegion + sw128_offset(i, c);
-                            const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
-                            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-                            uint32_t hi[4], lo[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float a = bf_lo(vv[q]) * w, bb = bf_hi(vv[q]) * w;
-                                hi[q] = pack_bf16x2(a, bb);
-                                lo[q] = pack_bf16x2(a - bf_lo(hi[q]), bb - bf_hi(hi[q]));
-                            }
-                            *reinterpret_cast<uint4 *>(s_xh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            *reinterpret_cast<uint4 *>(s_xh + Lay::kX + off) =
-                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    mbar_arrive(&bar_xh);
-                }
-
-                // ---- epilogue: y = Y1 + exp2(g_i) Y2 + D x
+                // ---- epilogue: y = r1 Y1 + r2 Y2 + D x
                 if (!mbar_wait(&bar_y2, par)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float eg = exp2f(gi);
+                const float r1 = ts.narrow ? ex2_approx(gi - ts.gL) : 1.f;
+                const float r2 = ts.narrow ? r1 : ex2_approx(gi);
                 __nv_bfloat16 *yrow = prm.y + ((b * g.L + tau + i) * g.H + h) * g.P;
-#pragma unroll 1
-                for (int c0 = 0; c0 < P; c0 += 16) {
-                    uint32_t r1[16], r2[16];
-                    tmem_ld16(lane + Lay::t_y1 + c0, r1);
-                    tmem_ld16(lane + Lay::t_y2 + c0, r2);
+#pragma unroll
+                for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
+                    uint32_t ra[16], rb[16];
+                    tmem_ld16(lane + Lay::t_y1 + c0, ra);
+                    tmem_ld16(lane + Lay::t_y2 + c0, rb);
                     tmem_ld_wait();
-                    // x row i, headdim c0..c0+15: two 16-byte chunks of the swizzled tile
                     const uint8_t *xr = sx + (c0 >> 6) * kRegion;
                     const int cc = (c0 & 63) >> 3;
                     const uint4 xa = *reinterpret_cast<const uint4 *>(xr + sw128_offset(i, cc));
@@ -502,12 +529,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     const uint32_t xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
                     uint32_t o[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float a = __uint_as_float(r1[2 * q]) +
-                                        eg * __uint_as_float(r2[2 * q]) + Dh * bf_lo(xv[q]);
-                        const float bb = __uint_as_float(r1[2 * q + 1]) +
-                                         eg * __uint_as_float(r2[2 * q + 1]) + Dh * bf_hi(xv[q]);
-                        o[q] = pack_bf16x2(a, bb);
+                    for (int e = 0; e < 8; ++e) {
+                        const float a = r1 * __uint_as_float(ra[2 * e]) +
+                                        r2 * __uint_as_float(rb[2 * e]) + Dh * bf_lo(xv[e]);
+                        const float bb = r1 * __uint_as_float(ra[2 * e + 1]) +
+                                         r2 * __uint_as_float(rb[2 * e + 1]) + Dh * bf_hi(xv[e]);
+                        o[e] = pack_bf16x2(a, bb);
                     }
                     if (i < n) {
                         uint4 *dst = reinterpret_cast<uint4 *>(yrow + c0);
@@ -519,19 +546,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 mbar_arrive(&bar_empty[s]);
 
                 // ---- the state jump must land before the next tile reads h
-                if (ti.do_state) {
+                if (do_state) {
                     if (!mbar_wait(&bar_ds, (uint32_t)(n_state & 1))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     ++n_state;
-                    if (ti.last && MODE == kModeFused && prm.final_state) {
-#pragma unroll 1
+                    if (last && want_final) {
+#pragma unroll
                         for (int mb = 0; mb < Lay::kSBlk; ++mb) {
                             const int sidx = mb * 128 + i;
-#pragma unroll 1
-                            for (int c0 = 0; c0 < P; c0 += 16) {
+#pragma unroll
+                            for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
                                 uint32_t r[16];
                                 tmem_ld16(lane + Lay::t_st + mb * P + c0, r);
                                 tmem_ld_wait();
@@ -593,13 +620,13 @@ cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtenso
 {
     const Geom &g = prm.g;
     if (g.P == 64 && g.S == 64)
-        return launch_cfg<64, 64, 2, MODE>(tx, tb, tcm, prm, st);
+        return launch_cfg<64, 64, 3, MODE>(tx, tb, tcm, prm, st);
     if (g.P == 64 && g.S == 128)
         return launch_cfg<64, 128, 2, MODE>(tx, tb, tcm, prm, st);
     if (g.P == 64 && g.S == 256)
         return launch_cfg<64, 256, 1, MODE>(tx, tb, tcm, prm, st);
     if (g.P == 128 && g.S == 64)
-        return launch_cfg<128, 64, 1, MODE>(tx, tb, tcm, prm, st);
+        return launch_cfg<128, 64, 2, MODE>(tx, tb, tcm, prm, st);
     if (g.P == 128 && g.S == 128)
         return launch_cfg<128, 128, 1, MODE>(tx, tb, tcm, prm, st);
     return cudaErrorNotSupported;

@@ -241,6 +241,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -254,6 +262,15 @@ __device__ __forceinline__ void tmem_st_wait() {
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk)
 {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// 2^x with the PTX ex2.approx.ftz.f32 instruction (MUFU); relative error
+// ~2^-22, far below the bf16 rounding of the operands it feeds.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
