@@ -118,14 +118,22 @@ ssd_status_t ssd_chunk_out(const void *x, const void *Bm, const void *Cm, const 
  * sequence once, carrying the state on chip from tile to tile, and writes y,
  * the final state (may be NULL) and, if chunk_states is not NULL, every
  * chunk's start state.  Arithmetic is that of ssd_state_pass followed by
- * ssd_chunk_out.  G_cum and dt_t are stage 1's outputs.  Returns
- * SSD_ERR_UNSUPPORTED for f32 calls and for shapes outside the tensor-core
- * path (see "Supported sizes"); use the two separate stages there.
+ * ssd_chunk_out.  G_cum and dt_t are stage 1's outputs.  Long sequences are
+ * cut into segments processed in parallel; each segment starts from the
+ * state its predecessor leaves in `workspace` (at least
+ * ssd_state_out_workspace_size bytes, 256-byte aligned; contents on entry do
+ * not matter).  Returns SSD_ERR_UNSUPPORTED for f32 calls and for shapes
+ * outside the tensor-core path (see "Supported sizes"); use the two separate
+ * stages there.
  */
 ssd_status_t ssd_state_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
                            const float *G_cum, const float *D, const float *init_state, void *y,
                            float *final_state, float *chunk_states, ssd_dims_t dims,
-                           ssd_dtype_t dtype, int chunk_size, void *stream);
+                           ssd_dtype_t dtype, int chunk_size, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* Workspace bytes ssd_state_out needs (depends on the current device's SM count). */
+size_t ssd_state_out_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size);
 
 /* Which kernels ssd_fwd runs for these arguments (chunk_size 0 = auto). */
 typedef enum {

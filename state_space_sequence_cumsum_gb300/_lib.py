@@ -24,6 +24,7 @@ SSD_F32 = 1
 
 # Every entry point include/ssd.h declares (checked by the tests).
 EXPORTS = ("ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out",
+           "ssd_state_out_workspace_size",
            "ssd_fwd_path", "ssd_fwd_workspace_size", "ssd_fwd", "ssd_fwd_noalloc",
            "ssd_fwd_chosen_chunk_size",
            "ssd_launch_count", "ssd_status_string", "ssd_stream_status")
@@ -67,7 +68,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "ssd_chunk_cumsum": ([fp, fp, fp, fp, D, i32, vp], st),
             "ssd_state_pass": ([vp, vp, fp, fp, fp, fp, fp, D, i32, i32, vp], st),
             "ssd_chunk_out": ([vp, vp, vp, fp, fp, fp, fp, vp, D, i32, i32, vp], st),
-            "ssd_state_out": ([vp, vp, vp, fp, fp, fp, fp, vp, fp, fp, D, i32, i32, vp], st),
+            "ssd_state_out": ([vp, vp, vp, fp, fp, fp, fp, vp, fp, fp, D, i32, i32, vp,
+                               ctypes.c_size_t, vp], st),
+            "ssd_state_out_workspace_size": ([D, i32, i32], ctypes.c_size_t),
             "ssd_fwd_path": ([D, i32, i32, i32], ctypes.c_int),
             "ssd_fwd_workspace_size": ([D, i32, i32, i32], ctypes.c_size_t),
             "ssd_fwd": ([vp, fp, fp, vp, vp, fp, fp, vp, fp, fp, D, i32, i32, vp,

@@ -86,6 +86,13 @@ struct Params {
     int64_t n_items;
     int64_t n_tiles;  // tiles per sequence
     int tiles_per_chunk;
+    // FUSED: each (batch, head) sequence is split into n_seg segments of
+    // seg_tiles tiles; segment k > 0 starts from the state segment k-1 leaves
+    // in seg_state, published by seg_count reaching kComputeThreads.
+    int64_t seg_tiles;
+    int n_seg;
+    float *seg_state;          // [B*H*n_seg][P][S]
+    unsigned int *seg_count;   // [B*H*n_seg], zero at launch
     unsigned int *status;
 };
 
@@ -102,12 +109,23 @@ __device__ __forceinline__ void decode_item(const Params &p, int64_t item, int64
         t0 = chunk * p.tiles_per_chunk;
         t1 = min64(t0 + p.tiles_per_chunk, p.n_tiles);
     } else {
-        h = item % p.g.H;
-        b = item / p.g.H;
-        t0 = 0;
-        t1 = p.n_tiles;
-        chunk = 0;
+        // segment-major: every segment k of every sequence comes before any
+        // segment k+1, so a segment's predecessor is always an earlier item
+        const int64_t nbh = p.g.B * p.g.H;
+        const int64_t seg = item / nbh, bh = item % nbh;
+        h = bh % p.g.H;
+        b = bh / p.g.H;
+        t0 = seg * p.seg_tiles;
+        t1 = min64(t0 + p.seg_tiles, p.n_tiles);
+        chunk = seg;
     }
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Per-tile scalars every role derives identically from G.
@@ -251,8 +269,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const float *grow = prm.Gc + (b * g.H + h) * g.L;
                 for (int64_t t = t0; t < t1; ++t, ++it) {
                     const TileScalars ts = tile_scalars(grow, t * kTile, g.L, g.T);
-                    const bool last = t + 1 == t1;
-                    const bool do_state = !last || want_final;
+                    const bool last_seq = MODE == kModeOut ? t + 1 == t1 : t + 1 == prm.n_tiles;
+                    const bool do_state = !last_seq || want_final;
                     const int s = (int)(it % STAGES);
                     const uint32_t sb = smem_u32(smem + s * Lay::kStage);
                     const uint32_t sc = sb + Lay::kB;
@@ -336,8 +354,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             for (int64_t t = t0; t < t1; ++t, ++it) {
                 const int64_t tau = t * kTile;
                 const TileScalars ts = tile_scalars(grow, tau, g.L, g.T);
-                const bool first = t == t0, last = t + 1 == t1;
-                const bool do_state = !last || want_final;
+                const bool first = t == t0, last_item = t + 1 == t1;
+                const bool last_seq = MODE == kModeOut ? last_item : t + 1 == prm.n_tiles;
+                const bool do_state = !last_seq || want_final;
                 const int n = ts.n;
                 const int s = (int)(it % STAGES);
                 const uint8_t *sx = smem + s * Lay::kStage + 2 * Lay::kB;
@@ -453,6 +472,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 tc_fence_before();
                 mbar_arrive(&bar_scores);
 
+                // ---- a later segment waits until its predecessor published its state
+                if (MODE == kModeFused && first && chunk > 0) {
+                    const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + chunk - 1;
+                    bool ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeThreads;
+                    const uint64_t t_start = globaltimer_ns();
+                    while (!ready) {
+                        if (globaltimer_ns() - t_start > 2000000000ull)
+                            break;
+                        __nanosleep(256);
+                        ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeThreads;
+                    }
+                    if (!ready) {
+                        ok = false;
+                        break;
+                    }
+                }
+
                 // ---- H = bf16(hscale * h) into K-major [p][s]; emit and decay the state
                 const float decay = ex2_approx(ts.gL);
                 const float hscale = ts.narrow ? decay : 1.f;
@@ -466,6 +502,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     if (first) {
                         if (MODE == kModeOut)
                             src = prm.h_src + ((bh * g.nc + chunk) * g.P) * g.S;
+                        else if (chunk > 0)  // later segment: the predecessor's state
+                            src = prm.seg_state + ((bh * prm.n_seg + chunk - 1) * g.P) * g.S;
                         else if (prm.h_src)
                             src = prm.h_src + bh * g.P * g.S;
                     }
@@ -479,8 +517,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         if (first) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                r[j] = __float_as_uint((src && s_ok) ? src[(int64_t)(c0 + j) * S + sidx]
-                                                                     : 0.f);
+                                r[j] = __float_as_uint(
+                                    (src && s_ok) ? __ldcg(src + (int64_t)(c0 + j) * S + sidx) : 0.f);
                         } else {
                             tmem_ld16(acc + c0, r);
                             tmem_ld_wait();
@@ -553,7 +591,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     tc_fence_after();
                     ++n_state;
-                    if (last && want_final) {
+                    if (MODE == kModeFused && last_item && !last_seq) {
+                        // hand the state to the next segment: store, fence, count
+                        float *dst = prm.seg_state + ((bh * prm.n_seg + chunk) * g.P) * g.S;
+#pragma unroll
+                        for (int mb = 0; mb < Lay::kSBlk; ++mb) {
+                            const int sidx = mb * 128 + i;
+#pragma unroll
+                            for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
+                                uint32_t r[16];
+                                tmem_ld16(lane + Lay::t_st + mb * P + c0, r);
+                                tmem_ld_wait();
+                                if (sidx < S) {
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j)
+                                        __stcg(dst + (int64_t)(c0 + j) * S + sidx,
+                                               __uint_as_float(r[j]));
+                                }
+                            }
+                        }
+                        __threadfence();
+                        atomicAdd(prm.seg_count + bh * prm.n_seg + chunk, 1u);
+                    }
+                    if (last_seq && want_final) {
 #pragma unroll
                         for (int mb = 0; mb < Lay::kSBlk; ++mb) {
                             const int sidx = mb * 128 + i;
@@ -632,9 +692,35 @@ cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtenso
     return cudaErrorNotSupported;
 }
 
+// Segmentation of the fused pass: enough (batch, head, segment) items for
+// about eight per SM, so the persistent CTAs end within one item of each
+// other; no segment shorter than two tiles.
+struct SegPlan {
+    int64_t seg_tiles;
+    int n_seg;
+    size_t state_bytes, count_bytes;
+};
+
+SegPlan seg_plan(const Geom &g)
+{
+    SegPlan sp;
+    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+    const int64_t nbh = g.B * g.H;
+    int64_t want = (8LL * sm_count() + nbh - 1) / nbh;
+    want = want < 1 ? 1 : want;
+    if (want > (n_tiles + 1) / 2)
+        want = (n_tiles + 1) / 2 < 1 ? 1 : (n_tiles + 1) / 2;
+    sp.seg_tiles = (n_tiles + want - 1) / want;
+    sp.n_seg = (int)((n_tiles + sp.seg_tiles - 1) / sp.seg_tiles);
+    sp.state_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg * g.P * g.S) * sizeof(float) : 0;
+    sp.count_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg) * sizeof(unsigned int) : 0;
+    return sp;
+}
+
 cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const float *dtT,
                 const float *Gc, const float *D, const float *h_src, float *states_out,
-                float *final_state, void *y, const Geom &g, cudaStream_t st)
+                float *final_state, void *y, const Geom &g, void *scratch, size_t scratch_bytes,
+                cudaStream_t st)
 {
     if (!chunk_tc_supported(g))
         return cudaErrorNotSupported;
@@ -649,7 +735,25 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
     prm.g = g;
     prm.n_tiles = (g.L + kTile - 1) / kTile;
     prm.tiles_per_chunk = g.T / kTile;
-    prm.n_items = mode == kModeOut ? g.B * g.nc * g.H : g.B * g.H;
+    prm.n_items = g.B * g.nc * g.H;
+    prm.seg_tiles = prm.n_tiles;
+    prm.n_seg = 1;
+    if (mode == kModeFused) {
+        const SegPlan sp = seg_plan(g);
+        prm.seg_tiles = sp.seg_tiles;
+        prm.n_seg = sp.n_seg;
+        prm.n_items = g.B * g.H * sp.n_seg;
+        if (sp.n_seg > 1) {
+            const size_t off = (sp.state_bytes + 255) / 256 * 256;
+            if (!scratch || scratch_bytes < off + sp.count_bytes)
+                return cudaErrorInvalidValue;
+            prm.seg_state = static_cast<float *>(scratch);
+            prm.seg_count = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + off);
+            cudaError_t e = cudaMemsetAsync(prm.seg_count, 0, sp.count_bytes, st);
+            if (e != cudaSuccess)
+                return e;
+        }
+    }
     prm.status = device_status_word();
     if (!prm.status)
         return cudaErrorUnknown;
@@ -675,14 +779,24 @@ cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, c
                                 const float *Gc, const float *states, const float *D, void *y,
                                 const Geom &g, cudaStream_t st)
 {
-    return run(kModeOut, x, Bm, Cm, dtT, Gc, D, states, nullptr, nullptr, y, g, st);
+    return run(kModeOut, x, Bm, Cm, dtT, Gc, D, states, nullptr, nullptr, y, g, nullptr, 0, st);
+}
+
+size_t fused_tc_scratch_bytes(const Geom &g)
+{
+    const SegPlan sp = seg_plan(g);
+    if (sp.n_seg <= 1)
+        return 0;
+    return (sp.state_bytes + 255) / 256 * 256 + (sp.count_bytes + 255) / 256 * 256;
 }
 
 cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                             const float *Gc, const float *D, const float *init, float *states,
-                            float *final_state, void *y, const Geom &g, cudaStream_t st)
+                            float *final_state, void *y, const Geom &g, void *scratch,
+                            size_t scratch_bytes, cudaStream_t st)
 {
-    return run(kModeFused, x, Bm, Cm, dtT, Gc, D, init, states, final_state, y, g, st);
+    return run(kModeFused, x, Bm, Cm, dtT, Gc, D, init, states, final_state, y, g, scratch,
+               scratch_bytes, st);
 }
 
 }  // namespace ssd

@@ -145,10 +145,15 @@ int choose_chunk_size(const Geom &g, ssd_dtype_t t)
 
 struct Workspace {
     float *Gc, *dtT, *states;
+    char *fused_scratch;
+    size_t fused_scratch_bytes;
     size_t bytes;
 };
 
-Workspace layout(const Geom &g, bool caller_states, char *base)
+// ssd_fwd's workspace: G_cum and dt_t, then either the chunk states the
+// staged path keeps between stages (when the caller does not want them) or
+// the fused path's segment hand-off scratch.
+Workspace layout(const Geom &g, bool fused, bool caller_states, char *base)
 {
     const size_t bhl = (size_t)(g.B * g.H * g.L) * sizeof(float);
     size_t off = 0;
@@ -157,14 +162,19 @@ Workspace layout(const Geom &g, bool caller_states, char *base)
     off = round_up(off + bhl, 256);
     w.dtT = reinterpret_cast<float *>(base + off);
     off = round_up(off + bhl, 256);
-    w.states = nullptr;
-    if (!caller_states) {
+    if (fused) {
+        w.fused_scratch_bytes = fused_tc_scratch_bytes(g);
+        w.fused_scratch = base + off;
+        off = round_up(off + w.fused_scratch_bytes, 256);
+    } else if (!caller_states) {
         w.states = reinterpret_cast<float *>(base + off);
         off = round_up(off + (size_t)(g.B * g.H * g.nc * g.P * g.S) * sizeof(float), 256);
     }
     w.bytes = off;
-    if (!base)
+    if (!base) {
         w.Gc = w.dtT = w.states = nullptr;
+        w.fused_scratch = nullptr;
+    }
     return w;
 }
 
@@ -257,10 +267,20 @@ ssd_status_t ssd_chunk_out(const void *x, const void *Bm, const void *Cm, const 
                                      dtype == SSD_BF16, (cudaStream_t)stream));
 }
 
+size_t ssd_state_out_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size)
+{
+    Geom g;
+    if (make_geom(dims, chunk_size, false, &g) != SSD_OK || (dtype != SSD_BF16 && dtype != SSD_F32))
+        return 0;
+    const size_t b = (dtype == SSD_BF16 && chunk_tc_supported(g)) ? fused_tc_scratch_bytes(g) : 0;
+    return b ? b : 256;
+}
+
 ssd_status_t ssd_state_out(const void *x, const void *Bm, const void *Cm, const float *dt_t,
                            const float *G_cum, const float *D, const float *init_state, void *y,
                            float *final_state, float *chunk_states, ssd_dims_t dims,
-                           ssd_dtype_t dtype, int chunk_size, void *stream)
+                           ssd_dtype_t dtype, int chunk_size, void *workspace,
+                           size_t workspace_bytes, void *stream)
 {
     Geom g;
     SSD_TRY(make_geom(dims, chunk_size, false, &g));
@@ -282,8 +302,13 @@ ssd_status_t ssd_state_out(const void *x, const void *Bm, const void *Cm, const 
                               dtype, chunk_size, stream);
     if (dtype != SSD_BF16 || !chunk_tc_supported(g))
         return SSD_ERR_UNSUPPORTED;
+    const size_t need_ws = fused_tc_scratch_bytes(g);
+    if (need_ws && (!workspace || workspace_bytes < need_ws ||
+                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return SSD_ERR_WORKSPACE;
     return cuda_status(launch_fused_tc(x, Bm, Cm, dt_t, G_cum, D, init_state, chunk_states,
-                                       final_state, y, g, (cudaStream_t)stream));
+                                       final_state, y, g, workspace, workspace_bytes,
+                                       (cudaStream_t)stream));
 }
 
 ssd_path_t ssd_fwd_path(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, int want_chunk_states)
@@ -320,7 +345,7 @@ size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size
         g.nc = (g.L + g.T - 1) / g.T;
     }
     const bool fused = choose_path(g, dtype, want_chunk_states != 0) == SSD_PATH_FUSED_TENSOR_CORES;
-    const size_t b = layout(g, want_chunk_states != 0 || fused, nullptr).bytes;
+    const size_t b = layout(g, fused, want_chunk_states != 0, nullptr).bytes;
     return b ? b : 256;
 }
 
@@ -355,18 +380,19 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
                               dims, dtype, g.T, stream);
 
     const bool fused = choose_path(g, dtype, chunk_states != nullptr) == SSD_PATH_FUSED_TENSOR_CORES;
-    const Workspace need_ws = layout(g, chunk_states != nullptr || fused, nullptr);
+    const Workspace need_ws = layout(g, fused, chunk_states != nullptr, nullptr);
     if (!workspace || workspace_bytes < need_ws.bytes ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return SSD_ERR_WORKSPACE;
-    const Workspace w = layout(g, chunk_states != nullptr || fused, static_cast<char *>(workspace));
+    const Workspace w = layout(g, fused, chunk_states != nullptr, static_cast<char *>(workspace));
     float *states = chunk_states ? chunk_states : w.states;
     const bool bf16 = dtype == SSD_BF16;
 
     SSD_TRY(cuda_status(launch_chunk_cumsum(dt, A, w.Gc, w.dtT, g, st)));
     if (fused)
         return cuda_status(launch_fused_tc(x, Bm, Cm, w.dtT, w.Gc, D, init_state, chunk_states,
-                                           final_state, y, g, st));
+                                           final_state, y, g, w.fused_scratch,
+                                           w.fused_scratch_bytes, st));
     SSD_TRY(cuda_status(
         run_state_pass(x, Bm, w.dtT, w.Gc, init_state, states, final_state, g, bf16, st)));
     return cuda_status(run_chunk_out(x, Bm, Cm, w.dtT, w.Gc, states, D, y, g, bf16, st));

@@ -57,8 +57,11 @@ bool chunk_tc_supported(const Geom &g);
 cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                                 const float *Gc, const float *states, const float *D, void *y,
                                 const Geom &g, cudaStream_t st);
+// Scratch the fused pass needs (segment hand-off states and counters), 0 if none.
+size_t fused_tc_scratch_bytes(const Geom &g);
 cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                             const float *Gc, const float *D, const float *init, float *states,
-                            float *final_state, void *y, const Geom &g, cudaStream_t st);
+                            float *final_state, void *y, const Geom &g, void *scratch,
+                            size_t scratch_bytes, cudaStream_t st);
 
 }  // namespace ssd

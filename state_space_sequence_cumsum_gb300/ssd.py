@@ -176,7 +176,8 @@ def ssd_fwd(x, dt, A, B, C, D, chunk_size=0, initial_state=None, return_final_st
 
 
 def ssd_state_out(x, B, C, dt_t, G_cum, D, chunk_size, initial_state=None, y=None,
-                  final_state=True, chunk_states=None, stream=None):
+                  final_state=True, chunk_states=None, workspace: "Workspace | None" = None,
+                  stream=None):
     """Fused stages 2+3 (tensor-core path).  Returns (y, final_state, chunk_states)."""
     d = _geom(x, B)
     nc = (d.seqlen + chunk_size - 1) // chunk_size
@@ -191,10 +192,15 @@ def ssd_state_out(x, B, C, dt_t, G_cum, D, chunk_size, initial_state=None, y=Non
                                    dtype=torch.float32)
     final_state = final_state if isinstance(final_state, torch.Tensor) else None
     chunk_states = chunk_states if isinstance(chunk_states, torch.Tensor) else None
-    check(_lib.load().ssd_state_out(_ptr(x), _ptr(B), _ptr(C), _ptr(dt_t), _ptr(G_cum),
-                                    _ptr(_f32(D, "D")), _ptr(_f32(initial_state, "init")), _ptr(y),
-                                    _ptr(final_state), _ptr(chunk_states), d, _dtype_code(x),
-                                    int(chunk_size), _stream(stream)), "ssd_state_out")
+    lib = _lib.load()
+    code = _dtype_code(x)
+    nbytes = int(lib.ssd_state_out_workspace_size(d, code, int(chunk_size))) or 256
+    ws = (workspace or Workspace()).get(nbytes, dev)
+    check(lib.ssd_state_out(_ptr(x), _ptr(B), _ptr(C), _ptr(dt_t), _ptr(G_cum),
+                            _ptr(_f32(D, "D")), _ptr(_f32(initial_state, "init")), _ptr(y),
+                            _ptr(final_state), _ptr(chunk_states), d, code, int(chunk_size),
+                            _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream)),
+          "ssd_state_out")
     return y, final_state, chunk_states
 
 
@@ -240,7 +246,7 @@ def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk
     if plan["kernels"][1] == "state_out":
         ssd_state_out(x, B, C, dtT, Gc, D, T, initial_state=initial_state, y=y,
                       final_state=final_state if final_state is not None else False,
-                      chunk_states=chunk_states, stream=s)
+                      chunk_states=chunk_states, workspace=workspace, stream=s)
         mark(2)
         return y, final_state, chunk_states
     ssd_state_pass(x, B, dtT, Gc, T, init_state=initial_state, chunk_states=states,
