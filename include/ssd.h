@@ -45,9 +45,8 @@
  *   L >= 0 (L == 0 copies init_state to final_state and launches nothing
  *   else).  The tensor-core (tcgen05) kernels serve bf16 with T a multiple
  *   of 128: the state pass for P in {64, 128} and S % 64 == 0; the chunk
- *   output and the fused pass for (P, S) in {64} x {64, 128, 256} and
- *   {128} x {64, 128}.  Other shapes and all f32 calls run f32-arithmetic
- *   CUDA-core kernels.
+ *   output and the fused pass for P == 64 and S in {64, 128, 256}.  Other
+ *   shapes and all f32 calls run f32-arithmetic CUDA-core kernels.
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H

@@ -65,8 +65,10 @@ struct CoLayout {
     static constexpr uint32_t kH = kSReg * kHRegion;
     static constexpr uint32_t off_g = off_h + kH;  // [2 tiles][g 128 | dt 128] f32
     static constexpr uint32_t bytes = off_g + 2 * 256 * 4;
-    // TMEM columns: CB (f32) is converted in place to the bf16 score operand
-    static constexpr uint32_t t_cb = 0, t_y1 = 128, t_y2 = 128 + P, t_st = 128 + 2 * P;
+    // TMEM columns: CB (f32), the bf16 score operand (two per column), Y1, Y2,
+    // and the f32 state accumulator
+    static constexpr uint32_t t_cb = 0, t_sc = 128, t_y1 = 192, t_y2 = 192 + P,
+                              t_st = 192 + 2 * P;
     static constexpr uint32_t cols_used = t_st + kSBlk * P;
     static constexpr uint32_t kTmemCols = cols_used <= 256 ? 256 : 512;
     static_assert(cols_used <= 512, "TMEM budget");
@@ -128,28 +130,6 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p)
     return v;
 }
 
-// Per-tile scalars every role derives identically from G.
-struct TileScalars {
-    float base, g0, gL;
-    int n;
-    bool narrow;
-};
-
-__device__ __forceinline__ TileScalars tile_scalars(const float *grow, int64_t tau, int64_t L,
-                                                    int T)
-{
-    TileScalars t;
-    t.n = (int)min64(kTile, L - tau);
-    // G restarts at chunk starts; a tile inside a chunk is relative to the
-    // token before it
-    t.base = (tau % T == 0) ? 0.f : grow[tau - 1];
-    t.g0 = grow[tau] - t.base;
-    t.gL = grow[tau + t.n - 1] - t.base;
-    const float range = t.g0 - t.gL;
-    t.narrow = range <= kNarrow && range >= -kNarrow;
-    return t;
-}
-
 __device__ __forceinline__ void tma4(void *dst, const void *tmap, uint64_t *bar, int c0, int c1,
                                      int c2, int c3)
 {
@@ -185,9 +165,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES];
-    __shared__ uint64_t bar_cb, bar_cbread, bar_scores, bar_xh, bar_y1, bar_h, bar_y2, bar_ds,
-        bar_g;
+    __shared__ uint64_t bar_cb, bar_scores, bar_xh, bar_h, bar_done, bar_g;
     __shared__ uint32_t tmem_slot;
+    __shared__ int s_mode[2];  // per tile parity: 1 = factorized (narrow) decay
 
     const Geom &g = prm.g;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -198,13 +178,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             mbar_init(&bar_empty[s], 1 + kComputeThreads);
         }
         mbar_init(&bar_cb, 1);
-        mbar_init(&bar_cbread, kComputeThreads);
         mbar_init(&bar_scores, kComputeThreads);
         mbar_init(&bar_xh, kComputeThreads);
-        mbar_init(&bar_y1, 1);
         mbar_init(&bar_h, kComputeThreads);
-        mbar_init(&bar_y2, 1);
-        mbar_init(&bar_ds, 1);
+        mbar_init(&bar_done, 1);
         mbar_init(&bar_g, kComputeThreads);
         fence_barrier_init();
     }
@@ -253,7 +230,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
         }
     } else if (warp == 9) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer.  Per tile: CB; then (X_hat and H ready)
+        // Y2 and the state jump; then (scores ready) Y1; one commit covers all.
         if ((tid & 31) == 0) {
             const uint32_t id_cb = idesc_bf16(128, 128, false, false);
             const uint32_t id_y1 = idesc_bf16(128, P, false, true);  // A (scores) from TMEM
@@ -261,14 +239,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint32_t id_ds = idesc_bf16(128, P, true, true);
             const uint32_t s_xh = smem_u32(smem + Lay::off_xh);
             const uint32_t s_h = smem_u32(smem + Lay::off_h);
-            int64_t it = 0, n_state = 0;
+            int64_t it = 0;
             bool ok = true;
             for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
                 int64_t b, h, t0, t1, chunk;
                 decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
-                const float *grow = prm.Gc + (b * g.H + h) * g.L;
                 for (int64_t t = t0; t < t1; ++t, ++it) {
-                    const TileScalars ts = tile_scalars(grow, t * kTile, g.L, g.T);
                     const bool last_seq = MODE == kModeOut ? t + 1 == t1 : t + 1 == prm.n_tiles;
                     const bool do_state = !last_seq || want_final;
                     const int s = (int)(it % STAGES);
@@ -280,8 +256,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         ok = false;
                         break;
                     }
-                    // CB reuses the previous tile's score columns: wait for its last MMAs
-                    if (it > 0 && !mbar_wait(&bar_y2, (uint32_t)((it - 1) & 1))) {
+                    // CB overwrites the previous tile's score columns
+                    if (it > 0 && !mbar_wait(&bar_done, (uint32_t)((it - 1) & 1))) {
                         ok = false;
                         break;
                     }
@@ -291,18 +267,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         mma_ss(tmem + Lay::t_cb, desc_k(sc, kRegion, ks), desc_k(sb, kRegion, ks),
                                id_cb, ks > 0);
                     mma_commit(&bar_cb);
-                    if (!mbar_wait(&bar_scores, par) || !mbar_wait(&bar_xh, par)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t y1b = ts.narrow ? s_xh : sx;  // X_hat or raw x
-#pragma unroll
-                    for (int ks = 0; ks < kTile / 16; ++ks)
-                        mma_ts(tmem + Lay::t_y1, tmem + Lay::t_cb + ks * 8, desc_mn(y1b, ks), id_y1,
-                               ks > 0);
-                    mma_commit(&bar_y1);
-                    if (!mbar_wait(&bar_h, par)) {
+                    if (!mbar_wait(&bar_xh, par) || !mbar_wait(&bar_h, par)) {
                         ok = false;
                         break;
                     }
@@ -311,7 +276,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int ks = 0; ks < S / 16; ++ks)
                         mma_ss(tmem + Lay::t_y2, desc_k(sc, kRegion, ks),
                                desc_k(s_h, Lay::kHRegion, ks), id_y2, ks > 0);
-                    mma_commit(&bar_y2);
                     if (do_state) {
 #pragma unroll
                         for (int mb = 0; mb < Lay::kSBlk; ++mb)
@@ -322,9 +286,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                     mma_ss(tmem + Lay::t_st + mb * P,
                                            desc_mn(sb + 2 * mb * kRegion, ks),
                                            desc_mn(s_xh + part * Lay::kX, ks), id_ds, 1u);
-                        mma_commit(&bar_ds);
-                        ++n_state;
                     }
+                    if (!mbar_wait(&bar_scores, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t y1b = s_mode[it & 1] ? s_xh : sx;  // X_hat or raw x
+#pragma unroll
+                    for (int ks = 0; ks < kTile / 16; ++ks)
+                        mma_ts(tmem + Lay::t_y1, tmem + Lay::t_sc + ks * 8, desc_mn(y1b, ks), id_y1,
+                               ks > 0);
+                    mma_commit(&bar_done);
                     mma_commit(&bar_empty[s]);
                 }
             }
@@ -334,7 +307,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     } else {
         // ---------------- two compute warpgroups.  Thread (wg, q, lane) owns
         // tile row / TMEM lane i = 32 q + lane; warpgroup wg owns half of the
-        // columns of every per-tile step.
+        // columns of every per-tile step.  Order per tile: X_hat, H (so the
+        // MMA can start the state jump early), scores, epilogue.
         const int wg = warp >> 2, q = warp & 3;
         const int i = q * 32 + (tid & 31);
         const uint32_t lane = tmem_at(tmem, (uint32_t)(q * 32), 0);
@@ -342,27 +316,62 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         uint8_t *s_xh = smem + Lay::off_xh;
         uint8_t *s_h = smem + Lay::off_h;
         constexpr int kPHalf = P / 2;
-        int64_t it = 0, n_state = 0;
+
+        // raw G / dt values of a tile, loaded one tile ahead
+        struct Raw {
+            float base, g0, gL, gi, dti;
+        };
+        auto load_raw = [&](int64_t item, int64_t t) {
+            int64_t b, h, t0, t1, chunk;
+            decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
+            const int64_t bh = b * g.H + h;
+            const float *grow = prm.Gc + bh * g.L;
+            const int64_t tau = t * kTile;
+            const int n = (int)min64(kTile, g.L - tau);
+            Raw r;
+            r.base = (tau % g.T == 0) ? 0.f : grow[tau - 1];
+            r.g0 = grow[tau];
+            r.gL = grow[tau + n - 1];
+            r.gi = i < n ? grow[tau + i] : 0.f;
+            r.dti = i < n ? prm.dtT[bh * g.L + tau + i] : 0.f;
+            return r;
+        };
+        Raw nxt{};
+        if ((int64_t)blockIdx.x < prm.n_items) {
+            int64_t b, h, t0, t1, chunk;
+            decode_item<MODE>(prm, blockIdx.x, b, h, t0, t1, chunk);
+            nxt = load_raw(blockIdx.x, t0);
+        }
+        int64_t it = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
             int64_t b, h, t0, t1, chunk;
             decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
             const int64_t bh = b * g.H + h;
-            const float *grow = prm.Gc + bh * g.L;
-            const float *drow = prm.dtT + bh * g.L;
             const float Dh = prm.D[h];
             for (int64_t t = t0; t < t1; ++t, ++it) {
                 const int64_t tau = t * kTile;
-                const TileScalars ts = tile_scalars(grow, tau, g.L, g.T);
+                const int n = (int)min64(kTile, g.L - tau);
                 const bool first = t == t0, last_item = t + 1 == t1;
                 const bool last_seq = MODE == kModeOut ? last_item : t + 1 == prm.n_tiles;
                 const bool do_state = !last_seq || want_final;
-                const int n = ts.n;
+                const Raw cur = nxt;
+                // prefetch the next tile's G / dt while this one is processed
+                if (!last_item)
+                    nxt = load_raw(item, t + 1);
+                else if (item + gridDim.x < prm.n_items) {
+                    int64_t b2, h2, u0, u1, c2;
+                    decode_item<MODE>(prm, item + gridDim.x, b2, h2, u0, u1, c2);
+                    nxt = load_raw(item + gridDim.x, u0);
+                }
+                const float gL = cur.gL - cur.base;
+                const float range = (cur.g0 - cur.base) - gL;
+                const bool narrow = range <= kNarrow && range >= -kNarrow;
+                const float gi = cur.gi - cur.base;
+                const float dti = cur.dti;
                 const int s = (int)(it % STAGES);
                 const uint8_t *sx = smem + s * Lay::kStage + 2 * Lay::kB;
                 const uint32_t par = (uint32_t)(it & 1);
-                const float gi = i < n ? grow[tau + i] - ts.base : 0.f;
-                const float dti = i < n ? drow[tau + i] : 0.f;
 
                 // ---- per-tile g / dt table (double-buffered by tile parity)
                 float *gtab = gtab_all + (it & 1) * 256;
@@ -370,15 +379,24 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     gtab[i] = gi;
                 else
                     gtab[128 + i] = dti;
+                if (tid == 0)
+                    s_mode[it & 1] = narrow ? 1 : 0;
                 mbar_arrive(&bar_g);
-                if (!mbar_wait(&bar_g, par) || !mbar_wait(&bar_full[s], (uint32_t)((it / STAGES) & 1))) {
+                if (!mbar_wait(&bar_g, par) ||
+                    !mbar_wait(&bar_full[s], (uint32_t)((it / STAGES) & 1))) {
                     ok = false;
                     break;
                 }
+                // the previous tile's MMAs (state jump, Y1 reading X_hat) are done
+                if (it > 0 && !mbar_wait(&bar_done, (uint32_t)((it - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 
                 // ---- X_hat = dt exp2(g_L - g) x as bf16 hi (+ lo for the state jump)
-                if (ts.narrow || do_state) {
-                    const float w = i < n ? dti * ex2_approx(ts.gL - gi) : 0.f;
+                if (narrow || do_state) {
+                    const float w = i < n ? dti * ex2_approx(gL - gi) : 0.f;
 #pragma unroll
                     for (int r = 0; r < Lay::kPReg; ++r) {
 #pragma unroll
@@ -404,74 +422,6 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
                 mbar_arrive(&bar_xh);
 
-                // ---- scores, in place over CB (f32 -> bf16 A operand in TMEM)
-                if (!mbar_wait(&bar_cb, par)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const int row_max = q * 32 + 31;  // warp-uniform bound for the collective ld/st
-                uint32_t cbv[4][16];
-#pragma unroll
-                for (int gq = 0; gq < 4; ++gq) {
-                    const int j0 = wg * 64 + gq * 16;
-                    if (j0 <= row_max)
-                        tmem_ld16(lane + Lay::t_cb + j0, cbv[gq]);
-                }
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&bar_cbread);  // every CB value is in registers before any write
-                if (!mbar_wait(&bar_cbread, par)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int gq = 0; gq < 4; ++gq) {
-                    const int j0 = wg * 64 + gq * 16;
-                    uint32_t pk[8];
-                    if (j0 <= row_max) {
-                        if (ts.narrow) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j = j0 + 2 * e;
-                                const float a = (j <= i && j < n) ? __uint_as_float(cbv[gq][2 * e]) : 0.f;
-                                const float bb =
-                                    (j + 1 <= i && j + 1 < n) ? __uint_as_float(cbv[gq][2 * e + 1]) : 0.f;
-                                pk[e] = pack_bf16x2(a, bb);
-                            }
-                        } else {
-                            const float4 *g4 = reinterpret_cast<const float4 *>(gtab + j0);
-                            const float4 *d4 = reinterpret_cast<const float4 *>(gtab + 128 + j0);
-#pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4) {
-                                const float4 gg = g4[v4], dd = d4[v4];
-                                const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
-                                const float dj[4] = {dd.x, dd.y, dd.z, dd.w};
-                                float val[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int j = j0 + 4 * v4 + e;
-                                    val[e] = (j <= i && j < n)
-                                                 ? __uint_as_float(cbv[gq][4 * v4 + e]) *
-                                                       ex2_approx(gi - gj[e]) * dj[e]
-                                                 : 0.f;
-                                }
-                                pk[2 * v4] = pack_bf16x2(val[0], val[1]);
-                                pk[2 * v4 + 1] = pack_bf16x2(val[2], val[3]);
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            pk[e] = 0u;
-                    }
-                    tmem_st8(lane + Lay::t_cb + j0 / 2, pk);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&bar_scores);
-
                 // ---- a later segment waits until its predecessor published its state
                 if (MODE == kModeFused && first && chunk > 0) {
                     const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + chunk - 1;
@@ -490,8 +440,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
 
                 // ---- H = bf16(hscale * h) into K-major [p][s]; emit and decay the state
-                const float decay = ex2_approx(ts.gL);
-                const float hscale = ts.narrow ? decay : 1.f;
+                const float decay = ex2_approx(gL);
+                const float hscale = narrow ? decay : 1.f;
                 const bool emit = MODE == kModeFused && prm.states_out && (tau % g.T == 0);
 #pragma unroll
                 for (int mb = 0; mb < Lay::kSBlk; ++mb) {
@@ -545,14 +495,70 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 tc_fence_before();
                 mbar_arrive(&bar_h);
 
-                // ---- epilogue: y = r1 Y1 + r2 Y2 + D x
-                if (!mbar_wait(&bar_y2, par)) {
+                // ---- scores: CB (f32) -> masked, decayed bf16 A operand in TMEM.
+                // Warpgroup wg converts keys [64 wg, 64 wg + 64), 16 at a time.
+                if (!mbar_wait(&bar_cb, par)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float r1 = ts.narrow ? ex2_approx(gi - ts.gL) : 1.f;
-                const float r2 = ts.narrow ? r1 : ex2_approx(gi);
+                const int row_max = q * 32 + 31;  // warp-uniform bound for the collective ld/st
+#pragma unroll
+                for (int gq = 0; gq < 4; ++gq) {
+                    const int j0 = wg * 64 + gq * 16;
+                    uint32_t pk[8];
+                    if (j0 <= row_max) {
+                        uint32_t cbv[16];
+                        tmem_ld16(lane + Lay::t_cb + j0, cbv);
+                        tmem_ld_wait();
+                        if (narrow) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = j0 + 2 * e;
+                                const float a = (j <= i && j < n) ? __uint_as_float(cbv[2 * e]) : 0.f;
+                                const float bb =
+                                    (j + 1 <= i && j + 1 < n) ? __uint_as_float(cbv[2 * e + 1]) : 0.f;
+                                pk[e] = pack_bf16x2(a, bb);
+                            }
+                        } else {
+                            const float4 *g4 = reinterpret_cast<const float4 *>(gtab + j0);
+                            const float4 *d4 = reinterpret_cast<const float4 *>(gtab + 128 + j0);
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                const float4 gg = g4[v4], dd = d4[v4];
+                                const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
+                                const float dj[4] = {dd.x, dd.y, dd.z, dd.w};
+                                float val[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int j = j0 + 4 * v4 + e;
+                                    val[e] = (j <= i && j < n) ? __uint_as_float(cbv[4 * v4 + e]) *
+                                                                     ex2_approx(gi - gj[e]) * dj[e]
+                                                               : 0.f;
+                                }
+                                pk[2 * v4] = pack_bf16x2(val[0], val[1]);
+                                pk[2 * v4 + 1] = pack_bf16x2(val[2], val[3]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pk[e] = 0u;
+                    }
+                    tmem_st8(lane + Lay::t_sc + j0 / 2, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bar_scores);
+
+                // ---- epilogue: y = r1 Y1 + r2 Y2 + D x
+                if (!mbar_wait(&bar_done, par)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float r1 = narrow ? ex2_approx(gi - gL) : 1.f;
+                const float r2 = narrow ? r1 : ex2_approx(gi);
                 __nv_bfloat16 *yrow = prm.y + ((b * g.L + tau + i) * g.H + h) * g.P;
 #pragma unroll
                 for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
@@ -583,17 +589,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 tc_fence_before();
                 mbar_arrive(&bar_empty[s]);
 
-                // ---- the state jump must land before the next tile reads h
-                if (do_state) {
-                    if (!mbar_wait(&bar_ds, (uint32_t)(n_state & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    ++n_state;
-                    if (MODE == kModeFused && last_item && !last_seq) {
-                        // hand the state to the next segment: store, fence, count
-                        float *dst = prm.seg_state + ((bh * prm.n_seg + chunk) * g.P) * g.S;
+                // ---- state leaving the item: the next segment's start, or the final state
+                if (do_state && last_item) {
+                    float *dst = nullptr;
+                    const bool handoff = MODE == kModeFused && !last_seq;
+                    if (handoff)
+                        dst = prm.seg_state + ((bh * prm.n_seg + chunk) * g.P) * g.S;
+                    else if (last_seq && want_final)
+                        dst = prm.final_state + bh * g.P * g.S;
+                    if (dst) {
 #pragma unroll
                         for (int mb = 0; mb < Lay::kSBlk; ++mb) {
                             const int sidx = mb * 128 + i;
@@ -610,26 +614,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                 }
                             }
                         }
+                    }
+                    if (handoff) {
                         __threadfence();
                         atomicAdd(prm.seg_count + bh * prm.n_seg + chunk, 1u);
-                    }
-                    if (last_seq && want_final) {
-#pragma unroll
-                        for (int mb = 0; mb < Lay::kSBlk; ++mb) {
-                            const int sidx = mb * 128 + i;
-#pragma unroll
-                            for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
-                                uint32_t r[16];
-                                tmem_ld16(lane + Lay::t_st + mb * P + c0, r);
-                                tmem_ld_wait();
-                                if (sidx < S) {
-#pragma unroll
-                                    for (int j = 0; j < 16; ++j)
-                                        prm.final_state[(bh * g.P + c0 + j) * g.S + sidx] =
-                                            __uint_as_float(r[j]);
-                                }
-                            }
-                        }
                     }
                 }
             }
@@ -685,10 +673,6 @@ cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtenso
         return launch_cfg<64, 128, 2, MODE>(tx, tb, tcm, prm, st);
     if (g.P == 64 && g.S == 256)
         return launch_cfg<64, 256, 1, MODE>(tx, tb, tcm, prm, st);
-    if (g.P == 128 && g.S == 64)
-        return launch_cfg<128, 64, 2, MODE>(tx, tb, tcm, prm, st);
-    if (g.P == 128 && g.S == 128)
-        return launch_cfg<128, 128, 1, MODE>(tx, tb, tcm, prm, st);
     return cudaErrorNotSupported;
 }
 
@@ -769,8 +753,7 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
 
 bool chunk_tc_supported(const Geom &g)
 {
-    const bool shape = (g.P == 64 && (g.S == 64 || g.S == 128 || g.S == 256)) ||
-                       (g.P == 128 && (g.S == 64 || g.S == 128));
+    const bool shape = g.P == 64 && (g.S == 64 || g.S == 128 || g.S == 256);
     return shape && g.T % kTile == 0 && g.L > 0 && g.L < (1LL << 31) && g.H <= 65535 &&
            g.G <= 65535 && g.B <= 65535;
 }

@@ -33,22 +33,30 @@ chunk_cumsum_kernel(const float *__restrict__ dt, const float *__restrict__ A,
     const int64_t t0 = (int64_t)c * T;
     const int n = (int)min64(T, L - t0);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int h = h0 + lane;
 
-    for (int r = warp; r < T; r += kThreads / 32) {
-        const int h = h0 + lane;
-        float v = 0.f;  // zero padding past the sequence end
-        if (r < n && h < H)
-            v = dt[((int64_t)b * L + t0 + r) * H + h];
-        tile[r * ld + lane] = v;
-    }
+    // [T x 32] slice of dt, one 128-byte row per warp instruction; the loads
+    // of a thread are independent, so they are all in flight together
+    const float *src = dt + ((int64_t)b * L + t0) * H + h;
+#pragma unroll 8
+    for (int r = warp; r < T; r += kThreads / 32)
+        tile[r * ld + lane] = (r < n && h < H) ? src[(int64_t)r * H] : 0.f;  // zero padding
     __syncthreads();
 
     const int per = (T + 31) / 32;
     for (int hl = warp; hl < kHeadsPerCta; hl += kThreads / 32) {
-        const int h = h0 + hl;
-        if (h >= H)
+        const int hh = h0 + hl;
+        if (hh >= H)
             break;
-        const float a = A[h];
+        float *drow = dtT ? dtT + ((int64_t)b * H + hh) * L + t0 : nullptr;
+        float *grow = Gc + ((int64_t)b * H + hh) * L + t0;
+        // dt transposed: consecutive lanes write consecutive tokens
+        if (drow)
+            for (int t = lane; t < n; t += 32)
+                drow[t] = tile[t * ld + hl];
+        // lane-serial partial sums over `per` consecutive tokens, then a
+        // warp-shuffle scan of the lane totals
+        const float a = A[hh];
         float run = 0.f, vals[kMaxPerLane];
 #pragma unroll
         for (int k = 0; k < kMaxPerLane; ++k) {
@@ -67,17 +75,16 @@ chunk_cumsum_kernel(const float *__restrict__ dt, const float *__restrict__ A,
                 incl += o;
         }
         const float excl = incl - run;
-        float *grow = Gc + ((int64_t)b * H + h) * L + t0;
-        float *drow = dtT ? dtT + ((int64_t)b * H + h) * L + t0 : nullptr;
+        __syncwarp();
 #pragma unroll
         for (int k = 0; k < kMaxPerLane; ++k) {
             const int t = lane * per + k;
-            if (k < per && t < n) {
-                grow[t] = (excl + vals[k]) * kLog2e;
-                if (drow)
-                    drow[t] = tile[t * ld + hl];
-            }
+            if (k < per && t < T)
+                tile[t * ld + hl] = (excl + vals[k]) * kLog2e;  // this warp's column only
         }
+        __syncwarp();
+        for (int t = lane; t < n; t += 32)
+            grow[t] = tile[t * ld + hl];
     }
 }
 

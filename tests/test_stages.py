@@ -80,8 +80,9 @@ def test_state_pass_without_outputs_is_a_noop():
 
 
 @pytest.mark.parametrize("B,L,H,P,S,G,T", [(2, 700, 4, 64, 128, 2, 256),
-                                           (1, 513, 2, 128, 128, 1, 128),
-                                           (1, 300, 4, 64, 256, 4, 128)])
+                                           (1, 513, 2, 64, 64, 1, 128),
+                                           (1, 300, 4, 64, 256, 4, 128),
+                                           (3, 2000, 5, 64, 128, 1, 256)])  # several segments
 def test_fused_state_out_with_chunk_states(B, L, H, P, S, G, T):
     """Fused stages 2+3 through ssd_state_out: y, final and every chunk state."""
     inp = case_inputs(B, L, H, P, S, G, T, init="randn", seed=L + S)
