@@ -9,7 +9,7 @@
 //
 // One kernel, two modes:
 //   OUT   -- a work item is (batch, chunk, head); h_c comes from chunk_states.
-//   FUSED -- a work item is (batch, head) over the whole sequence; the state
+//   FUSED -- a work item is (batch, head, segment of the sequence); the state
 //            is carried on chip from tile to tile, so chunk states never go
 //            through HBM unless the caller asks for them.
 // Tokens are processed in 128-token tiles (the tcgen05 M and K extent).  A
@@ -19,21 +19,31 @@
 // (exp2(G_i - G_j) = exp2(G_i - G_m) exp2(G_m - G_j) with both factors <= 1).
 //
 // Per tile (all contractions are tcgen05.mma kind::f16, f32 accumulate in TMEM):
-//   CB  = C B^T                 M 128 (i) x N 128 (j), K = S     [TMEM cols 0..127]
+//   CB  = C B^T                 M 128 (i) x N 128 (j), K = S     [TMEM]
 //   scores_ij = CB_ij exp2(g_i - g_j) dt_j for j <= i (masked entries are set
-//               to zero without evaluating the exponent), bf16 into shared memory
-//   Y1  = scores X              N = P, K = 128                   [TMEM]
-//   Y2  = C H^T, H = bf16(h_c)  N = P, K = S                     [TMEM]
-//   y   = Y1 + exp2(g_i) Y2 + D x      (f32 epilogue, bf16 store)
+//               to zero without evaluating the exponent), bf16 into TMEM
+//   Y1  = scores X              N = P, K = 128, A operand from TMEM
+//   Y2  = C H^T, H = bf16(h_c)  N = P, K = S
+//   y   = Y1 + exp2(g_i) Y2 + D x      (f32 epilogue, bf16)
 //   and, when a later tile needs the state: h <- exp2(g_L) h + B^T X_hat with
 //   X_hat = dt exp2(g_L - g) X split into bf16 hi + lo (two MMA passes); the
 //   state h^T [S, P] is an f32 TMEM accumulator.
+// When the tile's decay range is narrow the decay factorizes:
+//   exp2(g_i - g_j) dt_j = exp2(g_i - g_L) * [dt_j exp2(g_L - g_j)],
+// so the scores are just the masked CB and Y1 = scores X_hat with the row
+// factor exp2(g_i - g_L) applied in the epilogue; no per-element exponent.
 //
-// Roles: warps 0-3 are the compute warpgroup (thread i owns tile row i, i.e.
-// TMEM lane i); warp 4 lane 0 issues TMA loads into a STAGES-deep ring
-// (B, C and x tiles, 128-byte swizzle); warp 5 lane 0 issues the MMAs.  The
-// CTA is persistent over work items.  Every wait is bounded; a timeout sets
-// the kernel status word and the role leaves its loop.
+// Roles (one CTA per SM, persistent over work items):
+//   warps 0-7  two compute warpgroups; thread (wg, q, lane) owns tile row /
+//              TMEM lane i = 32 q + lane, warpgroup wg owns half of the
+//              columns of every per-tile step;
+//   warp 8     TMA loads of B, C and x tiles into a STAGES-deep ring
+//              (128-byte swizzle);
+//   warp 9     MMA issue;
+//   warp 10    TMA store of y: the epilogue writes y over the x tile it has
+//              consumed, this warp stores it and then frees the stage.
+// Every wait is bounded; a timeout sets the kernel status word and the role
+// leaves its loop.
 #include "common.cuh"
 #include "ssd_internal.h"
 #include "tc05.cuh"
@@ -43,8 +53,9 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;
-constexpr int kComputeThreads = 256;  // two warpgroups
-constexpr int kThreads = kComputeThreads + 64;
+constexpr int kComputeWarps = 8;  // two warpgroups
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kThreads = kComputeThreads + 96;
 constexpr uint32_t kRegion = 128 * 128;
 // A tile takes the factorized decay when |g_first - g_last| <= kNarrow
 // (log2 units): then exp2(g_i - g_L) <= 2^64 and dt exp2(g_L - g_j) >= dt 2^-64,
@@ -58,11 +69,11 @@ struct CoLayout {
     static constexpr int kSBlk = (S + 127) / 128;  // 128-row blocks of the state
     static constexpr uint32_t kB = kSReg * kRegion;
     static constexpr uint32_t kX = kPReg * kRegion;
-    static constexpr uint32_t kStage = 2 * kB + kX;  // B, C, x
+    static constexpr uint32_t kStage = 2 * kB + kX;  // B, C, x (then y)
     static constexpr uint32_t off_xh = STAGES * kStage;  // X_hat hi, then lo
     static constexpr uint32_t off_h = off_xh + 2 * kX;
-    static constexpr uint32_t kHRegion = P * 128;  // P rows x 128 bytes
-    static constexpr uint32_t kH = kSReg * kHRegion;
+    // H is stored MN-major: one 128-byte row of P bf16 per state index s
+    static constexpr uint32_t kH = S * 128;
     static constexpr uint32_t off_g = off_h + kH;  // [2 tiles][g 128 | dt 128] f32
     static constexpr uint32_t bytes = off_g + 2 * 256 * 4;
     // TMEM columns: CB (f32), the bf16 score operand (two per column), Y1, Y2,
@@ -71,6 +82,7 @@ struct CoLayout {
                               t_st = 192 + 2 * P;
     static constexpr uint32_t cols_used = t_st + kSBlk * P;
     static constexpr uint32_t kTmemCols = cols_used <= 256 ? 256 : 512;
+    static_assert(P == 64, "one 128-byte row of x / y / H per token or state index");
     static_assert(cols_used <= 512, "TMEM budget");
     // dynamic bytes + alignment pad + static barriers within the 227 KB opt-in limit
     static_assert(bytes + 1024 + 256 <= 232448, "shared memory budget");
@@ -83,50 +95,69 @@ struct Params {
     const float *h_src;   // OUT: chunk_states; FUSED: init_state (may be null)
     float *states_out;    // FUSED: chunk_states to emit (may be null)
     float *final_state;   // FUSED: may be null
-    __nv_bfloat16 *y;
     Geom g;
-    int64_t n_items;
-    int64_t n_tiles;  // tiles per sequence
-    int tiles_per_chunk;
+    // Work geometry in 32-bit (the launcher checks that it fits): per-tile
+    // index arithmetic stays in cheap 32-bit integer operations.
+    int n_items;
+    int n_tiles;  // tiles per sequence
+    int tpc_shift;  // log2(tiles per chunk); chunk_size / 128 is 1 or 2
+    int H, nc, nbh;
     // FUSED: each (batch, head) sequence is split into n_seg segments of
     // seg_tiles tiles; segment k > 0 starts from the state segment k-1 leaves
-    // in seg_state, published by seg_count reaching kComputeThreads.
-    int64_t seg_tiles;
+    // in seg_state, published by seg_count reaching kComputeWarps.
+    int seg_tiles;
     int n_seg;
     float *seg_state;          // [B*H*n_seg][P][S]
     unsigned int *seg_count;   // [B*H*n_seg], zero at launch
     unsigned int *status;
 };
 
+// A work item: tiles [t0, t1) of sequence (b, h); chunk is the chunk index
+// (OUT) or the segment index (FUSED).
+struct Item {
+    int b, h, bh, t0, t1, chunk;
+};
+
 template <int MODE>
-__device__ __forceinline__ void decode_item(const Params &p, int64_t item, int64_t &b, int64_t &h,
-                                            int64_t &t0, int64_t &t1, int64_t &chunk)
+__device__ __forceinline__ Item decode_item(const Params &p, int item)
 {
+    Item it;
+    const unsigned u = (unsigned)item;
     if (MODE == kModeOut) {
         // consecutive items share (b, chunk) so their B/C tiles hit in L2
-        h = item % p.g.H;
-        const int64_t bc = item / p.g.H;
-        chunk = bc % p.g.nc;
-        b = bc / p.g.nc;
-        t0 = chunk * p.tiles_per_chunk;
-        t1 = min64(t0 + p.tiles_per_chunk, p.n_tiles);
+        it.h = (int)(u % (unsigned)p.H);
+        const unsigned bc = u / (unsigned)p.H;
+        it.chunk = (int)(bc % (unsigned)p.nc);
+        it.b = (int)(bc / (unsigned)p.nc);
+        it.t0 = it.chunk << p.tpc_shift;
+        it.t1 = min(it.t0 + (1 << p.tpc_shift), p.n_tiles);
     } else {
         // segment-major: every segment k of every sequence comes before any
         // segment k+1, so a segment's predecessor is always an earlier item
-        const int64_t nbh = p.g.B * p.g.H;
-        const int64_t seg = item / nbh, bh = item % nbh;
-        h = bh % p.g.H;
-        b = bh / p.g.H;
-        t0 = seg * p.seg_tiles;
-        t1 = min64(t0 + p.seg_tiles, p.n_tiles);
-        chunk = seg;
+        const unsigned seg = u / (unsigned)p.nbh, bh = u % (unsigned)p.nbh;
+        it.h = (int)(bh % (unsigned)p.H);
+        it.b = (int)(bh / (unsigned)p.H);
+        it.t0 = (int)seg * p.seg_tiles;
+        it.t1 = min(it.t0 + p.seg_tiles, p.n_tiles);
+        it.chunk = (int)seg;
     }
+    it.bh = it.b * p.H + it.h;
+    return it;
 }
 
 __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p)
 {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// A load the compiler may not sink to its first use: the next tile's G / dt
+// words are fetched while the current tile runs.
+__device__ __forceinline__ float ld_early(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -140,17 +171,44 @@ __device__ __forceinline__ void tma4(void *dst, const void *tmap, uint64_t *bar,
         : "memory");
 }
 
+// TMA store of a swizzled shared-memory box; rows past the tensor's end are
+// not written.
+__device__ __forceinline__ void tma4_store(const void *tmap, const void *src, int c0, int c1,
+                                           int c2, int c3)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group"
+                 " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(tmap),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory source of every committed store has been read
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed store has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// One arrival per warp: the warp's lanes are synchronised (which orders
+// their earlier shared-memory and TMEM work before lane 0's release).
+__device__ __forceinline__ void warp_arrive(uint64_t *bar)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(bar);
+}
+
+// Descriptors are built once per buffer and stepped by adding the byte
+// offset >> 4 to the start-address field (shared memory < 256 KB, so the
+// 14-bit field never carries).
 // K-major operand (rows x K, 64 K-elements per 128-byte row, one region per
-// 64 K): descriptor for the 16-wide K step ks.
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, uint32_t region_bytes, int ks)
+// 64 K): base descriptor, and the step to the 16-wide K slice ks.
+__device__ __forceinline__ uint64_t desc_k0(uint32_t base) { return smem_desc(base, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_k(uint64_t d0, uint32_t region_bytes, int ks)
 {
-    return smem_desc(base + (ks >> 2) * region_bytes + (ks & 3) * 32, 16, 1024);
+    return d0 + (((ks >> 2) * region_bytes + (ks & 3) * 32) >> 4);
 }
-// MN-major operand (128 K-rows of 64 M/N elements per region): K step ks.
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int ks)
-{
-    return smem_desc(base + ks * 2048, kRegion, 1024);
-}
+// MN-major operand (one 128-byte row of 64 M/N elements per K index).
+__device__ __forceinline__ uint64_t desc_mn0(uint32_t base) { return smem_desc(base, kRegion, 1024); }
+__device__ __forceinline__ uint64_t desc_mn(uint64_t d0, int ks) { return d0 + ((ks * 2048) >> 4); }
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -158,14 +216,21 @@ __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 
 template <int P, int S, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
-                const __grid_constant__ CUtensorMap tm_c, const Params prm)
+                const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
+                const Params prm)
 {
     using Lay = CoLayout<P, S, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES];
-    __shared__ uint64_t bar_cb, bar_scores, bar_xh, bar_h, bar_done, bar_g;
+    // full: TMA landed; empty: stage free (MMA reads done + y store read);
+    // ys: y of the stage's tile written to shared memory.
+    __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES], bar_ys[STAGES];
+    // MMA completions: cb (CB), y (Y1 and Y2), ds (state jump and all before)
+    __shared__ uint64_t bar_cb, bar_y, bar_ds;
+    // compute warps done with: X_hat and the g / dt table, H and the state
+    // decay, the score operand
+    __shared__ uint64_t bar_xh, bar_h, bar_scores;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_mode[2];  // per tile parity: 1 = factorized (narrow) decay
 
@@ -175,14 +240,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1 + kComputeThreads);
+            mbar_init(&bar_empty[s], 2);
+            mbar_init(&bar_ys[s], kComputeWarps);
         }
         mbar_init(&bar_cb, 1);
-        mbar_init(&bar_scores, kComputeThreads);
-        mbar_init(&bar_xh, kComputeThreads);
-        mbar_init(&bar_h, kComputeThreads);
-        mbar_init(&bar_done, 1);
-        mbar_init(&bar_g, kComputeThreads);
+        mbar_init(&bar_y, 1);
+        mbar_init(&bar_ds, 1);
+        mbar_init(&bar_xh, kComputeWarps);
+        mbar_init(&bar_h, kComputeWarps);
+        mbar_init(&bar_scores, kComputeWarps);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -201,179 +267,221 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             prefetch_tmap(&tm_x);
             prefetch_tmap(&tm_b);
             prefetch_tmap(&tm_c);
-            int64_t it = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
-                int64_t b, h, t0, t1, chunk;
-                decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
-                const int64_t grp = h / g.hpg;
-                for (int64_t t = t0; t < t1; ++t, ++it) {
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const Item w = decode_item<MODE>(prm, item);
+                const int grp = w.h / g.hpg;
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
                     const int s = (int)(it % STAGES);
                     if (it >= STAGES &&
-                        !mbar_wait(&bar_empty[s], (uint32_t)(((it / STAGES) - 1) & 1))) {
-                        atomicOr(prm.status, 1u);
+                        !mbar_wait(&bar_empty[s], ((it / STAGES) - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     uint8_t *st = smem + s * Lay::kStage;
                     mbar_arrive_expect_tx(&bar_full[s], Lay::kStage);
-                    const int tok = (int)(t * kTile);
+                    const int tok = t * kTile;
                     for (int r = 0; r < Lay::kSReg; ++r) {
-                        tma4(st + r * kRegion, &tm_b, &bar_full[s], r * 64, (int)grp, tok, (int)b);
-                        tma4(st + Lay::kB + r * kRegion, &tm_c, &bar_full[s], r * 64, (int)grp,
-                             tok, (int)b);
+                        tma4(st + r * kRegion, &tm_b, &bar_full[s], r * 64, grp, tok, w.b);
+                        tma4(st + Lay::kB + r * kRegion, &tm_c, &bar_full[s], r * 64, grp, tok, w.b);
                     }
                     for (int r = 0; r < Lay::kPReg; ++r)
-                        tma4(st + 2 * Lay::kB + r * kRegion, &tm_x, &bar_full[s], r * 64, (int)h,
-                             tok, (int)b);
+                        tma4(st + 2 * Lay::kB + r * kRegion, &tm_x, &bar_full[s], r * 64, w.h, tok,
+                             w.b);
                 }
             }
+            if (!ok)
+                atomicOr(prm.status, 1u);
         }
     } else if (warp == 9) {
-        // ---------------- MMA issuer.  Per tile: CB; then (X_hat and H ready)
-        // Y2 and the state jump; then (scores ready) Y1; one commit covers all.
+        // ---------------- MMA issuer.  Per tile: CB; Y2 once H is ready; then
+        // Y1 (scores ready) and the state jump (X_hat ready) in whichever
+        // order their inputs arrive.
         if ((tid & 31) == 0) {
             const uint32_t id_cb = idesc_bf16(128, 128, false, false);
             const uint32_t id_y1 = idesc_bf16(128, P, false, true);  // A (scores) from TMEM
-            const uint32_t id_y2 = idesc_bf16(128, P, false, false);
+            const uint32_t id_y2 = idesc_bf16(128, P, false, true);  // H is MN-major
             const uint32_t id_ds = idesc_bf16(128, P, true, true);
-            const uint32_t s_xh = smem_u32(smem + Lay::off_xh);
-            const uint32_t s_h = smem_u32(smem + Lay::off_h);
-            int64_t it = 0;
+            // base descriptors: per stage B, C (K-major and, for B, MN-major
+            // as the state jump's A) and x; X_hat hi / lo; H
+            const uint64_t d_xh = desc_mn0(smem_u32(smem + Lay::off_xh));
+            const uint64_t d_h = desc_mn0(smem_u32(smem + Lay::off_h));
+            uint32_t it = 0;
             bool ok = true;
-            for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
-                int64_t b, h, t0, t1, chunk;
-                decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
-                for (int64_t t = t0; t < t1; ++t, ++it) {
-                    const bool last_seq = MODE == kModeOut ? t + 1 == t1 : t + 1 == prm.n_tiles;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const Item w = decode_item<MODE>(prm, item);
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
+                    const bool last_seq = MODE == kModeOut ? t + 1 == w.t1 : t + 1 == prm.n_tiles;
                     const bool do_state = !last_seq || want_final;
                     const int s = (int)(it % STAGES);
                     const uint32_t sb = smem_u32(smem + s * Lay::kStage);
-                    const uint32_t sc = sb + Lay::kB;
-                    const uint32_t sx = sb + 2 * Lay::kB;
-                    const uint32_t par = (uint32_t)(it & 1);
-                    if (!mbar_wait(&bar_full[s], (uint32_t)((it / STAGES) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    // CB overwrites the previous tile's score columns
-                    if (it > 0 && !mbar_wait(&bar_done, (uint32_t)((it - 1) & 1))) {
+                    const uint64_t d_bk = desc_k0(sb), d_ck = desc_k0(sb + Lay::kB);
+                    const uint64_t d_bmn = desc_mn0(sb), d_x = desc_mn0(sb + 2 * Lay::kB);
+                    const uint32_t par = it & 1;
+                    // CB overwrites the previous tile's CB, whose conversion
+                    // ended before that tile's Y1 was issued
+                    if (!mbar_wait(&bar_full[s], (it / STAGES) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < S / 16; ++ks)
-                        mma_ss(tmem + Lay::t_cb, desc_k(sc, kRegion, ks), desc_k(sb, kRegion, ks),
+                        mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
                                id_cb, ks > 0);
                     mma_commit(&bar_cb);
-                    if (!mbar_wait(&bar_xh, par) || !mbar_wait(&bar_h, par)) {
+                    if (!mbar_wait(&bar_h, par)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < S / 16; ++ks)
-                        mma_ss(tmem + Lay::t_y2, desc_k(sc, kRegion, ks),
-                               desc_k(s_h, Lay::kHRegion, ks), id_y2, ks > 0);
-                    if (do_state) {
+                        mma_ss(tmem + Lay::t_y2, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2,
+                               ks > 0);
+                    auto issue_y1 = [&]() {
+                        const uint64_t d_y1b = s_mode[it & 1] ? d_xh : d_x;  // X_hat or raw x
 #pragma unroll
-                        for (int mb = 0; mb < Lay::kSBlk; ++mb)
+                        for (int ks = 0; ks < kTile / 16; ++ks)
+                            mma_ts(tmem + Lay::t_y1, tmem + Lay::t_sc + ks * 8, desc_mn(d_y1b, ks),
+                                   id_y1, ks > 0);
+                        mma_commit(&bar_y);
+                    };
+                    auto issue_ds = [&]() {
+                        if (do_state) {
 #pragma unroll
-                            for (int part = 0; part < 2; ++part)
+                            for (int mb = 0; mb < Lay::kSBlk; ++mb)
 #pragma unroll
-                                for (int ks = 0; ks < kTile / 16; ++ks)
-                                    mma_ss(tmem + Lay::t_st + mb * P,
-                                           desc_mn(sb + 2 * mb * kRegion, ks),
-                                           desc_mn(s_xh + part * Lay::kX, ks), id_ds, 1u);
-                    }
-                    if (!mbar_wait(&bar_scores, par)) {
+                                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                                    for (int ks = 0; ks < kTile / 16; ++ks)
+                                        mma_ss(tmem + Lay::t_st + mb * P,
+                                               desc_mn(d_bmn + ((2 * mb * kRegion) >> 4), ks),
+                                               desc_mn(d_xh + ((part * Lay::kX) >> 4), ks), id_ds, 1u);
+                        }
+                        mma_commit(&bar_ds);
+                    };
+                    // X_hat is published before H, so it is ready here
+                    if (!mbar_wait(&bar_xh, par)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t y1b = s_mode[it & 1] ? s_xh : sx;  // X_hat or raw x
-#pragma unroll
-                    for (int ks = 0; ks < kTile / 16; ++ks)
-                        mma_ts(tmem + Lay::t_y1, tmem + Lay::t_sc + ks * 8, desc_mn(y1b, ks), id_y1,
-                               ks > 0);
-                    mma_commit(&bar_done);
+                    if (mbar_try_wait(&bar_scores, par)) {
+                        tc_fence_after();
+                        issue_y1();
+                        issue_ds();
+                    } else {
+                        issue_ds();
+                        if (!mbar_wait(&bar_scores, par)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_y1();
+                    }
                     mma_commit(&bar_empty[s]);
                 }
             }
             if (!ok)
                 atomicOr(prm.status, 1u);
         }
-    } else {
-        // ---------------- two compute warpgroups.  Thread (wg, q, lane) owns
-        // tile row / TMEM lane i = 32 q + lane; warpgroup wg owns half of the
-        // columns of every per-tile step.  Order per tile: X_hat, H (so the
-        // MMA can start the state jump early), scores, epilogue.
+    } else if (warp == 10) {
+        // ---------------- y store: the epilogue left y in the stage's x region
+        if ((tid & 31) == 0) {
+            prefetch_tmap(&tm_y);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const Item w = decode_item<MODE>(prm, item);
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
+                    const int s = (int)(it % STAGES);
+                    if (!mbar_wait(&bar_ys[s], (it / STAGES) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *sy = smem + s * Lay::kStage + 2 * Lay::kB;
+                    for (int r = 0; r < Lay::kPReg; ++r)
+                        tma4_store(&tm_y, sy + r * kRegion, r * 64, w.h, t * kTile, w.b);
+                    bulk_commit();
+                    bulk_wait_read();
+                    mbar_arrive(&bar_empty[s]);
+                }
+            }
+            bulk_wait_all();
+            if (!ok)
+                atomicOr(prm.status, 1u);
+        }
+    } else if (warp < kComputeWarps) {
+        // ---------------- two compute warpgroups.  Per tile: g / dt table,
+        // X_hat, H (publishing the state for the jump), scores, epilogue.
         const int wg = warp >> 2, q = warp & 3;
         const int i = q * 32 + (tid & 31);
+        const int row_lo = q * 32, row_hi = q * 32 + 31;  // this warp's rows
         const uint32_t lane = tmem_at(tmem, (uint32_t)(q * 32), 0);
         float *gtab_all = reinterpret_cast<float *>(smem + Lay::off_g);
         uint8_t *s_xh = smem + Lay::off_xh;
         uint8_t *s_h = smem + Lay::off_h;
         constexpr int kPHalf = P / 2;
+        const int c0w = wg * kPHalf;  // this warpgroup's first headdim column
 
-        // raw G / dt values of a tile, loaded one tile ahead
+        // raw G / dt words of a tile, loaded one tile ahead
         struct Raw {
             float base, g0, gL, gi, dti;
         };
-        auto load_raw = [&](int64_t item, int64_t t) {
-            int64_t b, h, t0, t1, chunk;
-            decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
-            const int64_t bh = b * g.H + h;
-            const float *grow = prm.Gc + bh * g.L;
-            const int64_t tau = t * kTile;
-            const int n = (int)min64(kTile, g.L - tau);
+        const int tpc_mask = (1 << prm.tpc_shift) - 1;
+        auto load_raw = [&](const Item &w, int t) {
+            const float *grow = prm.Gc + (int64_t)w.bh * g.L;
+            const int tau = t * kTile;
+            const int n = min(kTile, (int)g.L - tau);
             Raw r;
-            r.base = (tau % g.T == 0) ? 0.f : grow[tau - 1];
-            r.g0 = grow[tau];
-            r.gL = grow[tau + n - 1];
-            r.gi = i < n ? grow[tau + i] : 0.f;
-            r.dti = i < n ? prm.dtT[bh * g.L + tau + i] : 0.f;
+            r.base = (t & tpc_mask) == 0 ? 0.f : ld_early(grow + tau - 1);
+            r.g0 = ld_early(grow + tau);
+            r.gL = ld_early(grow + tau + n - 1);
+            r.gi = i < n ? ld_early(grow + tau + i) : r.base;
+            r.dti = i < n ? ld_early(prm.dtT + (int64_t)w.bh * g.L + tau + i) : 0.f;
             return r;
         };
         Raw nxt{};
-        if ((int64_t)blockIdx.x < prm.n_items) {
-            int64_t b, h, t0, t1, chunk;
-            decode_item<MODE>(prm, blockIdx.x, b, h, t0, t1, chunk);
-            nxt = load_raw(blockIdx.x, t0);
+        Item w_next{};
+        if ((int)blockIdx.x < prm.n_items) {
+            w_next = decode_item<MODE>(prm, blockIdx.x);
+            nxt = load_raw(w_next, w_next.t0);
         }
-        int64_t it = 0;
+        uint32_t it = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
-            int64_t b, h, t0, t1, chunk;
-            decode_item<MODE>(prm, item, b, h, t0, t1, chunk);
-            const int64_t bh = b * g.H + h;
-            const float Dh = prm.D[h];
-            for (int64_t t = t0; t < t1; ++t, ++it) {
-                const int64_t tau = t * kTile;
-                const int n = (int)min64(kTile, g.L - tau);
-                const bool first = t == t0, last_item = t + 1 == t1;
+        for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+            const Item w = w_next;
+            const int64_t bh = w.bh;
+            const int chunk = w.chunk;
+            const float Dh = prm.D[w.h];
+            const bool more = item + (int)gridDim.x < prm.n_items;
+            if (more)
+                w_next = decode_item<MODE>(prm, item + gridDim.x);
+            for (int t = w.t0; t < w.t1; ++t, ++it) {
+                const int tau = t * kTile;
+                const int n = min(kTile, (int)g.L - tau);
+                const bool first = t == w.t0, last_item = t + 1 == w.t1;
                 const bool last_seq = MODE == kModeOut ? last_item : t + 1 == prm.n_tiles;
                 const bool do_state = !last_seq || want_final;
                 const Raw cur = nxt;
                 // prefetch the next tile's G / dt while this one is processed
                 if (!last_item)
-                    nxt = load_raw(item, t + 1);
-                else if (item + gridDim.x < prm.n_items) {
-                    int64_t b2, h2, u0, u1, c2;
-                    decode_item<MODE>(prm, item + gridDim.x, b2, h2, u0, u1, c2);
-                    nxt = load_raw(item + gridDim.x, u0);
-                }
+                    nxt = load_raw(w, t + 1);
+                else if (more)
+                    nxt = load_raw(w_next, w_next.t0);
                 const float gL = cur.gL - cur.base;
                 const float range = (cur.g0 - cur.base) - gL;
                 const bool narrow = range <= kNarrow && range >= -kNarrow;
                 const float gi = cur.gi - cur.base;
                 const float dti = cur.dti;
                 const int s = (int)(it % STAGES);
-                const uint8_t *sx = smem + s * Lay::kStage + 2 * Lay::kB;
-                const uint32_t par = (uint32_t)(it & 1);
+                uint8_t *sx = smem + s * Lay::kStage + 2 * Lay::kB;
+                const uint32_t par = it & 1;
 
-                // ---- per-tile g / dt table (double-buffered by tile parity)
+                // ---- per-tile g / dt table (double-buffered by tile parity),
+                // published with X_hat
                 float *gtab = gtab_all + (it & 1) * 256;
                 if (wg == 0)
                     gtab[i] = gi;
@@ -381,14 +489,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     gtab[128 + i] = dti;
                 if (tid == 0)
                     s_mode[it & 1] = narrow ? 1 : 0;
-                mbar_arrive(&bar_g);
-                if (!mbar_wait(&bar_g, par) ||
-                    !mbar_wait(&bar_full[s], (uint32_t)((it / STAGES) & 1))) {
-                    ok = false;
-                    break;
-                }
-                // the previous tile's MMAs (state jump, Y1 reading X_hat) are done
-                if (it > 0 && !mbar_wait(&bar_done, (uint32_t)((it - 1) & 1))) {
+                // x landed; the previous tile's state jump (and everything
+                // before it: Y1 and Y2 reading X_hat and H) has completed
+                if (!mbar_wait(&bar_full[s], (it / STAGES) & 1) ||
+                    (it > 0 && !mbar_wait(&bar_ds, (it - 1) & 1))) {
                     ok = false;
                     break;
                 }
@@ -420,18 +524,18 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     fence_proxy_async_smem();
                 }
-                mbar_arrive(&bar_xh);
+                warp_arrive(&bar_xh);
 
                 // ---- a later segment waits until its predecessor published its state
                 if (MODE == kModeFused && first && chunk > 0) {
                     const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + chunk - 1;
-                    bool ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeThreads;
+                    bool ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
                     const uint64_t t_start = globaltimer_ns();
                     while (!ready) {
                         if (globaltimer_ns() - t_start > 2000000000ull)
                             break;
                         __nanosleep(256);
-                        ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeThreads;
+                        ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
                     }
                     if (!ready) {
                         ok = false;
@@ -439,86 +543,112 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
 
-                // ---- H = bf16(hscale * h) into K-major [p][s]; emit and decay the state
+                // ---- H = bf16(hscale * h), MN-major [s][p]; emit and decay the state
                 const float decay = ex2_approx(gL);
                 const float hscale = narrow ? decay : 1.f;
-                const bool emit = MODE == kModeFused && prm.states_out && (tau % g.T == 0);
+                const bool emit = MODE == kModeFused && prm.states_out && (t & tpc_mask) == 0;
 #pragma unroll
                 for (int mb = 0; mb < Lay::kSBlk; ++mb) {
                     const int sidx = mb * 128 + i;
                     const bool s_ok = sidx < S;
-                    const uint32_t acc = lane + Lay::t_st + mb * P;
-                    const float *src = nullptr;
+                    const uint32_t acc = lane + Lay::t_st + mb * P + c0w;
+                    uint32_t r[kPHalf];
                     if (first) {
+                        const float *src = nullptr;
                         if (MODE == kModeOut)
                             src = prm.h_src + ((bh * g.nc + chunk) * g.P) * g.S;
                         else if (chunk > 0)  // later segment: the predecessor's state
                             src = prm.seg_state + ((bh * prm.n_seg + chunk - 1) * g.P) * g.S;
                         else if (prm.h_src)
                             src = prm.h_src + bh * g.P * g.S;
+#pragma unroll
+                        for (int j = 0; j < kPHalf; ++j)
+                            r[j] = __float_as_uint(
+                                (src && s_ok) ? __ldcg(src + (int64_t)(c0w + j) * S + sidx) : 0.f);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kPHalf; c += 16)
+                            tmem_ld16(acc + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+                        tmem_ld_wait();
                     }
                     float *emit_dst =
-                        emit ? prm.states_out + ((bh * g.nc + tau / g.T) * g.P) * g.S : nullptr;
-                    uint8_t *hb = s_h + (sidx >> 6) * Lay::kHRegion;
-                    const int cs = sidx & 63;
+                        emit ? prm.states_out + ((bh * g.nc + (t >> prm.tpc_shift)) * g.P) * g.S
+                             : nullptr;
+                    uint32_t hp[kPHalf / 2];
 #pragma unroll
-                    for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
-                        uint32_t r[16];
-                        if (first) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                r[j] = __float_as_uint(
-                                    (src && s_ok) ? __ldcg(src + (int64_t)(c0 + j) * S + sidx) : 0.f);
-                        } else {
-                            tmem_ld16(acc + c0, r);
-                            tmem_ld_wait();
+                    for (int j = 0; j < kPHalf; j += 2) {
+                        const float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
+                        if (emit_dst && s_ok) {
+                            emit_dst[(int64_t)(c0w + j) * S + sidx] = v0;
+                            emit_dst[(int64_t)(c0w + j + 1) * S + sidx] = v1;
                         }
+                        hp[j / 2] = pack_bf16x2(v0 * hscale, v1 * hscale);
+                        r[j] = __float_as_uint(v0 * decay);
+                        r[j + 1] = __float_as_uint(v1 * decay);
+                    }
+                    if (s_ok) {  // row sidx, columns c0w .. c0w + 31: four 16-byte chunks
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float v = __uint_as_float(r[j]);
-                            if (s_ok) {
-                                if (emit_dst)
-                                    emit_dst[(int64_t)(c0 + j) * S + sidx] = v;
-                                *reinterpret_cast<__nv_bfloat16 *>(
-                                    hb + sw128_offset(c0 + j, cs >> 3) + (cs & 7) * 2) =
-                                    __float2bfloat16_rn(v * hscale);
-                            }
-                            r[j] = __float_as_uint(v * decay);
-                        }
-                        if (do_state)
-                            tmem_st16(acc + c0, r);
+                        for (int k = 0; k < kPHalf / 8; ++k)
+                            *reinterpret_cast<uint4 *>(s_h + sw128_offset(sidx, c0w / 8 + k)) =
+                                make_uint4(hp[4 * k], hp[4 * k + 1], hp[4 * k + 2], hp[4 * k + 3]);
+                    }
+                    if (do_state) {
+#pragma unroll
+                        for (int c = 0; c < kPHalf; c += 16)
+                            tmem_st16(acc + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
                     }
                 }
                 if (do_state)
                     tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&bar_h);
+                warp_arrive(&bar_h);
 
                 // ---- scores: CB (f32) -> masked, decayed bf16 A operand in TMEM.
-                // Warpgroup wg converts keys [64 wg, 64 wg + 64), 16 at a time.
-                if (!mbar_wait(&bar_cb, par)) {
+                // Warpgroup wg converts keys [64 wg, 64 wg + 64): one TMEM round
+                // trip for all of them.  The g / dt table is complete once every
+                // warp has published X_hat.
+                if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_xh, par)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int row_max = q * 32 + 31;  // warp-uniform bound for the collective ld/st
+                const bool full = n == kTile;
 #pragma unroll
-                for (int gq = 0; gq < 4; ++gq) {
-                    const int j0 = wg * 64 + gq * 16;
-                    uint32_t pk[8];
-                    if (j0 <= row_max) {
-                        uint32_t cbv[16];
-                        tmem_ld16(lane + Lay::t_cb + j0, cbv);
-                        tmem_ld_wait();
-                        if (narrow) {
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t cbv[2][16];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j = j0 + 2 * e;
-                                const float a = (j <= i && j < n) ? __uint_as_float(cbv[2 * e]) : 0.f;
-                                const float bb =
-                                    (j + 1 <= i && j + 1 < n) ? __uint_as_float(cbv[2 * e + 1]) : 0.f;
-                                pk[e] = pack_bf16x2(a, bb);
+                    for (int gq = 0; gq < 2; ++gq) {
+                        const int j0 = wg * 64 + half * 32 + gq * 16;
+                        if (j0 <= row_hi)  // warp-uniform: keys above the diagonal stay zero
+                            tmem_ld16(lane + Lay::t_cb + j0, cbv[gq]);
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int gq = 0; gq < 2; ++gq) {
+                        const int j0 = wg * 64 + half * 32 + gq * 16;
+                        uint32_t pk[8];
+                        if (j0 > row_hi) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                pk[e] = 0u;
+                        } else if (narrow) {
+                            if (full && j0 + 15 < row_lo) {  // whole group below the diagonal
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    pk[e] = pack_bf16x2(__uint_as_float(cbv[gq][2 * e]),
+                                                        __uint_as_float(cbv[gq][2 * e + 1]));
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const int j = j0 + 2 * e;
+                                    const float a =
+                                        (j <= i && j < n) ? __uint_as_float(cbv[gq][2 * e]) : 0.f;
+                                    const float bb = (j + 1 <= i && j + 1 < n)
+                                                         ? __uint_as_float(cbv[gq][2 * e + 1])
+                                                         : 0.f;
+                                    pk[e] = pack_bf16x2(a, bb);
+                                }
                             }
                         } else {
                             const float4 *g4 = reinterpret_cast<const float4 *>(gtab + j0);
@@ -532,62 +662,59 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     const int j = j0 + 4 * v4 + e;
-                                    val[e] = (j <= i && j < n) ? __uint_as_float(cbv[4 * v4 + e]) *
-                                                                     ex2_approx(gi - gj[e]) * dj[e]
-                                                               : 0.f;
+                                    val[e] = (j <= i && j < n)
+                                                 ? __uint_as_float(cbv[gq][4 * v4 + e]) *
+                                                       ex2_approx(gi - gj[e]) * dj[e]
+                                                 : 0.f;
                                 }
                                 pk[2 * v4] = pack_bf16x2(val[0], val[1]);
                                 pk[2 * v4 + 1] = pack_bf16x2(val[2], val[3]);
                             }
                         }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            pk[e] = 0u;
+                        tmem_st8(lane + Lay::t_sc + j0 / 2, pk);
                     }
-                    tmem_st8(lane + Lay::t_sc + j0 / 2, pk);
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bar_scores);
+                warp_arrive(&bar_scores);
 
-                // ---- epilogue: y = r1 Y1 + r2 Y2 + D x
-                if (!mbar_wait(&bar_done, par)) {
+                // ---- epilogue: y = r1 Y1 + r2 Y2 + D x, written over x in the stage
+                if (!mbar_wait(&bar_y, par)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const float r1 = narrow ? ex2_approx(gi - gL) : 1.f;
-                const float r2 = narrow ? r1 : ex2_approx(gi);
-                __nv_bfloat16 *yrow = prm.y + ((b * g.L + tau + i) * g.H + h) * g.P;
+                {
+                    const float r1 = narrow ? ex2_approx(gi - gL) : 1.f;
+                    const float r2 = narrow ? r1 : ex2_approx(gi);
 #pragma unroll
-                for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
-                    uint32_t ra[16], rb[16];
-                    tmem_ld16(lane + Lay::t_y1 + c0, ra);
-                    tmem_ld16(lane + Lay::t_y2 + c0, rb);
-                    tmem_ld_wait();
-                    const uint8_t *xr = sx + (c0 >> 6) * kRegion;
-                    const int cc = (c0 & 63) >> 3;
-                    const uint4 xa = *reinterpret_cast<const uint4 *>(xr + sw128_offset(i, cc));
-                    const uint4 xb = *reinterpret_cast<const uint4 *>(xr + sw128_offset(i, cc + 1));
-                    const uint32_t xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-                    uint32_t o[8];
+                    for (int c16 = 0; c16 < kPHalf; c16 += 16) {
+                        uint32_t ra[16], rb[16];
+                        tmem_ld16(lane + Lay::t_y1 + c0w + c16, ra);
+                        tmem_ld16(lane + Lay::t_y2 + c0w + c16, rb);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float a = r1 * __uint_as_float(ra[2 * e]) +
-                                        r2 * __uint_as_float(rb[2 * e]) + Dh * bf_lo(xv[e]);
-                        const float bb = r1 * __uint_as_float(ra[2 * e + 1]) +
-                                         r2 * __uint_as_float(rb[2 * e + 1]) + Dh * bf_hi(xv[e]);
-                        o[e] = pack_bf16x2(a, bb);
-                    }
-                    if (i < n) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + c0);
-                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                        for (int k = 0; k < 2; ++k) {
+                            uint8_t *xp = sx + sw128_offset(i, (c0w + c16) / 8 + k);
+                            const uint4 xv4 = *reinterpret_cast<const uint4 *>(xp);
+                            const uint32_t xv[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = 8 * k + 2 * e;
+                                const float a = r1 * __uint_as_float(ra[c]) +
+                                                r2 * __uint_as_float(rb[c]) + Dh * bf_lo(xv[e]);
+                                const float bb = r1 * __uint_as_float(ra[c + 1]) +
+                                                 r2 * __uint_as_float(rb[c + 1]) + Dh * bf_hi(xv[e]);
+                                o[e] = pack_bf16x2(a, bb);
+                            }
+                            *reinterpret_cast<uint4 *>(xp) = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
                     }
                 }
+                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&bar_empty[s]);
+                warp_arrive(&bar_ys[s]);
 
                 // ---- state leaving the item: the next segment's start, or the final state
                 if (do_state && last_item) {
@@ -598,26 +725,33 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     else if (last_seq && want_final)
                         dst = prm.final_state + bh * g.P * g.S;
                     if (dst) {
+                        if (!mbar_wait(&bar_ds, par)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
                         for (int mb = 0; mb < Lay::kSBlk; ++mb) {
                             const int sidx = mb * 128 + i;
+                            uint32_t r[kPHalf];
 #pragma unroll
-                            for (int c0 = wg * kPHalf; c0 < (wg + 1) * kPHalf; c0 += 16) {
-                                uint32_t r[16];
-                                tmem_ld16(lane + Lay::t_st + mb * P + c0, r);
-                                tmem_ld_wait();
-                                if (sidx < S) {
+                            for (int c = 0; c < kPHalf; c += 16)
+                                tmem_ld16(lane + Lay::t_st + mb * P + c0w + c,
+                                          *reinterpret_cast<uint32_t(*)[16]>(r + c));
+                            tmem_ld_wait();
+                            if (sidx < S) {
 #pragma unroll
-                                    for (int j = 0; j < 16; ++j)
-                                        __stcg(dst + (int64_t)(c0 + j) * S + sidx,
-                                               __uint_as_float(r[j]));
-                                }
+                                for (int j = 0; j < kPHalf; ++j)
+                                    __stcg(dst + (int64_t)(c0w + j) * S + sidx,
+                                           __uint_as_float(r[j]));
                             }
                         }
                     }
                     if (handoff) {
                         __threadfence();
-                        atomicAdd(prm.seg_count + bh * prm.n_seg + chunk, 1u);
+                        __syncwarp();
+                        if ((tid & 31) == 0)
+                            atomicAdd(prm.seg_count + bh * prm.n_seg + chunk, 1u);
                     }
                 }
             }
@@ -648,7 +782,7 @@ int sm_count()
 
 template <int P, int S, int STAGES, int MODE>
 cudaError_t launch_cfg(const CUtensorMap &tx, const CUtensorMap &tb, const CUtensorMap &tcm,
-                       const Params &prm, cudaStream_t st)
+                       const CUtensorMap &ty, const Params &prm, cudaStream_t st)
 {
     using Lay = CoLayout<P, S, STAGES>;
     const size_t smem = Lay::bytes + 1024;
@@ -656,23 +790,23 @@ cudaError_t launch_cfg(const CUtensorMap &tx, const CUtensorMap &tb, const CUten
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    const int64_t grid = min64(prm.n_items, (int64_t)sm_count());
-    k<<<(unsigned)grid, kThreads, smem, st>>>(tx, tb, tcm, prm);
+    const int grid = prm.n_items < sm_count() ? prm.n_items : sm_count();
+    k<<<(unsigned)grid, kThreads, smem, st>>>(tx, tb, tcm, ty, prm);
     note_launch();
     return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtensorMap &tcm,
-                     const Params &prm, cudaStream_t st)
+                     const CUtensorMap &ty, const Params &prm, cudaStream_t st)
 {
     const Geom &g = prm.g;
     if (g.P == 64 && g.S == 64)
-        return launch_cfg<64, 64, 3, MODE>(tx, tb, tcm, prm, st);
+        return launch_cfg<64, 64, 3, MODE>(tx, tb, tcm, ty, prm, st);
     if (g.P == 64 && g.S == 128)
-        return launch_cfg<64, 128, 2, MODE>(tx, tb, tcm, prm, st);
+        return launch_cfg<64, 128, 2, MODE>(tx, tb, tcm, ty, prm, st);
     if (g.P == 64 && g.S == 256)
-        return launch_cfg<64, 256, 1, MODE>(tx, tb, tcm, prm, st);
+        return launch_cfg<64, 256, 1, MODE>(tx, tb, tcm, ty, prm, st);
     return cudaErrorNotSupported;
 }
 
@@ -680,7 +814,7 @@ cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtenso
 // about eight per SM, so the persistent CTAs end within one item of each
 // other; no segment shorter than two tiles.
 struct SegPlan {
-    int64_t seg_tiles;
+    int seg_tiles;
     int n_seg;
     size_t state_bytes, count_bytes;
 };
@@ -694,7 +828,7 @@ SegPlan seg_plan(const Geom &g)
     want = want < 1 ? 1 : want;
     if (want > (n_tiles + 1) / 2)
         want = (n_tiles + 1) / 2 < 1 ? 1 : (n_tiles + 1) / 2;
-    sp.seg_tiles = (n_tiles + want - 1) / want;
+    sp.seg_tiles = (int)((n_tiles + want - 1) / want);
     sp.n_seg = (int)((n_tiles + sp.seg_tiles - 1) / sp.seg_tiles);
     sp.state_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg * g.P * g.S) * sizeof(float) : 0;
     sp.count_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg) * sizeof(unsigned int) : 0;
@@ -715,18 +849,20 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
     prm.h_src = h_src;
     prm.states_out = states_out;
     prm.final_state = final_state;
-    prm.y = static_cast<__nv_bfloat16 *>(y);
     prm.g = g;
-    prm.n_tiles = (g.L + kTile - 1) / kTile;
-    prm.tiles_per_chunk = g.T / kTile;
-    prm.n_items = g.B * g.nc * g.H;
+    prm.n_tiles = (int)((g.L + kTile - 1) / kTile);
+    prm.tpc_shift = g.T == 2 * kTile ? 1 : 0;
+    prm.H = (int)g.H;
+    prm.nc = (int)g.nc;
+    prm.nbh = (int)(g.B * g.H);
+    prm.n_items = (int)(g.B * g.nc * g.H);
     prm.seg_tiles = prm.n_tiles;
     prm.n_seg = 1;
     if (mode == kModeFused) {
         const SegPlan sp = seg_plan(g);
         prm.seg_tiles = sp.seg_tiles;
         prm.n_seg = sp.n_seg;
-        prm.n_items = g.B * g.H * sp.n_seg;
+        prm.n_items = (int)(g.B * g.H * sp.n_seg);
         if (sp.n_seg > 1) {
             const size_t off = (sp.state_bytes + 255) / 256 * 256;
             if (!scratch || scratch_bytes < off + sp.count_bytes)
@@ -741,12 +877,12 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
     prm.status = device_status_word();
     if (!prm.status)
         return cudaErrorUnknown;
-    CUtensorMap tx, tb, tcm;
+    CUtensorMap tx, tb, tcm, ty;
     if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g) ||
-        !make_tmap_tokens_groups(&tcm, Cm, g))
+        !make_tmap_tokens_groups(&tcm, Cm, g) || !make_tmap_tokens_heads(&ty, y, g))
         return cudaErrorInvalidValue;
-    return mode == kModeOut ? dispatch<kModeOut>(tx, tb, tcm, prm, st)
-                            : dispatch<kModeFused>(tx, tb, tcm, prm, st);
+    return mode == kModeOut ? dispatch<kModeOut>(tx, tb, tcm, ty, prm, st)
+                            : dispatch<kModeFused>(tx, tb, tcm, ty, prm, st);
 }
 
 }  // namespace
@@ -754,8 +890,10 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
 bool chunk_tc_supported(const Geom &g)
 {
     const bool shape = g.P == 64 && (g.S == 64 || g.S == 128 || g.S == 256);
-    return shape && g.T % kTile == 0 && g.L > 0 && g.L < (1LL << 31) && g.H <= 65535 &&
-           g.G <= 65535 && g.B <= 65535;
+    // work items and tile indices are 32-bit in the kernel
+    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+    return shape && (g.T == kTile || g.T == 2 * kTile) && g.L > 0 && g.L < (1LL << 31) &&
+           g.H <= 65535 && g.G <= 65535 && g.B <= 65535 && g.B * g.H * n_tiles < (1LL << 31);
 }
 
 cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,

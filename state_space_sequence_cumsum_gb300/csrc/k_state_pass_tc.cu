@@ -99,9 +99,9 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 128);
+            mbar_init(&bar_empty[s], 4);  // one arrival per compute warp
         }
-        mbar_init(&bar_ready, 128);
+        mbar_init(&bar_ready, 4);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
     }
@@ -209,7 +209,9 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bar_empty[s]);
+            __syncwarp();
+            if ((tid & 31) == 0)
+                mbar_arrive(&bar_empty[s]);
 
             // chunk start: store h (the state before this chunk), then decay it
             const bool emit = states && s_ok && (tau % g.T == 0);
@@ -230,7 +232,9 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&bar_ready);
+            __syncwarp();
+            if ((tid & 31) == 0)
+                mbar_arrive(&bar_ready);
             if (!mbar_wait(&bar_mma, (uint32_t)(i & 1))) {
                 atomicOr(status, 1u);
                 break;
