@@ -154,8 +154,12 @@ def profiled_traffic(kernel: str, workload: str):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms.  The sampler
+    is started before the timed region (and waited for until it has written
+    its first line); the summary keeps the samples whose timestamps fall in
+    the marked region, or the two nearest ones if the region is shorter than
+    the sampling interval."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -163,6 +167,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -170,14 +175,24 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            deadline = time.time() + 5.0
+            while time.time() < deadline and os.path.getsize(self.path) == 0:
+                time.sleep(0.01)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(0.05)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -187,72 +202,65 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not self.path:
             return None
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    samples.append((ts, float(parts[2]), float(parts[3]),
+                                    [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
+                except (ValueError, IndexError):
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
         os.unlink(self.path)
-        if not sm:
+        if not samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        t0, t1 = self.t0 or samples[0][0], self.t1 or samples[-1][0]
+        inside = [s for s in samples if t0 <= s[0] <= t1]
+        if not inside:  # region shorter than the interval: the nearest samples
+            inside = sorted(samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:2]
+        return {"sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": sorted({r for s in inside for r in s[3]}), "samples": len(inside)}
 
 
 # ------------------------------------------------------------------ oracle leg
 
-def oracle_sample(inp, s: Shape, pairs: int, threads: int):
-    """Run the float64 oracle on the first `pairs` (batch, head) pairs for the
-    full sequence; return (seconds, head-tokens processed)."""
+def oracle_row(inp, s: Shape, b: int, threads: int):
+    """Run the float64 oracle on batch row b (every head, the full sequence);
+    return (seconds, tokens processed)."""
     import oracle
-    H = s.nheads
-    hpg = H // s.ngroups
-    done, t = 0, 0.0
-    b = 0
-    while done < pairs and b < s.batch:
-        k = min(H, pairs - done)
-        heads = list(range(k))
-        groups = sorted({h // hpg for h in heads})
-        heads = [h for g in groups for h in range(g * hpg, (g + 1) * hpg)][:max(k, hpg)]
-        idx, gidx = torch.tensor(heads), torch.tensor(groups)
-        x = inp["x"][b:b + 1, :, idx]
-        dt = inp["dt"][b:b + 1, :, idx]
-        Bm, Cm = inp["B"][b:b + 1, :, gidx], inp["C"][b:b + 1, :, gidx]
-        init = None if inp["init"] is None else inp["init"][b:b + 1, idx]
-        args = [oracle._f64(v) for v in (x, dt, inp["A"][idx], Bm, Cm, inp["D"][idx])]
-        init = oracle._f64(init)
-        t0 = time.perf_counter()
-        oracle.fwd(*args, s.chunk_size, init=init, nthreads=threads)
-        t += time.perf_counter() - t0
-        done += len(heads)
-        b += 1
-    return t, done * s.seqlen
+    sl = slice(b, b + 1)
+    args = [oracle._f64(v) for v in (inp["x"][sl], inp["dt"][sl], inp["A"], inp["B"][sl],
+                                     inp["C"][sl], inp["D"])]
+    init = oracle._f64(None if inp["init"] is None else inp["init"][sl])
+    t0 = time.perf_counter()
+    oracle.fwd(*args, s.chunk_size, init=init, nthreads=threads)
+    return time.perf_counter() - t0, s.seqlen
 
 
-def cpu_baseline(inp, s: Shape, budget_s: float = 15.0):
+def cpu_baseline(inp, s: Shape, budget_s: float = 12.0):
+    """The oracle as it stands on the host cores, on a bounded sample: whole
+    batch rows (all heads, the full sequence) in turn until about budget_s
+    seconds of wall time have been spent."""
     import oracle
     oracle.build()
     threads = oracle.cpu_cores()
-    pairs = max(1, min(threads, s.batch * s.nheads))
-    t, head_tokens = oracle_sample(inp, s, pairs, threads)
-    # grow the sample toward ~budget_s of CPU work
-    while t < budget_s / 4 and pairs < s.batch * s.nheads:
-        pairs = min(s.batch * s.nheads, pairs * 4)
-        t, head_tokens = oracle_sample(inp, s, pairs, threads)
-    tokens = head_tokens / s.nheads  # a token is all heads of one position
-    return {"value": tokens / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": (f"float64 recurrence over {head_tokens // s.seqlen} (batch, head) pairs "
-                       f"x {s.seqlen} tokens = {tokens:.0f} full-width tokens in {t:.2f} s")}
+    t_acc, tokens, rows = 0.0, 0, 0
+    while t_acc < budget_s:
+        t, n = oracle_row(inp, s, rows % s.batch, threads)
+        t_acc += t
+        tokens += n
+        rows += 1
+    return {"value": round(tokens / t_acc, 1), "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"float64 recurrence, {rows} batch rows (all {s.nheads} heads x "
+                       f"{s.seqlen} tokens each, rows of the {s.batch}-row workload taken in "
+                       f"turn) = {tokens} tokens in {t_acc:.2f} s wall")}
 
 
 # ------------------------------------------------------------------ our arm
@@ -308,12 +316,14 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        clk.mark_start()
         t_wall0 = time.perf_counter()
         for k in range(args.steps):
             flush.fill_(float(k))
             step(events=ev[k])
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
+        clk.mark_end()
     if ws > 1:
         torch.distributed.barrier()
     launches = lib.ssd_launch_count() - launches0
@@ -429,14 +439,13 @@ def run_reference(args):
     shape, dtype, init, want_states = WORKLOADS[args.workload]
     inp = make_inputs(shape, dtype=dtype, init=init, seed=0)
     threads = oracle.cpu_cores()
-    pairs = max(1, min(threads, shape.batch * shape.nheads))
-    for _ in range(max(1, args.warmup)):
-        oracle_sample(inp, shape, pairs, threads)
+    for k in range(max(1, args.warmup)):
+        oracle_row(inp, shape, k % shape.batch, threads)
     times, toks = [], 0
-    for _ in range(args.steps):
-        t, ht = oracle_sample(inp, shape, pairs, threads)
+    for k in range(args.steps):
+        t, n = oracle_row(inp, shape, k % shape.batch, threads)
         times.append(t)
-        toks = ht / shape.nheads
+        toks = n
     sec = statistics.mean(times)
     value = toks / sec
     line = {
@@ -449,9 +458,9 @@ def run_reference(args):
                    "ngroups": shape.ngroups, "chunk_size": shape.chunk_size},
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle",
-                         "sample": (f"each step: float64 recurrence over {pairs} (batch, head) "
-                                    f"pairs x {shape.seqlen} tokens ({toks:.0f} full-width "
-                                    "tokens)")},
+                         "sample": (f"each step: float64 recurrence over one batch row of the "
+                                    f"workload (all {shape.nheads} heads x {shape.seqlen} "
+                                    f"tokens = {toks} tokens), rows taken in turn")},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
