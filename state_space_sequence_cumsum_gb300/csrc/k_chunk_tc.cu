@@ -44,6 +44,9 @@
 //              consumed, this warp stores it and then frees the stage.
 // Every wait is bounded; a timeout sets the kernel status word and the role
 // leaves its loop.
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 #include "ssd_internal.h"
 #include "tc05.cuh"
@@ -144,74 +147,6 @@ __device__ __forceinline__ Item decode_item(const Params &p, int item)
     it.bh = it.b * p.H + it.h;
     return it;
 }
-
-__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p)
-{
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// A load the compiler may not sink to its first use: the next tile's G / dt
-// words are fetched while the current tile runs.
-__device__ __forceinline__ float ld_early(const float *p)
-{
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void tma4(void *dst, const void *tmap, uint64_t *bar, int c0, int c1,
-                                     int c2, int c3)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-        : "memory");
-}
-
-// TMA store of a swizzled shared-memory box; rows past the tensor's end are
-// not written.
-__device__ __forceinline__ void tma4_store(const void *tmap, const void *src, int c0, int c1,
-                                           int c2, int c3)
-{
-    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group"
-                 " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(tmap),
-                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// the shared-memory source of every committed store has been read
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// every committed store has completed
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// One arrival per warp: the warp's lanes are synchronised (which orders
-// their earlier shared-memory and TMEM work before lane 0's release).
-__device__ __forceinline__ void warp_arrive(uint64_t *bar)
-{
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0)
-        mbar_arrive(bar);
-}
-
-// Descriptors are built once per buffer and stepped by adding the byte
-// offset >> 4 to the start-address field (shared memory < 256 KB, so the
-// 14-bit field never carries).
-// K-major operand (rows x K, 64 K-elements per 128-byte row, one region per
-// 64 K): base descriptor, and the step to the 16-wide K slice ks.
-__device__ __forceinline__ uint64_t desc_k0(uint32_t base) { return smem_desc(base, 16, 1024); }
-__device__ __forceinline__ uint64_t desc_k(uint64_t d0, uint32_t region_bytes, int ks)
-{
-    return d0 + (((ks >> 2) * region_bytes + (ks & 3) * 32) >> 4);
-}
-// MN-major operand (one 128-byte row of 64 M/N elements per K index).
-__device__ __forceinline__ uint64_t desc_mn0(uint32_t base) { return smem_desc(base, kRegion, 1024); }
-__device__ __forceinline__ uint64_t desc_mn(uint64_t d0, int ks) { return d0 + ((ks * 2048) >> 4); }
-
-__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 template <int P, int S, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -903,8 +838,18 @@ cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, c
     return run(kModeOut, x, Bm, Cm, dtT, Gc, D, states, nullptr, nullptr, y, g, nullptr, 0, st);
 }
 
+namespace {
+bool use_pair(const Geom &g)
+{
+    const char *env = getenv("SSD_FUSED_KERNEL");
+    return pair_tc_supported(g) && !(env && strcmp(env, "single") == 0);
+}
+}  // namespace
+
 size_t fused_tc_scratch_bytes(const Geom &g)
 {
+    if (use_pair(g))
+        return pair_tc_scratch_bytes(g);
     const SegPlan sp = seg_plan(g);
     if (sp.n_seg <= 1)
         return 0;
@@ -916,6 +861,9 @@ cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const
                             float *final_state, void *y, const Geom &g, void *scratch,
                             size_t scratch_bytes, cudaStream_t st)
 {
+    if (use_pair(g))
+        return launch_fused_pair_tc(x, Bm, Cm, dtT, Gc, D, init, states, final_state, y, g,
+                                    scratch, scratch_bytes, st);
     return run(kModeFused, x, Bm, Cm, dtT, Gc, D, init, states, final_state, y, g, scratch,
                scratch_bytes, st);
 }

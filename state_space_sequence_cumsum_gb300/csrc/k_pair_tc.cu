@@ -1,0 +1,831 @@
+// Fused SSD forward (state pass + chunk output) for TWO heads of one B/C
+// group per CTA, on tensor cores, bf16 inputs, headdim 64, dstate 64 or 128.
+//
+// "Accelerating Mamba-2 forward-pass kernels with CUDA Tile (cuTile)",
+// section "Kernel 2: fwd_pass_state" (state jump) and section
+// "Kernel 3: compute_out":
+//     Y = exp2(G) * (C h_c^T) + (exp2(G_i - G_j) * (C B^T) * M)(dt * X) + D X,
+//     h <- exp2(G_last) h + X^T (B * dt * exp2(G_last - G)).
+//
+// Heads of one group share B and C, so a CTA that carries two of them loads
+// each B / C tile once and computes C B^T once.  Per 128-token tile and head,
+// with g = G relative to the chunk start (non-increasing) and a reference
+// g_ref inside the tile's range,
+//     exp2(g_i - g_j) dt_j = exp2(g_i - g_ref) * [dt_j exp2(g_ref - g_j)]
+// splits the decay into a row factor and a column factor.  With g_ref the
+// midpoint of the tile's range both factors stay within 2^(range/2), so for
+// every tile whose range is at most kRefRange (log2 units) the score matrix
+// is the masked C B^T itself -- the same for both heads -- and
+//     Y_k   = D x / r  +  C H_k^T  +  (M * C B^T) X_hat_k      (one accumulator)
+//     y_k,i = r_i Y_k,i,      r_i = exp2(g_i - g_ref)
+// with X_hat_k = dt exp2(g_ref - g) x_k and H_k = bf16(exp2(g_ref) h_k).  The
+// state jump uses the same X_hat: h_end = exp2(g_L - g_ref) [exp2(g_ref) h +
+// B^T X_hat]; the factor exp2(g_L - g_ref) is kept as a pending scalar and
+// applied when the state is next read.  Both heads' contractions then run as
+// single N = 128 MMAs: C [H_0 | H_1]^T, B^T [X_hat_0 | X_hat_1] (bf16 hi + lo
+// passes, so the carried state keeps ~16 mantissa bits) and
+// (M * C B^T) [X_hat_0 | X_hat_1].
+//
+// A tile whose range exceeds kRefRange for a head (a very fast-decaying head)
+// takes the exact per-element form for that head: its scores
+// CB_ij exp2(g_i - g_j) dt_j are built in a TMEM region of their own and
+// multiply the raw x, the state reference is g_L, and its Y accumulator is
+// rescaled by exp2(g_i) (plus D x) before the score product is added.
+//
+// Roles (one CTA per SM, persistent over (batch, head pair, segment) items):
+//   warps 0-3 / 4-7  warpgroup k owns head k of the pair: thread i owns tile
+//                    row / TMEM lane i for X_hat, the state, and the output;
+//                    the shared scores are split between the warpgroups by keys;
+//   warp 8           TMA loads: x of each head as soon as its X_hat is built,
+//                    B and C as soon as the tile's MMAs that read them are done
+//                    (single-buffered: the loads overlap the rest of the tile);
+//   warp 9           MMA issue;
+//   warp 10          TMA store of y (staged in the H buffers).
+// Every wait is bounded; a timeout sets the kernel status word and the role
+// leaves its loop.
+#include "common.cuh"
+#include "ssd_internal.h"
+#include "tc05.cuh"
+
+namespace ssd {
+namespace {
+using namespace tc;
+
+constexpr int kTile = 128;
+constexpr int kWarps = 8;  // compute warps; warpgroup k owns head k
+constexpr int kThreads = kWarps * 32 + 96;
+constexpr uint32_t kRegion = 128 * 128;  // 128 rows of 128 bytes (64 bf16)
+// Tiles whose decay range (log2 units) is at most this take the factorized
+// form: both factors stay within 2^80, far inside the f32 / bf16 range.
+constexpr float kRefRange = 160.f;
+
+template <int S>
+struct PairLayout {
+    static constexpr int kSReg = S / 64;  // 64-wide dstate regions of B / C
+    static constexpr uint32_t kB = kSReg * kRegion;
+    static constexpr uint32_t off_b = 0, off_c = kB;
+    static constexpr uint32_t off_x = 2 * kB;                // x of head 0, head 1
+    static constexpr uint32_t off_xh = off_x + 2 * kRegion;  // X_hat hi0, hi1, lo0, lo1
+    static constexpr uint32_t off_h = off_xh + 4 * kRegion;  // H0, H1 (MN-major [s][p]); y staging
+    static constexpr uint32_t off_g = off_h + 2 * kRegion;   // [parity][head][g 128 | dt 128] f32
+    static constexpr uint32_t bytes = off_g + 2 * 2 * 256 * 4;
+    // TMEM columns: CB (f32), shared masked scores (bf16 pairs), Y of both
+    // heads, the f32 states h^T [S, P] of both heads, one wide-score region
+    static constexpr uint32_t t_cb = 0, t_sc = 128, t_y = 192, t_st = 320, t_wide = 448;
+    static_assert(S == 64 || S == 128, "state rows fit one 128-lane TMEM block");
+    static_assert(bytes + 1024 + 512 <= 232448, "shared memory budget");
+};
+
+struct PairParams {
+    const float *dtT, *Gc, *D, *init;
+    float *states_out, *final_state;
+    Geom g;
+    int n_items, n_tiles, tpc_shift;
+    int batch, H, npairs, hpg;
+    // each (batch, head) sequence is split into n_seg segments of seg_tiles
+    // tiles; segment k > 0 starts from the state segment k-1 leaves in
+    // seg_state, published by seg_count reaching 4 (one count per warp).
+    int seg_tiles, n_seg;
+    float *seg_state;         // [B*H*n_seg][P][S]
+    unsigned int *seg_count;  // [B*H*n_seg], zero at launch
+    unsigned int *status;
+};
+
+struct PItem {
+    int b, h0, grp, t0, t1, seg;
+};
+
+// Segment-major: every segment k of every head pair comes before any
+// segment k+1, so a segment's predecessor is always an earlier item.
+__device__ __forceinline__ PItem decode_pair(const PairParams &p, int item)
+{
+    PItem w;
+    const unsigned per_seg = (unsigned)(p.batch * p.npairs);
+    const unsigned seg = (unsigned)item / per_seg, r = (unsigned)item % per_seg;
+    w.b = (int)(r / (unsigned)p.npairs);
+    w.h0 = 2 * (int)(r % (unsigned)p.npairs);
+    w.grp = w.h0 / p.hpg;
+    w.seg = (int)seg;
+    w.t0 = w.seg * p.seg_tiles;
+    w.t1 = min(w.t0 + p.seg_tiles, p.n_tiles);
+    return w;
+}
+
+template <int S>
+__global__ void __launch_bounds__(kThreads, 1)
+pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
+               const PairParams prm)
+{
+    using Lay = PairLayout<S>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // TMA landed: B and C; x of head k
+    __shared__ uint64_t bar_bc, bar_x[2];
+    // MMA completions: CB; Y2; Y2 + state jump (B / C / X_hat free); Y1 (Y complete)
+    __shared__ uint64_t bar_cb, bar_y2, bar_ds, bar_y;
+    // compute warps (8 arrivals): X_hat + D x + modes; H + decayed state;
+    // scores (+ wide rescale); y staged
+    __shared__ uint64_t bar_xh, bar_h, bar_sc, bar_ys;
+    // the y store has read the H buffers
+    __shared__ uint64_t bar_hfree;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_mode[2][2];  // [tile parity][head]: 1 = factorized
+
+    const Geom &g = prm.g;
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    if (tid == 0) {
+        mbar_init(&bar_bc, 1);
+        mbar_init(&bar_x[0], 1);
+        mbar_init(&bar_x[1], 1);
+        mbar_init(&bar_cb, 1);
+        mbar_init(&bar_y2, 1);
+        mbar_init(&bar_ds, 1);
+        mbar_init(&bar_y, 1);
+        mbar_init(&bar_xh, kWarps);
+        mbar_init(&bar_h, kWarps);
+        mbar_init(&bar_sc, kWarps);
+        mbar_init(&bar_ys, kWarps);
+        mbar_init(&bar_hfree, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const bool want_final = prm.final_state != nullptr;
+
+    if (warp == 8) {
+        // ---------------- TMA loads.  The tile-it loads wait for tile it-1 to
+        // release each buffer: x of a factorized head once its X_hat is built,
+        // x of a wide head once its score product is done, B / C once CB, Y2
+        // and the state jump are done.
+        if ((tid & 31) == 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_b);
+            prefetch_tmap(&tm_c);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const PItem w = decode_pair(prm, item);
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
+                    const int tok = t * kTile;
+                    auto load_x = [&](int k) {
+                        mbar_arrive_expect_tx(&bar_x[k], kRegion);
+                        tma4(smem + Lay::off_x + k * kRegion, &tm_x, &bar_x[k], 0, w.h0 + k, tok, w.b);
+                    };
+                    auto load_bc = [&]() {
+                        mbar_arrive_expect_tx(&bar_bc, 2 * Lay::kB);
+                        for (int r = 0; r < Lay::kSReg; ++r) {
+                            tma4(smem + Lay::off_b + r * kRegion, &tm_b, &bar_bc, r * 64, w.grp, tok, w.b);
+                            tma4(smem + Lay::off_c + r * kRegion, &tm_c, &bar_bc, r * 64, w.grp, tok, w.b);
+                        }
+                    };
+                    if (it == 0) {
+                        load_x(0);
+                        load_x(1);
+                        load_bc();
+                        continue;
+                    }
+                    const uint32_t pp = (it - 1) & 1;
+                    if (!mbar_wait(&bar_xh, pp)) {
+                        ok = false;
+                        break;
+                    }
+                    const int m0 = s_mode[pp][0], m1 = s_mode[pp][1];
+                    if (m0)
+                        load_x(0);
+                    if (m1)
+                        load_x(1);
+                    if (!mbar_wait(&bar_ds, pp)) {
+                        ok = false;
+                        break;
+                    }
+                    load_bc();
+                    if (!m0 || !m1) {
+                        if (!mbar_wait(&bar_y, pp)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!m0)
+                            load_x(0);
+                        if (!m1)
+                            load_x(1);
+                    }
+                }
+            }
+            if (!ok)
+                atomicOr(prm.status, 1u);
+        }
+    } else if (warp == 9) {
+        // ---------------- MMA issue.  Per tile: CB; Y2 (both heads); the state
+        // jump (both heads, hi + lo); then Y1 once the scores are ready.
+        if ((tid & 31) == 0) {
+            const uint32_t id_cb = idesc_bf16(128, 128, false, false);
+            const uint32_t id_y2 = idesc_bf16(128, 128, false, true);  // H is MN-major
+            const uint32_t id_ds = idesc_bf16(128, 128, true, true);   // B^T, X_hat MN-major
+            const uint32_t id_y1p = idesc_bf16(128, 128, false, true);  // A (scores) from TMEM
+            const uint32_t id_y1h = idesc_bf16(128, 64, false, true);
+            const uint64_t d_bk = desc_k0(smem_u32(smem + Lay::off_b));
+            const uint64_t d_ck = desc_k0(smem_u32(smem + Lay::off_c));
+            const uint64_t d_bmn = desc_mn0(smem_u32(smem + Lay::off_b), kRegion);
+            const uint64_t d_h = desc_mn0(smem_u32(smem + Lay::off_h), kRegion);
+            const uint64_t d_hi = desc_mn0(smem_u32(smem + Lay::off_xh), kRegion);
+            const uint64_t d_lo = desc_mn0(smem_u32(smem + Lay::off_xh + 2 * kRegion), kRegion);
+            const uint64_t d_x = desc_mn0(smem_u32(smem + Lay::off_x), kRegion);
+            constexpr uint32_t kStep = kRegion >> 4;  // one region in descriptor units
+            uint32_t it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const PItem w = decode_pair(prm, item);
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
+                    const bool last_seq = t + 1 == prm.n_tiles;
+                    const bool do_state = !last_seq || want_final;
+                    const uint32_t par = it & 1;
+                    // CB overwrites the previous tile's CB, whose conversion
+                    // ended before that tile's Y1 was issued
+                    if (!mbar_wait(&bar_bc, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < S / 16; ++ks)
+                        mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
+                               id_cb, ks > 0);
+                    mma_commit(&bar_cb);
+                    if (!mbar_wait(&bar_xh, par) || !mbar_wait(&bar_h, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // Y += C [H_0 | H_1]^T  (Y holds D x / r, or zero for a wide head)
+#pragma unroll
+                    for (int ks = 0; ks < S / 16; ++ks)
+                        mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2, 1u);
+                    mma_commit(&bar_y2);
+                    if (do_state) {
+#pragma unroll
+                        for (int part = 0; part < 2; ++part)
+#pragma unroll
+                            for (int ks = 0; ks < kTile / 16; ++ks)
+                                mma_ss(tmem + Lay::t_st, desc_mn(d_bmn, ks),
+                                       desc_mn(part ? d_lo : d_hi, ks), id_ds, 1u);
+                    }
+                    mma_commit(&bar_ds);
+                    if (!mbar_wait(&bar_sc, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int m0 = s_mode[par][0], m1 = s_mode[par][1];
+                    if (m0 && m1) {
+#pragma unroll
+                        for (int ks = 0; ks < kTile / 16; ++ks)
+                            mma_ts(tmem + Lay::t_y, tmem + Lay::t_sc + ks * 8, desc_mn(d_hi, ks),
+                                   id_y1p, 1u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const int mk = k ? m1 : m0;
+                            // a wide head 0 uses the shared region when head 1 is wide too
+                            const uint32_t a = mk ? Lay::t_sc : ((k == 0 && !m1) ? Lay::t_sc : Lay::t_wide);
+                            const uint64_t bd = (mk ? d_hi : d_x) + k * kStep;
+#pragma unroll
+                            for (int ks = 0; ks < kTile / 16; ++ks)
+                                mma_ts(tmem + Lay::t_y + 64 * k, tmem + a + ks * 8, desc_mn(bd, ks),
+                                       id_y1h, 1u);
+                        }
+                    }
+                    mma_commit(&bar_y);
+                }
+            }
+            if (!ok)
+                atomicOr(prm.status, 1u);
+        }
+    } else if (warp == 10) {
+        // ---------------- y store from the H buffers
+        if ((tid & 31) == 0) {
+            prefetch_tmap(&tm_y);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const PItem w = decode_pair(prm, item);
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
+                    if (!mbar_wait(&bar_ys, it & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tma4_store(&tm_y, smem + Lay::off_h, 0, w.h0, t * kTile, w.b);
+                    tma4_store(&tm_y, smem + Lay::off_h + kRegion, 0, w.h0 + 1, t * kTile, w.b);
+                    bulk_commit();
+                    bulk_wait_read();
+                    mbar_arrive(&bar_hfree);
+                }
+            }
+            bulk_wait_all();
+            if (!ok)
+                atomicOr(prm.status, 1u);
+        }
+    } else if (warp < kWarps) {
+        // ---------------- compute: warpgroup k owns head h0 + k
+        const int k = warp >> 2, q = warp & 3;
+        const int i = q * 32 + (tid & 31);
+        const int row_lo = q * 32, row_hi = q * 32 + 31;
+        const uint32_t tl = tmem_at(tmem, (uint32_t)(q * 32), 0);
+        const uint32_t ty = tl + Lay::t_y + 64 * k, tst = tl + Lay::t_st + 64 * k;
+        const bool srow = q * 32 < S;  // warp-uniform: this warp's rows are state rows
+        float *gtab_all = reinterpret_cast<float *>(smem + Lay::off_g);
+        uint8_t *sx = smem + Lay::off_x + k * kRegion;
+        uint8_t *s_hi = smem + Lay::off_xh + k * kRegion;
+        uint8_t *s_lo = smem + Lay::off_xh + (2 + k) * kRegion;
+        uint8_t *s_h = smem + Lay::off_h + k * kRegion;
+        const int tpc_mask = (1 << prm.tpc_shift) - 1;
+
+        struct Raw {
+            float base, g0, gL, gi, dti;
+        };
+        auto load_raw = [&](const PItem &w, int t) {
+            const int64_t bh = (int64_t)w.b * prm.H + w.h0 + k;
+            const float *grow = prm.Gc + bh * g.L;
+            const int tau = t * kTile;
+            const int n = min(kTile, (int)g.L - tau);
+            Raw r;
+            r.base = (t & tpc_mask) == 0 ? 0.f : ld_early(grow + tau - 1);
+            r.g0 = ld_early(grow + tau);
+            r.gL = ld_early(grow + tau + n - 1);
+            r.gi = i < n ? ld_early(grow + tau + i) : r.base;
+            r.dti = i < n ? ld_early(prm.dtT + bh * g.L + tau + i) : 0.f;
+            return r;
+        };
+        Raw nxt{};
+        PItem w_next{};
+        if ((int)blockIdx.x < prm.n_items) {
+            w_next = decode_pair(prm, blockIdx.x);
+            nxt = load_raw(w_next, w_next.t0);
+        }
+        uint32_t it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+            const PItem w = w_next;
+            const int h = w.h0 + k;
+            const int64_t bh = (int64_t)w.b * prm.H + h;
+            const float Dh = prm.D[h];
+            const bool more = item + (int)gridDim.x < prm.n_items;
+            if (more)
+                w_next = decode_pair(prm, item + gridDim.x);
+            float pend = 1.f;  // true state = pend * stored state
+            for (int t = w.t0; t < w.t1; ++t, ++it) {
+                const int tau = t * kTile;
+                const int n = min(kTile, (int)g.L - tau);
+                const bool first = t == w.t0, last_item = t + 1 == w.t1;
+                const bool last_seq = t + 1 == prm.n_tiles;
+                const bool do_state = !last_seq || want_final;
+                const Raw cur = nxt;
+                if (!last_item)
+                    nxt = load_raw(w, t + 1);
+                else if (more)
+                    nxt = load_raw(w_next, w_next.t0);
+                const float gL = cur.gL - cur.base, g0 = cur.g0 - cur.base;
+                const float gi = cur.gi - cur.base, dti = cur.dti;
+                const float range = g0 - gL;
+                const bool narrow = range <= kRefRange && range >= -kRefRange;
+                // state reference: the tile midpoint (factorized) or the last token
+                const float gref = narrow ? 0.5f * (g0 + gL) : gL;
+                const uint32_t par = it & 1;
+
+                // ---- per-head g / dt table (wide scores), mode
+                float *gtab = gtab_all + (par * 2 + k) * 256;
+                gtab[i] = gi;
+                gtab[128 + i] = dti;
+                if (i == 0)
+                    s_mode[par][k] = narrow ? 1 : 0;
+                // x landed; the previous tile's state jump and Y1 are done
+                if (!mbar_wait(&bar_x[k], par) || (it > 0 && !mbar_wait(&bar_ds, par ^ 1u))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+
+                // ---- X_hat = dt exp2(gref - g) x (hi, lo) and Y = D x / r (0 if wide)
+                {
+                    const float e = ex2_approx(gref - gi);
+                    const float wv = i < n ? dti * e : 0.f;
+                    const float dsc = narrow ? Dh * e : 0.f;
+#pragma unroll
+                    for (int c2 = 0; c2 < 4; ++c2) {
+                        uint32_t dx[16];
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int c = 2 * c2 + cc;
+                            const uint32_t off = sw128_offset(i, c);
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
+                            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const float xa = bf_lo(vv[e2]), xb = bf_hi(vv[e2]);
+                                const float a = xa * wv, bb = xb * wv;
+                                hi[e2] = pack_bf16x2(a, bb);
+                                lo[e2] = pack_bf16x2(a - bf_lo(hi[e2]), bb - bf_hi(hi[e2]));
+                                dx[8 * cc + 2 * e2] = __float_as_uint(dsc * xa);
+                                dx[8 * cc + 2 * e2 + 1] = __float_as_uint(dsc * xb);
+                            }
+                            *reinterpret_cast<uint4 *>(s_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            if (do_state)
+                                *reinterpret_cast<uint4 *>(s_lo + off) =
+                                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        }
+                        tmem_st16(ty + 16 * c2, dx);
+                    }
+                }
+                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
+                warp_arrive(&bar_xh);
+
+                // ---- a later segment waits until its predecessor published its state
+                if (first && w.seg > 0) {
+                    const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + w.seg - 1;
+                    bool ready = ld_acquire_gpu(cnt) >= 4u;
+                    const uint64_t t_start = globaltimer_ns();
+                    while (!ready) {
+                        if (globaltimer_ns() - t_start > 2000000000ull)
+                            break;
+                        __nanosleep(256);
+                        ready = ld_acquire_gpu(cnt) >= 4u;
+                    }
+                    if (!ready) {
+                        ok = false;
+                        break;
+                    }
+                }
+                // the previous tile's y store has read the H buffers
+                if (it > 0 && !mbar_wait(&bar_hfree, par ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+
+                // ---- H = bf16(hsc h) (MN-major [s][p]); stored state <- exp2(gref) h
+                {
+                    const float eref = ex2_approx(gref);
+                    const float hsc = narrow ? eref : 1.f;
+                    const float ssc = eref;
+                    const bool emit = prm.states_out && (t & tpc_mask) == 0;
+                    if (srow) {
+                        const float *src = nullptr;
+                        if (first) {
+                            if (w.seg > 0)
+                                src = prm.seg_state + ((bh * prm.n_seg + w.seg - 1) * g.P) * g.S;
+                            else if (prm.init)
+                                src = prm.init + bh * g.P * g.S;
+                        }
+                        float *emit_dst =
+                            emit ? prm.states_out + ((bh * g.nc + (t >> prm.tpc_shift)) * g.P) * g.S
+                                 : nullptr;
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            uint32_t r[16];
+                            if (first) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    r[j] = __float_as_uint(
+                                        src ? __ldcg(src + (int64_t)(16 * qq + j) * S + i) : 0.f);
+                            } else {
+                                tmem_ld16(tst + 16 * qq, r);
+                                tmem_ld_wait();
+                            }
+                            const float pv = first ? 1.f : pend;
+                            uint32_t hp[8];
+#pragma unroll
+                            for (int j = 0; j < 16; j += 2) {
+                                const float v0 = pv * __uint_as_float(r[j]);
+                                const float v1 = pv * __uint_as_float(r[j + 1]);
+                                if (emit_dst) {
+                                    emit_dst[(int64_t)(16 * qq + j) * S + i] = v0;
+                                    emit_dst[(int64_t)(16 * qq + j + 1) * S + i] = v1;
+                                }
+                                hp[j / 2] = pack_bf16x2(v0 * hsc, v1 * hsc);
+                                r[j] = __float_as_uint(v0 * ssc);
+                                r[j + 1] = __float_as_uint(v1 * ssc);
+                            }
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, 2 * qq + c)) =
+                                    make_uint4(hp[4 * c], hp[4 * c + 1], hp[4 * c + 2], hp[4 * c + 3]);
+                            if (do_state)
+                                tmem_st16(tst + 16 * qq, r);
+                        }
+                    }
+                    pend = narrow ? ex2_approx(gL - gref) : 1.f;
+                }
+                if (do_state)
+                    tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                warp_arrive(&bar_h);
+
+                // ---- scores.  Shared masked CB (keys [64k, 64k + 64) here) when a
+                // head is factorized; the exact per-element scores of a wide head.
+                if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_xh, par)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                {
+                    const int m0 = s_mode[par][0], m1 = s_mode[par][1];
+                    if (m0 || m1) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t cbv[2][16];
+#pragma unroll
+                            for (int gq = 0; gq < 2; ++gq) {
+                                const int j0 = 64 * k + 32 * half + 16 * gq;
+                                if (j0 <= row_hi)
+                                    tmem_ld16(tl + Lay::t_cb + j0, cbv[gq]);
+                            }
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int gq = 0; gq < 2; ++gq) {
+                                const int j0 = 64 * k + 32 * half + 16 * gq;
+                                uint32_t pk[8];
+                                if (j0 > row_hi) {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        pk[e] = 0u;
+                                } else if (j0 + 15 < row_lo) {  // whole group below the diagonal
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        pk[e] = pack_bf16x2(__uint_as_float(cbv[gq][2 * e]),
+                                                            __uint_as_float(cbv[gq][2 * e + 1]));
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        const int j = j0 + 2 * e;
+                                        pk[e] = pack_bf16x2(j <= i ? __uint_as_float(cbv[gq][2 * e]) : 0.f,
+                                                            j + 1 <= i ? __uint_as_float(cbv[gq][2 * e + 1]) : 0.f);
+                                    }
+                                }
+                                tmem_st8(tl + Lay::t_sc + j0 / 2, pk);
+                            }
+                        }
+                    }
+                    if (!narrow) {
+                        // exact scores CB_ij exp2(g_i - g_j) dt_j of this head, all keys
+                        const uint32_t region = (k == 0 && !m1) ? Lay::t_sc : Lay::t_wide;
+#pragma unroll 1
+                        for (int j0 = 0; j0 < kTile; j0 += 16) {
+                            uint32_t cbv[16], pk[8];
+                            if (j0 <= row_hi) {  // warp-uniform
+                                tmem_ld16(tl + Lay::t_cb + j0, cbv);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    float v2[2];
+#pragma unroll
+                                    for (int u = 0; u < 2; ++u) {
+                                        const int j = j0 + 2 * e + u;
+                                        v2[u] = j <= i ? __uint_as_float(cbv[2 * e + u]) *
+                                                             ex2_approx(gi - gtab[j]) * gtab[128 + j]
+                                                       : 0.f;
+                                    }
+                                    pk[e] = pack_bf16x2(v2[0], v2[1]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    pk[e] = 0u;
+                            }
+                            tmem_st8(tl + region + j0 / 2, pk);
+                        }
+                        // Y = exp2(g_i) (C H^T) + D x, before the score product adds on
+                        if (!mbar_wait(&bar_y2, par)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const float er = ex2_approx(gi);
+#pragma unroll
+                        for (int c2 = 0; c2 < 4; ++c2) {
+                            uint32_t yv[16];
+                            tmem_ld16(ty + 16 * c2, yv);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int cc = 0; cc < 2; ++cc) {
+                                const uint4 v = *reinterpret_cast<const uint4 *>(sx + sw128_offset(i, 2 * c2 + cc));
+                                const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int e2 = 0; e2 < 4; ++e2) {
+                                    const int o = 8 * cc + 2 * e2;
+                                    yv[o] = __float_as_uint(er * __uint_as_float(yv[o]) + Dh * bf_lo(vv[e2]));
+                                    yv[o + 1] =
+                                        __float_as_uint(er * __uint_as_float(yv[o + 1]) + Dh * bf_hi(vv[e2]));
+                                }
+                            }
+                            tmem_st16(ty + 16 * c2, yv);
+                        }
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                warp_arrive(&bar_sc);
+
+                // ---- epilogue: y = r Y, staged in this head's H buffer
+                if (!mbar_wait(&bar_y, par)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                {
+                    const float r = narrow ? ex2_approx(gi - gref) : 1.f;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t yv[32];
+                        tmem_ld16(ty + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(yv));
+                        tmem_ld16(ty + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(yv + 16));
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2)
+                                o[e2] = pack_bf16x2(r * __uint_as_float(yv[8 * c + 2 * e2]),
+                                                    r * __uint_as_float(yv[8 * c + 2 * e2 + 1]));
+                            *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, 4 * half + c)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                warp_arrive(&bar_ys);
+
+                // ---- state leaving the item: the next segment's start, or the final state
+                if (do_state && last_item) {
+                    const bool handoff = !last_seq;
+                    float *dst = handoff ? prm.seg_state + ((bh * prm.n_seg + w.seg) * g.P) * g.S
+                                         : (want_final ? prm.final_state + bh * g.P * g.S : nullptr);
+                    if (dst) {
+                        if (!mbar_wait(&bar_ds, par)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (srow) {
+#pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t r[32];
+                                tmem_ld16(tst + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(r));
+                                tmem_ld16(tst + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    __stcg(dst + (int64_t)(32 * half + j) * S + i,
+                                           pend * __uint_as_float(r[j]));
+                            }
+                        }
+                    }
+                    if (handoff) {
+                        __threadfence();
+                        __syncwarp();
+                        if ((tid & 31) == 0)
+                            atomicAdd(prm.seg_count + bh * prm.n_seg + w.seg, 1u);
+                    }
+                }
+            }
+        }
+        if (!ok)
+            atomicOr(prm.status, 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+int sm_count_pair()
+{
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0)
+            n = 1;
+    }
+    return n;
+}
+
+// Segmentation: enough (batch, head pair, segment) items for about eight
+// per SM, no segment shorter than two tiles.
+struct PairSegPlan {
+    int seg_tiles, n_seg;
+    size_t state_bytes, count_bytes;
+};
+
+PairSegPlan pair_seg_plan(const Geom &g)
+{
+    PairSegPlan sp;
+    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+    const int64_t units = g.B * (g.H / 2);
+    int64_t want = (8LL * sm_count_pair() + units - 1) / units;
+    want = want < 1 ? 1 : want;
+    if (want > (n_tiles + 1) / 2)
+        want = (n_tiles + 1) / 2 < 1 ? 1 : (n_tiles + 1) / 2;
+    sp.seg_tiles = (int)((n_tiles + want - 1) / want);
+    sp.n_seg = (int)((n_tiles + sp.seg_tiles - 1) / sp.seg_tiles);
+    const int64_t nbh = g.B * g.H;
+    sp.state_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg * g.P * g.S) * sizeof(float) : 0;
+    sp.count_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg) * sizeof(unsigned int) : 0;
+    return sp;
+}
+
+template <int S>
+cudaError_t launch_pair(const CUtensorMap &tx, const CUtensorMap &tb, const CUtensorMap &tcm,
+                        const CUtensorMap &ty, const PairParams &prm, cudaStream_t st)
+{
+    using Lay = PairLayout<S>;
+    const size_t smem = Lay::bytes + 1024;
+    auto k = pair_tc_kernel<S>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int grid = prm.n_items < sm_count_pair() ? prm.n_items : sm_count_pair();
+    k<<<(unsigned)grid, kThreads, smem, st>>>(tx, tb, tcm, ty, prm);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool pair_tc_supported(const Geom &g)
+{
+    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+    return g.P == 64 && (g.S == 64 || g.S == 128) && g.hpg % 2 == 0 &&
+           (g.T == kTile || g.T == 2 * kTile) && g.L > 0 && g.L < (1LL << 31) && g.H <= 65535 &&
+           g.G <= 65535 && g.B <= 65535 && g.B * g.H * n_tiles < (1LL << 31);
+}
+
+size_t pair_tc_scratch_bytes(const Geom &g)
+{
+    const PairSegPlan sp = pair_seg_plan(g);
+    if (sp.n_seg <= 1)
+        return 0;
+    return (sp.state_bytes + 255) / 256 * 256 + (sp.count_bytes + 255) / 256 * 256;
+}
+
+cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                                 const float *Gc, const float *D, const float *init, float *states,
+                                 float *final_state, void *y, const Geom &g, void *scratch,
+                                 size_t scratch_bytes, cudaStream_t st)
+{
+    if (!pair_tc_supported(g))
+        return cudaErrorNotSupported;
+    PairParams prm{};
+    prm.dtT = dtT;
+    prm.Gc = Gc;
+    prm.D = D;
+    prm.init = init;
+    prm.states_out = states;
+    prm.final_state = final_state;
+    prm.g = g;
+    prm.n_tiles = (int)((g.L + kTile - 1) / kTile);
+    prm.tpc_shift = g.T == 2 * kTile ? 1 : 0;
+    prm.batch = (int)g.B;
+    prm.H = (int)g.H;
+    prm.npairs = (int)(g.H / 2);
+    prm.hpg = g.hpg;
+    const PairSegPlan sp = pair_seg_plan(g);
+    prm.seg_tiles = sp.seg_tiles;
+    prm.n_seg = sp.n_seg;
+    prm.n_items = (int)(g.B * (g.H / 2) * sp.n_seg);
+    if (sp.n_seg > 1) {
+        const size_t off = (sp.state_bytes + 255) / 256 * 256;
+        if (!scratch || scratch_bytes < off + sp.count_bytes)
+            return cudaErrorInvalidValue;
+        prm.seg_state = static_cast<float *>(scratch);
+        prm.seg_count = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + off);
+        cudaError_t e = cudaMemsetAsync(prm.seg_count, 0, sp.count_bytes, st);
+        if (e != cudaSuccess)
+            return e;
+    }
+    prm.status = device_status_word();
+    if (!prm.status)
+        return cudaErrorUnknown;
+    CUtensorMap tx, tb, tcm, ty;
+    if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g) ||
+        !make_tmap_tokens_groups(&tcm, Cm, g) || !make_tmap_tokens_heads(&ty, y, g))
+        return cudaErrorInvalidValue;
+    return g.S == 64 ? launch_pair<64>(tx, tb, tcm, ty, prm, st)
+                     : launch_pair<128>(tx, tb, tcm, ty, prm, st);
+}
+
+}  // namespace ssd

@@ -58,10 +58,21 @@ cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, c
                                 const float *Gc, const float *states, const float *D, void *y,
                                 const Geom &g, cudaStream_t st);
 // Scratch the fused pass needs (segment hand-off states and counters), 0 if none.
+// The fused pass runs the head-pair kernel where it applies (see below) unless
+// SSD_FUSED_KERNEL=single selects the one-head kernel.
 size_t fused_tc_scratch_bytes(const Geom &g);
 cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                             const float *Gc, const float *D, const float *init, float *states,
                             float *final_state, void *y, const Geom &g, void *scratch,
                             size_t scratch_bytes, cudaStream_t st);
+
+// Fused forward for two heads of one B/C group per CTA (bf16, P = 64,
+// S in {64, 128}, an even number of heads per group).
+bool pair_tc_supported(const Geom &g);
+size_t pair_tc_scratch_bytes(const Geom &g);
+cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                                 const float *Gc, const float *D, const float *init, float *states,
+                                 float *final_state, void *y, const Geom &g, void *scratch,
+                                 size_t scratch_bytes, cudaStream_t st);
 
 }  // namespace ssd

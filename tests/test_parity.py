@@ -151,3 +151,56 @@ def test_repeat_calls_are_deterministic():
     y1, f1, _ = run_fwd(inp, 128, False)
     y2, f2, _ = run_fwd(inp, 128, False)
     assert torch.equal(y1, y2) and torch.equal(f1, f2)
+
+
+# ---- fused head-pair kernel: decay modes per head, segments, both kernels
+
+def _decay_case(B, L, H, S, T, dts, As, seed):
+    """Inputs whose heads have fixed dt and A, so each head's per-tile decay
+    range log2(e) * |A| * dt * 128 is known: above 160 a head takes the exact
+    per-element scores, at or below it the factorized form."""
+    inp = case_inputs(B, L, H, 64, S, 1, T, init="randn", seed=seed)
+    for h, (d, a) in enumerate(zip(dts, As)):
+        inp["dt"][:, :, h] = d
+        inp["A"][h] = a
+    return inp
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+def test_fused_kernels_every_decay_mode(kernel, monkeypatch):
+    """Head pairs (0,1) wide+narrow, (2,3) narrow+wide, (4,5) wide+wide and
+    (6,7) two narrow heads with a range of 100-150 (factorized in the pair
+    kernel, exact per-element in the one-head kernel); ragged length, init
+    state, chunk states and final state."""
+    if kernel == "single":
+        monkeypatch.setenv("SSD_FUSED_KERNEL", "single")
+    dts = [0.6, 0.01, 0.02, 0.5, 0.8, 0.4, 0.2, 0.13]
+    As = [-16.0, -2.0, -1.0, -12.0, -16.0, -9.0, -4.0, -4.0]
+    T = 256
+    inp = _decay_case(2, 1000, 8, 128, T, dts, As, seed=41)
+    y, fin, st = run_fwd(inp, T)
+    ref = oracle_run(inp, T, want_states=True)
+    assert_parity(y, ref["y"], torch.bfloat16, "y")
+    assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
+    assert_parity(st, ref["chunk_states"], torch.bfloat16, "chunk_states")
+
+
+@pytest.mark.parametrize("S", [64, 128])
+def test_pair_kernel_many_segments(S):
+    """One batch row and four heads over 4095 tokens: the fused pass splits
+    each sequence into many segments handed off through global memory."""
+    check_case(1, 4095, 4, 64, S, 1, 128, torch.bfloat16, init="randn", seed=43 + S)
+
+
+def test_pair_and_single_kernels_agree(monkeypatch):
+    inp = case_inputs(2, 2000, 6, 64, 128, 3, 256, init="randn", seed=47)
+    g = to_gpu(inp)
+    y_p, f_p, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], 256,
+                              initial_state=g["init"])
+    monkeypatch.setenv("SSD_FUSED_KERNEL", "single")
+    y_s, f_s, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], 256,
+                              initial_state=g["init"])
+    ref = oracle_run(inp, 256)
+    for y, f, nm in ((y_p, f_p, "pair"), (y_s, f_s, "single")):
+        assert_parity(y, ref["y"], torch.bfloat16, nm + " y")
+        assert_parity(f, ref["final_state"], torch.bfloat16, nm + " final")
