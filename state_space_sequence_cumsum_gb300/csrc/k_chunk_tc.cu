@@ -303,7 +303,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         break;
                     }
                     tc_fence_after();
-                    if (mbar_try_wait(&bar_scores, par)) {
+                    if (mbar_test(&bar_scores, par)) {
                         tc_fence_after();
                         issue_y1();
                         issue_ds();

@@ -12,21 +12,24 @@
 // with g = G relative to the chunk start (non-increasing) and a reference
 // g_ref inside the tile's range,
 //     exp2(g_i - g_j) dt_j = exp2(g_i - g_ref) * [dt_j exp2(g_ref - g_j)]
-// splits the decay into a row factor and a column factor.  With g_ref the
-// midpoint of the tile's range both factors stay within 2^(range/2), so for
-// every tile whose range is at most kRefRange (log2 units) the score matrix
-// is the masked C B^T itself -- the same for both heads -- and
+// splits the decay into a row factor and a column factor.  While both factors
+// stay within 2^kRefRange (log2 units) the score matrix is the masked C B^T
+// itself -- the same for both heads -- and
 //     Y_k   = D x / r  +  C H_k^T  +  (M * C B^T) X_hat_k      (one accumulator)
 //     y_k,i = r_i Y_k,i,      r_i = exp2(g_i - g_ref)
 // with X_hat_k = dt exp2(g_ref - g) x_k and H_k = bf16(exp2(g_ref) h_k).  The
 // state jump uses the same X_hat: h_end = exp2(g_L - g_ref) [exp2(g_ref) h +
-// B^T X_hat]; the factor exp2(g_L - g_ref) is kept as a pending scalar and
-// applied when the state is next read.  Both heads' contractions then run as
+// B^T X_hat].  The state is stored as S with h = exp2(lp) S and the reference
+// is normally g_ref = -lp: then exp2(g_ref) h = S, so H = bf16(S) and the
+// stored state needs no rescaling -- the jump adds B^T X_hat to S and the
+// tile's decay goes into lp (lp <- lp + g_L).  Only when an exponent would
+// leave 2^(+-kRefRange) is the scale folded into S, with g_ref at the middle
+// of the tile's range (S <- exp2(g_ref) h, lp <- g_L - g_ref).  Both heads' contractions then run as
 // single N = 128 MMAs: C [H_0 | H_1]^T, B^T [X_hat_0 | X_hat_1] (bf16 hi + lo
 // passes, so the carried state keeps ~16 mantissa bits) and
 // (M * C B^T) [X_hat_0 | X_hat_1].
 //
-// A tile whose range exceeds kRefRange for a head (a very fast-decaying head)
+// A tile whose decay exceeds kRefRange for a head (a very fast-decaying head)
 // takes the exact per-element form for that head: its scores
 // CB_ij exp2(g_i - g_j) dt_j are built in a TMEM region of their own and
 // multiply the raw x, the state reference is g_L, and its Y accumulator is
@@ -55,9 +58,10 @@ constexpr int kTile = 128;
 constexpr int kWarps = 8;  // compute warps; warpgroup k owns head k
 constexpr int kThreads = kWarps * 32 + 96;
 constexpr uint32_t kRegion = 128 * 128;  // 128 rows of 128 bytes (64 bf16)
-// Tiles whose decay range (log2 units) is at most this take the factorized
-// form: both factors stay within 2^80, far inside the f32 / bf16 range.
-constexpr float kRefRange = 160.f;
+// The factorized form is used while every row and column factor stays within
+// 2^(+-kRefRange) (log2 units), well inside the f32 / bf16 range; a tile whose
+// decay range exceeds 2 kRefRange takes the exact per-element form.
+constexpr float kRefRange = 100.f;
 
 template <int S>
 struct PairLayout {
@@ -68,7 +72,9 @@ struct PairLayout {
     static constexpr uint32_t off_xh = off_x + 2 * kRegion;  // X_hat hi0, hi1, lo0, lo1
     static constexpr uint32_t off_h = off_xh + 4 * kRegion;  // H0, H1 (MN-major [s][p]); y staging
     static constexpr uint32_t off_g = off_h + 2 * kRegion;   // [parity][head][g 128 | dt 128] f32
-    static constexpr uint32_t bytes = off_g + 2 * 2 * 256 * 4;
+    // next tile's raw G / dt words per compute thread: [parity][5][256] f32
+    static constexpr uint32_t off_raw = off_g + 2 * 2 * 256 * 4;
+    static constexpr uint32_t bytes = off_raw + 2 * 5 * 256 * 4;
     // TMEM columns: CB (f32), shared masked scores (bf16 pairs), Y of both
     // heads, the f32 states h^T [S, P] of both heads, one wide-score region
     static constexpr uint32_t t_cb = 0, t_sc = 128, t_y = 192, t_st = 320, t_wide = 448;
@@ -82,9 +88,20 @@ struct PairParams {
     Geom g;
     int n_items, n_tiles, tpc_shift;
     int batch, H, npairs, hpg;
-    // each (batch, head) sequence is split into n_seg segments of seg_tiles
-    // tiles; segment k > 0 starts from the state segment k-1 leaves in
-    // seg_state, published by seg_count reaching 4 (one count per warp).
+    // Work assignment, one of:
+    //  wrap  -- (at least as many head pairs as CTAs) all pairs' tiles laid end
+    //           to end and cut into one contiguous piece per CTA; a CTA first
+    //           runs the start of the sequence crossing its upper cut (handing
+    //           its state off), then its whole sequences, then the rest of the
+    //           sequence crossing its lower cut, which its neighbour started
+    //           first.  A piece is at least one sequence long, so the hand-off
+    //           is always complete before it is needed.
+    //  segments -- each sequence is split into n_seg segments of seg_tiles
+    //           tiles, items (pair, segment) dealt round-robin, segment-major.
+    // Segment k > 0 starts from the state segment k-1 leaves in seg_state,
+    // published by seg_count reaching 4 (one count per warp).
+    int wrap;
+    long long wrap_units;  // B * H/2 * n_tiles
     int seg_tiles, n_seg;
     float *seg_state;         // [B*H*n_seg][P][S]
     unsigned int *seg_count;  // [B*H*n_seg], zero at launch
@@ -95,20 +112,61 @@ struct PItem {
     int b, h0, grp, t0, t1, seg;
 };
 
-// Segment-major: every segment k of every head pair comes before any
-// segment k+1, so a segment's predecessor is always an earlier item.
-__device__ __forceinline__ PItem decode_pair(const PairParams &p, int item)
+__device__ __forceinline__ PItem pair_item(const PairParams &p, int q, int t0, int t1, int seg)
 {
     PItem w;
-    const unsigned per_seg = (unsigned)(p.batch * p.npairs);
-    const unsigned seg = (unsigned)item / per_seg, r = (unsigned)item % per_seg;
-    w.b = (int)(r / (unsigned)p.npairs);
-    w.h0 = 2 * (int)(r % (unsigned)p.npairs);
+    w.b = q / p.npairs;
+    w.h0 = 2 * (q % p.npairs);
     w.grp = w.h0 / p.hpg;
-    w.seg = (int)seg;
-    w.t0 = w.seg * p.seg_tiles;
-    w.t1 = min(w.t0 + p.seg_tiles, p.n_tiles);
+    w.t0 = t0;
+    w.t1 = t1;
+    w.seg = seg;
     return w;
+}
+
+// This CTA's piece [lo, hi) of the pair-major tile sequence (wrap mode).
+__device__ __forceinline__ void wrap_piece(const PairParams &p, long long &lo, long long &hi)
+{
+    lo = (long long)blockIdx.x * p.wrap_units / gridDim.x;
+    hi = (long long)(blockIdx.x + 1) * p.wrap_units / gridDim.x;
+}
+
+// Number of items this CTA runs.
+__device__ __forceinline__ int my_item_count(const PairParams &p)
+{
+    if (!p.wrap)
+        return (int)blockIdx.x < p.n_items ? (p.n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    long long lo, hi;
+    wrap_piece(p, lo, hi);
+    const long long n = p.n_tiles;
+    const long long first_full = (lo + n - 1) / n, end_full = hi / n;  // whole sequences [first_full, end_full)
+    return (int)((hi % n != 0) + (end_full - first_full) + (lo % n != 0));
+}
+
+// The j-th item of this CTA, in the order it runs them.
+__device__ __forceinline__ PItem my_item(const PairParams &p, int j)
+{
+    if (!p.wrap) {
+        // segment-major: every segment k of every head pair comes before any
+        // segment k+1, so a segment's predecessor is always an earlier item
+        const int item = (int)blockIdx.x + j * (int)gridDim.x;
+        const unsigned per_seg = (unsigned)(p.batch * p.npairs);
+        const unsigned seg = (unsigned)item / per_seg, q = (unsigned)item % per_seg;
+        const int t0 = (int)seg * p.seg_tiles;
+        return pair_item(p, (int)q, t0, min(t0 + p.seg_tiles, p.n_tiles), (int)seg);
+    }
+    long long lo, hi;
+    wrap_piece(p, lo, hi);
+    const int n = p.n_tiles;
+    const long long first_full = (lo + n - 1) / n, end_full = hi / n;
+    const int head = hi % n != 0;
+    if (head && j == 0)  // start of the sequence crossing the upper cut: hands its state off
+        return pair_item(p, (int)(hi / n), 0, (int)(hi % n), 0);
+    j -= head;
+    if (j < end_full - first_full)
+        return pair_item(p, (int)(first_full + j), 0, n, 0);
+    // rest of the sequence crossing the lower cut, from its neighbour's state
+    return pair_item(p, (int)(lo / n), (int)(lo % n), n, 1);
 }
 
 template <int S>
@@ -172,8 +230,9 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             prefetch_tmap(&tm_c);
             uint32_t it = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
-                const PItem w = decode_pair(prm, item);
+            const int n_my = my_item_count(prm);
+            for (int j = 0; j < n_my && ok; ++j) {
+                const PItem w = my_item(prm, j);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     const int tok = t * kTile;
                     auto load_x = [&](int k) {
@@ -242,8 +301,9 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             constexpr uint32_t kStep = kRegion >> 4;  // one region in descriptor units
             uint32_t it = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
-                const PItem w = decode_pair(prm, item);
+            const int n_my = my_item_count(prm);
+            for (int j = 0; j < n_my && ok; ++j) {
+                const PItem w = my_item(prm, j);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     const bool last_seq = t + 1 == prm.n_tiles;
                     const bool do_state = !last_seq || want_final;
@@ -270,6 +330,9 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     for (int ks = 0; ks < S / 16; ++ks)
                         mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2, 1u);
                     mma_commit(&bar_y2);
+                    // The state jump (hi, lo) next: with Y2 it is the last reader of
+                    // the B / C tiles, so their reload for the next tile can start as
+                    // soon as it completes; then Y1 once the scores are ready.
                     if (do_state) {
 #pragma unroll
                         for (int part = 0; part < 2; ++part)
@@ -284,23 +347,26 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
-                    const int m0 = s_mode[par][0], m1 = s_mode[par][1];
-                    if (m0 && m1) {
-#pragma unroll
-                        for (int ks = 0; ks < kTile / 16; ++ks)
-                            mma_ts(tmem + Lay::t_y, tmem + Lay::t_sc + ks * 8, desc_mn(d_hi, ks),
-                                   id_y1p, 1u);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            const int mk = k ? m1 : m0;
-                            // a wide head 0 uses the shared region when head 1 is wide too
-                            const uint32_t a = mk ? Lay::t_sc : ((k == 0 && !m1) ? Lay::t_sc : Lay::t_wide);
-                            const uint64_t bd = (mk ? d_hi : d_x) + k * kStep;
+                    {
+                        const int m0 = s_mode[par][0], m1 = s_mode[par][1];
+                        if (m0 && m1) {
 #pragma unroll
                             for (int ks = 0; ks < kTile / 16; ++ks)
-                                mma_ts(tmem + Lay::t_y + 64 * k, tmem + a + ks * 8, desc_mn(bd, ks),
-                                       id_y1h, 1u);
+                                mma_ts(tmem + Lay::t_y, tmem + Lay::t_sc + ks * 8, desc_mn(d_hi, ks),
+                                       id_y1p, 1u);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const int mk = k ? m1 : m0;
+                                // a wide head 0 uses the shared region when head 1 is wide too
+                                const uint32_t a =
+                                    mk ? Lay::t_sc : ((k == 0 && !m1) ? Lay::t_sc : Lay::t_wide);
+                                const uint64_t bd = (mk ? d_hi : d_x) + k * kStep;
+#pragma unroll
+                                for (int ks = 0; ks < kTile / 16; ++ks)
+                                    mma_ts(tmem + Lay::t_y + 64 * k, tmem + a + ks * 8,
+                                           desc_mn(bd, ks), id_y1h, 1u);
+                            }
                         }
                     }
                     mma_commit(&bar_y);
@@ -315,8 +381,9 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             prefetch_tmap(&tm_y);
             uint32_t it = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
-                const PItem w = decode_pair(prm, item);
+            const int n_my = my_item_count(prm);
+            for (int j = 0; j < n_my && ok; ++j) {
+                const PItem w = my_item(prm, j);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     if (!mbar_wait(&bar_ys, it & 1)) {
                         ok = false;
@@ -348,56 +415,86 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         uint8_t *s_h = smem + Lay::off_h + k * kRegion;
         const int tpc_mask = (1 << prm.tpc_shift) - 1;
 
+        // Raw G / dt words of a tile (the token before it, its first and last
+        // token, this row's G and dt), copied one tile ahead by cp.async into
+        // this thread's slots [parity][word][thread] so no register waits on them.
         struct Raw {
             float base, g0, gL, gi, dti;
         };
-        auto load_raw = [&](const PItem &w, int t) {
+        float *raw_all = reinterpret_cast<float *>(smem + Lay::off_raw);
+        const int ct = tid;  // compute thread index 0..255
+        auto prefetch_raw = [&](const PItem &w, int t, uint32_t buf) {
+            float *slot = raw_all + buf * 5 * 256 + ct;
             const int64_t bh = (int64_t)w.b * prm.H + w.h0 + k;
             const float *grow = prm.Gc + bh * g.L;
             const int tau = t * kTile;
             const int n = min(kTile, (int)g.L - tau);
+            if ((t & tpc_mask) == 0)
+                slot[0] = 0.f;
+            else
+                cp_async4(slot, grow + tau - 1);
+            cp_async4(slot + 256, grow + tau);
+            cp_async4(slot + 512, grow + tau + n - 1);
+            if (i < n) {
+                cp_async4(slot + 768, grow + tau + i);
+                cp_async4(slot + 1024, prm.dtT + bh * g.L + tau + i);
+            } else {  // a row past the sequence end: g = the base (relative 0), dt = 0
+                if ((t & tpc_mask) == 0)
+                    slot[768] = 0.f;
+                else
+                    cp_async4(slot + 768, grow + tau - 1);
+                slot[1024] = 0.f;
+            }
+            cp_async_commit();
+        };
+        auto read_raw = [&](uint32_t buf) {
+            cp_async_wait_all();
+            const float *slot = raw_all + buf * 5 * 256 + ct;
             Raw r;
-            r.base = (t & tpc_mask) == 0 ? 0.f : ld_early(grow + tau - 1);
-            r.g0 = ld_early(grow + tau);
-            r.gL = ld_early(grow + tau + n - 1);
-            r.gi = i < n ? ld_early(grow + tau + i) : r.base;
-            r.dti = i < n ? ld_early(prm.dtT + bh * g.L + tau + i) : 0.f;
+            r.base = slot[0];
+            r.g0 = slot[256];
+            r.gL = slot[512];
+            r.gi = slot[768];
+            r.dti = slot[1024];
             return r;
         };
-        Raw nxt{};
+        const int n_my = my_item_count(prm);
         PItem w_next{};
-        if ((int)blockIdx.x < prm.n_items) {
-            w_next = decode_pair(prm, blockIdx.x);
-            nxt = load_raw(w_next, w_next.t0);
+        if (n_my > 0) {
+            w_next = my_item(prm, 0);
+            prefetch_raw(w_next, w_next.t0, 0);
         }
         uint32_t it = 0;
         bool ok = true;
-        for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+        for (int j = 0; j < n_my && ok; ++j) {
             const PItem w = w_next;
             const int h = w.h0 + k;
             const int64_t bh = (int64_t)w.b * prm.H + h;
             const float Dh = prm.D[h];
-            const bool more = item + (int)gridDim.x < prm.n_items;
+            const bool more = j + 1 < n_my;
             if (more)
-                w_next = decode_pair(prm, item + gridDim.x);
-            float pend = 1.f;  // true state = pend * stored state
+                w_next = my_item(prm, j + 1);
+            // true state = exp2(lp) * stored state: the per-tile decay is kept as
+            // this scalar instead of rescaling the state in TMEM every tile
+            float lp = 0.f;
             for (int t = w.t0; t < w.t1; ++t, ++it) {
                 const int tau = t * kTile;
                 const int n = min(kTile, (int)g.L - tau);
                 const bool first = t == w.t0, last_item = t + 1 == w.t1;
                 const bool last_seq = t + 1 == prm.n_tiles;
                 const bool do_state = !last_seq || want_final;
-                const Raw cur = nxt;
-                if (!last_item)
-                    nxt = load_raw(w, t + 1);
-                else if (more)
-                    nxt = load_raw(w_next, w_next.t0);
+                const Raw cur = read_raw(it & 1);
                 const float gL = cur.gL - cur.base, g0 = cur.g0 - cur.base;
                 const float gi = cur.gi - cur.base, dti = cur.dti;
-                const float range = g0 - gL;
-                const bool narrow = range <= kRefRange && range >= -kRefRange;
-                // state reference: the tile midpoint (factorized) or the last token
-                const float gref = narrow ? 0.5f * (g0 + gL) : gL;
+                // Reference gref of the factorized form: keep the stored state's
+                // scale (gref = -lp) while every exponent gref - g_j, g_i - gref
+                // stays within kRefRange; else fold the scale into the state with
+                // gref at the middle of the tile's range; beyond 2 kRefRange the
+                // exact per-element form for this head (gref = g_L).
+                const float gmin = fminf(g0, gL), gmax = fmaxf(g0, gL);
+                const bool keep = !first && -lp - gmin <= kRefRange && gmax + lp <= kRefRange;
+                const bool narrow = keep || gmax - gmin <= 2.f * kRefRange;
+                const float gref = keep ? -lp : (narrow ? 0.5f * (gmin + gmax) : gL);
                 const uint32_t par = it & 1;
 
                 // ---- per-head g / dt table (wide scores), mode
@@ -472,11 +569,11 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     break;
                 }
 
-                // ---- H = bf16(hsc h) (MN-major [s][p]); stored state <- exp2(gref) h
+                // ---- H = bf16(exp2(gref) h) for the factorized form, bf16(h) for the
+                // exact one (MN-major [s][p]).  The stored state is rewritten only
+                // when its scale is folded in: S <- exp2(lp) S, times exp2(g_L) if exact.
                 {
-                    const float eref = ex2_approx(gref);
-                    const float hsc = narrow ? eref : 1.f;
-                    const float ssc = eref;
+                    const bool fold = !keep;
                     const bool emit = prm.states_out && (t & tpc_mask) == 0;
                     if (srow) {
                         const float *src = nullptr;
@@ -489,47 +586,59 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         float *emit_dst =
                             emit ? prm.states_out + ((bh * g.nc + (t >> prm.tpc_shift)) * g.P) * g.S
                                  : nullptr;
+                        const float pv = first ? 1.f : ex2_approx(lp);
+                        const float hs2 = keep ? 1.f : pv * (narrow ? ex2_approx(gref) : 1.f);
+                        const float ss2 = pv * ex2_approx(gref);
+                        // the whole 64-column state row in one TMEM round trip
+                        uint32_t r[64];
+                        if (first) {
 #pragma unroll
-                        for (int qq = 0; qq < 4; ++qq) {
-                            uint32_t r[16];
-                            if (first) {
+                            for (int j = 0; j < 64; ++j)
+                                r[j] = __float_as_uint(src ? __ldcg(src + (int64_t)j * S + i) : 0.f);
+                        } else {
+#pragma unroll
+                            for (int qq = 0; qq < 4; ++qq)
+                                tmem_ld16(tst + 16 * qq, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * qq));
+                            tmem_ld_wait();
+                        }
+                        if (emit_dst) {
+#pragma unroll
+                            for (int j = 0; j < 64; ++j)
+                                emit_dst[(int64_t)j * S + i] = pv * __uint_as_float(r[j]);
+                        }
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint32_t hp[4];
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2)
+                                hp[e2] = pack_bf16x2(hs2 * __uint_as_float(r[8 * c + 2 * e2]),
+                                                     hs2 * __uint_as_float(r[8 * c + 2 * e2 + 1]));
+                            *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, c)) =
+                                make_uint4(hp[0], hp[1], hp[2], hp[3]);
+                        }
+                        if (fold && do_state) {
+#pragma unroll
+                            for (int qq = 0; qq < 4; ++qq) {
+                                uint32_t o[16];
 #pragma unroll
                                 for (int j = 0; j < 16; ++j)
-                                    r[j] = __float_as_uint(
-                                        src ? __ldcg(src + (int64_t)(16 * qq + j) * S + i) : 0.f);
-                            } else {
-                                tmem_ld16(tst + 16 * qq, r);
-                                tmem_ld_wait();
+                                    o[j] = __float_as_uint(ss2 * __uint_as_float(r[16 * qq + j]));
+                                tmem_st16(tst + 16 * qq, o);
                             }
-                            const float pv = first ? 1.f : pend;
-                            uint32_t hp[8];
-#pragma unroll
-                            for (int j = 0; j < 16; j += 2) {
-                                const float v0 = pv * __uint_as_float(r[j]);
-                                const float v1 = pv * __uint_as_float(r[j + 1]);
-                                if (emit_dst) {
-                                    emit_dst[(int64_t)(16 * qq + j) * S + i] = v0;
-                                    emit_dst[(int64_t)(16 * qq + j + 1) * S + i] = v1;
-                                }
-                                hp[j / 2] = pack_bf16x2(v0 * hsc, v1 * hsc);
-                                r[j] = __float_as_uint(v0 * ssc);
-                                r[j + 1] = __float_as_uint(v1 * ssc);
-                            }
-#pragma unroll
-                            for (int c = 0; c < 2; ++c)
-                                *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, 2 * qq + c)) =
-                                    make_uint4(hp[4 * c], hp[4 * c + 1], hp[4 * c + 2], hp[4 * c + 3]);
-                            if (do_state)
-                                tmem_st16(tst + 16 * qq, r);
                         }
                     }
-                    pend = narrow ? ex2_approx(gL - gref) : 1.f;
+                    lp = gL - gref;
+                    if (fold && do_state)
+                        tmem_st_wait();
                 }
-                if (do_state)
-                    tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before();
                 warp_arrive(&bar_h);
+                // prefetch the next tile's G / dt while this one is processed
+                if (!last_item)
+                    prefetch_raw(w, t + 1, (it + 1) & 1);
+                else if (more)
+                    prefetch_raw(w_next, w_next.t0, (it + 1) & 1);
 
                 // ---- scores.  Shared masked CB (keys [64k, 64k + 64) here) when a
                 // head is factorized; the exact per-element scores of a wide head.
@@ -678,6 +787,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         }
                         tc_fence_after();
                         if (srow) {
+                            const float pscale = ex2_approx(lp);
 #pragma unroll
                             for (int half = 0; half < 2; ++half) {
                                 uint32_t r[32];
@@ -687,7 +797,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 #pragma unroll
                                 for (int j = 0; j < 32; ++j)
                                     __stcg(dst + (int64_t)(32 * half + j) * S + i,
-                                           pend * __uint_as_float(r[j]));
+                                           pscale * __uint_as_float(r[j]));
                             }
                         }
                     }
@@ -724,9 +834,13 @@ int sm_count_pair()
     return n;
 }
 
-// Segmentation: enough (batch, head pair, segment) items for about eight
-// per SM, no segment shorter than two tiles.
+// Work plan.  With at least one head pair per SM: the wrap schedule (one
+// contiguous piece of the pair-major tile sequence per CTA, at most one
+// hand-off slot per sequence).  Otherwise segmentation: enough (batch, head
+// pair, segment) items for about eight per SM, no segment shorter than two
+// tiles.
 struct PairSegPlan {
+    bool wrap;
     int seg_tiles, n_seg;
     size_t state_bytes, count_bytes;
 };
@@ -736,13 +850,21 @@ PairSegPlan pair_seg_plan(const Geom &g)
     PairSegPlan sp;
     const int64_t n_tiles = (g.L + kTile - 1) / kTile;
     const int64_t units = g.B * (g.H / 2);
+    const int64_t nbh = g.B * g.H;
+    sp.wrap = units >= sm_count_pair() && n_tiles > 1;
+    if (sp.wrap) {
+        sp.seg_tiles = (int)n_tiles;
+        sp.n_seg = 2;  // slot 0: the state a sequence's first part hands to its second
+        sp.state_bytes = (size_t)(nbh * 2 * g.P * g.S) * sizeof(float);
+        sp.count_bytes = (size_t)(nbh * 2) * sizeof(unsigned int);
+        return sp;
+    }
     int64_t want = (8LL * sm_count_pair() + units - 1) / units;
     want = want < 1 ? 1 : want;
     if (want > (n_tiles + 1) / 2)
         want = (n_tiles + 1) / 2 < 1 ? 1 : (n_tiles + 1) / 2;
     sp.seg_tiles = (int)((n_tiles + want - 1) / want);
     sp.n_seg = (int)((n_tiles + sp.seg_tiles - 1) / sp.seg_tiles);
-    const int64_t nbh = g.B * g.H;
     sp.state_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg * g.P * g.S) * sizeof(float) : 0;
     sp.count_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg) * sizeof(unsigned int) : 0;
     return sp;
@@ -758,10 +880,23 @@ cudaError_t launch_pair(const CUtensorMap &tx, const CUtensorMap &tb, const CUte
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    const int grid = prm.n_items < sm_count_pair() ? prm.n_items : sm_count_pair();
-    k<<<(unsigned)grid, kThreads, smem, st>>>(tx, tb, tcm, ty, prm);
+    const int grid = prm.wrap ? sm_count_pair()
+                              : (prm.n_items < sm_count_pair() ? prm.n_items : sm_count_pair());
+    // CTAs wait on each other's state hand-offs, so the grid (one CTA per SM)
+    // must be co-resident: a cooperative launch guarantees it or fails.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, k, tx, tb, tcm, ty, prm);
     note_launch();
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -777,7 +912,7 @@ bool pair_tc_supported(const Geom &g)
 size_t pair_tc_scratch_bytes(const Geom &g)
 {
     const PairSegPlan sp = pair_seg_plan(g);
-    if (sp.n_seg <= 1)
+    if (!sp.wrap && sp.n_seg <= 1)
         return 0;
     return (sp.state_bytes + 255) / 256 * 256 + (sp.count_bytes + 255) / 256 * 256;
 }
@@ -806,8 +941,10 @@ cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, 
     const PairSegPlan sp = pair_seg_plan(g);
     prm.seg_tiles = sp.seg_tiles;
     prm.n_seg = sp.n_seg;
-    prm.n_items = (int)(g.B * (g.H / 2) * sp.n_seg);
-    if (sp.n_seg > 1) {
+    prm.wrap = sp.wrap ? 1 : 0;
+    prm.wrap_units = (long long)(g.B * (g.H / 2)) * prm.n_tiles;
+    prm.n_items = (int)(g.B * (g.H / 2) * (sp.wrap ? 1 : sp.n_seg));
+    if (sp.wrap || sp.n_seg > 1) {
         const size_t off = (sp.state_bytes + 255) / 256 * 256;
         if (!scratch || scratch_bytes < off + sp.count_bytes)
             return cudaErrorInvalidValue;
