@@ -59,8 +59,9 @@ constexpr int kWarps = 8;  // compute warps; warpgroup k owns head k
 constexpr int kThreads = kWarps * 32 + 96;
 constexpr uint32_t kRegion = 128 * 128;  // 128 rows of 128 bytes (64 bf16)
 // The factorized form is used while every row and column factor stays within
-// 2^(+-kRefRange) (log2 units), well inside the f32 / bf16 range; a tile whose
-// decay range exceeds 2 kRefRange takes the exact per-element form.
+// 2^(+-kRefRange) (log2 units); a tile whose decay range exceeds 2 kRefRange
+// takes the exact per-element form.  Scale products are never formed as one
+// scalar (2^-100 * 2^-100 is below the f32 range); each factor is applied in turn.
 constexpr float kRefRange = 100.f;
 
 template <int S>
@@ -586,9 +587,12 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         float *emit_dst =
                             emit ? prm.states_out + ((bh * g.nc + (t >> prm.tpc_shift)) * g.P) * g.S
                                  : nullptr;
+                        // The pending scale and the new reference scale are applied one
+                        // after the other: their product can fall below the f32 range
+                        // even though each scaled value does not.
                         const float pv = first ? 1.f : ex2_approx(lp);
-                        const float hs2 = keep ? 1.f : pv * (narrow ? ex2_approx(gref) : 1.f);
-                        const float ss2 = pv * ex2_approx(gref);
+                        const float eref = ex2_approx(gref);
+                        const float hsc = narrow ? eref : 1.f;
                         // the whole 64-column state row in one TMEM round trip
                         uint32_t r[64];
                         if (first) {
@@ -606,6 +610,13 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             for (int j = 0; j < 64; ++j)
                                 emit_dst[(int64_t)j * S + i] = pv * __uint_as_float(r[j]);
                         }
+                        if (fold) {  // r <- the true state h
+#pragma unroll
+                            for (int j = 0; j < 64; ++j)
+                                r[j] = __float_as_uint(pv * __uint_as_float(r[j]));
+                        }
+                        // keep: H = bf16(S); fold: H = bf16(hsc h)
+                        const float hs2 = keep ? 1.f : hsc;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             uint32_t hp[4];
@@ -616,13 +627,13 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, c)) =
                                 make_uint4(hp[0], hp[1], hp[2], hp[3]);
                         }
-                        if (fold && do_state) {
+                        if (fold && do_state) {  // stored state <- exp2(gref) h
 #pragma unroll
                             for (int qq = 0; qq < 4; ++qq) {
                                 uint32_t o[16];
 #pragma unroll
                                 for (int j = 0; j < 16; ++j)
-                                    o[j] = __float_as_uint(ss2 * __uint_as_float(r[16 * qq + j]));
+                                    o[j] = __float_as_uint(eref * __uint_as_float(r[16 * qq + j]));
                                 tmem_st16(tst + 16 * qq, o);
                             }
                         }

@@ -206,3 +206,19 @@ def test_pair_and_single_kernels_agree(monkeypatch):
     for y, f, nm in ((y_p, f_p, "pair"), (y_s, f_s, "single")):
         assert_parity(y, ref["y"], torch.bfloat16, nm + " y")
         assert_parity(f, ref["final_state"], torch.bfloat16, nm + " final")
+
+
+def test_pair_kernel_fast_decay_with_noise():
+    """A head whose per-tile decay range is 130-190 (log2) with per-token dt
+    noise, next to an ordinary head, over 64 tiles: each tile folds the
+    state's scale at a reference far from the previous one, so two scale
+    factors near 2^-75 meet (their product is below the f32 range)."""
+    inp = case_inputs(1, 8192, 2, 64, 128, 1, 128, init="randn", seed=53)
+    gen = torch.Generator().manual_seed(53)
+    noise = torch.randn(1, 8192, generator=gen)
+    inp["dt"][:, :, 0] = 0.06 * torch.exp(0.15 * noise)
+    inp["A"][0] = -14.0
+    y, fin, _ = run_fwd(inp, 128, want_states=False)
+    ref = oracle_run(inp, 128)
+    assert_parity(y, ref["y"], torch.bfloat16, "y")
+    assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
