@@ -112,6 +112,9 @@ def kernel_bytes(kernel: str, s: Shape, dtype, init: str, want_states: bool) -> 
         return xb + bb + 2 * blh * 4 + init_b + states + st
     if kernel == "chunk_out":
         return xb + 2 * bb + 2 * blh * 4 + states + s.nheads * 4 + xb
+    if kernel == "fused_pair":  # the whole forward in one kernel, G formed in the kernel
+        return (xb + 2 * bb + blh * 4 + 2 * s.nheads * 4 + init_b + xb + st +
+                (states if want_states else 0))
     if kernel == "state_out":  # fused stages 2+3
         return (xb + 2 * bb + 2 * blh * 4 + s.nheads * 4 + init_b + xb + st +
                 (states if want_states else 0))

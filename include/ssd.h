@@ -139,7 +139,9 @@ typedef enum {
     SSD_PATH_INVALID = -1,
     SSD_PATH_STAGED_CUDA_CORES = 0,   /* cumsum -> state_pass -> chunk_out, f32 CUDA cores */
     SSD_PATH_STAGED_TENSOR_CORES = 1, /* cumsum -> state_pass -> chunk_out, tcgen05 */
-    SSD_PATH_FUSED_TENSOR_CORES = 2   /* cumsum -> state_out (fused), tcgen05 */
+    SSD_PATH_FUSED_TENSOR_CORES = 2,  /* cumsum -> state_out (fused), tcgen05 */
+    SSD_PATH_FUSED_PAIR_TENSOR_CORES = 3 /* one fused kernel, two heads of a group per CTA,
+                                            G formed in the kernel; tcgen05 */
 } ssd_path_t;
 ssd_path_t ssd_fwd_path(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, int want_chunk_states);
 

@@ -28,7 +28,8 @@ EXPORTS = ("ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out
            "ssd_fwd_path", "ssd_fwd_workspace_size", "ssd_fwd", "ssd_fwd_noalloc",
            "ssd_fwd_chosen_chunk_size",
            "ssd_launch_count", "ssd_status_string", "ssd_stream_status")
-PATH_NAMES = {0: "staged-cuda-cores", 1: "staged-tensor-cores", 2: "fused-tensor-cores"}
+PATH_NAMES = {0: "staged-cuda-cores", 1: "staged-tensor-cores", 2: "fused-tensor-cores",
+              3: "fused-pair-tensor-cores"}
 
 
 class ssd_dims_t(ctypes.Structure):

@@ -838,18 +838,14 @@ cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, c
     return run(kModeOut, x, Bm, Cm, dtT, Gc, D, states, nullptr, nullptr, y, g, nullptr, 0, st);
 }
 
-namespace {
-bool use_pair(const Geom &g)
+bool fused_pair_enabled(const Geom &g)
 {
     const char *env = getenv("SSD_FUSED_KERNEL");
     return pair_tc_supported(g) && !(env && strcmp(env, "single") == 0);
 }
-}  // namespace
 
 size_t fused_tc_scratch_bytes(const Geom &g)
 {
-    if (use_pair(g))
-        return pair_tc_scratch_bytes(g);
     const SegPlan sp = seg_plan(g);
     if (sp.n_seg <= 1)
         return 0;
@@ -861,9 +857,6 @@ cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const
                             float *final_state, void *y, const Geom &g, void *scratch,
                             size_t scratch_bytes, cudaStream_t st)
 {
-    if (use_pair(g))
-        return launch_fused_pair_tc(x, Bm, Cm, dtT, Gc, D, init, states, final_state, y, g,
-                                    scratch, scratch_bytes, st);
     return run(kModeFused, x, Bm, Cm, dtT, Gc, D, init, states, final_state, y, g, scratch,
                scratch_bytes, st);
 }

@@ -73,9 +73,9 @@ struct PairLayout {
     static constexpr uint32_t off_xh = off_x + 2 * kRegion;  // X_hat hi0, hi1, lo0, lo1
     static constexpr uint32_t off_h = off_xh + 4 * kRegion;  // H0, H1 (MN-major [s][p]); y staging
     static constexpr uint32_t off_g = off_h + 2 * kRegion;   // [parity][head][g 128 | dt 128] f32
-    // next tile's raw G / dt words per compute thread: [parity][5][256] f32
+    // the next tile's dt of both heads: [parity][128 rows][2 heads] f32
     static constexpr uint32_t off_raw = off_g + 2 * 2 * 256 * 4;
-    static constexpr uint32_t bytes = off_raw + 2 * 5 * 256 * 4;
+    static constexpr uint32_t bytes = off_raw + 2 * 128 * 2 * 4;
     // TMEM columns: CB (f32), shared masked scores (bf16 pairs), Y of both
     // heads, the f32 states h^T [S, P] of both heads, one wide-score region
     static constexpr uint32_t t_cb = 0, t_sc = 128, t_y = 192, t_st = 320, t_wide = 448;
@@ -84,7 +84,7 @@ struct PairLayout {
 };
 
 struct PairParams {
-    const float *dtT, *Gc, *D, *init;
+    const float *dt, *A, *D, *init;  // dt in the input layout [B, L, H]
     float *states_out, *final_state;
     Geom g;
     int n_items, n_tiles, tpc_shift;
@@ -416,65 +416,95 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         uint8_t *s_h = smem + Lay::off_h + k * kRegion;
         const int tpc_mask = (1 << prm.tpc_shift) - 1;
 
-        // Raw G / dt words of a tile (the token before it, its first and last
-        // token, this row's G and dt), copied one tile ahead by cp.async into
-        // this thread's slots [parity][word][thread] so no register waits on them.
-        struct Raw {
-            float base, g0, gL, gi, dti;
-        };
+        // dt of a tile for both heads (adjacent in the [B, L, H] input), copied
+        // one tile ahead by cp.async: thread i of warpgroup 0 copies row i's
+        // pair of words into slot [parity][i][2].  Each thread waits for its
+        // copy before arriving at the X_hat barrier, so every compute thread
+        // may read the whole tile once it has passed that barrier.  G within
+        // the tile is then a prefix sum each warp computes with shuffles, so
+        // no separate cumsum pass is needed.
         float *raw_all = reinterpret_cast<float *>(smem + Lay::off_raw);
-        const int ct = tid;  // compute thread index 0..255
-        auto prefetch_raw = [&](const PItem &w, int t, uint32_t buf) {
-            float *slot = raw_all + buf * 5 * 256 + ct;
-            const int64_t bh = (int64_t)w.b * prm.H + w.h0 + k;
-            const float *grow = prm.Gc + bh * g.L;
+        const int lane_id = tid & 31;
+        auto prefetch_dt = [&](const PItem &w, int t, uint32_t buf) {
+            if (k != 0)
+                return;
+            float *slot = raw_all + (buf * 128 + i) * 2;
             const int tau = t * kTile;
             const int n = min(kTile, (int)g.L - tau);
-            if ((t & tpc_mask) == 0)
-                slot[0] = 0.f;
-            else
-                cp_async4(slot, grow + tau - 1);
-            cp_async4(slot + 256, grow + tau);
-            cp_async4(slot + 512, grow + tau + n - 1);
             if (i < n) {
-                cp_async4(slot + 768, grow + tau + i);
-                cp_async4(slot + 1024, prm.dtT + bh * g.L + tau + i);
-            } else {  // a row past the sequence end: g = the base (relative 0), dt = 0
-                if ((t & tpc_mask) == 0)
-                    slot[768] = 0.f;
-                else
-                    cp_async4(slot + 768, grow + tau - 1);
-                slot[1024] = 0.f;
+                cp_async8(slot, prm.dt + ((int64_t)w.b * g.L + tau + i) * prm.H + w.h0);
+            } else {  // past the sequence end: dt = 0
+                slot[0] = 0.f;
+                slot[1] = 0.f;
             }
             cp_async_commit();
         };
-        auto read_raw = [&](uint32_t buf) {
-            cp_async_wait_all();
-            const float *slot = raw_all + buf * 5 * 256 + ct;
-            Raw r;
-            r.base = slot[0];
-            r.g0 = slot[256];
-            r.gL = slot[512];
-            r.gi = slot[768];
-            r.dti = slot[1024];
-            return r;
+        // Within-tile G (log2 units, relative to the token before the tile):
+        // this row's g and dt, the first row's g and the tile total g_L.
+        struct TileG {
+            float gi, dti, g0, gL;
+        };
+        auto tile_g = [&](uint32_t buf, float a_l2) {
+            const float *slot = raw_all + buf * 128 * 2 + k;
+            float incl[4], d[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                d[m] = slot[(32 * m + lane_id) * 2];
+                float v = a_l2 * d[m];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane_id >= o)
+                        v += u;
+                }
+                incl[m] = v;
+            }
+            float tot[4], pre = 0.f, mine_pre = 0.f, mine = 0.f, mine_d = 0.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                tot[m] = __shfl_sync(0xffffffffu, incl[m], 31);
+                if (m == q) {
+                    mine_pre = pre;
+                    mine = incl[m];
+                    mine_d = d[m];
+                }
+                pre += tot[m];
+            }
+            TileG tg;
+            tg.gi = mine_pre + mine;
+            tg.dti = mine_d;
+            tg.g0 = __shfl_sync(0xffffffffu, incl[0], 0);
+            tg.gL = pre;  // rows past the end add nothing
+            return tg;
         };
         const int n_my = my_item_count(prm);
         PItem w_next{};
+        float a_next = 0.f, d_next = 0.f;  // A and D of the next item's head, loaded early
+        TileG nxt_g{};  // G of the tile about to start, formed during the previous tile
         if (n_my > 0) {
             w_next = my_item(prm, 0);
-            prefetch_raw(w_next, w_next.t0, 0);
+            prefetch_dt(w_next, w_next.t0, 0);
+            a_next = ld_early(prm.A + w_next.h0 + k);
+            d_next = ld_early(prm.D + w_next.h0 + k);
+            cp_async_wait_all();
         }
+        // the first tile's dt is visible to all 256 compute threads
+        asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+        if (n_my > 0)
+            nxt_g = tile_g(0, kLog2e * a_next);
         uint32_t it = 0;
         bool ok = true;
         for (int j = 0; j < n_my && ok; ++j) {
             const PItem w = w_next;
             const int h = w.h0 + k;
             const int64_t bh = (int64_t)w.b * prm.H + h;
-            const float Dh = prm.D[h];
+            const float Dh = d_next, a_l2 = kLog2e * a_next;
             const bool more = j + 1 < n_my;
-            if (more)
+            if (more) {
                 w_next = my_item(prm, j + 1);
+                a_next = ld_early(prm.A + w_next.h0 + k);
+                d_next = ld_early(prm.D + w_next.h0 + k);
+            }
             // true state = exp2(lp) * stored state: the per-tile decay is kept as
             // this scalar instead of rescaling the state in TMEM every tile
             float lp = 0.f;
@@ -484,9 +514,13 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 const bool first = t == w.t0, last_item = t + 1 == w.t1;
                 const bool last_seq = t + 1 == prm.n_tiles;
                 const bool do_state = !last_seq || want_final;
-                const Raw cur = read_raw(it & 1);
-                const float gL = cur.gL - cur.base, g0 = cur.g0 - cur.base;
-                const float gi = cur.gi - cur.base, dti = cur.dti;
+                const TileG cur = nxt_g;
+                const float gL = cur.gL, g0 = cur.g0, gi = cur.gi, dti = cur.dti;
+                // the next tile's dt, for its G formed while this tile's Y1 runs
+                if (!last_item)
+                    prefetch_dt(w, t + 1, (it + 1) & 1);
+                else if (more)
+                    prefetch_dt(w_next, w_next.t0, (it + 1) & 1);
                 // Reference gref of the factorized form: keep the stored state's
                 // scale (gref = -lp) while every exponent gref - g_j, g_i - gref
                 // stays within kRefRange; else fold the scale into the state with
@@ -546,6 +580,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 fence_proxy_async_smem();
                 tmem_st_wait();
                 tc_fence_before();
+                cp_async_wait_all();  // the next tile's dt (see prefetch_dt)
                 warp_arrive(&bar_xh);
 
                 // ---- a later segment waits until its predecessor published its state
@@ -645,11 +680,6 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 fence_proxy_async_smem();
                 tc_fence_before();
                 warp_arrive(&bar_h);
-                // prefetch the next tile's G / dt while this one is processed
-                if (!last_item)
-                    prefetch_raw(w, t + 1, (it + 1) & 1);
-                else if (more)
-                    prefetch_raw(w_next, w_next.t0, (it + 1) & 1);
 
                 // ---- scores.  Shared masked CB (keys [64k, 64k + 64) here) when a
                 // head is factorized; the exact per-element scores of a wide head.
@@ -755,6 +785,11 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&bar_sc);
+                // the next tile's G while Y1 runs on the tensor cores
+                if (!last_item)
+                    nxt_g = tile_g((it + 1) & 1, a_l2);
+                else if (more)
+                    nxt_g = tile_g((it + 1) & 1, kLog2e * a_next);
 
                 // ---- epilogue: y = r Y, staged in this head's H buffer
                 if (!mbar_wait(&bar_y, par)) {
@@ -928,16 +963,16 @@ size_t pair_tc_scratch_bytes(const Geom &g)
     return (sp.state_bytes + 255) / 256 * 256 + (sp.count_bytes + 255) / 256 * 256;
 }
 
-cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
-                                 const float *Gc, const float *D, const float *init, float *states,
+cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dt,
+                                 const float *A, const float *D, const float *init, float *states,
                                  float *final_state, void *y, const Geom &g, void *scratch,
                                  size_t scratch_bytes, cudaStream_t st)
 {
     if (!pair_tc_supported(g))
         return cudaErrorNotSupported;
     PairParams prm{};
-    prm.dtT = dtT;
-    prm.Gc = Gc;
+    prm.dt = dt;
+    prm.A = A;
     prm.D = D;
     prm.init = init;
     prm.states_out = states;

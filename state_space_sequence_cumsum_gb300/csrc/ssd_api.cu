@@ -120,7 +120,7 @@ ssd_path_t choose_path(const Geom &g, ssd_dtype_t t, bool want_states)
     const char *env = getenv("SSD_FWD_PATH");
     if (env && strcmp(env, "staged") == 0)
         return SSD_PATH_STAGED_TENSOR_CORES;
-    return SSD_PATH_FUSED_TENSOR_CORES;
+    return fused_pair_enabled(g) ? SSD_PATH_FUSED_PAIR_TENSOR_CORES : SSD_PATH_FUSED_TENSOR_CORES;
 }
 
 // Stage 2 dispatch: tcgen05 kernel for bf16 shapes it serves, else CUDA cores.
@@ -152,12 +152,22 @@ struct Workspace {
 
 // ssd_fwd's workspace: G_cum and dt_t, then either the chunk states the
 // staged path keeps between stages (when the caller does not want them) or
-// the fused path's segment hand-off scratch.
-Workspace layout(const Geom &g, bool fused, bool caller_states, char *base)
+// the fused path's segment hand-off scratch.  The head-pair fused path forms
+// G itself and needs only its hand-off scratch.
+Workspace layout(const Geom &g, ssd_path_t path, bool caller_states, char *base)
 {
     const size_t bhl = (size_t)(g.B * g.H * g.L) * sizeof(float);
     size_t off = 0;
     Workspace w{};
+    if (path == SSD_PATH_FUSED_PAIR_TENSOR_CORES) {
+        w.fused_scratch_bytes = pair_tc_scratch_bytes(g);
+        w.fused_scratch = base;
+        w.bytes = round_up(w.fused_scratch_bytes, 256);
+        if (!base)
+            w.fused_scratch = nullptr;
+        return w;
+    }
+    const bool fused = path == SSD_PATH_FUSED_TENSOR_CORES;
     w.Gc = reinterpret_cast<float *>(base + off);
     off = round_up(off + bhl, 256);
     w.dtT = reinterpret_cast<float *>(base + off);
@@ -344,8 +354,8 @@ size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size
         g.T = choose_chunk_size(g, dtype);
         g.nc = (g.L + g.T - 1) / g.T;
     }
-    const bool fused = choose_path(g, dtype, want_chunk_states != 0) == SSD_PATH_FUSED_TENSOR_CORES;
-    const size_t b = layout(g, fused, want_chunk_states != 0, nullptr).bytes;
+    const size_t b = layout(g, choose_path(g, dtype, want_chunk_states != 0),
+                            want_chunk_states != 0, nullptr).bytes;
     return b ? b : 256;
 }
 
@@ -379,12 +389,17 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
         return ssd_state_pass(x, Bm, nullptr, nullptr, init_state, chunk_states, final_state,
                               dims, dtype, g.T, stream);
 
-    const bool fused = choose_path(g, dtype, chunk_states != nullptr) == SSD_PATH_FUSED_TENSOR_CORES;
-    const Workspace need_ws = layout(g, fused, chunk_states != nullptr, nullptr);
-    if (!workspace || workspace_bytes < need_ws.bytes ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    const ssd_path_t path = choose_path(g, dtype, chunk_states != nullptr);
+    const bool fused = path == SSD_PATH_FUSED_TENSOR_CORES;
+    const Workspace need_ws = layout(g, path, chunk_states != nullptr, nullptr);
+    if (need_ws.bytes && (!workspace || workspace_bytes < need_ws.bytes ||
+                          (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return SSD_ERR_WORKSPACE;
-    const Workspace w = layout(g, fused, chunk_states != nullptr, static_cast<char *>(workspace));
+    const Workspace w = layout(g, path, chunk_states != nullptr, static_cast<char *>(workspace));
+    if (path == SSD_PATH_FUSED_PAIR_TENSOR_CORES)
+        return cuda_status(launch_fused_pair_tc(x, Bm, Cm, dt, A, D, init_state, chunk_states,
+                                                final_state, y, g, w.fused_scratch,
+                                                w.fused_scratch_bytes, st));
     float *states = chunk_states ? chunk_states : w.states;
     const bool bf16 = dtype == SSD_BF16;
 

@@ -57,9 +57,8 @@ bool chunk_tc_supported(const Geom &g);
 cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                                 const float *Gc, const float *states, const float *D, void *y,
                                 const Geom &g, cudaStream_t st);
-// Scratch the fused pass needs (segment hand-off states and counters), 0 if none.
-// The fused pass runs the head-pair kernel where it applies (see below) unless
-// SSD_FUSED_KERNEL=single selects the one-head kernel.
+// Scratch the one-head fused pass needs (segment hand-off states and
+// counters), 0 if none.
 size_t fused_tc_scratch_bytes(const Geom &g);
 cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                             const float *Gc, const float *D, const float *init, float *states,
@@ -67,11 +66,14 @@ cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const
                             size_t scratch_bytes, cudaStream_t st);
 
 // Fused forward for two heads of one B/C group per CTA (bf16, P = 64,
-// S in {64, 128}, an even number of heads per group).
+// S in {64, 128}, an even number of heads per group), straight from dt and A
+// (it forms G itself).  ssd_fwd uses it where it applies unless
+// SSD_FUSED_KERNEL=single asks for the cumsum + one-head fused pair.
 bool pair_tc_supported(const Geom &g);
+bool fused_pair_enabled(const Geom &g);
 size_t pair_tc_scratch_bytes(const Geom &g);
-cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
-                                 const float *Gc, const float *D, const float *init, float *states,
+cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dt,
+                                 const float *A, const float *D, const float *init, float *states,
                                  float *final_state, void *y, const Geom &g, void *scratch,
                                  size_t scratch_bytes, cudaStream_t st);
 

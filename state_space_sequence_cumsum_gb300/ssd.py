@@ -214,8 +214,12 @@ def ssd_fwd_path(x, B, chunk_size=0, want_states=False) -> str:
 def ssd_fwd_plan(x, B, chunk_size, want_states=False) -> dict:
     """The C-ABI stage calls ssd_fwd makes for these arguments, in order."""
     path = ssd_fwd_path(x, B, chunk_size, want_states)
-    kernels = (["chunk_cumsum", "state_out"] if path == "fused-tensor-cores"
-               else ["chunk_cumsum", "state_pass", "chunk_out"])
+    if path == "fused-pair-tensor-cores":
+        kernels = ["fused_pair"]  # one kernel: ssd_fwd itself
+    elif path == "fused-tensor-cores":
+        kernels = ["chunk_cumsum", "state_out"]
+    else:
+        kernels = ["chunk_cumsum", "state_pass", "chunk_out"]
     return {"path": path, "chunk_size": int(chunk_size), "kernels": kernels}
 
 
@@ -229,16 +233,25 @@ def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk
     Sd = B.shape[3]
     T = plan["chunk_size"]
     dev = x.device
+
+    def mark(i):
+        if events is not None:
+            events[i].record(s)
+
+    if plan["kernels"] == ["fused_pair"]:
+        mark(0)
+        ssd_fwd(x, dt, A, B, C, D, chunk_size=T, initial_state=initial_state, y=y,
+                final_state=final_state, chunk_states=chunk_states,
+                return_final_state=final_state is not None,
+                return_chunk_states=chunk_states is not None, workspace=workspace, stream=s)
+        mark(1)
+        return y, final_state, chunk_states
     Gc = workspace.tensor("G_cum", (b, H, L), torch.float32, dev)
     dtT = workspace.tensor("dt_t", (b, H, L), torch.float32, dev)
     nc = (L + T - 1) // T
     states = chunk_states
     if states is None and plan["kernels"][1] != "state_out":
         states = workspace.tensor("chunk_states", (b, H, nc, P, Sd), torch.float32, dev)
-
-    def mark(i):
-        if events is not None:
-            events[i].record(s)
 
     mark(0)
     ssd_chunk_cumsum(dt, A, T, G_cum=Gc, dt_t=dtT, stream=s)

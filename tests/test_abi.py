@@ -95,8 +95,9 @@ def test_fwd_workspace_checks(lib):
 
 
 def test_workspace_size_grows_with_problem(lib):
-    small = lib.ssd_fwd_workspace_size(_lib.dims(1, 1024, 8, 64, 128, 1), 0, 128, 0)
-    big = lib.ssd_fwd_workspace_size(_lib.dims(1, 4096, 8, 64, 128, 1), 0, 128, 0)
+    # one head per group: the cumsum + fused path, whose G / dt_t buffers grow with L
+    small = lib.ssd_fwd_workspace_size(_lib.dims(1, 1024, 8, 64, 128, 8), 0, 128, 0)
+    big = lib.ssd_fwd_workspace_size(_lib.dims(1, 4096, 8, 64, 128, 8), 0, 128, 0)
     assert big > small > 0
     assert lib.ssd_fwd_workspace_size(_lib.dims(0, 1, 1, 1, 1, 1), 0, 64, 0) == 0
     # asking for caller-owned chunk states never needs more workspace

@@ -74,7 +74,7 @@ def test_staged_tensor_core_path_matches_oracle(T, monkeypatch):
 def test_fused_and_staged_paths_agree(monkeypatch):
     inp = case_inputs(1, 1000, 8, 64, 128, 1, 256, init="randn", seed=37)
     g = to_gpu(inp)
-    assert ssd.ssd_fwd_path(g["x"], g["B"], 256) == "fused-tensor-cores"
+    assert ssd.ssd_fwd_path(g["x"], g["B"], 256) == "fused-pair-tensor-cores"
     y_f, f_f, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], 256,
                               initial_state=g["init"])
     monkeypatch.setenv("SSD_FWD_PATH", "staged")
