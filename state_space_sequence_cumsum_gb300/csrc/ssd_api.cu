@@ -106,6 +106,8 @@ cudaError_t run_chunk_out(const void *x, const void *Bm, const void *Cm, const f
 {
     if (bf16 && chunk_tc_supported(g))
         return launch_chunk_out_tc(x, Bm, Cm, dtT, Gc, states, D, y, g, st);
+    if (bf16 && chunk_out_big_supported(g))
+        return launch_chunk_out_big(x, Bm, Cm, dtT, Gc, states, D, y, g, st);
     return launch_chunk_out_simt(x, Bm, Cm, dtT, Gc, states, D, y, g, bf16, st);
 }
 

@@ -57,6 +57,13 @@ bool chunk_tc_supported(const Geom &g);
 cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                                 const float *Gc, const float *states, const float *D, void *y,
                                 const Geom &g, cudaStream_t st);
+// Tensor-core chunk output for dstate 384 / 512 (bf16, P = 64, chunk 128),
+// streaming B / C in 128-wide dstate blocks.
+bool chunk_out_big_supported(const Geom &g);
+cudaError_t launch_chunk_out_big(const void *x, const void *Bm, const void *Cm, const float *dtT,
+                                 const float *Gc, const float *states, const float *D, void *y,
+                                 const Geom &g, cudaStream_t st);
+
 // Scratch the one-head fused pass needs (segment hand-off states and
 // counters), 0 if none.
 size_t fused_tc_scratch_bytes(const Geom &g);

@@ -58,7 +58,9 @@ def test_state_pass(dtype, B, L, H, P, S, G, T):
                                            (2, 333, 2, 128, 128, 1, 256),
                                            (1, 260, 4, 64, 256, 1, 128),
                                            (1, 390, 2, 64, 64, 2, 256),
-                                           (1, 200, 2, 128, 64, 1, 128)])
+                                           (1, 200, 2, 128, 64, 1, 128),
+                                           (2, 645, 4, 64, 512, 2, 128),   # dstate blocks, ragged
+                                           (1, 384, 3, 64, 384, 1, 128)])
 def test_chunk_out_from_oracle_states(dtype, B, L, H, P, S, G, T):
     inp = case_inputs(B, L, H, P, S, G, T, dtype=dtype, init="randn", seed=L + S)
     g = to_gpu(inp)
