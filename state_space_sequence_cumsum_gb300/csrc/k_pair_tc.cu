@@ -331,24 +331,10 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     for (int ks = 0; ks < S / 16; ++ks)
                         mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2, 1u);
                     mma_commit(&bar_y2);
-                    // The state jump (hi, lo) next: with Y2 it is the last reader of
-                    // the B / C tiles, so their reload for the next tile can start as
-                    // soon as it completes; then Y1 once the scores are ready.
-                    if (do_state) {
-#pragma unroll
-                        for (int part = 0; part < 2; ++part)
-#pragma unroll
-                            for (int ks = 0; ks < kTile / 16; ++ks)
-                                mma_ss(tmem + Lay::t_st, desc_mn(d_bmn, ks),
-                                       desc_mn(part ? d_lo : d_hi, ks), id_ds, 1u);
-                    }
-                    mma_commit(&bar_ds);
-                    if (!mbar_wait(&bar_sc, par)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    {
+                    // Y1 once the scores are ready: both heads in one N = 128 MMA
+                    // when both are factorized, else per head.
+                    auto issue_y1 = [&]() {
+                        tc_fence_after();
                         const int m0 = s_mode[par][0], m1 = s_mode[par][1];
                         if (m0 && m1) {
 #pragma unroll
@@ -369,8 +355,37 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                            desc_mn(bd, ks), id_y1h, 1u);
                             }
                         }
+                        mma_commit(&bar_y);
+                    };
+                    // The state jump (hi, lo) next: with Y2 it is the last reader of
+                    // the B / C tiles, so their reload for the next tile can start as
+                    // soon as it completes.  It goes in four groups of four MMAs;
+                    // between groups Y1 overtakes the rest of the jump as soon as the
+                    // scores are ready, since the tensor pipe runs in issue order and
+                    // the epilogue waits only for Y1.
+                    bool y1_sent = false;
+                    if (do_state) {
+#pragma unroll 1
+                        for (int grp = 0; grp < 4; ++grp) {
+                            const uint64_t db = d_bmn + (grp & 1) * (4 * 128);
+                            const uint64_t dxh = ((grp >> 1) ? d_lo : d_hi) + (grp & 1) * (4 * 128);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                mma_ss(tmem + Lay::t_st, desc_mn(db, u), desc_mn(dxh, u), id_ds, 1u);
+                            if (!y1_sent && grp < 3 && mbar_test(&bar_sc, par)) {
+                                issue_y1();
+                                y1_sent = true;
+                            }
+                        }
                     }
-                    mma_commit(&bar_y);
+                    mma_commit(&bar_ds);
+                    if (!y1_sent) {
+                        if (!mbar_wait(&bar_sc, par)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_y1();
+                    }
                 }
             }
             if (!ok)
@@ -545,11 +560,19 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
                 tc_fence_after();
 
-                // ---- X_hat = dt exp2(gref - g) x (hi, lo) and Y = D x / r (0 if wide)
+                // ---- X_hat = dt exp2(gref - g) x (hi, lo) and Y = D x / r (0 if wide).
+                // Packed bf16 arithmetic with the weight w split as w_hi + w_lo:
+                // hi = bf16(x w_hi); the rounding residual x w_hi - hi is exact in
+                // bf16 (x and w_hi carry 8 significant bits each), so
+                // lo = bf16(x w_lo + residual) leaves hi + lo within ~2^-16 of x w.
                 {
                     const float e = ex2_approx(gref - gi);
                     const float wv = i < n ? dti * e : 0.f;
                     const float dsc = narrow ? Dh * e : 0.f;
+                    const uint32_t whi = pack_bf16x2(wv, wv);
+                    const float wv_lo = wv - bf_lo(whi);
+                    const uint32_t wlo = pack_bf16x2(wv_lo, wv_lo);
+                    const uint64_t dsc2 = f2_pack(__float_as_uint(dsc), __float_as_uint(dsc));
 #pragma unroll
                     for (int c2 = 0; c2 < 4; ++c2) {
                         uint32_t dx[16];
@@ -562,12 +585,10 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             uint32_t hi[4], lo[4];
 #pragma unroll
                             for (int e2 = 0; e2 < 4; ++e2) {
-                                const float xa = bf_lo(vv[e2]), xb = bf_hi(vv[e2]);
-                                const float a = xa * wv, bb = xb * wv;
-                                hi[e2] = pack_bf16x2(a, bb);
-                                lo[e2] = pack_bf16x2(a - bf_lo(hi[e2]), bb - bf_hi(hi[e2]));
-                                dx[8 * cc + 2 * e2] = __float_as_uint(dsc * xa);
-                                dx[8 * cc + 2 * e2 + 1] = __float_as_uint(dsc * xb);
+                                hi[e2] = bf2_mul(vv[e2], whi);
+                                lo[e2] = bf2_fma(vv[e2], wlo, bf2_fma(vv[e2], whi, hi[e2] ^ 0x80008000u));
+                                f2_unpack(f2_mul(bf2_to_f2(vv[e2]), dsc2), dx[8 * cc + 2 * e2],
+                                          dx[8 * cc + 2 * e2 + 1]);
                             }
                             *reinterpret_cast<uint4 *>(s_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                             if (do_state)
@@ -645,30 +666,40 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             for (int j = 0; j < 64; ++j)
                                 emit_dst[(int64_t)j * S + i] = pv * __uint_as_float(r[j]);
                         }
+                        // scaling runs on f32 pairs
+                        auto scaled = [&](int j, uint64_t s2, uint32_t &a, uint32_t &b) {
+                            f2_unpack(f2_mul(f2_pack(r[j], r[j + 1]), s2), a, b);
+                        };
                         if (fold) {  // r <- the true state h
+                            const uint64_t pv2 = f2_pack(__float_as_uint(pv), __float_as_uint(pv));
 #pragma unroll
-                            for (int j = 0; j < 64; ++j)
-                                r[j] = __float_as_uint(pv * __uint_as_float(r[j]));
+                            for (int j = 0; j < 64; j += 2)
+                                scaled(j, pv2, r[j], r[j + 1]);
                         }
                         // keep: H = bf16(S); fold: H = bf16(hsc h)
-                        const float hs2 = keep ? 1.f : hsc;
+                        const uint64_t hs2 = f2_pack(__float_as_uint(hsc), __float_as_uint(hsc));
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             uint32_t hp[4];
 #pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2)
-                                hp[e2] = pack_bf16x2(hs2 * __uint_as_float(r[8 * c + 2 * e2]),
-                                                     hs2 * __uint_as_float(r[8 * c + 2 * e2 + 1]));
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                const int j = 8 * c + 2 * e2;
+                                uint32_t a = r[j], b = r[j + 1];
+                                if (!keep)
+                                    scaled(j, hs2, a, b);
+                                hp[e2] = pack_bf16x2(__uint_as_float(a), __uint_as_float(b));
+                            }
                             *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, c)) =
                                 make_uint4(hp[0], hp[1], hp[2], hp[3]);
                         }
                         if (fold && do_state) {  // stored state <- exp2(gref) h
+                            const uint64_t er2 = f2_pack(__float_as_uint(eref), __float_as_uint(eref));
 #pragma unroll
                             for (int qq = 0; qq < 4; ++qq) {
                                 uint32_t o[16];
 #pragma unroll
-                                for (int j = 0; j < 16; ++j)
-                                    o[j] = __float_as_uint(eref * __uint_as_float(r[16 * qq + j]));
+                                for (int j = 0; j < 16; j += 2)
+                                    scaled(16 * qq + j, er2, o[j], o[j + 1]);
                                 tmem_st16(tst + 16 * qq, o);
                             }
                         }
@@ -799,6 +830,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tc_fence_after();
                 {
                     const float r = narrow ? ex2_approx(gi - gref) : 1.f;
+                    const uint64_t r2 = f2_pack(__float_as_uint(r), __float_as_uint(r));
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         uint32_t yv[32];
@@ -809,9 +841,11 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         for (int c = 0; c < 4; ++c) {
                             uint32_t o[4];
 #pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2)
-                                o[e2] = pack_bf16x2(r * __uint_as_float(yv[8 * c + 2 * e2]),
-                                                    r * __uint_as_float(yv[8 * c + 2 * e2 + 1]));
+                            for (int e2 = 0; e2 < 4; ++e2) {
+                                uint32_t a, b;
+                                f2_unpack(f2_mul(f2_pack(yv[8 * c + 2 * e2], yv[8 * c + 2 * e2 + 1]), r2), a, b);
+                                o[e2] = pack_bf16x2(__uint_as_float(a), __uint_as_float(b));
+                            }
                             *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, 4 * half + c)) =
                                 make_uint4(o[0], o[1], o[2], o[3]);
                         }

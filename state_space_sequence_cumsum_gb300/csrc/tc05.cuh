@@ -295,6 +295,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+// ------------------------------------------------------------------ packed arithmetic
+// Two bf16 lanes: round(a * b) and round(a * b + c), one rounding each.
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Two f32 lanes in one 64-bit register pair (low word = first lane).
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, uint32_t &lo, uint32_t &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+// bf16 pair (low half = first element) to an f32 pair
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t v) { return f2_pack(v << 16, v & 0xffff0000u); }
+
 // ------------------------------------------------------------------ cp.async (4-byte)
 __device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src)
 {
