@@ -113,61 +113,84 @@ struct PItem {
     int b, h0, grp, t0, t1, seg;
 };
 
-__device__ __forceinline__ PItem pair_item(const PairParams &p, int q, int t0, int t1, int seg)
+__device__ __forceinline__ PItem pair_item(const PairParams &p, unsigned q, int t0, int t1, int seg)
 {
     PItem w;
-    w.b = q / p.npairs;
-    w.h0 = 2 * (q % p.npairs);
-    w.grp = w.h0 / p.hpg;
+    w.b = (int)(q / (unsigned)p.npairs);
+    w.h0 = 2 * (int)(q % (unsigned)p.npairs);
+    w.grp = (int)((unsigned)w.h0 / (unsigned)p.hpg);
     w.t0 = t0;
     w.t1 = t1;
     w.seg = seg;
     return w;
 }
 
-// This CTA's piece [lo, hi) of the pair-major tile sequence (wrap mode).
-__device__ __forceinline__ void wrap_piece(const PairParams &p, long long &lo, long long &hi)
-{
-    lo = (long long)blockIdx.x * p.wrap_units / gridDim.x;
-    hi = (long long)(blockIdx.x + 1) * p.wrap_units / gridDim.x;
-}
+// This CTA's share of the work, worked out once per CTA (the 64-bit
+// arithmetic of the wrap plan stays out of the per-item code).
+struct Plan {
+    int count;               // items of this CTA
+    int head;                // wrap: the first item starts the sequence crossing the upper cut
+    int hi_q, hi_t;          //   that sequence and the tile where the cut falls
+    int first_full, n_full;  //   whole sequences [first_full, first_full + n_full)
+    int lo_q, lo_t;          //   the sequence crossing the lower cut, from tile lo_t on
+};
 
-// Number of items this CTA runs.
-__device__ __forceinline__ int my_item_count(const PairParams &p)
+__device__ __noinline__ void make_plan(const PairParams &p, Plan &pl)
 {
-    if (!p.wrap)
-        return (int)blockIdx.x < p.n_items ? (p.n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-    long long lo, hi;
-    wrap_piece(p, lo, hi);
+    if (!p.wrap) {
+        pl.count = (int)blockIdx.x < p.n_items ? (p.n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        pl.head = pl.hi_q = pl.hi_t = pl.first_full = pl.n_full = pl.lo_q = pl.lo_t = 0;
+        return;
+    }
+    // this CTA's piece [lo, hi) of the pair-major tile sequence
+    const long long lo = (long long)blockIdx.x * p.wrap_units / gridDim.x;
+    const long long hi = (long long)(blockIdx.x + 1) * p.wrap_units / gridDim.x;
     const long long n = p.n_tiles;
-    const long long first_full = (lo + n - 1) / n, end_full = hi / n;  // whole sequences [first_full, end_full)
-    return (int)((hi % n != 0) + (end_full - first_full) + (lo % n != 0));
+    const long long first_full = (lo + n - 1) / n, end_full = hi / n;
+    pl.head = hi % n != 0;
+    pl.hi_q = (int)(hi / n);
+    pl.hi_t = (int)(hi % n);
+    pl.first_full = (int)first_full;
+    pl.n_full = (int)(end_full - first_full);
+    pl.lo_q = (int)(lo / n);
+    pl.lo_t = (int)(lo % n);
+    pl.count = pl.head + pl.n_full + (lo % n != 0);
 }
 
 // The j-th item of this CTA, in the order it runs them.
-__device__ __forceinline__ PItem my_item(const PairParams &p, int j)
+__device__ __forceinline__ PItem my_item(const PairParams &p, const Plan &pl, int j)
 {
+    unsigned q;
+    int t0, t1, seg;
     if (!p.wrap) {
         // segment-major: every segment k of every head pair comes before any
         // segment k+1, so a segment's predecessor is always an earlier item
-        const int item = (int)blockIdx.x + j * (int)gridDim.x;
+        const unsigned item = blockIdx.x + (unsigned)j * gridDim.x;
         const unsigned per_seg = (unsigned)(p.batch * p.npairs);
-        const unsigned seg = (unsigned)item / per_seg, q = (unsigned)item % per_seg;
-        const int t0 = (int)seg * p.seg_tiles;
-        return pair_item(p, (int)q, t0, min(t0 + p.seg_tiles, p.n_tiles), (int)seg);
+        const unsigned sg = item / per_seg;
+        q = item - sg * per_seg;
+        seg = (int)sg;
+        t0 = seg * p.seg_tiles;
+        t1 = min(t0 + p.seg_tiles, p.n_tiles);
+    } else if (pl.head && j == 0) {
+        // start of the sequence crossing the upper cut: hands its state off
+        q = (unsigned)pl.hi_q;
+        t0 = 0;
+        t1 = pl.hi_t;
+        seg = 0;
+    } else if (j - pl.head < pl.n_full) {
+        q = (unsigned)(pl.first_full + j - pl.head);
+        t0 = 0;
+        t1 = p.n_tiles;
+        seg = 0;
+    } else {
+        // rest of the sequence crossing the lower cut, from its neighbour's state
+        q = (unsigned)pl.lo_q;
+        t0 = pl.lo_t;
+        t1 = p.n_tiles;
+        seg = 1;
     }
-    long long lo, hi;
-    wrap_piece(p, lo, hi);
-    const int n = p.n_tiles;
-    const long long first_full = (lo + n - 1) / n, end_full = hi / n;
-    const int head = hi % n != 0;
-    if (head && j == 0)  // start of the sequence crossing the upper cut: hands its state off
-        return pair_item(p, (int)(hi / n), 0, (int)(hi % n), 0);
-    j -= head;
-    if (j < end_full - first_full)
-        return pair_item(p, (int)(first_full + j), 0, n, 0);
-    // rest of the sequence crossing the lower cut, from its neighbour's state
-    return pair_item(p, (int)(lo / n), (int)(lo % n), n, 1);
+    return pair_item(p, q, t0, t1, seg);
 }
 
 template <int S>
@@ -191,6 +214,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     __shared__ uint64_t bar_hfree;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_mode[2][2];  // [tile parity][head]: 1 = factorized
+    __shared__ Plan s_plan;
 
     const Geom &g = prm.g;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -209,6 +233,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         mbar_init(&bar_ys, kWarps);
         mbar_init(&bar_hfree, 1);
         fence_barrier_init();
+        make_plan(prm, s_plan);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_slot, 512);
@@ -231,9 +256,9 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             prefetch_tmap(&tm_c);
             uint32_t it = 0;
             bool ok = true;
-            const int n_my = my_item_count(prm);
+            const int n_my = s_plan.count;
             for (int j = 0; j < n_my && ok; ++j) {
-                const PItem w = my_item(prm, j);
+                const PItem w = my_item(prm, s_plan, j);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     const int tok = t * kTile;
                     auto load_x = [&](int k) {
@@ -302,9 +327,9 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             constexpr uint32_t kStep = kRegion >> 4;  // one region in descriptor units
             uint32_t it = 0;
             bool ok = true;
-            const int n_my = my_item_count(prm);
+            const int n_my = s_plan.count;
             for (int j = 0; j < n_my && ok; ++j) {
-                const PItem w = my_item(prm, j);
+                const PItem w = my_item(prm, s_plan, j);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     const bool last_seq = t + 1 == prm.n_tiles;
                     const bool do_state = !last_seq || want_final;
@@ -364,28 +389,35 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     // scores are ready, since the tensor pipe runs in issue order and
                     // the epilogue waits only for Y1.
                     bool y1_sent = false;
-                    if (do_state) {
+                    const int n_grp = do_state ? 4 : 0;
 #pragma unroll 1
-                        for (int grp = 0; grp < 4; ++grp) {
+                    for (int grp = 0; grp <= n_grp; ++grp) {
+                        if (grp == n_grp)
+                            mma_commit(&bar_ds);
+                        if (!y1_sent) {
+                            bool ready = grp > 0 && mbar_test(&bar_sc, par);
+                            if (grp == n_grp && !ready) {
+                                if (!mbar_wait(&bar_sc, par)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ready = true;
+                            }
+                            if (ready) {
+                                issue_y1();
+                                y1_sent = true;
+                            }
+                        }
+                        if (grp < n_grp) {
                             const uint64_t db = d_bmn + (grp & 1) * (4 * 128);
                             const uint64_t dxh = ((grp >> 1) ? d_lo : d_hi) + (grp & 1) * (4 * 128);
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
                                 mma_ss(tmem + Lay::t_st, desc_mn(db, u), desc_mn(dxh, u), id_ds, 1u);
-                            if (!y1_sent && grp < 3 && mbar_test(&bar_sc, par)) {
-                                issue_y1();
-                                y1_sent = true;
-                            }
                         }
                     }
-                    mma_commit(&bar_ds);
-                    if (!y1_sent) {
-                        if (!mbar_wait(&bar_sc, par)) {
-                            ok = false;
-                            break;
-                        }
-                        issue_y1();
-                    }
+                    if (!ok)
+                        break;
                 }
             }
             if (!ok)
@@ -397,9 +429,9 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             prefetch_tmap(&tm_y);
             uint32_t it = 0;
             bool ok = true;
-            const int n_my = my_item_count(prm);
+            const int n_my = s_plan.count;
             for (int j = 0; j < n_my && ok; ++j) {
-                const PItem w = my_item(prm, j);
+                const PItem w = my_item(prm, s_plan, j);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     if (!mbar_wait(&bar_ys, it & 1)) {
                         ok = false;
@@ -492,12 +524,12 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tg.gL = pre;  // rows past the end add nothing
             return tg;
         };
-        const int n_my = my_item_count(prm);
+        const int n_my = s_plan.count;
         PItem w_next{};
         float a_next = 0.f, d_next = 0.f;  // A and D of the next item's head, loaded early
         TileG nxt_g{};  // G of the tile about to start, formed during the previous tile
         if (n_my > 0) {
-            w_next = my_item(prm, 0);
+            w_next = my_item(prm, s_plan, 0);
             prefetch_dt(w_next, w_next.t0, 0);
             a_next = ld_early(prm.A + w_next.h0 + k);
             d_next = ld_early(prm.D + w_next.h0 + k);
@@ -516,7 +548,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const float Dh = d_next, a_l2 = kLog2e * a_next;
             const bool more = j + 1 < n_my;
             if (more) {
-                w_next = my_item(prm, j + 1);
+                w_next = my_item(prm, s_plan, j + 1);
                 a_next = ld_early(prm.A + w_next.h0 + k);
                 d_next = ld_early(prm.D + w_next.h0 + k);
             }

@@ -94,7 +94,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t limit_ns = 2000000000ull)
 {
-    if (mbar_try_wait(bar, parity))
+    if (mbar_test(bar, parity))
         return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
@@ -393,11 +393,16 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 // One arrival per warp: the warp's lanes are synchronised (which orders
 // their earlier shared-memory and TMEM work before lane 0's release).
+// One arrival per warp, after every lane's prior writes (the warp barrier
+// orders them); the arriving lane is picked by elect.sync, so no branch.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar)
 {
     __syncwarp();
-    if ((threadIdx.x & 31) == 0)
-        mbar_arrive(bar);
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 
 // Descriptors are built once per buffer and stepped by adding the byte
