@@ -172,6 +172,27 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
                      void *stream);
 
 /*
+ * Single-token decode step on a carried state (section "Mamba-2 架构": the
+ * recurrence for one token, i.e. how a final state from ssd_fwd is used
+ * during generation).  dims.seqlen must be 1; per (b, h), g = h / (H / G):
+ *     state[p,s] <- exp(A[h] dt[b,h]) state[p,s] + dt[b,h] x[b,h,p] Bm[b,g,s]
+ *     y[b,h,p]    = sum_s Cm[b,g,s] state[p,s] + D[h] x[b,h,p]
+ * (the state after the update feeds y, as in the chunked forward).
+ * Layouts are those of the forward with L = 1: x, y [B, 1, H, P], dt [B, 1, H],
+ * Bm, Cm [B, 1, G, S], state_in / state_out [B, H, P, S] f32.  state_out may
+ * be state_in (in-place update) or a separate buffer; partly overlapping
+ * buffers return SSD_ERR_INVALID_ARG.  Unlike the other entry points this
+ * one asks only for element alignment (a token's slice of a [B, L, ...]
+ * tensor is rarely 16-byte aligned); 16-byte aligned state and B / C with
+ * dstate % 4 == 0 take the vectorised kernel.  Arithmetic is f32 (inputs
+ * widened, exp of the decay in f32); y is rounded to the call's dtype.
+ */
+ssd_status_t ssd_decode_step(const void *x, const float *dt, const float *A, const void *Bm,
+                             const void *Cm, const float *D, const float *state_in,
+                             float *state_out, void *y, ssd_dims_t dims, ssd_dtype_t dtype,
+                             void *stream);
+
+/*
  * ssd_fwd without a workspace argument, for callers that cannot allocate
  * device memory (code running inside an allocator or memory-pool callback, a
  * host framework that owns all device allocations, a latency-critical loop

@@ -88,6 +88,14 @@ ssd_status_t need(const void *p, bool nonempty)
 
 ssd_status_t opt(const void *p) { return (!p || aligned16(p)) ? SSD_OK : SSD_ERR_ALIGNMENT; }
 
+// A required pointer aligned to its element size.
+ssd_status_t need_elem(const void *p, size_t esz)
+{
+    if (!p)
+        return SSD_ERR_INVALID_ARG;
+    return (reinterpret_cast<uintptr_t>(p) % esz == 0) ? SSD_OK : SSD_ERR_ALIGNMENT;
+}
+
 #define SSD_TRY(expr)                                  \
     do {                                               \
         ssd_status_t _s = (expr);                      \
@@ -413,6 +421,38 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
     SSD_TRY(cuda_status(
         run_state_pass(x, Bm, w.dtT, w.Gc, init_state, states, final_state, g, bf16, st)));
     return cuda_status(run_chunk_out(x, Bm, Cm, w.dtT, w.Gc, states, D, y, g, bf16, st));
+}
+
+ssd_status_t ssd_decode_step(const void *x, const float *dt, const float *A, const void *Bm,
+                             const void *Cm, const float *D, const float *state_in,
+                             float *state_out, void *y, ssd_dims_t dims, ssd_dtype_t dtype,
+                             void *stream)
+{
+    if (dims.seqlen != 1)
+        return SSD_ERR_INVALID_ARG;
+    Geom g;
+    SSD_TRY(make_geom(dims, 1, false, &g));
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return SSD_ERR_INVALID_ARG;
+    // one token's slices of larger tensors are rarely 16-byte aligned, so this
+    // entry point asks only for element alignment (the kernel picks its vector
+    // width from the actual alignment)
+    const size_t esz = dtype == SSD_BF16 ? 2 : 4;
+    for (const void *p : {x, static_cast<const void *>(Bm), static_cast<const void *>(Cm),
+                          static_cast<const void *>(y)})
+        SSD_TRY(need_elem(p, esz));
+    for (const void *p : {static_cast<const void *>(dt), static_cast<const void *>(A),
+                          static_cast<const void *>(D), static_cast<const void *>(state_in),
+                          static_cast<const void *>(state_out)})
+        SSD_TRY(need_elem(p, 4));
+    // the state may be updated in place, but not through partly overlapping buffers
+    const size_t sb = (size_t)g.B * g.H * g.P * g.S * sizeof(float);
+    const char *si = reinterpret_cast<const char *>(state_in);
+    const char *so = reinterpret_cast<const char *>(state_out);
+    if (si != so && si < so + sb && so < si + sb)
+        return SSD_ERR_INVALID_ARG;
+    return cuda_status(launch_decode_step(x, dt, A, Bm, Cm, D, state_in, state_out, y, g,
+                                          dtype == SSD_BF16, (cudaStream_t)stream));
 }
 
 ssd_status_t ssd_stream_status(void *stream)

@@ -60,6 +60,10 @@ cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, c
 // Tensor-core chunk output for dstate 384 / 512 (bf16, P = 64, chunk 128),
 // streaming B / C in 128-wide dstate blocks.
 bool chunk_out_big_supported(const Geom &g);
+// Single-token decode step (k_decode.cu); state_in may equal state_out.
+cudaError_t launch_decode_step(const void *x, const float *dt, const float *A, const void *Bm,
+                               const void *Cm, const float *D, const float *state_in, float *state_out,
+                               void *y, const Geom &g, bool bf16, cudaStream_t st);
 cudaError_t launch_chunk_out_big(const void *x, const void *Bm, const void *Cm, const float *dtT,
                                  const float *Gc, const float *states, const float *D, void *y,
                                  const Geom &g, cudaStream_t st);

@@ -17,7 +17,7 @@ from ._lib import SsdError, check, dims as _dims
 __all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out", "ssd_fwd",
            "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd_staged",
            "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_stream_status",
-           "ssd_status_string", "SsdError", "Workspace"]
+           "ssd_status_string", "ssd_decode_step", "SsdError", "Workspace"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -107,6 +107,36 @@ def ssd_chunk_out(x, B, C, dt_t, G_cum, chunk_states, D, chunk_size, y=None, str
                                     _dtype_code(x), int(chunk_size), _stream(stream)),
           "ssd_chunk_out")
     return y
+
+
+def ssd_decode_step(x, dt, A, B, C, D, state, state_out=None, y=None, stream=None):
+    """One token of the recurrence on a carried state.
+
+    x [batch, 1, H, P] (or [batch, H, P]), dt [batch, 1, H] (or [batch, H]),
+    B, C [batch, 1, G, S] (or [batch, G, S]) in x's dtype; A, D [H] f32;
+    state [batch, H, P, S] f32.  The updated state goes to ``state_out``
+    (default: ``state`` itself, updated in place).  Returns (y, state_out),
+    y shaped like x."""
+    x4 = x if x.dim() == 4 else x.unsqueeze(1)
+    B4 = B if B.dim() == 4 else B.unsqueeze(1)
+    C4 = C if C.dim() == 4 else C.unsqueeze(1)
+    d = _geom(x4, B4)
+    if C4.shape != B4.shape:
+        raise ValueError("B and C must have the same shape")
+    if d.seqlen != 1:
+        raise ValueError("the decode step takes one token")
+    if tuple(state.shape) != (d.batch, d.nheads, d.headdim, d.dstate):
+        raise ValueError("state must be [batch, nheads, headdim, dstate]")
+    if state_out is None:
+        state_out = state
+    if y is None:
+        y = torch.empty_like(x)
+    check(_lib.load().ssd_decode_step(_ptr(x), _ptr(_f32(dt, "dt")), _ptr(_f32(A, "A")), _ptr(B),
+                                      _ptr(C), _ptr(_f32(D, "D")), _ptr(_f32(state, "state")),
+                                      _ptr(_f32(state_out, "state_out")), _ptr(y), d,
+                                      _dtype_code(x), _stream(stream)),
+          "ssd_decode_step")
+    return y, state_out
 
 
 def ssd_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, dtype, chunk_size,

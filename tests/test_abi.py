@@ -109,3 +109,24 @@ def test_auto_chunk_size_is_supported(lib):
     for L in (1, 64, 1000, 4096, 262144):
         T = lib.ssd_fwd_chosen_chunk_size(_lib.dims(1, L, 8, 64, 128, 1), 0)
         assert T in (64, 128, 256)
+
+
+def test_decode_step_validation(lib):
+    before = lib.ssd_launch_count()
+    d1 = _lib.dims(2, 1, 4, 16, 32, 2)
+    args = lambda si=FAKE, so=FAKE, y=FAKE, x=FAKE: (x, FAKE, FAKE, FAKE, FAKE, FAKE, si, so, y)
+    # more than one token
+    assert lib.ssd_decode_step(*args(), _lib.dims(2, 2, 4, 16, 32, 2), 0, None) == \
+        _lib.SSD_ERR_INVALID_ARG
+    assert lib.ssd_decode_step(*args(x=None), d1, 0, None) == _lib.SSD_ERR_INVALID_ARG
+    # element alignment only: 8-byte offsets are fine, odd addresses are not
+    assert lib.ssd_decode_step(*args(y=ctypes.c_void_p(0x10001)), d1, 0, None) == \
+        _lib.SSD_ERR_ALIGNMENT
+    assert lib.ssd_decode_step(*args(si=ctypes.c_void_p(0x10002), so=ctypes.c_void_p(0x10002)),
+                               d1, 1, None) == _lib.SSD_ERR_ALIGNMENT
+    assert lib.ssd_decode_step(*args(so=None), d1, 0, None) == _lib.SSD_ERR_INVALID_ARG
+    assert lib.ssd_decode_step(*args(), d1, 5, None) == _lib.SSD_ERR_INVALID_ARG  # dtype
+    # partly overlapping state buffers (the same buffer is fine: in place)
+    assert lib.ssd_decode_step(*args(si=FAKE, so=ctypes.c_void_p(0x10000 + 256)), d1, 0,
+                               None) == _lib.SSD_ERR_INVALID_ARG
+    assert lib.ssd_launch_count() == before

@@ -243,6 +243,23 @@ def test_two_halves_with_carry_equal_full_run(oracle_mod, split):
     assert_close(o2["final_state"], full["final_state"], 1e-12, "final")
 
 
+def test_token_by_token_with_carry_equals_full_run(oracle_mod):
+    """The decode step's reference: L one-token calls, each starting from the
+    previous call's final state, reproduce one L-token call (section
+    "Mamba-2 架构": the recurrence needs nothing but the carried state)."""
+    c = case(2, 9, 3, 4, 6, 3, 4, seed=29)
+    full = run(oracle_mod, c, 4)
+    state, ys = c["init"], []
+    for t in range(9):
+        one = {k: (v[:, t:t + 1] if k in ("x", "dt", "B", "C") else v) for k, v in c.items()}
+        one["init"] = state
+        o = run(oracle_mod, one, 1)
+        ys.append(o["y"])
+        state = o["final_state"]
+    assert_close(np.concatenate(ys, axis=1), full["y"], 1e-12, "y")
+    assert_close(state, full["final_state"], 1e-12, "final")
+
+
 def test_chunk_states_are_prefix_final_states(oracle_mod):
     c = case(1, 70, 2, 3, 4, 1, 16, seed=17)
     out = run(oracle_mod, c, 16, want_states=True)
