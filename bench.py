@@ -8,6 +8,10 @@ x/B/C, f32 dt/A/D, zero initial state, final state returned).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--no-cpu-baseline]
 
+Decode workloads (``--workload decode-...``) time ssd_decode_step instead:
+one step is one token for every sequence of the batch on its carried f32
+state, and the line's metric is decode tokens (sequences) per second.
+
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (the
 units -- batch rows and heads -- are independent; no collective on the data
 path), so scaling is weak and `value` counts the tokens of all ranks.
@@ -61,6 +65,12 @@ for _L in (1024, 4096, 16384, 65536, 262144, 4095):
         WORKLOADS[f"sweep-B{_sh.batch}-L{_L}-H64-P64-S{_S}-T128"] = (_sh, torch.bfloat16, "zero",
                                                                      False)
 DEFAULT = "mamba2-2.7b-layer-B4-L4096-H80-P64-S128-T256"
+# single-token decode steps on a carried state: name -> (batch, H, P, S, G, dtype)
+DECODE = {
+    "decode-B128-H80-P64-S128": (128, 80, 64, 128, 1, torch.bfloat16),
+    "decode-B4-H80-P64-S128": (4, 80, 64, 128, 1, torch.bfloat16),
+}
+DECODE_METRIC = "SSD decode step: sequences (tokens) per second on 1 GB300, carried f32 state"
 
 
 # ------------------------------------------------------------------ accounting
@@ -430,6 +440,162 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# ------------------------------------------------------------------ decode step
+
+def decode_bytes(b, H, P, S, G, dtype) -> int:
+    """Algorithmic bytes of one decode step: the f32 state read and written
+    once, x read and y written, B and C, dt, A and D."""
+    e = elem_bytes(dtype)
+    return 2 * b * H * P * S * 4 + 2 * b * H * P * e + 2 * b * G * S * e + b * H * 4 + 2 * H * 4
+
+
+def run_decode(args):
+    """Decode steps of a batch of sequences on their carried states: one step
+    is one ssd_decode_step call (one token per sequence)."""
+    import state_space_sequence_cumsum_gb300 as ssd
+    from state_space_sequence_cumsum_gb300 import _lib
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    b, H, P, S, G, dtype = DECODE[args.workload]
+    steps_tok = max(3, args.warmup) + 2 * args.steps + 2
+    shape = Shape(b, steps_tok, H, P, S, G, 64)
+    inp = make_inputs(shape, dtype=dtype, init="randn", seed=rank, init_std=0.5)
+    lib = _lib.load()
+    g = {k: v.to(dev) for k, v in inp.items()}
+    # per-token inputs, each its own (aligned) tensor
+    tok = [tuple(g[k][:, t:t + 1].contiguous() for k in ("x", "dt", "B", "C"))
+           for t in range(steps_tok)]
+    state = g["init"].clone()
+    y = torch.empty_like(tok[0][0])
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(t):
+        x, dt, Bt, Ct = tok[t]
+        ssd.ssd_decode_step(x, dt, g["A"], Bt, Ct, g["D"], state, y=y)
+
+    t_next = 0
+    for _ in range(max(3, args.warmup)):
+        step(t_next)
+        t_next += 1
+    torch.cuda.synchronize(dev)
+    if ssd.ssd_stream_status() != 0:
+        raise RuntimeError("kernel status during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    launches0 = lib.ssd_launch_count()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            ev[k][0].record(stream)
+            step(t_next)
+            ev[k][1].record(stream)
+            t_next += 1
+        torch.cuda.synchronize(dev)
+        clk.mark_end()
+    if ws > 1:
+        torch.distributed.barrier()
+    launches = lib.ssd_launch_count() - launches0
+    ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    peaks, peak_src = load_peaks()
+    kb = decode_bytes(b, H, P, S, G, dtype)
+    achieved = kb / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "decode", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": profiled_traffic("decode", args.workload), "algorithmic_bytes": kb,
+                "kernel_ms": round(ms, 5), "peak_source": peak_src}
+
+    # e2e: the step's token inputs from pinned host memory, y back; the state
+    # stays resident on the device, as it does between decode steps
+    host = [tuple(v.cpu().pin_memory() for v in tok[t]) for t in range(2)]
+    dev_in = tuple(torch.empty_like(v) for v in tok[0])
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host[0])
+    d2h = y_host.numel() * y_host.element_size()
+
+    def e2e_step(k):
+        for d, h in zip(dev_in, host[k % 2]):
+            d.copy_(h, non_blocking=True)
+        ssd.ssd_decode_step(dev_in[0], dev_in[1], g["A"], dev_in[2], dev_in[3], g["D"], state, y=y)
+        y_host.copy_(y, non_blocking=True)
+
+    for k in range(2):
+        e2e_step(k)
+    torch.cuda.synchronize(dev)
+    e_ms = []
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step(k)
+        c.record(stream)
+        c.synchronize()
+        e_ms.append(a.elapsed_time(c))
+    e_ms_mean = statistics.mean(e_ms)
+    if ssd.ssd_stream_status() != 0:
+        raise RuntimeError("kernel status in the timed region")
+    line = {
+        "metric": DECODE_METRIC, "value": round(ws * b / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "batch": b, "nheads": H, "headdim": P,
+                   "dstate": S, "ngroups": G, "state": "f32, updated in place",
+                   "parallelism": f"replicas{ws}",
+                   "l2": "flushed before every timed step (512 MB write, outside the events)"},
+        "roofline": roofline,
+        "e2e": {"value": round(ws * b / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e_ms_mean, 4)},
+        "gpu_launches": int(launches),
+    }
+    clocks = clk.summary()
+    if clocks:
+        line["clocks"] = clocks
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_cpu_baseline(inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def decode_cpu_baseline(inp, budget_s: float = 5.0):
+    """The oracle as it stands on a bounded sample: one-token calls on the
+    carried state of one batch row at a time, rows in turn."""
+    import oracle
+    oracle.build()
+    threads = oracle.cpu_cores()
+    nb = inp["x"].shape[0]
+    t_acc, n, rows = 0.0, 0, 0
+    while t_acc < budget_s:
+        r = slice(rows % nb, rows % nb + 1)
+        args_ = [oracle._f64(v) for v in (inp["x"][r, :1], inp["dt"][r, :1], inp["A"],
+                                          inp["B"][r, :1], inp["C"][r, :1], inp["D"])]
+        init = oracle._f64(inp["init"][r])
+        t0 = time.perf_counter()
+        oracle.fwd(*args_, 1, init=init, nthreads=threads)
+        t_acc += time.perf_counter() - t0
+        n += 1
+        rows += 1
+    return {"value": round(n / t_acc, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"float64 one-token recurrence on {n} single-row states in {t_acc:.2f} s wall"}
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -470,16 +636,45 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_decode_reference(args):
+    """Reference arm of a decode workload: the oracle on the host cores, one
+    single-row one-token call per step."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    b, H, P, S, G, dtype = DECODE[args.workload]
+    inp = make_inputs(Shape(b, 1, H, P, S, G, 64), dtype=dtype, init="randn", seed=0,
+                      init_std=0.5)
+    cb = decode_cpu_baseline(inp, budget_s=max(1.0, 0.05 * args.steps))
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": cb["value"], "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(1, args.warmup),
+        "ms_per_step": round(1e3 / cb["value"], 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": b, "nheads": H, "headdim": P,
+                   "dstate": S, "ngroups": G},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(DECODE))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.workload in DECODE:
+        if args.impl == "reference":
+            run_decode_reference(args)
+        else:
+            run_decode(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

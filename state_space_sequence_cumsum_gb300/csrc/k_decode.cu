@@ -13,11 +13,11 @@
 // kernel lpr lanes of a warp share a row (lpr = the largest power of two
 // dividing the row's count of 4-float vectors, at most 32), each lane taking
 // every lpr-th vector, at most four per row; C . h is reduced over those
-// lanes with shuffles.  Each warp pass loads two row sets before it
-// computes, so every lane keeps several 16-byte loads in flight.  Other
-// dstates (S % 4 != 0, or more than four vectors per lane) take a plain
-// kernel with one warp per row.  With L = 1 the row index is also the index
-// of x and y, and row / P that of dt.
+// lanes with shuffles.  Work items are blocks of rows of one (b, h), so the
+// index arithmetic, the decay and the B / C vectors are set up once per
+// block.  Other dstates (S % 4 != 0, more than four vectors per lane, or
+// unaligned state / B / C) take a plain kernel with one warp per row.  With
+// L = 1 the row index is also the index of x and y, and row / P that of dt.
 #include "common.cuh"
 #include "ssd_internal.h"
 
@@ -31,6 +31,7 @@ struct DecGeom {
     int P, H, G, hpg, S;
     int lpr;       // lanes per row (power of two, divides 32)
     int vpl;       // vectors per lane per row
+    int passes;    // warp passes per work item (main kernel)
 };
 
 // four inputs of B or C as f32: one 8-byte load for bf16, 16 bytes for f32
@@ -51,7 +52,7 @@ __device__ __forceinline__ void load4(const float *p, float (&v)[4])
     v[3] = u.w;
 }
 
-// Where row r's inputs live, and its decay and input weight.
+// Where row r's inputs live, and its decay and input weight (plain kernel).
 struct RowIn {
     int64_t bg;  // b * G + group: B / C vector
     float decay, dtx, xp, dh;
@@ -72,7 +73,12 @@ __device__ __forceinline__ RowIn row_inputs(int64_t r, const TI *x, const float 
     return o;
 }
 
-template <typename TI>
+// Main kernel.  A work item is a block of rows of one (b, h): its index
+// arithmetic, decay and B / C vectors are set up once and reused by every
+// row of the block.  A warp pass covers NSET row sets of 32 / lpr rows; the
+// state loads of all of them are issued before any is used (NSET * MAXV
+// 16-byte loads in flight per lane).
+template <typename TI, int MAXV>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const TI *__restrict__ x,
                                                              const float *__restrict__ dt,
                                                              const float *__restrict__ A,
@@ -82,65 +88,80 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const TI *__restric
                                                              const float *state_in, float *state_out,
                                                              TI *__restrict__ y, DecGeom g)
 {
-    constexpr int kMaxV = 4;
+    constexpr int NSET = 8 / MAXV;
     const int lane = threadIdx.x & 31;
     const int sub = lane & (g.lpr - 1), rw = lane / g.lpr;
-    const int rpw = 32 / g.lpr;  // rows per warp pass per row set
-    const int64_t warp0 = (int64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kDecThreads / 32);
+    const int rpw = 32 / g.lpr;                 // rows of one row set
+    const int rows_per_item = NSET * rpw * g.passes;
+    const unsigned npb = ((unsigned)g.P + rows_per_item - 1) / rows_per_item;
+    const unsigned n_items = (unsigned)(g.rows / g.P) * npb;
+    const unsigned warp0 = blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
+    const unsigned nwarps = gridDim.x * (kDecThreads / 32);
 
-    for (int64_t base = warp0 * 2 * rpw; base < g.rows; base += nwarps * 2 * rpw) {
-        int64_t row[2];
-        float4 hv[2][kMaxV];
-        // the state loads of both row sets first
+    for (unsigned item = warp0; item < n_items; item += nwarps) {
+        const unsigned bh = item / npb, pb = item - bh * npb;
+        const unsigned h = bh % (unsigned)g.H, b = bh / (unsigned)g.H;
+        const unsigned bg = b * (unsigned)g.G + h / (unsigned)g.hpg;
+        const float dtv = dt[bh];
+        const float decay = expf(A[h] * dtv);
+        const float dh = D[h];
+        float bv[MAXV][4], cv[MAXV][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t r = base + u * rpw + rw;
-            row[u] = r < g.rows ? r : -1;
-            if (row[u] >= 0) {
-                const float4 *src = reinterpret_cast<const float4 *>(state_in + r * g.S);
-#pragma unroll
-                for (int k = 0; k < kMaxV; ++k)
-                    if (k < g.vpl)
-                        hv[u][k] = src[sub + k * g.lpr];
+        for (int k = 0; k < MAXV; ++k)
+            if (k < g.vpl) {
+                load4(Bm + (size_t)bg * g.S + 4 * (sub + k * g.lpr), bv[k]);
+                load4(Cm + (size_t)bg * g.S + 4 * (sub + k * g.lpr), cv[k]);
             }
-        }
+        // this head's state, x and y (offsets within a head fit 32 bits)
+        const size_t head0 = (size_t)bh * g.P;
+        const float4 *sin4 = reinterpret_cast<const float4 *>(state_in + head0 * g.S) + sub;
+        float4 *sout4 = reinterpret_cast<float4 *>(state_out + head0 * g.S) + sub;
+        const TI *xh = x + head0;
+        TI *yh = y + head0;
+        const int vrow = g.S >> 2;  // 16-byte vectors per row
+        for (int pass = 0; pass < g.passes; ++pass) {
+            const int pbase = (int)pb * rows_per_item + pass * NSET * rpw + rw;
+            float4 hv[NSET][MAXV];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t r = row[u];
-            float acc = 0.f, xp = 0.f, dh = 0.f;
-            if (r >= 0) {
-                const RowIn in = row_inputs(r, x, dt, A, D, g);
-                xp = in.xp;
-                dh = in.dh;
-                const TI *bp = Bm + in.bg * g.S;
-                const TI *cp = Cm + in.bg * g.S;
-                float4 *dst = reinterpret_cast<float4 *>(state_out + r * g.S);
+            for (int u = 0; u < NSET; ++u) {
+                const int p = pbase + u * rpw;
+                if (p < g.P) {
 #pragma unroll
-                for (int k = 0; k < kMaxV; ++k) {
-                    if (k < g.vpl) {
-                        const int vi = sub + k * g.lpr;
-                        float bv[4], cv[4];
-                        load4(bp + 4 * vi, bv);
-                        load4(cp + 4 * vi, cv);
-                        float4 h4 = hv[u][k];
-                        h4.x = fmaf(in.decay, h4.x, in.dtx * bv[0]);
-                        h4.y = fmaf(in.decay, h4.y, in.dtx * bv[1]);
-                        h4.z = fmaf(in.decay, h4.z, in.dtx * bv[2]);
-                        h4.w = fmaf(in.decay, h4.w, in.dtx * bv[3]);
-                        acc = fmaf(cv[0], h4.x, acc);
-                        acc = fmaf(cv[1], h4.y, acc);
-                        acc = fmaf(cv[2], h4.z, acc);
-                        acc = fmaf(cv[3], h4.w, acc);
-                        dst[vi] = h4;
-                    }
+                    for (int k = 0; k < MAXV; ++k)
+                        if (k < g.vpl)
+                            hv[u][k] = sin4[p * vrow + k * g.lpr];
                 }
             }
-            // C . h over the row's lanes (every lane takes part in the shuffles)
-            for (int o = g.lpr >> 1; o > 0; o >>= 1)
-                acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (r >= 0 && sub == 0)
-                y[r] = from_f32<TI>(acc + dh * xp);
+#pragma unroll
+            for (int u = 0; u < NSET; ++u) {
+                const int p = pbase + u * rpw;
+                float acc = 0.f, xp = 0.f;
+                if (p < g.P) {
+                    xp = to_f32(xh[p]);
+                    const float dtx = dtv * xp;
+                    float4 *dst = sout4 + p * vrow;
+#pragma unroll
+                    for (int k = 0; k < MAXV; ++k) {
+                        if (k < g.vpl) {
+                            float4 h4 = hv[u][k];
+                            h4.x = fmaf(decay, h4.x, dtx * bv[k][0]);
+                            h4.y = fmaf(decay, h4.y, dtx * bv[k][1]);
+                            h4.z = fmaf(decay, h4.z, dtx * bv[k][2]);
+                            h4.w = fmaf(decay, h4.w, dtx * bv[k][3]);
+                            acc = fmaf(cv[k][0], h4.x, acc);
+                            acc = fmaf(cv[k][1], h4.y, acc);
+                            acc = fmaf(cv[k][2], h4.z, acc);
+                            acc = fmaf(cv[k][3], h4.w, acc);
+                            dst[k * g.lpr] = h4;
+                        }
+                    }
+                }
+                // C . h over the row's lanes (every lane takes part in the shuffles)
+                for (int o = g.lpr >> 1; o > 0; o >>= 1)
+                    acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (p < g.P && sub == 0)
+                    yh[p] = from_f32<TI>(acc + dh * xp);
+            }
         }
     }
 }
@@ -204,13 +225,29 @@ cudaError_t launch_dec(const void *x, const float *dt, const float *A, const voi
             dg.lpr *= 2;
         dg.vpl = vpr / dg.lpr;
         if (dg.vpl <= 4) {
-            const int rows_per_block = (kDecThreads / 32) * 2 * (32 / dg.lpr);
-            int64_t blocks = (dg.rows + rows_per_block - 1) / rows_per_block;
+            const int maxv = dg.vpl == 1 ? 1 : (dg.vpl == 2 ? 2 : 4);
+            // two passes per item unless that leaves fewer than 16 warps per SM
+            const int rows_per_pass = (8 / maxv) * (32 / dg.lpr);
+            const int64_t heads = dg.rows / dg.P;
+            const int64_t items2 = heads * ((dg.P + 2 * rows_per_pass - 1) / (2 * rows_per_pass));
+            dg.passes = items2 >= (int64_t)sm_count_decode() * 16 ? 2 : 1;
+            const int rows_per_item = rows_per_pass * dg.passes;
+            const int64_t items = heads * ((dg.P + rows_per_item - 1) / rows_per_item);
+            int64_t blocks = (items + kDecThreads / 32 - 1) / (kDecThreads / 32);
             if (blocks > cap)
                 blocks = cap;
-            decode_kernel<TI><<<(unsigned)blocks, kDecThreads, 0, st>>>(
-                static_cast<const TI *>(x), dt, A, static_cast<const TI *>(Bm),
-                static_cast<const TI *>(Cm), D, state_in, state_out, static_cast<TI *>(y), dg);
+            const TI *xt = static_cast<const TI *>(x), *bt = static_cast<const TI *>(Bm),
+                     *ct = static_cast<const TI *>(Cm);
+            TI *yt = static_cast<TI *>(y);
+            if (maxv == 1)
+                decode_kernel<TI, 1><<<(unsigned)blocks, kDecThreads, 0, st>>>(
+                    xt, dt, A, bt, ct, D, state_in, state_out, yt, dg);
+            else if (maxv == 2)
+                decode_kernel<TI, 2><<<(unsigned)blocks, kDecThreads, 0, st>>>(
+                    xt, dt, A, bt, ct, D, state_in, state_out, yt, dg);
+            else
+                decode_kernel<TI, 4><<<(unsigned)blocks, kDecThreads, 0, st>>>(
+                    xt, dt, A, bt, ct, D, state_in, state_out, yt, dg);
             note_launch(1);
             return cudaGetLastError();
         }
