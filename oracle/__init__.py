@@ -15,6 +15,10 @@ CUDA Tile (cuTile)" (dbyun.net/article/14364):
   "Kernel 2: fwd_pass_state" defines them.
 * ``chunk_cumsum``  -- section "Kernel 1": the within-chunk cumulative sum of
   A[h]*dt scaled by log2(e).
+* ``bwd``           -- the gradients of ``fwd``'s recurrence with respect to
+  every input, by the adjoint recurrence (reverse-mode differentiation of
+  the same token loop; the pages name the backward pass but do not give
+  it).  Pinned by central finite differences.
 
 The arithmetic lives in ``ssd_oracle.c`` (plain C, float64, OpenMP over
 (batch, head)).  Inputs of any dtype are widened exactly to float64 before
@@ -58,6 +62,8 @@ def _bind(path: str):
     lib.ssd_oracle_chunk_cumsum.restype = ctypes.c_int
     lib.ssd_oracle_fwd.argtypes = [i64] * 7 + [dp] * 10 + [ctypes.c_int]
     lib.ssd_oracle_fwd.restype = ctypes.c_int
+    lib.ssd_oracle_bwd.argtypes = [i64] * 6 + [dp] * 16 + [ctypes.c_int]
+    lib.ssd_oracle_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -134,6 +140,36 @@ def fwd(x, dt, A, Bm, Cm, D, chunk_size: int, init=None, want_states: bool = Fal
     return out
 
 
+def bwd(x, dt, A, Bm, Cm, D, dy, init=None, dfinal=None, nthreads: int = 0,
+        _lib_override=None) -> dict:
+    """Gradients of the token recurrence by its adjoint (float64).
+
+    For a scalar loss with dloss/dy = dy [B,L,H,P] and dloss/dfinal = dfinal
+    [B,H,P,S] (None: zero), returns dx, ddt, dA, dB, dC, dD and dinit
+    (dinit is the gradient with respect to the initial state, zeros when
+    init is None)."""
+    x, dt, A, Bm, Cm, D, dy, init, dfinal = (_f64(v) for v in (x, dt, A, Bm, Cm, D, dy, init,
+                                                                 dfinal))
+    B, L, H, P = x.shape
+    G, S = Bm.shape[2], Bm.shape[3]
+    if dy.shape != x.shape or dt.shape != (B, L, H) or Bm.shape != (B, L, G, S) \
+            or Cm.shape != Bm.shape or A.shape != (H,) or D.shape != (H,):
+        raise ValueError("oracle bwd: inconsistent input shapes")
+    for st in (init, dfinal):
+        if st is not None and st.shape != (B, H, P, S):
+            raise ValueError("oracle bwd: states must be [B,H,P,S]")
+    out = {"dx": np.empty_like(x), "ddt": np.empty_like(dt), "dA": np.empty(H),
+           "dB": np.empty_like(Bm), "dC": np.empty_like(Cm), "dD": np.empty(H),
+           "dinit": np.empty((B, H, P, S))}
+    rc = (_lib_override or _load()).ssd_oracle_bwd(
+        B, L, H, P, S, G, _ptr(x), _ptr(dt), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(D), _ptr(init),
+        _ptr(dy), _ptr(dfinal), _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]),
+        _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dinit"]), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle bwd failed (rc={rc})")
+    return out
+
+
 def cpu_cores() -> int:
     """Threads the oracle's OpenMP loop uses by default on this host."""
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -153,6 +189,9 @@ class Variant:
 
     def chunk_cumsum(self, *args, **kw):
         return chunk_cumsum(*args, _lib_override=self._lib, **kw)
+
+    def bwd(self, *args, **kw):
+        return bwd(*args, _lib_override=self._lib, **kw)
 
     _f64 = staticmethod(_f64)
 

@@ -140,3 +140,153 @@ int ssd_oracle_fwd(int64_t B, int64_t L, int64_t H, int64_t P, int64_t S,
     }
     return rc;
 }
+
+/* Gradients of the token recurrence ("Mamba-2 架构") by its adjoint, for a
+ * scalar loss whose gradients with respect to y and the final state are dy
+ * and dfinal (dfinal may be NULL: zero).  Per (b, h), g = h / (H / G):
+ *
+ *   forward, keeping every state:  h_{-1} = init,
+ *     a_t = exp(A dt_t),  h_t = a_t h_{t-1} + dt_t x_t B_t^T,  y_t = h_t C_t + D x_t
+ *   backward, t = L-1 .. 0, with the adjoint state dh (P x S) = dfinal:
+ *     dh    += dy_t C_t^T                         (y_t reads h_t)
+ *     dC_t  += h_t^T dy_t                         (summed over the group's heads)
+ *     dD    += dy_t . x_t
+ *     dx_t   = D dy_t + dt_t dh B_t
+ *     dB_t  += dt_t dh^T x_t                      (summed over the group's heads)
+ *     da     = sum dh * h_{t-1}
+ *     ddt_t  = x_t^T dh B_t + A a_t da
+ *     dA    += dt_t a_t da
+ *     dh     = a_t dh                             (to h_{t-1})
+ *   dinit = dh  (if dinit is not NULL).
+ *
+ * Layouts as in ssd_oracle_fwd; dy like y, dfinal / dinit like init; dx like
+ * x, ddt like dt, dA / dD [H], dB / dC like Bm / Cm.  Parallel over (b, g):
+ * the heads of a group run in turn, so the group sums need no atomics.
+ * Memory: (L + 1) P S doubles per thread (every state is kept). */
+int ssd_oracle_bwd(int64_t B, int64_t L, int64_t H, int64_t P, int64_t S, int64_t G,
+                   const double *x, const double *dt, const double *A,
+                   const double *Bm, const double *Cm, const double *D,
+                   const double *init, const double *dy, const double *dfinal,
+                   double *dx, double *ddt, double *dA, double *dB, double *dC,
+                   double *dD, double *dinit, int nthreads)
+{
+    if (B < 0 || L < 0 || H <= 0 || P <= 0 || S <= 0 || G <= 0 || H % G != 0)
+        return -1;
+    if (!x || !dt || !A || !Bm || !Cm || !D || !dy || !dx || !ddt || !dA || !dB || !dC || !dD)
+        return -1;
+    const int64_t hpg = H / G;
+    const int64_t PS = P * S;
+    memset(dB, 0, (size_t)(B * L * G * S) * sizeof(double));
+    memset(dC, 0, (size_t)(B * L * G * S) * sizeof(double));
+    /* per-(b, h) partial sums of dA and dD, reduced at the end in a fixed order */
+    double *pA = (double *)calloc((size_t)(B * H), sizeof(double));
+    double *pD = (double *)calloc((size_t)(B * H), sizeof(double));
+    if (!pA || !pD) {
+        free(pA);
+        free(pD);
+        return -2;
+    }
+    int rc = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t bg = 0; bg < B * G; ++bg) {
+        const int64_t b = bg / G, g = bg % G;
+        double *traj = (double *)malloc((size_t)((L + 1) * PS) * sizeof(double));
+        double *adj = (double *)malloc((size_t)PS * sizeof(double));
+        if (!traj || !adj) {
+            free(traj);
+            free(adj);
+            rc = -2;
+            continue;
+        }
+        for (int64_t h = g * hpg; h < (g + 1) * hpg; ++h) {
+            const int64_t bh = b * H + h;
+            /* forward: traj[t + 1] = h_t, traj[0] = init */
+            if (init)
+                memcpy(traj, init + bh * PS, (size_t)PS * sizeof(double));
+            else
+                memset(traj, 0, (size_t)PS * sizeof(double));
+            for (int64_t t = 0; t < L; ++t) {
+                const double dtv = dt[(b * L + t) * H + h];
+                const double a = exp(A[h] * dtv);
+                const double *xt = x + ((b * L + t) * H + h) * P;
+                const double *bt = Bm + ((b * L + t) * G + g) * S;
+                const double *prev = traj + t * PS;
+                double *cur = traj + (t + 1) * PS;
+                for (int64_t p = 0; p < P; ++p)
+                    for (int64_t s = 0; s < S; ++s)
+                        cur[p * S + s] = a * prev[p * S + s] + dtv * xt[p] * bt[s];
+            }
+            /* backward */
+            if (dfinal)
+                memcpy(adj, dfinal + bh * PS, (size_t)PS * sizeof(double));
+            else
+                memset(adj, 0, (size_t)PS * sizeof(double));
+            double sA = 0.0, sD = 0.0;
+            for (int64_t t = L - 1; t >= 0; --t) {
+                const double dtv = dt[(b * L + t) * H + h];
+                const double a = exp(A[h] * dtv);
+                const double *xt = x + ((b * L + t) * H + h) * P;
+                const double *bt = Bm + ((b * L + t) * G + g) * S;
+                const double *ct = Cm + ((b * L + t) * G + g) * S;
+                const double *dyt = dy + ((b * L + t) * H + h) * P;
+                const double *ht = traj + (t + 1) * PS;
+                const double *hprev = traj + t * PS;
+                double *dxt = dx + ((b * L + t) * H + h) * P;
+                double *dbt = dB + ((b * L + t) * G + g) * S;
+                double *dct = dC + ((b * L + t) * G + g) * S;
+                for (int64_t p = 0; p < P; ++p)
+                    for (int64_t s = 0; s < S; ++s)
+                        adj[p * S + s] += dyt[p] * ct[s];
+                for (int64_t s = 0; s < S; ++s) {
+                    double acc = 0.0;
+                    for (int64_t p = 0; p < P; ++p)
+                        acc += ht[p * S + s] * dyt[p];
+                    dct[s] += acc;
+                }
+                double ddirect = 0.0, da = 0.0;
+                for (int64_t p = 0; p < P; ++p) {
+                    sD += dyt[p] * xt[p];
+                    double hb = 0.0;
+                    for (int64_t s = 0; s < S; ++s) {
+                        hb += adj[p * S + s] * bt[s];
+                        da += adj[p * S + s] * hprev[p * S + s];
+                    }
+                    dxt[p] = D[h] * dyt[p] + dtv * hb;
+                    ddirect += xt[p] * hb;
+                }
+                for (int64_t s = 0; s < S; ++s) {
+                    double acc = 0.0;
+                    for (int64_t p = 0; p < P; ++p)
+                        acc += adj[p * S + s] * xt[p];
+                    dbt[s] += dtv * acc;
+                }
+                ddt[(b * L + t) * H + h] = ddirect + A[h] * a * da;
+                sA += dtv * a * da;
+                for (int64_t k = 0; k < PS; ++k)
+                    adj[k] *= a;
+            }
+            if (dinit)
+                memcpy(dinit + bh * PS, adj, (size_t)PS * sizeof(double));
+            pA[bh] = sA;
+            pD[bh] = sD;
+        }
+        free(traj);
+        free(adj);
+    }
+    for (int64_t h = 0; h < H; ++h) {
+        double sa = 0.0, sd = 0.0;
+        for (int64_t b = 0; b < B; ++b) {
+            sa += pA[b * H + h];
+            sd += pD[b * H + h];
+        }
+        dA[h] = sa;
+        dD[h] = sd;
+    }
+    free(pA);
+    free(pD);
+    return rc;
+}
