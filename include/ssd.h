@@ -172,6 +172,36 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
                      void *stream);
 
 /*
+ * Backward pass: gradients of the forward (ssd_fwd's y and final state) with
+ * respect to every input, for a scalar loss whose gradients with respect to
+ * y and the final state are dy [B, L, H, P] (call dtype) and dfinal
+ * [B, H, P, S] f32 (NULL = zero).  The pages name the backward pass but do
+ * not give it; it is the adjoint of the recurrence of section "Mamba-2 架构"
+ * worked chunk by chunk (64-token chunks) like the forward:
+ *   a reverse state pass carries the state gradient from the last chunk to
+ *   the first, dh_in = exp(L_T) dh_out + sum_i exp(L_i) dy_i C_i^T, and each
+ *   (batch, chunk, head) then forms its dx, ddt, dB, dC, dA, dD terms from
+ *   the chunk's start state (recomputed by the forward state pass) and the
+ *   gradient of its end state.
+ * Outputs (caller-owned device memory, every one written):
+ *   dx [B, L, H, P] (call dtype), ddt [B, L, H] f32, dA [H] f32, dB, dC
+ *   [B, L, G, S] (call dtype; summed over the heads of each group), dD [H]
+ *   f32, dinit [B, H, P, S] f32 (may be NULL: not wanted; the gradient with
+ *   respect to init_state, or to the zero initial state when init_state is
+ *   NULL).
+ * Arithmetic is f32 on CUDA cores (bf16 inputs widened).  Supported: P <= 64
+ * and the sizes of ssd_fwd; other headdims return SSD_ERR_UNSUPPORTED.
+ * workspace: ssd_bwd_workspace_size(dims, dtype) bytes, 256-byte aligned;
+ * contents on entry do not matter.
+ */
+size_t ssd_bwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype);
+ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void *Bm,
+                     const void *Cm, const float *D, const float *init_state, const void *dy,
+                     const float *dfinal, void *dx, float *ddt, float *dA, void *dB, void *dC,
+                     float *dD, float *dinit, ssd_dims_t dims, ssd_dtype_t dtype,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Single-token decode step on a carried state (section "Mamba-2 架构": the
  * recurrence for one token, i.e. how a final state from ssd_fwd is used
  * during generation).  dims.seqlen must be 1; per (b, h), g = h / (H / G):

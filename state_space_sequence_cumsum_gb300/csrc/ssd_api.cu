@@ -2,6 +2,7 @@
 // stage orchestration and the kernel status word.  See include/ssd.h for the
 // contract of every entry point.
 #include <atomic>
+#include <initializer_list>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -198,6 +199,30 @@ Workspace layout(const Geom &g, ssd_path_t path, bool caller_states, char *base)
     return w;
 }
 
+// Workspace of ssd_bwd: G and dt^T [B,H,L], the forward chunk states and
+// their gradients [B,H,nc,P,S], the dB / dC f32 accumulators [B,L,G,S].
+struct BwdWs {
+    float *Gc, *dtT, *states, *dstates, *dB, *dC;
+    size_t bytes;
+};
+BwdWs bwd_layout(const Geom &g, char *base)
+{
+    BwdWs w{};
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        char *p = base ? base + off : nullptr;
+        off += round_up(n * sizeof(float), 256);
+        return reinterpret_cast<float *>(p);
+    };
+    w.Gc = take((size_t)(g.B * g.H * g.L));
+    w.dtT = take((size_t)(g.B * g.H * g.L));
+    w.states = take((size_t)(g.B * g.H * g.nc * g.P * g.S));
+    w.dstates = take((size_t)(g.B * g.H * g.nc * g.P * g.S));
+    w.dB = take((size_t)(g.B * g.L * g.G * g.S));
+    w.dC = take((size_t)(g.B * g.L * g.G * g.S));
+    w.bytes = off;
+    return w;
+}
 }  // namespace
 }  // namespace ssd
 
@@ -421,6 +446,63 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
     SSD_TRY(cuda_status(
         run_state_pass(x, Bm, w.dtT, w.Gc, init_state, states, final_state, g, bf16, st)));
     return cuda_status(run_chunk_out(x, Bm, Cm, w.dtT, w.Gc, states, D, y, g, bf16, st));
+}
+
+size_t ssd_bwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype)
+{
+    Geom g;
+    if (make_geom(dims, bwd_chunk_size(), false, &g) != SSD_OK ||
+        (dtype != SSD_BF16 && dtype != SSD_F32))
+        return 0;
+    return bwd_layout(g, nullptr).bytes;
+}
+
+ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void *Bm,
+                     const void *Cm, const float *D, const float *init_state, const void *dy,
+                     const float *dfinal, void *dx, float *ddt, float *dA, void *dB, void *dC,
+                     float *dD, float *dinit, ssd_dims_t dims, ssd_dtype_t dtype,
+                     void *workspace, size_t workspace_bytes, void *stream)
+{
+    Geom g;
+    SSD_TRY(make_geom(dims, bwd_chunk_size(), false, &g));
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return SSD_ERR_INVALID_ARG;
+    if (!bwd_supported(g))
+        return SSD_ERR_UNSUPPORTED;
+    const bool ne = g.L > 0;
+    for (const void *p : std::initializer_list<const void *>{x, dt, Bm, Cm, dy, dx, ddt, dB, dC})
+        SSD_TRY(need(p, ne));
+    SSD_TRY(need(A, true));
+    SSD_TRY(need(D, true));
+    SSD_TRY(need(dA, true));
+    SSD_TRY(need(dD, true));
+    SSD_TRY(opt(init_state));
+    SSD_TRY(opt(dfinal));
+    SSD_TRY(opt(dinit));
+    const BwdWs need_ws = bwd_layout(g, nullptr);
+    if (ne && (!workspace || workspace_bytes < need_ws.bytes ||
+               (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return SSD_ERR_WORKSPACE;
+    // every argument is valid: nothing was launched before this point
+    cudaStream_t st = (cudaStream_t)stream;
+    SSD_TRY(cuda_status(cudaMemsetAsync(dA, 0, (size_t)g.H * sizeof(float), st)));
+    SSD_TRY(cuda_status(cudaMemsetAsync(dD, 0, (size_t)g.H * sizeof(float), st)));
+    const size_t sbytes = (size_t)(g.B * g.H * g.P * g.S) * sizeof(float);
+    if (!ne) {  // no tokens: the initial state is the final state
+        if (!dinit)
+            return SSD_OK;
+        return cuda_status(dfinal ? cudaMemcpyAsync(dinit, dfinal, sbytes, cudaMemcpyDeviceToDevice, st)
+                                  : cudaMemsetAsync(dinit, 0, sbytes, st));
+    }
+    const BwdWs w = bwd_layout(g, static_cast<char *>(workspace));
+    const bool bf16 = dtype == SSD_BF16;
+    SSD_TRY(cuda_status(launch_chunk_cumsum(dt, A, w.Gc, w.dtT, g, st)));
+    SSD_TRY(cuda_status(run_state_pass(x, Bm, w.dtT, w.Gc, init_state, w.states, nullptr, g, bf16, st)));
+    const size_t bc = (size_t)(g.B * g.L * g.G * g.S) * sizeof(float);
+    SSD_TRY(cuda_status(cudaMemsetAsync(w.dB, 0, bc, st)));
+    SSD_TRY(cuda_status(cudaMemsetAsync(w.dC, 0, bc, st)));
+    return cuda_status(launch_bwd(x, Bm, Cm, dy, w.dtT, w.Gc, A, D, w.states, dfinal, w.dstates,
+                                  dx, ddt, dA, dD, w.dB, w.dC, dB, dC, dinit, g, bf16, st));
 }
 
 ssd_status_t ssd_decode_step(const void *x, const float *dt, const float *A, const void *Bm,

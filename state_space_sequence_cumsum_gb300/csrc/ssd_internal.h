@@ -60,6 +60,16 @@ cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, c
 // Tensor-core chunk output for dstate 384 / 512 (bf16, P = 64, chunk 128),
 // streaming B / C in 128-wide dstate blocks.
 bool chunk_out_big_supported(const Geom &g);
+// Backward pass (k_bwd.cu): 64-token chunks, P <= 64.  states / dstates /
+// Gc / dtT are per 64-token chunk; dBacc / dCacc are zeroed f32 [B,L,G,S]
+// accumulators; dA / dD are zeroed f32 [H] accumulators.
+bool bwd_supported(const Geom &g);
+int bwd_chunk_size();
+cudaError_t launch_bwd(const void *x, const void *Bm, const void *Cm, const void *dy,
+                       const float *dtT, const float *Gc, const float *A, const float *D,
+                       const float *states, const float *dfinal, float *dstates, void *dx,
+                       float *ddt, float *dA, float *dD, float *dBacc, float *dCacc, void *dB,
+                       void *dC, float *dinit, const Geom &g, bool bf16, cudaStream_t st);
 // Single-token decode step (k_decode.cu); state_in may equal state_out.
 cudaError_t launch_decode_step(const void *x, const float *dt, const float *A, const void *Bm,
                                const void *Cm, const float *D, const float *state_in, float *state_out,

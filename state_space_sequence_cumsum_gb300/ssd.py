@@ -17,7 +17,8 @@ from ._lib import SsdError, check, dims as _dims
 __all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out", "ssd_fwd",
            "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd_staged",
            "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_stream_status",
-           "ssd_status_string", "ssd_decode_step", "SsdError", "Workspace"]
+           "ssd_status_string", "ssd_decode_step", "ssd_bwd", "SsdFunction", "SsdError",
+           "Workspace"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -137,6 +138,55 @@ def ssd_decode_step(x, dt, A, B, C, D, state, state_out=None, y=None, stream=Non
                                       _dtype_code(x), _stream(stream)),
           "ssd_decode_step")
     return y, state_out
+
+
+def ssd_bwd(x, dt, A, B, C, D, dy, initial_state=None, dfinal=None, want_dinit=True,
+            workspace=None, stream=None):
+    """Gradients of ssd_fwd's outputs (y and the final state) with respect to
+    every input.  dy is the loss gradient of y (x's dtype), dfinal that of
+    the final state (f32, None = zero).  Returns a dict with dx, ddt, dA, dB,
+    dC, dD and dinit (None unless want_dinit)."""
+    d = _geom(x, B)
+    code = _dtype_code(x)
+    lib = _lib.load()
+    nbytes = lib.ssd_bwd_workspace_size(d, code)
+    if nbytes == 0:
+        raise ValueError("ssd_bwd: invalid sizes")
+    ws = workspace if workspace is not None else Workspace()
+    buf = ws.get(nbytes, x.device)
+    out = {"dx": torch.empty_like(x), "ddt": torch.empty_like(dt),
+           "dA": torch.empty_like(A), "dB": torch.empty_like(B), "dC": torch.empty_like(C),
+           "dD": torch.empty_like(D),
+           "dinit": (torch.empty((d.batch, d.nheads, d.headdim, d.dstate), dtype=torch.float32,
+                                 device=x.device) if want_dinit else None)}
+    check(lib.ssd_bwd(_ptr(x), _ptr(_f32(dt, "dt")), _ptr(_f32(A, "A")), _ptr(B), _ptr(C),
+                      _ptr(_f32(D, "D")), _ptr(_f32(initial_state, "initial_state")), _ptr(dy),
+                      _ptr(_f32(dfinal, "dfinal")), _ptr(out["dx"]), _ptr(out["ddt"]),
+                      _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                      _ptr(out["dinit"]), d, code, ctypes.c_void_p(buf.data_ptr()),
+                      ctypes.c_size_t(nbytes), _stream(stream)),
+          "ssd_bwd")
+    return out
+
+
+class SsdFunction(torch.autograd.Function):
+    """torch.autograd binding: forward is ssd_fwd (y, final state), backward
+    is ssd_bwd.  Both run in the library's kernels."""
+
+    @staticmethod
+    def forward(ctx, x, dt, A, B, C, D, initial_state=None):
+        y, final, _ = ssd_fwd(x, dt, A, B, C, D, chunk_size=0, initial_state=initial_state,
+                              return_final_state=True)
+        ctx.save_for_backward(x, dt, A, B, C, D, initial_state)
+        return y, final
+
+    @staticmethod
+    def backward(ctx, dy, dfinal):
+        x, dt, A, B, C, D, init = ctx.saved_tensors
+        g = ssd_bwd(x, dt, A, B, C, D, dy.contiguous(), initial_state=init,
+                    dfinal=None if dfinal is None else dfinal.contiguous(),
+                    want_dinit=init is not None)
+        return g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], g["dD"], g["dinit"]
 
 
 def ssd_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, dtype, chunk_size,

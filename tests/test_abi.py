@@ -130,3 +130,18 @@ def test_decode_step_validation(lib):
     assert lib.ssd_decode_step(*args(si=FAKE, so=ctypes.c_void_p(0x10000 + 256)), d1, 0,
                                None) == _lib.SSD_ERR_INVALID_ARG
     assert lib.ssd_launch_count() == before
+
+
+def test_bwd_validation(lib):
+    before = lib.ssd_launch_count()
+    d = _lib.dims(2, 100, 4, 16, 32, 2)
+    need = lib.ssd_bwd_workspace_size(d, 0)
+    assert need > 0 and need % 256 == 0
+    args = [FAKE] * 6 + [None, FAKE, None] + [FAKE] * 6 + [None, d, 0]
+    assert lib.ssd_bwd(*args, None, need, None) == _lib.SSD_ERR_WORKSPACE
+    assert lib.ssd_bwd(*args, FAKE, need - 256, None) == _lib.SSD_ERR_WORKSPACE
+    # headdim above 64 is not served by the backward
+    big = _lib.dims(2, 100, 4, 128, 32, 2)
+    a2 = [FAKE] * 6 + [None, FAKE, None] + [FAKE] * 6 + [None, big, 0]
+    assert lib.ssd_bwd(*a2, FAKE, 1 << 40, None) == _lib.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_launch_count() == before
