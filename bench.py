@@ -71,6 +71,9 @@ DECODE = {
     "decode-B4-H80-P64-S128": (4, 80, 64, 128, 1, torch.bfloat16),
 }
 DECODE_METRIC = "SSD decode step: sequences (tokens) per second on 1 GB300, carried f32 state"
+# backward passes: name -> forward workload whose gradients are taken
+BACKWARD = {"bwd-mamba2-2.7b-layer-B4-L4096-H80-P64-S128": "mamba2-2.7b-layer-B4-L4096-H80-P64-S128-T256"}
+BWD_METRIC = "SSD backward tokens/sec on 1 GB300 (all input gradients from dy and dfinal)"
 
 
 # ------------------------------------------------------------------ accounting
@@ -596,6 +599,192 @@ def decode_cpu_baseline(inp, budget_s: float = 5.0):
             "sample": f"float64 one-token recurrence on {n} single-row states in {t_acc:.2f} s wall"}
 
 
+# ------------------------------------------------------------------ backward pass
+
+def bwd_compulsory_bytes(s: Shape, dtype, init: str) -> int:
+    """Read x, dy, B, C, dt, A, D (and init), the final-state gradient; write
+    dx, dB, dC, ddt, dA, dD and the initial-state gradient."""
+    e = elem_bytes(dtype)
+    blh = s.batch * s.seqlen * s.nheads
+    st = s.batch * s.nheads * s.headdim * s.dstate * 4
+    n = 3 * blh * s.headdim * e                                   # x, dy read; dx written
+    n += 4 * s.batch * s.seqlen * s.ngroups * s.dstate * e         # B, C read; dB, dC written
+    n += 2 * blh * 4 + 4 * s.nheads * 4                            # dt, ddt; A, D, dA, dD
+    n += 2 * st + (st if init == "randn" else 0)                   # dfinal, dinit (, init)
+    return n
+
+
+def bwd_flops(s: Shape, T: int = 64) -> int:
+    """Contractions per (batch, chunk of Tc tokens): per head dy x^T, the
+    masked score products for dx, dB, dC (T^2 (P + 2 S)) and seven T S P
+    products (the forward state pass, the reverse state pass, the state
+    terms of dx, dB, dC, C h_in^T and B dS^T); per group C B^T (T^2 S)."""
+    total = 0
+    for c in range((s.seqlen + T - 1) // T):
+        tc = min(T, s.seqlen - c * T)
+        per_head = tc * tc * (2 * s.headdim + 2 * s.dstate) + 7 * tc * s.dstate * s.headdim
+        total += 2 * s.batch * (s.nheads * per_head + s.ngroups * tc * tc * s.dstate)
+    return total
+
+
+def run_bwd(args):
+    """One step = one ssd_bwd call (every stage of the backward) on the
+    forward workload's inputs with random dy and dfinal."""
+    import state_space_sequence_cumsum_gb300 as ssd
+    from state_space_sequence_cumsum_gb300 import _lib
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    fwd_name = BACKWARD[args.workload]
+    shape, dtype, init, _ = WORKLOADS[fwd_name]
+    inp = make_inputs(shape, dtype=dtype, init=init, seed=rank)
+    rng = np.random.default_rng(rank + 11)
+    dy = torch.from_numpy(rng.standard_normal((shape.batch, shape.seqlen, shape.nheads,
+                                               shape.headdim)).astype(np.float32)).to(dtype)
+    dfin = torch.from_numpy(rng.standard_normal((shape.batch, shape.nheads, shape.headdim,
+                                                 shape.dstate)).astype(np.float32))
+    lib = _lib.load()
+    g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    dyd, dfd = dy.to(dev), dfin.to(dev)
+    wsp = ssd.Workspace()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return ssd.ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], dyd,
+                           initial_state=g["init"], dfinal=dfd, workspace=wsp)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if ssd.ssd_stream_status() != 0:
+        raise RuntimeError("kernel status during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    launches0 = lib.ssd_launch_count()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark_end()
+    launches = lib.ssd_launch_count() - launches0
+    ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    peaks, peak_src = load_peaks()
+    cb = bwd_compulsory_bytes(shape, dtype, init)
+    fl = bwd_flops(shape)
+    t_bytes = cb / (peaks["hbm_gbs"] * 1e9)
+    t_flops = fl / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_bytes >= t_flops else "tensor"
+    t_roof = max(t_bytes, t_flops)
+    roofline = ({"bound": "hbm", "achieved": round(cb / (ms / 1e3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                 "unit": "GB/s"} if bound == "hbm" else
+                {"bound": "tensor", "achieved": round(fl / (ms / 1e3) / 1e12, 2),
+                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"})
+    roofline.update({"frac": round(t_roof / (ms / 1e3), 4), "traffic": None, "kernel": "ssd_bwd (whole call)",
+                     "algorithmic_bytes": cb, "algorithmic_flops": fl, "peak_source": peak_src})
+
+    # e2e: the step's inputs (x, dt, B, C, dy, dfinal and init) from pinned host
+    # memory, every gradient back
+    host = {"x": inp["x"], "dt": inp["dt"], "B": inp["B"], "C": inp["C"], "dy": dy, "df": dfin}
+    if inp["init"] is not None:
+        host["init"] = inp["init"]
+    host = {k: v.pin_memory() for k, v in host.items()}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    res = step()
+    outs_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in res.items()
+                 if v is not None}
+    d2h = sum(v.numel() * v.element_size() for v in outs_host.values())
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        r = ssd.ssd_bwd(dev_in["x"], dev_in["dt"], g["A"], dev_in["B"], dev_in["C"], g["D"],
+                        dev_in["dy"], initial_state=dev_in.get("init"), dfinal=dev_in["df"],
+                        workspace=wsp)
+        for k, v in outs_host.items():
+            v.copy_(r[k], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e_ms = []
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        c.record(stream)
+        c.synchronize()
+        e_ms.append(a.elapsed_time(c))
+    e_ms_mean = statistics.mean(e_ms)
+    if ssd.ssd_stream_status() != 0:
+        raise RuntimeError("kernel status in the timed region")
+    tokens = shape.tokens
+    line = {
+        "metric": BWD_METRIC, "value": round(ws * tokens / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "forward": fwd_name, "batch": shape.batch,
+                   "seqlen": shape.seqlen, "nheads": shape.nheads, "headdim": shape.headdim,
+                   "dstate": shape.dstate, "ngroups": shape.ngroups, "chunk_size": 64,
+                   "parallelism": f"replicas{ws}",
+                   "l2": "flushed before every timed step (512 MB write, outside the events)"},
+        "roofline": roofline,
+        "e2e": {"value": round(ws * tokens / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e_ms_mean, 4)},
+        "gpu_launches": int(launches),
+    }
+    clocks = clk.summary()
+    if clocks:
+        line["clocks"] = clocks
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = bwd_cpu_baseline(inp, dy, dfin, shape)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bwd_cpu_baseline(inp, dy, dfin, s: Shape, budget_s: float = 10.0):
+    """The oracle's adjoint as it stands, on a bounded sample: one batch row
+    (every head) over a prefix of the sequence, prefixes doubled until about
+    budget_s of wall time is reached."""
+    import oracle
+    oracle.build()
+    threads = oracle.cpu_cores()
+    Lp, t_acc, tok = 256, 0.0, 0
+    while t_acc < budget_s and Lp <= s.seqlen:
+        sl = (slice(0, 1), slice(0, Lp))
+        t0 = time.perf_counter()
+        oracle.bwd(inp["x"][sl], inp["dt"][sl], inp["A"], inp["B"][sl], inp["C"][sl], inp["D"],
+                   dy[sl], init=None if inp["init"] is None else inp["init"][:1],
+                   dfinal=dfin[:1], nthreads=threads)
+        t_acc += time.perf_counter() - t0
+        tok += Lp
+        Lp *= 2
+    return {"value": round(tok / t_acc, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": (f"float64 adjoint recurrence, batch row 0 (all {s.nheads} heads), sequence "
+                       f"prefixes of 256, 512, ... tokens: {tok} tokens in {t_acc:.2f} s wall")}
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
@@ -660,16 +849,49 @@ def run_decode_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_bwd_reference(args):
+    """Reference arm of a backward workload: the oracle's adjoint on the host
+    cores, a bounded sample per step."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    shape, dtype, init, _ = WORKLOADS[BACKWARD[args.workload]]
+    inp = make_inputs(shape, dtype=dtype, init=init, seed=0)
+    rng = np.random.default_rng(11)
+    dy = torch.from_numpy(rng.standard_normal((shape.batch, shape.seqlen, shape.nheads,
+                                               shape.headdim)).astype(np.float32)).to(dtype)
+    dfin = torch.from_numpy(rng.standard_normal((shape.batch, shape.nheads, shape.headdim,
+                                                 shape.dstate)).astype(np.float32))
+    cb = bwd_cpu_baseline(inp, dy, dfin, shape, budget_s=max(2.0, 0.5 * args.steps))
+    line = {
+        "impl": "reference", "metric": BWD_METRIC, "value": cb["value"], "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(1, args.warmup),
+        "ms_per_step": round(1e3 * shape.tokens / cb["value"], 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "forward": BACKWARD[args.workload]},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS) + sorted(DECODE))
+    ap.add_argument("--workload", default=DEFAULT,
+                    choices=sorted(WORKLOADS) + sorted(DECODE) + sorted(BACKWARD))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.workload in DECODE:
+    if args.workload in BACKWARD:
+        if args.impl == "reference":
+            run_bwd_reference(args)
+        else:
+            run_bwd(args)
+    elif args.workload in DECODE:
         if args.impl == "reference":
             run_decode_reference(args)
         else:
