@@ -15,6 +15,9 @@ CUDA Tile (cuTile)" (dbyun.net/article/14364):
   "Kernel 2: fwd_pass_state" defines them.
 * ``chunk_cumsum``  -- section "Kernel 1": the within-chunk cumulative sum of
   A[h]*dt scaled by log2(e).
+* ``gated_rmsnorm`` -- the gate and RMS normalisation that follow the scan
+  (the post's operator-fusion section names them; the Mamba-2 form, y times
+  silu(z) then a grouped RMS norm and a per-channel weight, is the reading).
 * ``bwd``           -- the gradients of ``fwd``'s recurrence with respect to
   every input, by the adjoint recurrence (reverse-mode differentiation of
   the same token loop; the pages name the backward pass but do not give
@@ -168,6 +171,24 @@ def bwd(x, dt, A, Bm, Cm, D, dy, init=None, dfinal=None, nthreads: int = 0,
     if rc != 0:
         raise ValueError(f"oracle bwd failed (rc={rc})")
     return out
+
+
+def gated_rmsnorm(y, z, weight, eps: float, group_size: int) -> np.ndarray:
+    """The output epilogue that follows the scan ("Mamba-2 forward-pass
+    kernels" post, section on operator fusion: gating and normalisation after
+    the scan), in its Mamba-2 form: per token, with g = y * silu(z) and
+    silu(z) = z / (1 + exp(-z)),
+        out = g / sqrt(mean(g^2 over each group of group_size channels) + eps) * weight.
+    y, z: [..., D] (D = nheads * headdim channels per token, any dtype, widened
+    exactly); weight [D]; returns float64 [..., D]."""
+    y, z, w = _f64(y), _f64(z), _f64(weight)
+    D = y.shape[-1]
+    if z.shape != y.shape or w.shape != (D,) or group_size <= 0 or D % group_size:
+        raise ValueError("oracle gated_rmsnorm: inconsistent shapes")
+    g = y * (z / (1.0 + np.exp(-z)))
+    gg = g.reshape(g.shape[:-1] + (D // group_size, group_size))
+    ms = np.mean(gg * gg, axis=-1, keepdims=True)
+    return (gg / np.sqrt(ms + eps)).reshape(g.shape) * w
 
 
 def cpu_cores() -> int:
