@@ -71,6 +71,9 @@ DECODE = {
     "decode-B4-H80-P64-S128": (4, 80, 64, 128, 1, torch.bfloat16),
 }
 DECODE_METRIC = "SSD decode step: sequences (tokens) per second on 1 GB300, carried f32 state"
+# gated RMS norm after the scan: name -> (tokens, dim, group_size, dtype)
+NORM = {"gated-norm-B4-L4096-H80-P64": (4 * 4096, 80 * 64, 80 * 64, torch.bfloat16)}
+NORM_METRIC = "Gated RMS norm (y * silu(z), one group per token) tokens/sec on 1 GB300"
 # backward passes: name -> forward workload whose gradients are taken
 BACKWARD = {"bwd-mamba2-2.7b-layer-B4-L4096-H80-P64-S128": "mamba2-2.7b-layer-B4-L4096-H80-P64-S128-T256"}
 BWD_METRIC = "SSD backward tokens/sec on 1 GB300 (all input gradients from dy and dfinal)"
@@ -599,6 +602,110 @@ def decode_cpu_baseline(inp, budget_s: float = 5.0):
             "sample": f"float64 one-token recurrence on {n} single-row states in {t_acc:.2f} s wall"}
 
 
+# ------------------------------------------------------------------ gated norm
+
+def run_norm(args):
+    """One step = one ssd_gated_rmsnorm call over every token of the workload."""
+    import state_space_sequence_cumsum_gb300 as ssd
+    from state_space_sequence_cumsum_gb300 import _lib
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    ntok, dim, gs, dtype = NORM[args.workload]
+    gen = torch.Generator().manual_seed(rank)
+    y = torch.randn((ntok, dim), generator=gen).to(dtype)
+    z = torch.randn((ntok, dim), generator=gen).to(dtype)
+    w = 1.0 + 0.1 * torch.randn(dim, generator=gen)
+    lib = _lib.load()
+    yd, zd, wd = y.to(dev), z.to(dev), w.to(dev)
+    out = torch.empty_like(yd)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        ssd.ssd_gated_rmsnorm(yd, zd, wd, group_size=gs, out=out)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    launches0 = lib.ssd_launch_count()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            ev[k][0].record(stream)
+            ssd.ssd_gated_rmsnorm(yd, zd, wd, group_size=gs, out=out)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark_end()
+    launches = lib.ssd_launch_count() - launches0
+    ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    peaks, peak_src = load_peaks()
+    kb = 3 * ntok * dim * elem_bytes(dtype) + dim * 4
+    achieved = kb / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "gated_rmsnorm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": profiled_traffic("gated_rmsnorm", args.workload), "algorithmic_bytes": kb,
+                "kernel_ms": round(ms, 5), "peak_source": peak_src}
+    hy, hz = y.pin_memory(), z.pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e_ms = []
+    for k in range(args.steps + 1):
+        flush.fill_(float(k))
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        yd.copy_(hy, non_blocking=True)
+        zd.copy_(hz, non_blocking=True)
+        ssd.ssd_gated_rmsnorm(yd, zd, wd, group_size=gs, out=out)
+        ho.copy_(out, non_blocking=True)
+        c.record(stream)
+        c.synchronize()
+        if k:
+            e_ms.append(a.elapsed_time(c))
+    e_ms_mean = statistics.mean(e_ms)
+    line = {
+        "metric": NORM_METRIC, "value": round(ws * ntok / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens": ntok, "dim": dim, "group_size": gs,
+                   "parallelism": f"replicas{ws}",
+                   "l2": "flushed before every timed step (512 MB write, outside the events)"},
+        "roofline": roofline,
+        "e2e": {"value": round(ws * ntok / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * ntok * dim * elem_bytes(dtype),
+                "d2h_bytes_per_step": ntok * dim * elem_bytes(dtype), "ms_per_step": round(e_ms_mean, 4)},
+        "gpu_launches": int(launches),
+    }
+    clocks = clk.summary()
+    if clocks:
+        line["clocks"] = clocks
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        n, t_acc = 0, 0.0
+        while t_acc < 5.0 and n < ntok:
+            t0 = time.perf_counter()
+            oracle.gated_rmsnorm(y[n:n + 256], z[n:n + 256], w, 1e-5, gs)
+            t_acc += time.perf_counter() - t0
+            n += 256
+        line["cpu_baseline"] = {"value": round(n / t_acc, 1), "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"numpy float64 on {n} tokens in blocks of 256, {t_acc:.2f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ------------------------------------------------------------------ backward pass
 
 def bwd_compulsory_bytes(s: Shape, dtype, init: str) -> int:
@@ -883,10 +990,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT,
-                    choices=sorted(WORKLOADS) + sorted(DECODE) + sorted(BACKWARD))
+                    choices=sorted(WORKLOADS) + sorted(DECODE) + sorted(BACKWARD) + sorted(NORM))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.workload in BACKWARD:
+    if args.workload in NORM:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the gated norm's reference arm is "
+                              "the oracle sample reported as cpu_baseline on our arm's line"}))
+        else:
+            run_norm(args)
+    elif args.workload in BACKWARD:
         if args.impl == "reference":
             run_bwd_reference(args)
         else:

@@ -202,6 +202,24 @@ ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void 
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Gated RMS norm, the gating and normalisation that follow the scan (the
+ * post's operator-fusion section names gating, normalisation and the output
+ * projection after the scan; gate and norm run here as one pass, the
+ * projection is a plain GEMM).  Per token, over each group of group_size
+ * consecutive channels of the token's dim = nheads * headdim channels:
+ *     g   = y * silu(z),  silu(z) = z / (1 + exp(-z))
+ *     out = g / sqrt(mean(g^2 over the group) + eps) * weight
+ * y, z, out: [ntokens, dim] in the call's dtype (e.g. ssd_fwd's y viewed as
+ * [B*L, H*P]); weight: [dim] f32.  out may be y or z (in place).  Arithmetic
+ * f32.  Only element alignment is required; 16-byte aligned buffers with
+ * group_size a multiple of 8 (bf16) or 4 (f32) take 16-byte vectors.
+ * dim % group_size != 0 or eps < 0 returns SSD_ERR_INVALID_ARG.
+ */
+ssd_status_t ssd_gated_rmsnorm(const void *y, const void *z, const float *weight, void *out,
+                               int64_t ntokens, int64_t dim, int64_t group_size, float eps,
+                               ssd_dtype_t dtype, void *stream);
+
+/*
  * Single-token decode step on a carried state (section "Mamba-2 架构": the
  * recurrence for one token, i.e. how a final state from ssd_fwd is used
  * during generation).  dims.seqlen must be 1; per (b, h), g = h / (H / G):

@@ -505,6 +505,27 @@ ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void 
                                   dx, ddt, dA, dD, w.dB, w.dC, dB, dC, dinit, g, bf16, st));
 }
 
+ssd_status_t ssd_gated_rmsnorm(const void *y, const void *z, const float *weight, void *out,
+                               int64_t ntokens, int64_t dim, int64_t group_size, float eps,
+                               ssd_dtype_t dtype, void *stream)
+{
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return SSD_ERR_INVALID_ARG;
+    if (ntokens < 0 || dim < 1 || group_size < 1 || dim % group_size != 0 || !(eps >= 0.f) ||
+        eps > 1e30f)
+        return SSD_ERR_INVALID_ARG;
+    if (group_size > (1 << 30) || ntokens > (1LL << 40) || (double)ntokens * (double)dim > 4e15)
+        return SSD_ERR_UNSUPPORTED;
+    const size_t esz = dtype == SSD_BF16 ? 2 : 4;
+    if (ntokens > 0) {
+        for (const void *p : std::initializer_list<const void *>{y, z, out})
+            SSD_TRY(need_elem(p, esz));
+        SSD_TRY(need_elem(weight, 4));
+    }
+    return cuda_status(launch_gated_rmsnorm(y, z, weight, out, ntokens, dim, group_size, eps,
+                                            dtype == SSD_BF16, (cudaStream_t)stream));
+}
+
 ssd_status_t ssd_decode_step(const void *x, const float *dt, const float *A, const void *Bm,
                              const void *Cm, const float *D, const float *state_in,
                              float *state_out, void *y, ssd_dims_t dims, ssd_dtype_t dtype,

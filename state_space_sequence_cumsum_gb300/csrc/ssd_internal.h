@@ -70,6 +70,10 @@ cudaError_t launch_bwd(const void *x, const void *Bm, const void *Cm, const void
                        const float *states, const float *dfinal, float *dstates, void *dx,
                        float *ddt, float *dA, float *dD, float *dBacc, float *dCacc, void *dB,
                        void *dC, float *dinit, const Geom &g, bool bf16, cudaStream_t st);
+// Gated RMS norm (k_norm.cu): rows of group_size channels, ntokens * dim / gs rows.
+cudaError_t launch_gated_rmsnorm(const void *y, const void *z, const float *w, void *out,
+                                 int64_t ntokens, int64_t dim, int64_t gs, float eps, bool bf16,
+                                 cudaStream_t st);
 // Single-token decode step (k_decode.cu); state_in may equal state_out.
 cudaError_t launch_decode_step(const void *x, const float *dt, const float *A, const void *Bm,
                                const void *Cm, const float *D, const float *state_in, float *state_out,

@@ -17,7 +17,8 @@ from ._lib import SsdError, check, dims as _dims
 __all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out", "ssd_fwd",
            "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd_staged",
            "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_stream_status",
-           "ssd_status_string", "ssd_decode_step", "ssd_bwd", "SsdFunction", "SsdError",
+           "ssd_status_string", "ssd_decode_step", "ssd_bwd", "ssd_gated_rmsnorm",
+           "SsdFunction", "SsdError",
            "Workspace"]
 
 
@@ -138,6 +139,24 @@ def ssd_decode_step(x, dt, A, B, C, D, state, state_out=None, y=None, stream=Non
                                       _dtype_code(x), _stream(stream)),
           "ssd_decode_step")
     return y, state_out
+
+
+def ssd_gated_rmsnorm(y, z, weight, eps=1e-5, group_size=None, out=None, stream=None):
+    """out = rmsnorm(y * silu(z)) * weight over groups of ``group_size``
+    channels of the last dimension (default: all of it); y and z of one
+    dtype (bf16 or f32) and shape [..., dim], weight [dim] f32.  ``out`` may
+    be y or z (in place)."""
+    if z.shape != y.shape or z.dtype != y.dtype:
+        raise ValueError("y and z must have the same shape and dtype")
+    dim = y.shape[-1]
+    gs = dim if group_size is None else int(group_size)
+    if out is None:
+        out = torch.empty_like(y)
+    check(_lib.load().ssd_gated_rmsnorm(_ptr(y), _ptr(z), _ptr(_f32(weight, "weight")), _ptr(out),
+                                        y.numel() // dim if dim else 0, dim, gs, float(eps),
+                                        _dtype_code(y), _stream(stream)),
+          "ssd_gated_rmsnorm")
+    return out
 
 
 def ssd_bwd(x, dt, A, B, C, D, dy, initial_state=None, dfinal=None, want_dinit=True,

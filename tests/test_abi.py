@@ -145,3 +145,15 @@ def test_bwd_validation(lib):
     a2 = [FAKE] * 6 + [None, FAKE, None] + [FAKE] * 6 + [None, big, 0]
     assert lib.ssd_bwd(*a2, FAKE, 1 << 40, None) == _lib.SSD_ERR_UNSUPPORTED
     assert lib.ssd_launch_count() == before
+
+
+def test_gated_rmsnorm_validation(lib):
+    before = lib.ssd_launch_count()
+    f = lib.ssd_gated_rmsnorm
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 96, 40, 1e-5, 0, None) == _lib.SSD_ERR_INVALID_ARG  # 96 % 40
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 96, 32, -1.0, 0, None) == _lib.SSD_ERR_INVALID_ARG  # eps < 0
+    assert f(None, FAKE, FAKE, FAKE, 4, 96, 32, 1e-5, 0, None) == _lib.SSD_ERR_INVALID_ARG
+    assert f(FAKE, ctypes.c_void_p(0x10001), FAKE, FAKE, 4, 96, 32, 1e-5, 0, None) == \
+        _lib.SSD_ERR_ALIGNMENT
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 96, 32, 1e-5, 9, None) == _lib.SSD_ERR_INVALID_ARG
+    assert lib.ssd_launch_count() == before
