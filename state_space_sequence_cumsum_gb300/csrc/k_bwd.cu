@@ -438,6 +438,19 @@ __global__ void convert_kernel(const float *__restrict__ src, TO *__restrict__ d
 
 }  // namespace
 
+cudaError_t launch_convert_f32(const float *src, void *dst, int64_t n, bool bf16, cudaStream_t st)
+{
+    if (n <= 0)
+        return cudaSuccess;
+    const int blocks = (int)min64((n + 255) / 256, 4096);
+    if (bf16)
+        convert_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(src, static_cast<__nv_bfloat16 *>(dst), n);
+    else
+        convert_kernel<float><<<blocks, 256, 0, st>>>(src, static_cast<float *>(dst), n);
+    note_launch(1);
+    return cudaGetLastError();
+}
+
 bool bwd_supported(const Geom &g) { return g.P <= kBT && g.S <= 512 && g.L >= 1; }
 
 int bwd_chunk_size() { return kBT; }

@@ -1,0 +1,490 @@
+// Chunk gradients of the backward pass on tensor cores (bf16, headdim 64,
+// dstate 64 or 128, 128-token chunks).
+//
+// The chunked adjoint of the forward of "Accelerating Mamba-2 forward-pass
+// kernels with CUDA Tile (cuTile)" (sections "Kernel 2" and "Kernel 3"; the
+// pages name the backward pass without giving it).  Per (batch, chunk, head),
+// with W_ij = exp2(G_i - G_j) for j <= i < n (else 0), e_T(j) = exp2(G_last -
+// G_j), e(i) = exp2(G_i), h_in the chunk's start state and dS the gradient of
+// its end state:
+//
+//   phase A (tcgen05):  dyx  = dY X^T      CB   = C B^T
+//                       Chin = C h_in^T    BdS  = B dS^T
+//   compute:            Q1   = W * CB                         (bf16, [i][j])
+//                       Q2   = W * dyx * dt_j                 (bf16, [i][j])
+//                       Xs   = dt e_T X,   Ys = e dY          (bf16 row scalings)
+//   phase B (tcgen05):  dX1  = Q1^T dY
+//                       dB   = Q2^T C + Xs dS                 (the group's dB share)
+//                       dC   = Q2 B   + Ys h_in               (the group's dC share)
+//   epilogue:           dx_j = D dy_j + dt_j (dX1_j + e_T(j) BdS_j)
+//                       ddt_j = x_j . dX1_j + e_T(j) x_j . BdS_j + A da_j
+//   with the decay gradient dL_i = sum_j Q1_ij dyx_ij dt_j - dt_i x_i . dX1_i
+//                                  + e(i) dy_i . Chin_i - R_i,
+//        R_j = e_T(j) dt_j x_j . BdS_j,  dL_last += sum_j R_j + exp2(G_last) (dS . h_in),
+//        da = suffix sums of dL,  dA += sum dt da,  dD += sum dy . x.
+//
+// Every operand is a bf16 tile in shared memory in the 128-byte-swizzled
+// layout (x, dy, B, C by TMA; h_in, dS, Q1, Q2, Xs, Ys written by the compute
+// warps), so each contraction is one tcgen05.mma chain with f32 accumulators
+// in TMEM: dyx cols [0,128), CB [128,256), Chin [256,320), BdS [384,448); in
+// phase B dX1 [0,64), dB [128,128+S), dC [256,256+S).  dB and dC are summed
+// over the heads of a group with vector f32 atomics; dx goes out through a
+// TMA store.  Roles: warps 0-3 compute (thread i = row / TMEM lane i), one
+// thread of warp 4 issues TMA and MMA.  Every wait is bounded; a timeout sets
+// the status word and the CTA leaves after freeing TMEM.
+#include "common.cuh"
+#include "ssd_internal.h"
+#include "tc05.cuh"
+
+namespace ssd {
+namespace {
+using namespace tc;
+
+constexpr int kT = 128;
+constexpr int kThreads = 160;
+constexpr uint32_t kRegion = 128 * 128;  // 128 rows x 128 bytes
+
+template <int S>
+struct BtLayout {
+    static constexpr uint32_t kSR = S / 64;                   // 64-wide dstate regions
+    static constexpr uint32_t kStateRegion = 64 * 128;        // 64 rows (p) x 128 bytes
+    static constexpr uint32_t off_x = 0;                      // x [t][p]
+    static constexpr uint32_t off_dy = off_x + kRegion;       // dy [t][p]
+    static constexpr uint32_t off_b = off_dy + kRegion;       // B [t][s], kSR regions
+    static constexpr uint32_t off_c = off_b + kSR * kRegion;  // C [t][s]
+    static constexpr uint32_t off_hin = off_c + kSR * kRegion;       // h_in [p][s] bf16
+    static constexpr uint32_t off_ds = off_hin + kSR * kStateRegion;  // dS [p][s] bf16
+    static constexpr uint32_t off_q1 = off_ds + kSR * kStateRegion;   // Q1 [i][j], 2 regions
+    static constexpr uint32_t off_q2 = off_q1 + 2 * kRegion;          // Q2 [i][j], 2 regions
+    static constexpr uint32_t off_xs = off_q2 + 2 * kRegion;          // Xs [t][p] (then dx staging)
+    static constexpr uint32_t off_ys = off_xs + kRegion;              // Ys [t][p]
+    static constexpr uint32_t off_vec = off_ys + kRegion;             // g, dt, dl: 3 x 128 f32
+    static constexpr uint32_t bytes = off_vec + 3 * 128 * 4;
+    static_assert(bytes + 1024 + 256 <= 232448, "shared memory budget");
+    static constexpr uint32_t t_dyx = 0, t_cb = 128, t_chin = 256, t_bds = 384;
+    static constexpr uint32_t t_dx = 0, t_db = 128, t_dc = 256;
+};
+
+struct BtParams {
+    const float *Gc, *dtT, *A, *D, *states, *dstates;
+    float *ddt, *dA, *dD, *dBacc, *dCacc;
+    Geom g;
+    unsigned int *status;
+};
+
+// Named barrier 1 over the four compute warps.  The non-aligned form counts
+// threads, so lanes may arrive while their warp is diverged (after a
+// lane-0-only block); the aligned bar.sync would be undefined there.
+__device__ __forceinline__ void compute_sync() { asm volatile("barrier.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+template <int S>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
+                    const __grid_constant__ CUtensorMap tm_dx, BtParams prm)
+{
+    using Lay = BtLayout<S>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t bar_in, bar_st, bar_a, bar_q, bar_b;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float red[4][4];
+    __shared__ int s_ok;
+
+    const Geom &g = prm.g;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int64_t bh = blockIdx.y, b = bh / g.H, h = bh % g.H, grp = h / g.hpg;
+    const int64_t tau = (int64_t)c * kT;
+    const int n = (int)min64(kT, g.L - tau);
+
+    if (tid == 0) {
+        mbar_init(&bar_in, 1);
+        mbar_init(&bar_st, 4);
+        mbar_init(&bar_a, 1);
+        mbar_init(&bar_q, 4);
+        mbar_init(&bar_b, 1);
+        fence_barrier_init();
+        s_ok = 1;
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    float *sg = reinterpret_cast<float *>(smem + Lay::off_vec);
+    float *sdt = sg + 128, *sdl = sdt + 128;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // ---------------- TMA loads, then the two MMA phases
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_dy);
+            prefetch_tmap(&tm_b);
+            prefetch_tmap(&tm_c);
+            mbar_arrive_expect_tx(&bar_in, (2 + 2 * Lay::kSR) * kRegion);
+            tma4(smem + Lay::off_x, &tm_x, &bar_in, 0, (int)h, (int)tau, (int)b);
+            tma4(smem + Lay::off_dy, &tm_dy, &bar_in, 0, (int)h, (int)tau, (int)b);
+            for (uint32_t r = 0; r < Lay::kSR; ++r) {
+                tma4(smem + Lay::off_b + r * kRegion, &tm_b, &bar_in, (int)(r * 64), (int)grp, (int)tau, (int)b);
+                tma4(smem + Lay::off_c + r * kRegion, &tm_c, &bar_in, (int)(r * 64), (int)grp, (int)tau, (int)b);
+            }
+            bool ok = mbar_wait(&bar_in, 0);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t base = smem_u32(smem);
+                // dyx = dY X^T: M i, N j, K p (one region)
+                const uint32_t id_tt = idesc_bf16(128, 128, false, false);
+                const uint64_t d_dy = desc_k0(base + Lay::off_dy), d_x = desc_k0(base + Lay::off_x);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_ss(tmem + Lay::t_dyx, desc_k(d_dy, kRegion, ks), desc_k(d_x, kRegion, ks), id_tt, ks > 0);
+                // CB = C B^T: K = s over the dstate regions
+                const uint64_t d_c = desc_k0(base + Lay::off_c), d_b = desc_k0(base + Lay::off_b);
+#pragma unroll
+                for (int ks = 0; ks < S / 16; ++ks)
+                    mma_ss(tmem + Lay::t_cb, desc_k(d_c, kRegion, ks), desc_k(d_b, kRegion, ks), id_tt, ks > 0);
+                ok = mbar_wait(&bar_st, 0);
+                if (ok) {
+                    tc_fence_after();
+                    // Chin = C h_in^T and BdS = B dS^T: N = p (64 rows of the state tiles), K = s
+                    const uint32_t id_tp = idesc_bf16(128, 64, false, false);
+                    const uint64_t d_hk = desc_k0(base + Lay::off_hin), d_sk = desc_k0(base + Lay::off_ds);
+#pragma unroll
+                    for (int ks = 0; ks < S / 16; ++ks) {
+                        mma_ss(tmem + Lay::t_chin, desc_k(d_c, kRegion, ks), desc_k(d_hk, Lay::kStateRegion, ks),
+                               id_tp, ks > 0);
+                        mma_ss(tmem + Lay::t_bds, desc_k(d_b, kRegion, ks), desc_k(d_sk, Lay::kStateRegion, ks),
+                               id_tp, ks > 0);
+                    }
+                    mma_commit(&bar_a);
+                    ok = mbar_wait(&bar_q, 0);
+                    if (ok) {
+                        tc_fence_after();
+                        // dX1 = Q1^T dY: A = Q1 viewed M (j) -major, B = dY viewed N (p) -major, K = i
+                        const uint64_t d_q1 = desc_mn0(base + Lay::off_q1, kRegion);
+                        const uint64_t d_q2m = desc_mn0(base + Lay::off_q2, kRegion);
+                        const uint64_t d_dym = desc_mn0(base + Lay::off_dy, kRegion);
+                        const uint64_t d_cm = desc_mn0(base + Lay::off_c, kRegion);
+                        const uint64_t d_bm = desc_mn0(base + Lay::off_b, kRegion);
+                        const uint64_t d_dsm = desc_mn0(base + Lay::off_ds, Lay::kStateRegion);
+                        const uint64_t d_hm = desc_mn0(base + Lay::off_hin, Lay::kStateRegion);
+                        const uint64_t d_xs = desc_k0(base + Lay::off_xs), d_ys = desc_k0(base + Lay::off_ys);
+                        const uint64_t d_q2k = desc_k0(base + Lay::off_q2);
+                        const uint32_t id_dx = idesc_bf16(128, 64, true, true);
+                        const uint32_t id_ms = idesc_bf16(128, S, true, true);
+                        const uint32_t id_ks = idesc_bf16(128, S, false, true);
+#pragma unroll
+                        for (int ks = 0; ks < kT / 16; ++ks)
+                            mma_ss(tmem + Lay::t_dx, desc_mn(d_q1, ks), desc_mn(d_dym, ks), id_dx, ks > 0);
+                        // dB = Q2^T C + Xs dS
+#pragma unroll
+                        for (int ks = 0; ks < kT / 16; ++ks)
+                            mma_ss(tmem + Lay::t_db, desc_mn(d_q2m, ks), desc_mn(d_cm, ks), id_ms, ks > 0);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ss(tmem + Lay::t_db, desc_k(d_xs, kRegion, ks), desc_mn(d_dsm, ks), id_ks, 1u);
+                        // dC = Q2 B + Ys h_in
+#pragma unroll
+                        for (int ks = 0; ks < kT / 16; ++ks)
+                            mma_ss(tmem + Lay::t_dc, desc_k(d_q2k, kRegion, ks), desc_mn(d_bm, ks), id_ks, ks > 0);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_ss(tmem + Lay::t_dc, desc_k(d_ys, kRegion, ks), desc_mn(d_hm, ks), id_ks, 1u);
+                        mma_commit(&bar_b);
+                    }
+                }
+            }
+            if (!ok) {
+                atomicOr(prm.status, 1u);
+                s_ok = 0;
+            }
+        }
+    } else {
+        // ---------------- compute: thread i owns row / TMEM lane i
+        const int i = tid;
+        const uint32_t tl = tmem_at(tmem, (uint32_t)(warp * 32), 0);
+        const bool valid = i < n;
+        const float *grow = prm.Gc + bh * g.L + tau;
+        sg[i] = valid ? grow[i] : 0.f;
+        sdt[i] = valid ? prm.dtT[bh * g.L + tau + i] : 0.f;
+        // h_in and dS: f32 [P][S] in global -> bf16 [p][s], swizzled rows of 64 s.
+        // Warp w takes rows p = w, w + 4, ...; lane l four consecutive s.
+        float dshin = 0.f;
+        {
+            const float *hin_g = prm.states + (bh * g.nc + c) * 64 * S;
+            const float *ds_g = prm.dstates + (bh * g.nc + c) * 64 * S;
+            constexpr int kLanesPerRow = S / 4;           // 32 (S 128) or 16 (S 64)
+            constexpr int kRowsPerPass = 32 / kLanesPerRow;
+            const int sub = lane % kLanesPerRow, rsub = lane / kLanesPerRow;
+            for (int p = warp * kRowsPerPass + rsub; p < 64; p += 4 * kRowsPerPass) {
+                const int s = 4 * sub;
+                const float4 hv = *reinterpret_cast<const float4 *>(hin_g + p * S + s);
+                const float4 dv = *reinterpret_cast<const float4 *>(ds_g + p * S + s);
+                dshin += hv.x * dv.x + hv.y * dv.y + hv.z * dv.z + hv.w * dv.w;
+                const uint32_t reg = (uint32_t)(s / 64), col = (uint32_t)(s % 64);
+                const uint32_t off = reg * Lay::kStateRegion + sw128_offset((uint32_t)p, col / 8) + (col % 8) * 2;
+                *reinterpret_cast<uint2 *>(smem + Lay::off_hin + off) =
+                    make_uint2(pack_bf16x2(hv.x, hv.y), pack_bf16x2(hv.z, hv.w));
+                *reinterpret_cast<uint2 *>(smem + Lay::off_ds + off) =
+                    make_uint2(pack_bf16x2(dv.x, dv.y), pack_bf16x2(dv.z, dv.w));
+            }
+        }
+        fence_proxy_async_smem();
+        warp_arrive(&bar_st);
+        compute_sync();  // G and dt of every row are visible
+        const float glast = sg[n - 1];
+        const float gi = sg[i], dti = sdt[i];
+        const float eT = valid ? exp2f(glast - gi) : 0.f, ei = valid ? exp2f(gi) : 0.f;
+
+        // ok is made warp-uniform: the TMEM loads below are warp-collective
+        bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_in, 0) && mbar_wait(&bar_a, 0));
+        float rowq = 0.f, yst = 0.f, xb = 0.f, dyx_ii = 0.f;
+        if (ok) {
+            tc_fence_after();
+            const uint8_t *sxr = smem + Lay::off_x, *sdyr = smem + Lay::off_dy;
+            // e(i) dy_i . Chin_i and x_i . BdS_i; Xs and Ys rows
+#pragma unroll
+            for (int c2 = 0; c2 < 4; ++c2) {
+                uint32_t ch[16], bd[16];
+                tmem_ld16(tl + Lay::t_chin + 16 * c2, ch);
+                tmem_ld16(tl + Lay::t_bds + 16 * c2, bd);
+                tmem_ld_wait();
+                uint32_t xs_pk[8], ys_pk[8];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)(2 * c2 + cc));
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(sxr + off);
+                    const uint4 dv = *reinterpret_cast<const uint4 *>(sdyr + off);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const int o = 8 * cc + 2 * e2;
+                        const float x0 = bf_lo(xw[e2]), x1 = bf_hi(xw[e2]);
+                        const float d0 = bf_lo(dw[e2]), d1 = bf_hi(dw[e2]);
+                        yst = fmaf(d0, __uint_as_float(ch[o]), fmaf(d1, __uint_as_float(ch[o + 1]), yst));
+                        xb = fmaf(x0, __uint_as_float(bd[o]), fmaf(x1, __uint_as_float(bd[o + 1]), xb));
+                        xs_pk[4 * cc + e2] = pack_bf16x2(dti * eT * x0, dti * eT * x1);
+                        ys_pk[4 * cc + e2] = pack_bf16x2(ei * d0, ei * d1);
+                    }
+                }
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)(2 * c2 + cc));
+                    *reinterpret_cast<uint4 *>(smem + Lay::off_xs + off) =
+                        make_uint4(xs_pk[4 * cc], xs_pk[4 * cc + 1], xs_pk[4 * cc + 2], xs_pk[4 * cc + 3]);
+                    *reinterpret_cast<uint4 *>(smem + Lay::off_ys + off) =
+                        make_uint4(ys_pk[4 * cc], ys_pk[4 * cc + 1], ys_pk[4 * cc + 2], ys_pk[4 * cc + 3]);
+                }
+            }
+            // Q1 = W * CB and Q2 = W * dyx * dt_j, row i, 16 keys at a time
+#pragma unroll 1
+            for (int j0 = 0; j0 < kT; j0 += 16) {
+                uint32_t cb[16], dx[16];
+                tmem_ld16(tl + Lay::t_cb + j0, cb);
+                tmem_ld16(tl + Lay::t_dyx + j0, dx);
+                tmem_ld_wait();
+                uint32_t q1[8], q2[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float a[2], bq[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int j = j0 + 2 * e + u;
+                        const float w = (valid && j <= i) ? exp2f(gi - sg[j]) : 0.f;
+                        const float cbv = __uint_as_float(cb[2 * e + u]);
+                        const float dyxv = __uint_as_float(dx[2 * e + u]);
+                        a[u] = w * cbv;
+                        bq[u] = w * dyxv * sdt[j];
+                        rowq = fmaf(a[u], dyxv * sdt[j], rowq);
+                        if (j == i)
+                            dyx_ii = dyxv;
+                    }
+                    q1[e] = pack_bf16x2(a[0], a[1]);
+                    q2[e] = pack_bf16x2(bq[0], bq[1]);
+                }
+                const int reg = j0 / 64, ch0 = (j0 % 64) / 8;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const uint32_t off = reg * kRegion + sw128_offset((uint32_t)i, (uint32_t)(ch0 + cc));
+                    *reinterpret_cast<uint4 *>(smem + Lay::off_q1 + off) =
+                        make_uint4(q1[4 * cc], q1[4 * cc + 1], q1[4 * cc + 2], q1[4 * cc + 3]);
+                    *reinterpret_cast<uint4 *>(smem + Lay::off_q2 + off) =
+                        make_uint4(q2[4 * cc], q2[4 * cc + 1], q2[4 * cc + 2], q2[4 * cc + 3]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(&bar_q);
+
+        // ---------------- epilogue
+        ok = __all_sync(0xffffffffu, ok && mbar_wait(&bar_b, 0));
+        float colq = 0.f, ddt_direct = 0.f, rj = 0.f;
+        if (ok) {
+            tc_fence_after();
+            const float Dh = prm.D[h];
+            const uint8_t *sxr = smem + Lay::off_x, *sdyr = smem + Lay::off_dy;
+            uint8_t *stage = smem + Lay::off_xs;  // Xs was read by phase B: dx staging
+#pragma unroll
+            for (int c2 = 0; c2 < 4; ++c2) {
+                uint32_t d1[16], bd[16];
+                tmem_ld16(tl + Lay::t_dx + 16 * c2, d1);
+                tmem_ld16(tl + Lay::t_bds + 16 * c2, bd);
+                tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)(2 * c2 + cc));
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(sxr + off);
+                    const uint4 dv = *reinterpret_cast<const uint4 *>(sdyr + off);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const int o = 8 * cc + 2 * e2;
+                        const float x0 = bf_lo(xw[e2]), x1 = bf_hi(xw[e2]);
+                        const float a0 = __uint_as_float(d1[o]), a1 = __uint_as_float(d1[o + 1]);
+                        colq = fmaf(x0, a0, fmaf(x1, a1, colq));
+                        const float g0 = a0 + eT * __uint_as_float(bd[o]);
+                        const float g1 = a1 + eT * __uint_as_float(bd[o + 1]);
+                        o4[e2] = pack_bf16x2(Dh * bf_lo(dw[e2]) + dti * g0, Dh * bf_hi(dw[e2]) + dti * g1);
+                    }
+                    *reinterpret_cast<uint4 *>(stage + off) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                }
+            }
+            ddt_direct = colq + eT * xb;
+            rj = eT * dti * xb;
+            fence_proxy_async_smem();
+            // dB and dC rows of this chunk's tokens.  The TMEM loads are
+            // warp-collective (.sync.aligned): every lane runs them, and only the
+            // rows of valid tokens are added.
+            {
+                const int64_t row = (b * g.L + tau + (valid ? i : 0)) * g.G + grp;
+                float *dbrow = prm.dBacc + row * S;
+                float *dcrow = prm.dCacc + row * S;
+#pragma unroll
+                for (int s0 = 0; s0 < S; s0 += 16) {
+                    uint32_t vb[16], vc[16];
+                    tmem_ld16(tl + Lay::t_db + s0, vb);
+                    tmem_ld16(tl + Lay::t_dc + s0, vc);
+                    tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4) {
+                            red_add_v4(dbrow + s0 + q, __uint_as_float(vb[q]), __uint_as_float(vb[q + 1]),
+                                       __uint_as_float(vb[q + 2]), __uint_as_float(vb[q + 3]));
+                            red_add_v4(dcrow + s0 + q, __uint_as_float(vc[q]), __uint_as_float(vc[q + 1]),
+                                       __uint_as_float(vc[q + 2]), __uint_as_float(vc[q + 3]));
+                        }
+                    }
+                }
+            }
+        }
+        // dL_i (the column part and the end-state part come from the other rows)
+        sdl[i] = valid ? rowq - colq * dti + ei * yst - rj : 0.f;
+        // CTA sums: R_j, dS . h_in, dy . x
+        float v0 = valid ? rj : 0.f, v1 = dshin, v2 = valid ? dyx_ii : 0.f;
+        for (int o = 16; o > 0; o >>= 1) {
+            v0 += __shfl_xor_sync(0xffffffffu, v0, o);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+            v2 += __shfl_xor_sync(0xffffffffu, v2, o);
+        }
+        if (lane == 0) {
+            red[0][warp] = v0;
+            red[1][warp] = v1;
+            red[2][warp] = v2;
+        }
+        compute_sync();
+        if (ok && i == 0) {
+            const float rsum = red[0][0] + red[0][1] + red[0][2] + red[0][3];
+            const float dsh = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+            const float dd = red[2][0] + red[2][1] + red[2][2] + red[2][3];
+            sdl[n - 1] += rsum + exp2f(glast) * dsh;
+            // suffix sums of dL: da_k; dA gets sum dt_k da_k (stored in sdl as da)
+            float da = 0.f, dasum = 0.f;
+            for (int k = n - 1; k >= 0; --k) {
+                da += sdl[k];
+                sdl[k] = da;
+                dasum = fmaf(sdt[k], da, dasum);
+            }
+            atomicAdd(prm.dA + h, dasum);
+            atomicAdd(prm.dD + h, dd);
+        }
+        compute_sync();
+        if (ok && valid)
+            prm.ddt[(b * g.L + tau + i) * g.H + h] = ddt_direct + prm.A[h] * sdl[i];
+        // dx rows out by TMA (rows past the sequence end are not written)
+        if (ok && i == 0) {
+            prefetch_tmap(&tm_dx);
+            tma4_store(&tm_dx, smem + Lay::off_xs, 0, (int)h, (int)tau, (int)b);
+            bulk_commit();
+            bulk_wait_all();
+        }
+        if (!ok && lane == 0)
+            atomicOr(prm.status, 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int S>
+cudaError_t launch_bt(const CUtensorMap &tx, const CUtensorMap &tdy, const CUtensorMap &tb,
+                      const CUtensorMap &tc_, const CUtensorMap &tdx, const BtParams &p, cudaStream_t st)
+{
+    const size_t smem = BtLayout<S>::bytes + 1024;
+    auto k = bwd_chunk_tc_kernel<S>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid((unsigned)p.g.nc, (unsigned)(p.g.B * p.g.H));
+    k<<<grid, kThreads, smem, st>>>(tx, tdy, tb, tc_, tdx, p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const Geom &g)
+{
+    return g.P == 64 && (g.S == 64 || g.S == 128) && g.T == kT && g.L > 0 && g.nc <= 2147483647LL &&
+           g.B * g.H <= 65535 && g.L < (1LL << 31);
+}
+
+cudaError_t launch_bwd_chunk_tc(const void *x, const void *Bm, const void *Cm, const void *dy,
+                                const float *dtT, const float *Gc, const float *A, const float *D,
+                                const float *states, const float *dstates, void *dx, float *ddt,
+                                float *dA, float *dD, float *dBacc, float *dCacc, const Geom &g,
+                                cudaStream_t st)
+{
+    if (!bwd_tc_supported(g))
+        return cudaErrorNotSupported;
+    unsigned int *status = device_status_word();
+    if (!status)
+        return cudaErrorUnknown;
+    CUtensorMap tx, tdy, tb, tc_, tdx;
+    if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_heads(&tdy, dy, g) ||
+        !make_tmap_tokens_groups(&tb, Bm, g) || !make_tmap_tokens_groups(&tc_, Cm, g) ||
+        !make_tmap_tokens_heads(&tdx, dx, g))
+        return cudaErrorInvalidValue;
+    BtParams p{Gc, dtT, A, D, states, dstates, ddt, dA, dD, dBacc, dCacc, g, status};
+    if (g.S == 64)
+        return launch_bt<64>(tx, tdy, tb, tc_, tdx, p, st);
+    return launch_bt<128>(tx, tdy, tb, tc_, tdx, p, st);
+}
+
+}  // namespace ssd

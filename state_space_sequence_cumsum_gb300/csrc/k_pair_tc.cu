@@ -536,7 +536,8 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             cp_async_wait_all();
         }
         // the first tile's dt is visible to all 256 compute threads
-        asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+        // (non-aligned form: the copies above leave lanes diverged)
+        asm volatile("barrier.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
         if (n_my > 0)
             nxt_g = tile_g(0, kLog2e * a_next);
         uint32_t it = 0;

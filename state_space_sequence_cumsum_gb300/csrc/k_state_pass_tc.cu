@@ -75,7 +75,7 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
-template <int P>
+template <int P, bool REV>
 __global__ void __launch_bounds__(kThreads, 1)
 state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ dtT,
@@ -122,7 +122,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int s = (int)(i % kStages);
             uint8_t *stage = smem + s * Lay::kStage;
             mbar_arrive_expect_tx(&bar_full[s], Lay::kStage);
-            const int tok = (int)(i * kTile);
+            const int tok = (int)((REV ? n_tiles - 1 - i : i) * kTile);
             for (int r = 0; r < Lay::kXRegions; ++r)
                 tma_load_4d(stage + r * kRegion, &tm_x, &bar_full[s], r * 64, (int)h, tok, (int)b);
             for (int r = 0; r < 2; ++r)
@@ -179,13 +179,16 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         uint8_t *sxh = smem + Lay::off_xh;
         for (int64_t i = 0; i < n_tiles; ++i) {
             const int s = (int)(i % kStages);
-            const int64_t tau = i * kTile;
+            const int64_t tau = (REV ? n_tiles - 1 - i : i) * kTile;
             const int n = (int)min64(kTile, g.L - tau);
             // tile-local log2 decay: G restarts at chunk starts, so a tile in
             // the middle of a chunk subtracts G at the token before it
             const float base = (tau % g.T == 0) ? 0.f : grow[tau - 1];
             const float gL = grow[tau + n - 1] - base;
-            const float w = row < n ? drow[tau + row] * exp2f(gL - (grow[tau + row] - base)) : 0.f;
+            // forward: dt_t exp2(G_last - G_t); reverse (tile = chunk): exp2(G_t)
+            const float w = row < n ? (REV ? exp2f(grow[tau + row] - base)
+                                           : drow[tau + row] * exp2f(gL - (grow[tau + row] - base)))
+                                    : 0.f;
             const float decay = exp2f(gL);
 
             if (!mbar_wait(&bar_full[s], (uint32_t)((i / kStages) & 1))) {
@@ -261,13 +264,13 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     }
 }
 
-template <int P>
+template <int P, bool REV>
 cudaError_t launch_p(const CUtensorMap &tx, const CUtensorMap &tb, const float *dtT,
                      const float *Gc, const float *init, float *states, float *final_state,
                      const Geom &g, unsigned int *status, cudaStream_t st)
 {
     const size_t smem = SpLayout<P>::bytes + 1024;
-    auto k = state_pass_tc_kernel<P>;
+    auto k = state_pass_tc_kernel<P, REV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
@@ -298,8 +301,32 @@ cudaError_t launch_state_pass_tc(const void *x, const void *Bm, const float *dtT
     if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g))
         return cudaErrorInvalidValue;
     if (g.P == 64)
-        return launch_p<64>(tx, tb, dtT, Gc, init, states, final_state, g, status, st);
-    return launch_p<128>(tx, tb, dtT, Gc, init, states, final_state, g, status, st);
+        return launch_p<64, false>(tx, tb, dtT, Gc, init, states, final_state, g, status, st);
+    return launch_p<128, false>(tx, tb, dtT, Gc, init, states, final_state, g, status, st);
+}
+
+// The reverse pass of the backward: the same contraction run from the last
+// 128-token chunk to the first, on dy and C with the weights exp2(G_t), so
+// the carried matrix is the state gradient:
+//     dstates[c] = dS (gradient of chunk c's end state);  dS <- exp2(G_last) dS + dy^T (C * exp2(G))
+// starting from dfinal (NULL: zero); dinit receives dS after chunk 0.
+bool reverse_state_pass_tc_supported(const Geom &g) { return state_pass_tc_supported(g) && g.T == kTile; }
+
+cudaError_t launch_reverse_state_pass_tc(const void *dy, const void *Cm, const float *Gc,
+                                         const float *dfinal, float *dstates, float *dinit,
+                                         const Geom &g, cudaStream_t st)
+{
+    if (!reverse_state_pass_tc_supported(g))
+        return cudaErrorNotSupported;
+    unsigned int *status = device_status_word();
+    if (!status)
+        return cudaErrorUnknown;
+    CUtensorMap tx, tb;
+    if (!make_tmap_tokens_heads(&tx, dy, g) || !make_tmap_tokens_groups(&tb, Cm, g))
+        return cudaErrorInvalidValue;
+    if (g.P == 64)
+        return launch_p<64, true>(tx, tb, Gc, Gc, dfinal, dstates, dinit, g, status, st);
+    return launch_p<128, true>(tx, tb, Gc, Gc, dfinal, dstates, dinit, g, status, st);
 }
 
 }  // namespace ssd

@@ -454,6 +454,7 @@ size_t ssd_bwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype)
     if (make_geom(dims, bwd_chunk_size(), false, &g) != SSD_OK ||
         (dtype != SSD_BF16 && dtype != SSD_F32))
         return 0;
+    // the 64-token-chunk layout is the larger of the two paths' layouts
     return bwd_layout(g, nullptr).bytes;
 }
 
@@ -494,8 +495,30 @@ ssd_status_t ssd_bwd(const void *x, const float *dt, const float *A, const void 
         return cuda_status(dfinal ? cudaMemcpyAsync(dinit, dfinal, sbytes, cudaMemcpyDeviceToDevice, st)
                                   : cudaMemsetAsync(dinit, 0, sbytes, st));
     }
-    const BwdWs w = bwd_layout(g, static_cast<char *>(workspace));
     const bool bf16 = dtype == SSD_BF16;
+    // tensor-core path: 128-token chunks, the forward and reverse state passes
+    // and the chunk gradients on tcgen05 (SSD_BWD_KERNEL=cuda-cores forces the
+    // CUDA-core path)
+    Geom gt;
+    const char *force = std::getenv("SSD_BWD_KERNEL");
+    const bool tc = bf16 && !(force && std::strcmp(force, "cuda-cores") == 0) &&
+                    make_geom(dims, 128, false, &gt) == SSD_OK && bwd_tc_supported(gt) &&
+                    state_pass_tc_supported(gt) && reverse_state_pass_tc_supported(gt);
+    if (tc) {
+        const BwdWs w = bwd_layout(gt, static_cast<char *>(workspace));
+        SSD_TRY(cuda_status(launch_chunk_cumsum(dt, A, w.Gc, w.dtT, gt, st)));
+        SSD_TRY(cuda_status(launch_state_pass_tc(x, Bm, w.dtT, w.Gc, init_state, w.states, nullptr, gt, st)));
+        SSD_TRY(cuda_status(launch_reverse_state_pass_tc(dy, Cm, w.Gc, dfinal, w.dstates, dinit, gt, st)));
+        const size_t bct = (size_t)(gt.B * gt.L * gt.G * gt.S) * sizeof(float);
+        SSD_TRY(cuda_status(cudaMemsetAsync(w.dB, 0, bct, st)));
+        SSD_TRY(cuda_status(cudaMemsetAsync(w.dC, 0, bct, st)));
+        SSD_TRY(cuda_status(launch_bwd_chunk_tc(x, Bm, Cm, dy, w.dtT, w.Gc, A, D, w.states, w.dstates, dx,
+                                                ddt, dA, dD, w.dB, w.dC, gt, st)));
+        const int64_t nbc = gt.B * gt.L * gt.G * gt.S;
+        SSD_TRY(cuda_status(launch_convert_f32(w.dB, dB, nbc, true, st)));
+        return cuda_status(launch_convert_f32(w.dC, dC, nbc, true, st));
+    }
+    const BwdWs w = bwd_layout(g, static_cast<char *>(workspace));
     SSD_TRY(cuda_status(launch_chunk_cumsum(dt, A, w.Gc, w.dtT, g, st)));
     SSD_TRY(cuda_status(run_state_pass(x, Bm, w.dtT, w.Gc, init_state, w.states, nullptr, g, bf16, st)));
     const size_t bc = (size_t)(g.B * g.L * g.G * g.S) * sizeof(float);

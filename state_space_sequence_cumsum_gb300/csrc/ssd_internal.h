@@ -60,6 +60,22 @@ cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, c
 // Tensor-core chunk output for dstate 384 / 512 (bf16, P = 64, chunk 128),
 // streaming B / C in 128-wide dstate blocks.
 bool chunk_out_big_supported(const Geom &g);
+// Reverse state pass of the backward on tensor cores (k_state_pass_tc.cu):
+// bf16, P in {64, 128}, S % 64 == 0, 128-token chunks.
+bool reverse_state_pass_tc_supported(const Geom &g);
+cudaError_t launch_reverse_state_pass_tc(const void *dy, const void *Cm, const float *Gc,
+                                         const float *dfinal, float *dstates, float *dinit,
+                                         const Geom &g, cudaStream_t st);
+// Chunk gradients of the backward on tensor cores (k_bwd_tc.cu): bf16,
+// P == 64, S in {64, 128}, 128-token chunks; states / dstates / Gc / dtT per
+// 128-token chunk; dBacc / dCacc / dA / dD zeroed f32 accumulators.
+bool bwd_tc_supported(const Geom &g);
+cudaError_t launch_bwd_chunk_tc(const void *x, const void *Bm, const void *Cm, const void *dy,
+                                const float *dtT, const float *Gc, const float *A, const float *D,
+                                const float *states, const float *dstates, void *dx, float *ddt,
+                                float *dA, float *dD, float *dBacc, float *dCacc, const Geom &g,
+                                cudaStream_t st);
+cudaError_t launch_convert_f32(const float *src, void *dst, int64_t n, bool bf16, cudaStream_t st);
 // Backward pass (k_bwd.cu): 64-token chunks, P <= 64.  states / dstates /
 // Gc / dtT are per 64-token chunk; dBacc / dCacc are zeroed f32 [B,L,G,S]
 // accumulators; dA / dD are zeroed f32 [H] accumulators.

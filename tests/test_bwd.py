@@ -9,6 +9,18 @@ the forward's parity tests) -- except that outputs in a bf16 call's dtype
 magnitudes (max / rms of 10-17 on these inputs), so that rounding alone
 moves them by up to ~6e-2 * rms: those outputs are held element by element
 to the rounding bound, |gpu - oracle| <= 2^-8 |oracle| + 1e-4 * rms.
+
+bf16 calls with headdim 64 and dstate 64 / 128 take the tensor-core path
+(128-token chunks, tcgen05 contractions with bf16 operands -- the scaled
+decay matrices, the row-scaled x / dy and the states are rounded to bf16,
+as in the forward): every output is held element by element to
+|gpu - oracle| <= 2^-5 |oracle| + 4e-2 * rms.  dB and dC sum bf16-rounded
+terms over tokens and a group's heads and have heavy tails (max / rms up to
+17).  A float64 simulation of the same chunked formulas (exact to 2e-14 of
+the oracle) with the decay matrix, the row-scaled x and the end-state
+gradient rounded to bf16 reaches 3.4e-2 * rms beyond 2^-5 |oracle| on the
+(2, 300, 8, 64, 128, 2) case; a missing or wrong term is off by O(rms).  Those shapes are also run on the CUDA-core path
+(SSD_BWD_KERNEL=cuda-cores).
 """
 import numpy as np
 import pytest
@@ -41,6 +53,19 @@ def run_case(B, L, H, P, S, G, dtype, init=True, dfinal=True, seed=0):
     return out, ref
 
 
+def uses_tensor_cores(P, S, dtype):
+    return dtype == torch.bfloat16 and P == 64 and S in (64, 128)
+
+
+def check_tc(out, ref):
+    for k in ("dx", "dB", "dC", "ddt", "dA", "dD", "dinit"):
+        g = out[k].detach().to("cpu", torch.float64).numpy()
+        r = ref[k]
+        rms = float(np.sqrt(np.mean(r * r)))
+        excess = np.max(np.abs(g - r) - 2.0 ** -5 * np.abs(r)) / rms
+        assert excess <= 4e-2, f"{k}: error beyond 2^-5 |ref| is {excess:.3e} * rms"
+
+
 def check(out, ref, dtype):
     for k in ("dx", "dB", "dC"):
         if dtype == torch.float32:
@@ -66,9 +91,23 @@ def check(out, ref, dtype):
     (1, 70, 2, 32, 512, 1, torch.bfloat16),    # largest dstate
     (3, 1, 3, 8, 16, 3, torch.float32),        # one token
 ])
-def test_bwd_matches_oracle(B, L, H, P, S, G, dtype):
+def test_bwd_matches_oracle(B, L, H, P, S, G, dtype, monkeypatch):
     out, ref = run_case(B, L, H, P, S, G, dtype)
+    if uses_tensor_cores(P, S, dtype):
+        check_tc(out, ref)
+        monkeypatch.setenv("SSD_BWD_KERNEL", "cuda-cores")
+        out, ref = run_case(B, L, H, P, S, G, dtype)
     check(out, ref, dtype)
+
+
+@pytest.mark.parametrize("B,L,H,P,S,G", [
+    (2, 300, 4, 64, 64, 1),     # ragged last chunk, dstate 64
+    (1, 128, 2, 64, 128, 1),    # exactly one chunk
+    (2, 520, 6, 64, 128, 3),    # grouped, ragged
+])
+def test_bwd_tensor_core_path(B, L, H, P, S, G):
+    out, ref = run_case(B, L, H, P, S, G, torch.bfloat16, seed=6)
+    check_tc(out, ref)
 
 
 def test_bwd_without_initial_state_or_final_gradient():
@@ -93,4 +132,4 @@ def test_autograd_function():
                      wy.to(torch.bfloat16), init=inp["init"], dfinal=wf)
     got = {"dx": g["x"].grad, "ddt": g["dt"].grad, "dA": g["A"].grad, "dB": g["B"].grad,
            "dC": g["C"].grad, "dD": g["D"].grad, "dinit": g["init"].grad}
-    check(got, ref, torch.bfloat16)
+    check_tc(got, ref)
