@@ -40,6 +40,7 @@ using namespace tc;
 
 constexpr int kTile = 128;
 constexpr int kThreads = 160;
+constexpr int kMaxSeg = 64;  // segments of one sequence in the segmented pass
 constexpr uint32_t kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region
 
 template <int P>
@@ -75,13 +76,25 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Segments of a sequence, all run at once (blockIdx.z = segment).  Mode 1:
+// each segment from a zero state, no chunk states, its end state into
+// slot(seg) (seg < n_seg - 1).  Mode 2: segment k > 0 from slot(k - 1),
+// chunk states emitted, the final state from the last segment.  Mode 0: one
+// segment, the whole sequence (the plain pass).  slot(k) of (batch, head) bh
+// is slot_base + bh * slot_bh + k * slot_k floats, a [P, S] state.
+struct SpSeg {
+    int mode, seg_tiles, n_seg;
+    float *slot_base;
+    int64_t slot_bh, slot_k;
+};
+
 template <int P, bool REV>
 __global__ void __launch_bounds__(kThreads, 1)
 state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ dtT,
                      const float *__restrict__ Gc, const float *__restrict__ init,
                      float *__restrict__ states, float *__restrict__ final_state, Geom g,
-                     unsigned int *status)
+                     unsigned int *status, SpSeg sg)
 {
     using Lay = SpLayout<P>;
     constexpr int kStages = Lay::kStages;
@@ -94,7 +107,17 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int tid = threadIdx.x, warp = tid >> 5;
     const int sigma = blockIdx.x;
     const int64_t bh = blockIdx.y, b = bh / g.H, h = bh % g.H, grp = h / g.hpg;
-    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+    const int64_t n_all = (g.L + kTile - 1) / kTile;
+    const int seg = blockIdx.z;
+    const int64_t t_begin = sg.mode ? (int64_t)seg * sg.seg_tiles : 0;
+    const int64_t t_end = sg.mode ? min64(n_all, t_begin + sg.seg_tiles) : n_all;
+    const int64_t n_tiles = t_end - t_begin;  // tiles of this CTA
+    float *slot_prev = (sg.mode == 2 && seg > 0)
+                           ? sg.slot_base + bh * sg.slot_bh + (int64_t)(seg - 1) * sg.slot_k
+                           : nullptr;
+    float *slot_out = (sg.mode == 1 && seg < sg.n_seg - 1)
+                          ? sg.slot_base + bh * sg.slot_bh + (int64_t)seg * sg.slot_k
+                          : nullptr;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -122,7 +145,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int s = (int)(i % kStages);
             uint8_t *stage = smem + s * Lay::kStage;
             mbar_arrive_expect_tx(&bar_full[s], Lay::kStage);
-            const int tok = (int)((REV ? n_tiles - 1 - i : i) * kTile);
+            const int tok = (int)((REV ? t_end - 1 - i : t_begin + i) * kTile);
             for (int r = 0; r < Lay::kXRegions; ++r)
                 tma_load_4d(stage + r * kRegion, &tm_x, &bar_full[s], r * 64, (int)h, tok, (int)b);
             for (int r = 0; r < 2; ++r)
@@ -167,9 +190,16 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         for (int c0 = 0; c0 < P; c0 += 16) {
             uint32_t r[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                r[j] = __float_as_uint((init && s_ok) ? init[(bh * g.P + c0 + j) * g.S + s_idx]
-                                                      : 0.f);
+            for (int j = 0; j < 16; ++j) {
+                float v = 0.f;
+                if (s_ok && sg.mode != 1) {
+                    if (slot_prev)
+                        v = slot_prev[(int64_t)(c0 + j) * g.S + s_idx];
+                    else if (init)
+                        v = init[(bh * g.P + c0 + j) * g.S + s_idx];
+                }
+                r[j] = __float_as_uint(v);
+            }
             tmem_st16(lane_base + c0, r);
         }
         tmem_st_wait();
@@ -179,7 +209,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         uint8_t *sxh = smem + Lay::off_xh;
         for (int64_t i = 0; i < n_tiles; ++i) {
             const int s = (int)(i % kStages);
-            const int64_t tau = (REV ? n_tiles - 1 - i : i) * kTile;
+            const int64_t tau = (REV ? t_end - 1 - i : t_begin + i) * kTile;
             const int n = (int)min64(kTile, g.L - tau);
             // tile-local log2 decay: G restarts at chunk starts, so a tile in
             // the middle of a chunk subtracts G at the token before it
@@ -217,7 +247,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 mbar_arrive(&bar_empty[s]);
 
             // chunk start: store h (the state before this chunk), then decay it
-            const bool emit = states && s_ok && (tau % g.T == 0);
+            const bool emit = states && s_ok && sg.mode != 1 && (tau % g.T == 0);
             float *dst = emit ? states + ((bh * g.nc + tau / g.T) * g.P) * g.S + s_idx : nullptr;
 #pragma unroll
             for (int c0 = 0; c0 < P; c0 += 16) {
@@ -244,7 +274,12 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             }
             tc_fence_after();
         }
-        if (final_state && s_ok) {
+        // the end state: a segment's (mode 1) or the sequence's final state
+        float *end_dst = slot_out ? slot_out
+                                  : ((final_state && sg.mode != 1 && (sg.mode == 0 || seg == sg.n_seg - 1))
+                                         ? final_state + bh * g.P * g.S
+                                         : nullptr);
+        if (end_dst && s_ok) {
 #pragma unroll
             for (int c0 = 0; c0 < P; c0 += 16) {
                 uint32_t r[16];
@@ -252,7 +287,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    final_state[(bh * g.P + c0 + j) * g.S + s_idx] = __uint_as_float(r[j]);
+                    end_dst[(int64_t)(c0 + j) * g.S + s_idx] = __uint_as_float(r[j]);
             }
         }
     }
@@ -267,15 +302,15 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
 template <int P, bool REV>
 cudaError_t launch_p(const CUtensorMap &tx, const CUtensorMap &tb, const float *dtT,
                      const float *Gc, const float *init, float *states, float *final_state,
-                     const Geom &g, unsigned int *status, cudaStream_t st)
+                     const Geom &g, unsigned int *status, cudaStream_t st, const SpSeg &sg = SpSeg{})
 {
     const size_t smem = SpLayout<P>::bytes + 1024;
     auto k = state_pass_tc_kernel<P, REV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    dim3 grid((unsigned)((g.S + 127) / 128), (unsigned)(g.B * g.H));
-    k<<<grid, kThreads, smem, st>>>(tx, tb, dtT, Gc, init, states, final_state, g, status);
+    dim3 grid((unsigned)((g.S + 127) / 128), (unsigned)(g.B * g.H), (unsigned)(sg.mode ? sg.n_seg : 1));
+    k<<<grid, kThreads, smem, st>>>(tx, tb, dtT, Gc, init, states, final_state, g, status, sg);
     note_launch();
     return cudaGetLastError();
 }
@@ -305,6 +340,45 @@ cudaError_t launch_state_pass_tc(const void *x, const void *Bm, const float *dtT
     return launch_p<128, false>(tx, tb, dtT, Gc, init, states, final_state, g, status, st);
 }
 
+// Start states of the segments from their local end states (mode 1):
+// slot(k) <- exp2(D_k) slot(k-1) + slot(k), slot(-1) = init (or 0), where D_k
+// is segment k's total log2 decay, the sum of G at each of its chunks' last
+// valid tokens.  One thread per state element; the first n_seg - 1 threads
+// of each block form the decay factors.  The slot loads are independent of
+// the carried state, so they are issued eight at a time ahead of the chain.
+__global__ void __launch_bounds__(256)
+seg_combine_kernel(const float *__restrict__ Gc, const float *__restrict__ init, Geom g, SpSeg sg)
+{
+    __shared__ float sdec[kMaxSeg];
+    const int64_t bh = blockIdx.y;
+    const int chunks_per_seg = sg.seg_tiles * kTile / g.T;
+    for (int k = threadIdx.x; k < sg.n_seg - 1; k += blockDim.x) {
+        float d = 0.f;
+        for (int c = k * chunks_per_seg; c < (k + 1) * chunks_per_seg && c < g.nc; ++c)
+            d += Gc[bh * g.L + min64(g.L, (int64_t)(c + 1) * g.T) - 1];
+        sdec[k] = exp2f(d);
+    }
+    __syncthreads();
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= g.P * g.S)
+        return;
+    float h = init ? init[bh * g.P * g.S + e] : 0.f;
+    float *slot = sg.slot_base + bh * sg.slot_bh + e;
+    for (int k0 = 0; k0 < sg.n_seg - 1; k0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = k0 + j < sg.n_seg - 1 ? slot[(int64_t)(k0 + j) * sg.slot_k] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (k0 + j < sg.n_seg - 1) {
+                h = fmaf(sdec[k0 + j], h, v[j]);
+                slot[(int64_t)(k0 + j) * sg.slot_k] = h;
+            }
+        }
+    }
+}
+
 // The reverse pass of the backward: the same contraction run from the last
 // 128-token chunk to the first, on dy and C with the weights exp2(G_t), so
 // the carried matrix is the state gradient:
@@ -327,6 +401,84 @@ cudaError_t launch_reverse_state_pass_tc(const void *dy, const void *Cm, const f
     if (g.P == 64)
         return launch_p<64, true>(tx, tb, Gc, Gc, dfinal, dstates, dinit, g, status, st);
     return launch_p<128, true>(tx, tb, Gc, Gc, dfinal, dstates, dinit, g, status, st);
+}
+
+}  // namespace ssd
+
+namespace ssd {
+
+// Segment plan of the segmented state pass.  The kernel holds one CTA per SM
+// and the split runs the sequence twice, so it pays only when the (batch,
+// head, dstate slice) units fill a third of the SMs or less: then n segments
+// per unit, units * n <= SMs (one wave), cost 2/n of the unsplit pass.
+// Segments are at least four tiles and a whole number of chunks.  n_seg 1
+// means "not worth it".
+void state_pass_seg_plan(const Geom &g, int sms, int *seg_tiles, int *n_seg)
+{
+    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+    const int64_t units = g.B * g.H * ((g.S + 127) / 128);
+    const int tpc = g.T / kTile;  // tiles per chunk
+    int64_t want = sms / units;
+    if (want > kMaxSeg)
+        want = kMaxSeg;
+    if (want * 4 > n_tiles)
+        want = n_tiles / 4;
+    if (want < 3) {
+        *n_seg = 1;
+        *seg_tiles = (int)n_tiles;
+        return;
+    }
+    int64_t st = (n_tiles + want - 1) / want;
+    st = (st + tpc - 1) / tpc * tpc;
+    *seg_tiles = (int)st;
+    *n_seg = (int)((n_tiles + st - 1) / st);
+}
+
+// Long sequences with few (batch, head) units: pass 1 (every segment's end
+// state from zero, in parallel), the short serial combine, pass 2 (every
+// segment from its true start state, emitting chunk states).  The segment
+// start states are kept in the chunk-state array at the segments' first
+// chunks, so no other scratch is needed.  Returns cudaErrorNotSupported when
+// the plain pass should be used.
+cudaError_t launch_state_pass_tc_segmented(const void *x, const void *Bm, const float *dtT,
+                                           const float *Gc, const float *init, float *states,
+                                           float *final_state, const Geom &g, cudaStream_t st)
+{
+    if (!state_pass_tc_supported(g) || !states)
+        return cudaErrorNotSupported;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorNotSupported;
+    SpSeg sg{};
+    state_pass_seg_plan(g, sms, &sg.seg_tiles, &sg.n_seg);
+    if (sg.n_seg < 2)
+        return cudaErrorNotSupported;
+    unsigned int *status = device_status_word();
+    if (!status)
+        return cudaErrorUnknown;
+    CUtensorMap tx, tb;
+    if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g))
+        return cudaErrorInvalidValue;
+    // slot(k) = the chunk state at segment k+1's first chunk
+    const int64_t chunks_per_seg = (int64_t)sg.seg_tiles * kTile / g.T;
+    sg.slot_base = states + chunks_per_seg * g.P * g.S;
+    sg.slot_bh = g.nc * g.P * g.S;
+    sg.slot_k = chunks_per_seg * g.P * g.S;
+    cudaError_t e;
+    sg.mode = 1;
+    e = g.P == 64 ? launch_p<64, false>(tx, tb, dtT, Gc, nullptr, nullptr, nullptr, g, status, st, sg)
+                  : launch_p<128, false>(tx, tb, dtT, Gc, nullptr, nullptr, nullptr, g, status, st, sg);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 cgrid((unsigned)((g.P * g.S + 255) / 256), (unsigned)(g.B * g.H));
+    seg_combine_kernel<<<cgrid, 256, 0, st>>>(Gc, init, g, sg);
+    note_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    sg.mode = 2;
+    return g.P == 64 ? launch_p<64, false>(tx, tb, dtT, Gc, init, states, final_state, g, status, st, sg)
+                     : launch_p<128, false>(tx, tb, dtT, Gc, init, states, final_state, g, status, st, sg);
 }
 
 }  // namespace ssd

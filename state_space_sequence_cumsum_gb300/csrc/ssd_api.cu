@@ -134,13 +134,24 @@ ssd_path_t choose_path(const Geom &g, ssd_dtype_t t, bool want_states)
     return fused_pair_enabled(g) ? SSD_PATH_FUSED_PAIR_TENSOR_CORES : SSD_PATH_FUSED_TENSOR_CORES;
 }
 
-// Stage 2 dispatch: tcgen05 kernel for bf16 shapes it serves, else CUDA cores.
+// Stage 2 dispatch: tcgen05 kernel for bf16 shapes it serves (split into
+// parallel segments when the (batch, head) units cannot fill the GPU), else
+// CUDA cores.  SSD_STATE_PASS=plain keeps the unsplit pass (a measurement and
+// test switch).
 cudaError_t run_state_pass(const void *x, const void *Bm, const float *dtT, const float *Gc,
                            const float *init, float *states, float *final_state, const Geom &g,
                            bool bf16, cudaStream_t st)
 {
-    if (bf16 && state_pass_tc_supported(g))
+    if (bf16 && state_pass_tc_supported(g)) {
+        const char *env = getenv("SSD_STATE_PASS");
+        if (states && !(env && strcmp(env, "plain") == 0)) {
+            const cudaError_t e =
+                launch_state_pass_tc_segmented(x, Bm, dtT, Gc, init, states, final_state, g, st);
+            if (e != cudaErrorNotSupported)
+                return e;
+        }
         return launch_state_pass_tc(x, Bm, dtT, Gc, init, states, final_state, g, st);
+    }
     return launch_state_pass_simt(x, Bm, dtT, Gc, init, states, final_state, g, bf16, st);
 }
 

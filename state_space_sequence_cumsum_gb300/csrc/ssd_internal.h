@@ -51,6 +51,14 @@ bool state_pass_tc_supported(const Geom &g);
 cudaError_t launch_state_pass_tc(const void *x, const void *Bm, const float *dtT,
                                  const float *Gc, const float *init, float *states,
                                  float *final_state, const Geom &g, cudaStream_t st);
+// The same pass split into segments of the sequence run in parallel (end
+// states from zero, a serial combine, then the segments again from their true
+// start states), for long sequences with few (batch, head) units; needs the
+// chunk-state array.  cudaErrorNotSupported: too few tiles to split.
+void state_pass_seg_plan(const Geom &g, int sms, int *seg_tiles, int *n_seg);
+cudaError_t launch_state_pass_tc_segmented(const void *x, const void *Bm, const float *dtT,
+                                           const float *Gc, const float *init, float *states,
+                                           float *final_state, const Geom &g, cudaStream_t st);
 
 // Tensor-core chunk output (stage 3) and fused single-pass forward (bf16).
 bool chunk_tc_supported(const Geom &g);

@@ -38,7 +38,9 @@ def test_chunk_cumsum(L, H, T):
                                            (1, 300, 2, 128, 192, 1, 256),   # ragged dstate slice
                                            (2, 1000, 4, 64, 64, 2, 256),    # half-empty slice
                                            (1, 129, 3, 64, 256, 3, 128),    # tile + 1 token
-                                           (1, 4095, 2, 64, 128, 1, 256)])  # ragged, many tiles
+                                           (1, 4095, 2, 64, 128, 1, 256),   # ragged, many tiles
+                                           (1, 2900, 2, 64, 128, 1, 128),   # segments, short last
+                                           (1, 6000, 1, 128, 256, 1, 256)])  # segments, two tiles a chunk
 def test_state_pass(dtype, B, L, H, P, S, G, T):
     inp = case_inputs(B, L, H, P, S, G, T, dtype=dtype, init="randn", seed=L + P)
     g = to_gpu(inp)
@@ -69,6 +71,31 @@ def test_chunk_out_from_oracle_states(dtype, B, L, H, P, S, G, T):
     states = torch.from_numpy(ref["chunk_states"]).float().cuda()
     y = ssd.ssd_chunk_out(g["x"], g["B"], g["C"], dtT, Gc, states, g["D"], T)
     assert_parity(y, ref["y"], dtype, "y")
+
+
+@pytest.mark.parametrize("init", ["zero", "randn"])
+@pytest.mark.parametrize("B,L,H,P,S,G,T", [(1, 5000, 2, 64, 128, 1, 128),
+                                           (1, 9000, 1, 64, 512, 1, 256),
+                                           (2, 3333, 3, 128, 128, 3, 128)])
+def test_segmented_and_plain_state_pass_agree(B, L, H, P, S, G, T, init, monkeypatch):
+    """Few (batch, head) units and a long sequence split the tensor-core state
+    pass into parallel segments; SSD_STATE_PASS=plain runs it unsplit.  Both
+    follow "Kernel 2: fwd_pass_state", so they agree to f32 rounding and each
+    matches the oracle."""
+    inp = case_inputs(B, L, H, P, S, G, T, init=init, seed=L + S + P)
+    g = to_gpu(inp)
+    Gc, dtT = ssd.ssd_chunk_cumsum(g["dt"], g["A"], T)
+    init_state = g["init"] if init == "randn" else None
+    st, fin = ssd.ssd_state_pass(g["x"], g["B"], dtT, Gc, T, init_state=init_state)
+    monkeypatch.setenv("SSD_STATE_PASS", "plain")
+    st_p, fin_p = ssd.ssd_state_pass(g["x"], g["B"], dtT, Gc, T, init_state=init_state)
+    assert ssd.ssd_stream_status() == 0
+    scale = max(1.0, fin_p.abs().max().item())
+    assert (st - st_p).abs().max().item() <= 1e-4 * scale
+    assert (fin - fin_p).abs().max().item() <= 1e-4 * scale
+    ref = oracle_run(inp, T, want_states=True)
+    assert_parity(st, ref["chunk_states"], torch.bfloat16, "chunk_states")
+    assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
 
 
 def test_state_pass_without_outputs_is_a_noop():
