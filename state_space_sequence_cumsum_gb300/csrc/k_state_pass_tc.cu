@@ -7,29 +7,38 @@
 // as one tensor-core contraction over the chunk's tokens.
 //
 // GB300 mapping
-//   * CTA = (128-wide dstate slice sigma, batch*head).  The state slice
-//     h^T [128 s, P] is the tcgen05 accumulator itself and stays in TMEM for
-//     the whole sequence (lane = s, column = p); each step scales it by
-//     exp2(G_last) in place and the MMA accumulates the jump onto it.
+//   * CTA = (128-wide dstate slice sigma, batch*head[, segment]).  State row
+//     s = sigma*128 + row, h^T[s, 0..P), lives in registers for the whole
+//     sequence, split between the two compute threads of that row.
 //   * Tokens are walked in 128-token tiles (the MMA K extent).  For
 //     chunk_size 256 a chunk is two tiles; the decay of the first tile is
 //     G at its last token, of the second G_last - G at the first tile's last
 //     token, so the product of the two steps is the chunk's exp2(G_last).
+//   * Per tile the tensor core computes the jump J = B^T X_hat [128 s, P]
+//     into one of two TMEM buffers (a fresh accumulation, not onto h), and
+//     the compute threads fold it in, h <- exp2(G_last) h + J, in f32
+//     registers.  With two jump buffers and two X_hat buffers, the MMAs of
+//     tile i+1 run while tile i is folded in and stored: the carried state
+//     is not a round trip through the tensor core per tile.
 //   * x [128 t, P] and B [128 t, 128 s] tiles arrive by TMA (128-byte
-//     swizzle) into a 3-stage ring; both are token-major, so the contraction
-//     over tokens uses MN-major operands: A = B^T (M = s), B = X_hat (N = p).
+//     swizzle) into a ring of stages; both are token-major, so the
+//     contraction over tokens uses MN-major operands: A = B^T (M = s),
+//     B = X_hat (N = p).
 //   * The pages scale B by dt * exp2(G_last - G) (b_dt_d); here the same
 //     per-token weight w_t is applied to x instead (X_hat = w * X, P < S so
-//     fewer elements), written back to shared memory in the swizzled layout.
-//     w_t <= dt_t because G is non-increasing, so nothing can overflow.
-//   * X_hat is split into two bf16 operands, hi = bf16(w x) and
-//     lo = bf16(w x - hi), and both are contracted (two MMA passes): the jump
-//     then carries ~16 mantissa bits instead of bf16's 8, so the carried
-//     state does not accumulate bf16 rounding of the weighted inputs.
-//   * Roles: warps 0-3 (one thread per token row / state row) build X_hat,
-//     store chunk states and rescale the accumulator; one thread of warp 4
-//     issues TMA loads and MMAs.  Every mbarrier wait is bounded; a timeout
-//     sets the kernel status word and the CTA leaves its loop.
+//     fewer elements), written over x in place in the stage.  w_t <= dt_t
+//     because G is non-increasing, so nothing can overflow.
+//   * X_hat is split into two bf16 operands, hi (over x in the stage) and
+//     lo (its own buffer) with hi + lo = w x to ~2^-16, and both are
+//     contracted: the jump then
+//     carries ~16 mantissa bits instead of bf16's 8, so the carried state
+//     does not accumulate bf16 rounding of the weighted inputs.
+//   * Roles: warps 0-7, two warpgroups over the same 128 rows, each with half
+//     of every row, build X_hat (thread = token row), fold the jumps in and
+//     store chunk states (thread = state row); one thread of warp 8 issues
+//     the MMAs, one thread of warp 9 the TMA loads.  Every mbarrier
+//     wait is bounded; a timeout sets the kernel status word and the role
+//     leaves its loop.
 #include "common.cuh"
 #include "ssd_internal.h"
 #include "tc05.cuh"
@@ -39,7 +48,8 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;
-constexpr int kThreads = 160;
+constexpr int kCompute = 256;  // warps 0-7: two warpgroups over the same 128 rows
+constexpr int kThreads = kCompute + 64;  // + warp 8 (MMA issue), warp 9 (TMA)
 constexpr int kMaxSeg = 64;  // segments of one sequence in the segmented pass
 constexpr uint32_t kRegion = 128 * 128;  // one 128-row x 128-byte swizzled region
 
@@ -47,23 +57,53 @@ template <int P>
 struct SpLayout {
     static constexpr int kStages = P <= 64 ? 3 : 2;
     static constexpr int kXRegions = P / 64;
-    static constexpr uint32_t kX = kXRegions * kRegion;
-    static constexpr uint32_t kB = 2 * kRegion;
-    static constexpr uint32_t kStage = kX + kB;
-    static constexpr uint32_t off_xh = kStages * kStage;  // X_hat hi, then lo
-    static constexpr uint32_t bytes = off_xh + 2 * kX;
-    static constexpr uint32_t kTmemCols = P < 32 ? 32 : P;
+    static constexpr uint32_t kX = kXRegions * kRegion;  // x tile, then X_hat hi over it
+    static constexpr uint32_t kB = 2 * kRegion;          // B tile [128 t, 128 s]
+    static constexpr uint32_t off_b = kX;
+    static constexpr uint32_t kStage = kX + kB;          // what TMA brings per stage
+    static constexpr uint32_t kTxBytes = kStage;
+    // X_hat lo, two buffers (tile parity): tile i+1's is written while the
+    // MMAs of tile i read the other one
+    static constexpr uint32_t off_lo = kStages * kStage;
+    // chunk states leave through a [P, 128] f32 staging box and a TMA store
+    // (P = 64; P = 128 has no room and stores from registers)
+    static constexpr bool kTmaEmit = P <= 64;
+    static constexpr uint32_t off_stg = off_lo + 2 * kX;
+    // G and dt of each stage's tile (128 + 128 f32), staged by the load warp
+    static constexpr uint32_t off_gd = off_stg + (kTmaEmit ? P * 128 * 4 : 0);
+    static constexpr uint32_t bytes = off_gd + kStages * 1024;
+    static constexpr uint32_t kTmemCols = 2 * P;         // two jump buffers
     static_assert(bytes + 1024 + 256 <= 232448, "shared memory budget");
 };
 
-// (w * a pair of bf16) as hi = bf16(value) and lo = bf16(value - hi), packed.
-__device__ __forceinline__ void split_scaled(uint32_t v, float w, uint32_t &hi, uint32_t &lo)
+// w * (a pair of bf16) as hi + lo, two packed bf16 pairs, with w = w_hi + w_lo
+// (w_hi = bf16(w)): hi = bf16(x w_hi); the residual x w_hi - hi is exact in
+// bf16 (x and w_hi carry 8 significant bits each), so lo = bf16(x w_lo +
+// residual) and hi + lo is within ~2^-16 of x w.
+__device__ __forceinline__ void split_scaled(uint32_t v, uint32_t whi, uint32_t wlo, uint32_t &hi,
+                                             uint32_t &lo)
 {
-    const float a = __uint_as_float(v << 16) * w;
-    const float b = __uint_as_float(v & 0xffff0000u) * w;
-    hi = pack_bf16x2(a, b);
-    const float ah = __uint_as_float(hi << 16), bh = __uint_as_float(hi & 0xffff0000u);
-    lo = pack_bf16x2(a - ah, b - bh);
+    hi = bf2_mul(v, whi);
+    lo = bf2_fma(v, wlo, bf2_fma(v, whi, hi ^ 0x80008000u));
+}
+
+// the 256 compute threads (named barrier 1; warps 8 and 9 never join it)
+__device__ __forceinline__ void compute_sync()
+{
+    asm volatile("barrier.sync 1, %0;" ::"n"(kCompute) : "memory");
+}
+
+// TMA store of an unswizzled box, marked evict-first in L2: chunk states are
+// written once and not read by this kernel, so they should not push x, B and
+// G out of L2
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int c0, int c1)
+{
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], pol;\n\t}" ::"l"(tmap),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_t *bar, int c0,
@@ -91,20 +131,22 @@ struct SpSeg {
 template <int P, bool REV>
 __global__ void __launch_bounds__(kThreads, 1)
 state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
-                     const __grid_constant__ CUtensorMap tm_b, const float *__restrict__ dtT,
+                     const __grid_constant__ CUtensorMap tm_b,
+                     const __grid_constant__ CUtensorMap tm_st, const float *__restrict__ dtT,
                      const float *__restrict__ Gc, const float *__restrict__ init,
                      float *__restrict__ states, float *__restrict__ final_state, Geom g,
-                     unsigned int *status, SpSeg sg)
+                     unsigned int *status, SpSeg sg, int tma_emit)
 {
     using Lay = SpLayout<P>;
     constexpr int kStages = Lay::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_ready, bar_mma;
+    __shared__ uint64_t bar_full[kStages], bar_xready[kStages], bar_empty[kStages];
+    __shared__ uint64_t bar_jfull[2], bar_jfree[2];
     __shared__ uint32_t tmem_slot;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sigma = blockIdx.x;
     const int64_t bh = blockIdx.y, b = bh / g.H, h = bh % g.H, grp = h / g.hpg;
     const int64_t n_all = (g.L + kTile - 1) / kTile;
@@ -112,20 +154,19 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int64_t t_begin = sg.mode ? (int64_t)seg * sg.seg_tiles : 0;
     const int64_t t_end = sg.mode ? min64(n_all, t_begin + sg.seg_tiles) : n_all;
     const int64_t n_tiles = t_end - t_begin;  // tiles of this CTA
-    float *slot_prev = (sg.mode == 2 && seg > 0)
-                           ? sg.slot_base + bh * sg.slot_bh + (int64_t)(seg - 1) * sg.slot_k
-                           : nullptr;
-    float *slot_out = (sg.mode == 1 && seg < sg.n_seg - 1)
-                          ? sg.slot_base + bh * sg.slot_bh + (int64_t)seg * sg.slot_k
-                          : nullptr;
+    // first token of the i-th tile this CTA walks
+    auto tile_tau = [&](int64_t i) -> int64_t { return (REV ? t_end - 1 - i : t_begin + i) * kTile; };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 4);  // one arrival per compute warp
+            mbar_init(&bar_xready[s], kCompute / 32);  // one arrival per compute warp
+            mbar_init(&bar_empty[s], 1);   // MMA commit
         }
-        mbar_init(&bar_ready, 4);
-        mbar_init(&bar_mma, 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&bar_jfull[j], 1);
+            mbar_init(&bar_jfree[j], kCompute / 32);
+        }
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -137,159 +178,241 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    if (tid == 128) {
-        // ---------------- TMA producer + MMA issuer (one thread)
-        prefetch_tmap(&tm_x);
-        prefetch_tmap(&tm_b);
-        auto issue = [&](int64_t i) {
-            const int s = (int)(i % kStages);
-            uint8_t *stage = smem + s * Lay::kStage;
-            mbar_arrive_expect_tx(&bar_full[s], Lay::kStage);
-            const int tok = (int)((REV ? t_end - 1 - i : t_begin + i) * kTile);
-            for (int r = 0; r < Lay::kXRegions; ++r)
-                tma_load_4d(stage + r * kRegion, &tm_x, &bar_full[s], r * 64, (int)h, tok, (int)b);
-            for (int r = 0; r < 2; ++r)
-                tma_load_4d(stage + Lay::kX + r * kRegion, &tm_b, &bar_full[s],
-                            sigma * 128 + r * 64, (int)grp, tok, (int)b);
+    if (warp == kCompute / 32 + 1) {
+        // ---------------- load warp: x and B by TMA (lane 0); G and dt of the
+        // tile by the whole warp, loaded a tile ahead into registers so their
+        // latency overlaps the wait for a free stage
+        const float *grow = Gc + bh * g.L;
+        const float *drow = dtT + bh * g.L;
+        float pg[4], pd[4];
+        auto gload = [&](int64_t i) {
+            const int64_t tau = tile_tau(i);
+            const int n = (int)min64(kTile, g.L - tau);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int t = 4 * lane + k;
+                pg[k] = t < n ? grow[tau + t] : 0.f;
+                pd[k] = (!REV && t < n) ? drow[tau + t] : 0.f;
+            }
         };
-        for (int64_t i = 0; i < kStages && i < n_tiles; ++i)
-            issue(i);
-        const uint32_t idesc = idesc_bf16(128, P, true, true);
-        const uint32_t xh = smem_u32(smem + Lay::off_xh);
+        if (lane == 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_b);
+        }
+        if (n_tiles > 0)
+            gload(0);
         for (int64_t i = 0; i < n_tiles; ++i) {
             const int s = (int)(i % kStages);
-            if (!mbar_wait(&bar_ready, (uint32_t)(i & 1))) {
-                atomicOr(status, 1u);
+            if (i >= kStages &&
+                !__all_sync(0xffffffffu, mbar_wait(&bar_empty[s], (uint32_t)((i / kStages - 1) & 1)))) {
+                if (lane == 0)
+                    atomicOr(status, 1u);
                 break;
             }
-            tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + s * Lay::kStage + Lay::kX);
+            float *sgd = reinterpret_cast<float *>(smem + Lay::off_gd + s * 1024);
 #pragma unroll
-            for (int part = 0; part < 2; ++part)  // X_hat hi, then lo
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks)
-                    mma_ss(tmem, smem_desc(a0 + ks * 2048, kRegion, 1024),
-                           smem_desc(xh + part * Lay::kX + ks * 2048, kRegion, 1024), idesc, 1u);
-            mma_commit(&bar_mma);
-            if (i + kStages < n_tiles) {
-                const uint32_t par = (uint32_t)((i / kStages) & 1);
-                if (!mbar_wait(&bar_empty[s], par) || !mbar_wait(&bar_mma, (uint32_t)(i & 1))) {
+            for (int k = 0; k < 4; ++k) {
+                sgd[4 * lane + k] = pg[k];
+                sgd[128 + 4 * lane + k] = pd[k];
+            }
+            if (i + 1 < n_tiles)
+                gload(i + 1);
+            __syncwarp();  // the warp's G / dt stores precede lane 0's arrival
+            if (lane == 0) {
+                uint8_t *stage = smem + s * Lay::kStage;
+                mbar_arrive_expect_tx(&bar_full[s], Lay::kTxBytes);
+                const int tok = (int)tile_tau(i);
+                for (int r = 0; r < Lay::kXRegions; ++r)
+                    tma_load_4d(stage + r * kRegion, &tm_x, &bar_full[s], r * 64, (int)h, tok, (int)b);
+                for (int r = 0; r < 2; ++r)
+                    tma_load_4d(stage + Lay::off_b + r * kRegion, &tm_b, &bar_full[s],
+                                sigma * 128 + r * 64, (int)grp, tok, (int)b);
+            }
+        }
+    } else if (warp == kCompute / 32) {
+        // ---------------- MMA issuer: J[i & 1] = B^T (X_hat hi + X_hat lo)
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(128, P, true, true);
+            for (int64_t i = 0; i < n_tiles; ++i) {
+                const int s = (int)(i % kStages), jb = (int)(i & 1);
+                if (!mbar_wait(&bar_xready[s], (uint32_t)((i / kStages) & 1)) ||
+                    (i >= 2 && !mbar_wait(&bar_jfree[jb], (uint32_t)(((i - 2) >> 1) & 1)))) {
                     atomicOr(status, 1u);
                     break;
                 }
-                issue(i + kStages);
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + s * Lay::kStage);
+                const uint32_t lo = smem_u32(smem + Lay::off_lo + jb * Lay::kX);
+                const uint32_t d = tmem + (uint32_t)(jb * P);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)  // X_hat hi, then lo
+#pragma unroll
+                    for (int ks = 0; ks < kTile / 16; ++ks)
+                        mma_ss(d, smem_desc(st + Lay::off_b + ks * 2048, kRegion, 1024),
+                               smem_desc(part ? lo + ks * 2048 : st + ks * 2048, kRegion, 1024),
+                               idesc, (part | ks) ? 1u : 0u);
+                mma_commit(&bar_jfull[jb]);
+                mma_commit(&bar_empty[s]);
             }
         }
-    } else if (tid < 128) {
-        // ---------------- compute threads: token row `tid`, state row s = sigma*128 + tid
-        const int row = tid;
+    } else {
+        // ---------------- compute threads: token row `row` for X_hat, state row
+        // s = sigma*128 + row for the carried state.  Warpgroup wg takes half
+        // of each row: X_hat chunks and state columns p0 .. p0 + P/2.
+        constexpr int PH = P / 2;
+        constexpr int NQ = Lay::kXRegions * 4;  // 16-byte X_hat chunks per row per warpgroup
+        const int row = tid & 127, wg = tid >> 7;
+        const int p0 = wg * PH;
         const int64_t s_idx = (int64_t)sigma * 128 + row;
         const bool s_ok = s_idx < g.S;
-        const uint32_t lane_base = tmem_at(tmem, (uint32_t)(warp * 32), 0);
+        const uint32_t lane_base = tmem_at(tmem, (uint32_t)((warp & 3) * 32), 0);
+        float *stg = reinterpret_cast<float *>(smem + Lay::off_stg);
+        const int bw = g.S < 128 ? (int)g.S : 128;  // staging box width (state rows)
+        const float *slot_prev = (sg.mode == 2 && seg > 0)
+                                     ? sg.slot_base + bh * sg.slot_bh + (int64_t)(seg - 1) * sg.slot_k
+                                     : nullptr;
+        float hs[PH];
 #pragma unroll
-        for (int c0 = 0; c0 < P; c0 += 16) {
-            uint32_t r[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float v = 0.f;
-                if (s_ok && sg.mode != 1) {
-                    if (slot_prev)
-                        v = slot_prev[(int64_t)(c0 + j) * g.S + s_idx];
-                    else if (init)
-                        v = init[(bh * g.P + c0 + j) * g.S + s_idx];
-                }
-                r[j] = __float_as_uint(v);
+        for (int p = 0; p < PH; ++p) {
+            float v = 0.f;
+            if (s_ok && sg.mode != 1) {
+                if (slot_prev)
+                    v = slot_prev[(int64_t)(p0 + p) * g.S + s_idx];
+                else if (init)
+                    v = init[(bh * g.P + p0 + p) * g.S + s_idx];
             }
-            tmem_st16(lane_base + c0, r);
+            hs[p] = v;
         }
-        tmem_st_wait();
 
-        const float *grow = Gc + bh * g.L;
-        const float *drow = dtT + bh * g.L;
-        uint8_t *sxh = smem + Lay::off_xh;
-        for (int64_t i = 0; i < n_tiles; ++i) {
-            const int s = (int)(i % kStages);
-            const int64_t tau = (REV ? t_end - 1 - i : t_begin + i) * kTile;
+        // G at the previous tile's last token: the base of a tile in the
+        // middle of a chunk (forward walk; the reverse walk has tile = chunk)
+        float gl_prev = 0.f;
+        // weight of this thread's token row and decay of tile i, from the
+        // stage's G / dt: forward w = dt_t exp2(G_last - G_t), reverse exp2(G_t)
+        auto weights = [&](int64_t i, float &w, float &decay) {
+            const float *sgd = reinterpret_cast<const float *>(smem + Lay::off_gd + (i % kStages) * 1024);
+            const int64_t tau = tile_tau(i);
             const int n = (int)min64(kTile, g.L - tau);
-            // tile-local log2 decay: G restarts at chunk starts, so a tile in
-            // the middle of a chunk subtracts G at the token before it
-            const float base = (tau % g.T == 0) ? 0.f : grow[tau - 1];
-            const float gL = grow[tau + n - 1] - base;
-            // forward: dt_t exp2(G_last - G_t); reverse (tile = chunk): exp2(G_t)
-            const float w = row < n ? (REV ? exp2f(grow[tau + row] - base)
-                                           : drow[tau + row] * exp2f(gL - (grow[tau + row] - base)))
-                                    : 0.f;
-            const float decay = exp2f(gL);
-
-            if (!mbar_wait(&bar_full[s], (uint32_t)((i / kStages) & 1))) {
-                atomicOr(status, 1u);
-                break;
-            }
-            const uint8_t *sx = smem + s * Lay::kStage;
+            // tile-local log2 decay: G restarts at chunk starts
+            const float gb = (tau % g.T == 0) ? 0.f : gl_prev;
+            const float gl = sgd[n - 1];
+            const float gr = sgd[row];
+            const float gL = gl - gb;
+            w = row < n ? (REV ? exp2f(gr - gb) : sgd[128 + row] * exp2f(gL - (gr - gb))) : 0.f;
+            decay = exp2f(gL);
+            gl_prev = gl;
+        };
+        // this warpgroup's half of X_hat of tile i: hi over x, lo in buffer i & 1
+        auto build = [&](int64_t i, float &decay) -> bool {
+            const int s = (int)(i % kStages);
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_full[s], (uint32_t)((i / kStages) & 1))))
+                return false;
+            float w;
+            weights(i, w, decay);
+            const uint32_t whi = pack_bf16x2(w, w);
+            const float w_lo = w - __uint_as_float(whi << 16);
+            const uint32_t wlo = pack_bf16x2(w_lo, w_lo);
+            uint8_t *stage = smem + s * Lay::kStage;
+            uint8_t *slo = smem + Lay::off_lo + (uint32_t)(i & 1) * Lay::kX;
 #pragma unroll
-            for (int r = 0; r < Lay::kXRegions; ++r) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t off = r * kRegion + sw128_offset(row, c);
-                    const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
-                    uint4 hi, lo;
-                    split_scaled(v.x, w, hi.x, lo.x);
-                    split_scaled(v.y, w, hi.y, lo.y);
-                    split_scaled(v.z, w, hi.z, lo.z);
-                    split_scaled(v.w, w, hi.w, lo.w);
-                    *reinterpret_cast<uint4 *>(sxh + off) = hi;
-                    *reinterpret_cast<uint4 *>(sxh + Lay::kX + off) = lo;
-                }
+            for (int q = 0; q < NQ; ++q) {
+                const int qq = wg * NQ + q;
+                const uint32_t off = (qq >> 3) * kRegion + sw128_offset(row, qq & 7);
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + off);
+                uint4 hi, lo;
+                split_scaled(v.x, whi, wlo, hi.x, lo.x);
+                split_scaled(v.y, whi, wlo, hi.y, lo.y);
+                split_scaled(v.z, whi, wlo, hi.z, lo.z);
+                split_scaled(v.w, whi, wlo, hi.w, lo.w);
+                *reinterpret_cast<uint4 *>(stage + off) = hi;
+                *reinterpret_cast<uint4 *>(slo + off) = lo;
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if ((tid & 31) == 0)
-                mbar_arrive(&bar_empty[s]);
+            if (lane == 0)
+                mbar_arrive(&bar_xready[s]);
+            return true;
+        };
 
-            // chunk start: store h (the state before this chunk), then decay it
-            const bool emit = states && s_ok && sg.mode != 1 && (tau % g.T == 0);
-            float *dst = emit ? states + ((bh * g.nc + tau / g.T) * g.P) * g.S + s_idx : nullptr;
+        bool ok = true;
+        float d_cur = 1.f, d_next = 1.f;
+        if (n_tiles > 0)
+            ok = build(0, d_cur);
+        for (int64_t i = 0; ok && i < n_tiles; ++i) {
+            // chunk start: store h, the state before this chunk
+            const int64_t tau = tile_tau(i);
+            if (states && sg.mode != 1 && tau % g.T == 0) {
+                const int64_t row0 = (bh * g.nc + tau / g.T) * g.P;  // row of p = 0 in [.., S]
+                if (Lay::kTmaEmit && tma_emit) {
+                    // the staging box is free once the previous store has read it
+                    if (tid == 0)
+                        bulk_wait_read();
+                    compute_sync();
+                    if (row < bw) {
 #pragma unroll
-            for (int c0 = 0; c0 < P; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + c0, r);
+                        for (int p = 0; p < PH; ++p)
+                            stg[(p0 + p) * bw + row] = hs[p];
+                    }
+                    fence_proxy_async_smem();
+                    compute_sync();
+                    if (tid == 0) {
+                        tma_store_2d(&tm_st, stg, sigma * 128, (int)row0);
+                        bulk_commit();
+                    }
+                } else if (s_ok) {
+                    float *dst = states + (row0 + p0) * g.S + s_idx;
+#pragma unroll
+                    for (int p = 0; p < PH; ++p)
+                        dst[(int64_t)p * g.S] = hs[p];
+                }
+            }
+            if (i + 1 < n_tiles && !(ok = build(i + 1, d_next)))
+                break;
+            // fold in this warpgroup's columns of the jump of tile i
+            const int jb = (int)(i & 1);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_jfull[jb], (uint32_t)((i >> 1) & 1)))))
+                break;
+            tc_fence_after();
+            constexpr int kQ = PH / 16 < 4 ? PH / 16 : 4;  // 16-column loads in flight
+#pragma unroll
+            for (int c0 = 0; c0 < PH; c0 += 16 * kQ) {
+                uint32_t r[kQ][16];
+#pragma unroll
+                for (int q = 0; q < kQ; ++q)
+                    tmem_ld16(lane_base + (uint32_t)(jb * P + p0 + c0 + 16 * q), r[q]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float v = __uint_as_float(r[j]);
-                    if (emit)
-                        dst[(int64_t)(c0 + j) * g.S] = v;
-                    r[j] = __float_as_uint(v * decay);
-                }
-                tmem_st16(lane_base + c0, r);
+                for (int q = 0; q < kQ; ++q)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        hs[c0 + 16 * q + j] = fmaf(d_cur, hs[c0 + 16 * q + j], __uint_as_float(r[q][j]));
             }
-            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if ((tid & 31) == 0)
-                mbar_arrive(&bar_ready);
-            if (!mbar_wait(&bar_mma, (uint32_t)(i & 1))) {
+            if (lane == 0)
+                mbar_arrive(&bar_jfree[jb]);
+            d_cur = d_next;
+        }
+        if (!ok) {
+            if (lane == 0)
                 atomicOr(status, 1u);
-                break;
+        } else {
+            // the end state: a segment's (mode 1) or the sequence's final state
+            float *end_dst = nullptr;
+            if (sg.mode == 1) {
+                if (seg < sg.n_seg - 1)
+                    end_dst = sg.slot_base + bh * sg.slot_bh + (int64_t)seg * sg.slot_k;
+            } else if (final_state && (sg.mode == 0 || seg == sg.n_seg - 1)) {
+                end_dst = final_state + bh * g.P * g.S;
             }
-            tc_fence_after();
-        }
-        // the end state: a segment's (mode 1) or the sequence's final state
-        float *end_dst = slot_out ? slot_out
-                                  : ((final_state && sg.mode != 1 && (sg.mode == 0 || seg == sg.n_seg - 1))
-                                         ? final_state + bh * g.P * g.S
-                                         : nullptr);
-        if (end_dst && s_ok) {
+            if (end_dst && s_ok) {
 #pragma unroll
-            for (int c0 = 0; c0 < P; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(lane_base + c0, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    end_dst[(int64_t)(c0 + j) * g.S + s_idx] = __uint_as_float(r[j]);
+                for (int p = 0; p < PH; ++p)
+                    end_dst[(int64_t)(p0 + p) * g.S + s_idx] = hs[p];
             }
         }
+        if (Lay::kTmaEmit && tma_emit && tid == 0)
+            bulk_wait_all();  // the staging box must outlive its last store
     }
     tc_fence_before();
     __syncthreads();
@@ -304,13 +427,21 @@ cudaError_t launch_p(const CUtensorMap &tx, const CUtensorMap &tb, const float *
                      const float *Gc, const float *init, float *states, float *final_state,
                      const Geom &g, unsigned int *status, cudaStream_t st, const SpSeg &sg = SpSeg{})
 {
+    // chunk states [B, H, nc, P, S] as f32 rows of S; box {min(S, 128), P}
+    CUtensorMap tst;
+    memset(&tst, 0, sizeof(tst));
+    const int64_t rows = g.B * g.H * g.nc * g.P;
+    const int tma_emit = SpLayout<P>::kTmaEmit && states && rows < (1LL << 31) &&
+                         make_tmap_f32_rows(&tst, states, (uint64_t)g.S, (uint64_t)rows,
+                                            (uint32_t)(g.S < 128 ? g.S : 128), (uint32_t)P);
     const size_t smem = SpLayout<P>::bytes + 1024;
     auto k = state_pass_tc_kernel<P, REV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     dim3 grid((unsigned)((g.S + 127) / 128), (unsigned)(g.B * g.H), (unsigned)(sg.mode ? sg.n_seg : 1));
-    k<<<grid, kThreads, smem, st>>>(tx, tb, dtT, Gc, init, states, final_state, g, status, sg);
+    k<<<grid, kThreads, smem, st>>>(tx, tb, tst, dtT, Gc, init, states, final_state, g, status, sg,
+                                    tma_emit);
     note_launch();
     return cudaGetLastError();
 }

@@ -42,6 +42,8 @@ cudaError_t launch_chunk_out_simt(const void *x, const void *Bm, const void *Cm,
 // TMA tensor maps (bf16, 128-byte swizzle, zero fill out of bounds).
 bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                     const uint64_t *strides_bytes, const uint32_t *box);
+bool make_tmap_f32_rows(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                        uint32_t box_cols, uint32_t box_rows);
 bool make_tmap_tokens_heads(CUtensorMap *map, const void *base, const Geom &g);
 bool make_tmap_tokens_groups(CUtensorMap *map, const void *base, const Geom &g);
 

@@ -13,8 +13,10 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 }  // namespace
 
-bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                    const uint64_t *strides_bytes, const uint32_t *box)
+namespace {
+bool encode(CUtensorMap *map, CUtensorMapDataType type, const void *base, int rank,
+            const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+            CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo)
 {
     std::call_once(g_once, [] {
         void *fn = nullptr;
@@ -36,12 +38,30 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t
         if (i + 1 < rank)
             gstride[i] = strides_bytes[i];
     }
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
-                          const_cast<void *>(base), gdim, gstride, bdim, estride,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = g_encode(map, type, (cuuint32_t)rank, const_cast<void *>(base), gdim, gstride,
+                          bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                    const uint64_t *strides_bytes, const uint32_t *box)
+{
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
+// f32 matrix [rows, cols] with a row pitch of cols * 4 bytes; box {box_cols,
+// box_rows}, unswizzled (shared memory holds the box row-major).
+bool make_tmap_f32_rows(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                        uint32_t box_cols, uint32_t box_rows)
+{
+    const uint64_t dims[2] = {cols, rows};
+    const uint64_t st[1] = {cols * 4};
+    const uint32_t box[2] = {box_cols, box_rows};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, 2, dims, st, box,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // x, y [B, L, H, P] viewed as 4-D {P, H, L, B}; box {64, 1, 128, 1}.
