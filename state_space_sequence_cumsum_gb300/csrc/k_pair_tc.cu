@@ -100,8 +100,10 @@ struct PairParams {
     //  segments -- each sequence is split into n_seg segments of seg_tiles
     //           tiles, items (pair, segment) dealt round-robin, segment-major.
     // Segment k > 0 starts from the state segment k-1 leaves in seg_state,
-    // published by seg_count reaching 4 (one count per warp).
-    int wrap;
+    // published by seg_count reaching 4 (one count per warp) -- unless
+    // `prefilled`: then a state pass has already put every segment's start
+    // state in seg_state, all items are independent and none hands off.
+    int wrap, prefilled;
     long long wrap_units;  // B * H/2 * n_tiles
     int seg_tiles, n_seg;
     float *seg_state;         // [B*H*n_seg][P][S]
@@ -638,7 +640,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 warp_arrive(&bar_xh);
 
                 // ---- a later segment waits until its predecessor published its state
-                if (first && w.seg > 0) {
+                if (first && w.seg > 0 && !prm.prefilled) {
                     const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + w.seg - 1;
                     bool ready = ld_acquire_gpu(cnt) >= 4u;
                     const uint64_t t_start = globaltimer_ns();
@@ -890,9 +892,10 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
                 // ---- state leaving the item: the next segment's start, or the final state
                 if (do_state && last_item) {
-                    const bool handoff = !last_seq;
+                    const bool handoff = !last_seq && !prm.prefilled;
                     float *dst = handoff ? prm.seg_state + ((bh * prm.n_seg + w.seg) * g.P) * g.S
-                                         : (want_final ? prm.final_state + bh * g.P * g.S : nullptr);
+                                         : ((last_seq && want_final) ? prm.final_state + bh * g.P * g.S
+                                                                     : nullptr);
                     if (dst) {
                         if (!mbar_wait(&bar_ds, par)) {
                             ok = false;
@@ -949,13 +952,19 @@ int sm_count_pair()
 
 // Work plan.  With at least one head pair per SM: the wrap schedule (one
 // contiguous piece of the pair-major tile sequence per CTA, at most one
-// hand-off slot per sequence).  Otherwise segmentation: enough (batch, head
-// pair, segment) items for about eight per SM, no segment shorter than two
-// tiles.
+// hand-off slot per sequence).  With at most half as many head pairs as SMs:
+// prefilled segments -- one wave of (pair, segment) items, every segment's
+// start state computed beforehand by the segmented tensor-core state pass, so
+// no item waits for another.  Otherwise segmentation with hand-offs: enough
+// (batch, head pair, segment) items for about eight per SM, no segment
+// shorter than two tiles.  SSD_PAIR_PREFILL=0 turns the prefilled plan off (a
+// test and measurement switch).
+constexpr int kMaxPrefillSeg = 64;  // segments the state pass's combine handles
+
 struct PairSegPlan {
-    bool wrap;
+    bool wrap, prefill;
     int seg_tiles, n_seg;
-    size_t state_bytes, count_bytes;
+    size_t state_bytes, count_bytes, gd_bytes;  // gd: G and dt^T for the prefill
 };
 
 PairSegPlan pair_seg_plan(const Geom &g)
@@ -965,12 +974,34 @@ PairSegPlan pair_seg_plan(const Geom &g)
     const int64_t units = g.B * (g.H / 2);
     const int64_t nbh = g.B * g.H;
     sp.wrap = units >= sm_count_pair() && n_tiles > 1;
+    sp.prefill = false;
+    sp.gd_bytes = 0;
     if (sp.wrap) {
         sp.seg_tiles = (int)n_tiles;
         sp.n_seg = 2;  // slot 0: the state a sequence's first part hands to its second
         sp.state_bytes = (size_t)(nbh * 2 * g.P * g.S) * sizeof(float);
         sp.count_bytes = (size_t)(nbh * 2) * sizeof(unsigned int);
         return sp;
+    }
+    const char *env = getenv("SSD_PAIR_PREFILL");
+    const int tpc = g.T / kTile;
+    int64_t want1 = sm_count_pair() / units;
+    if (want1 > kMaxPrefillSeg)
+        want1 = kMaxPrefillSeg;
+    if (want1 * 2 * tpc > n_tiles)
+        want1 = n_tiles / (2 * tpc);
+    if (want1 >= 2 && state_pass_tc_supported(g) && !(env && strcmp(env, "0") == 0)) {
+        int64_t st = (n_tiles + want1 - 1) / want1;
+        st = (st + tpc - 1) / tpc * tpc;
+        sp.seg_tiles = (int)st;
+        sp.n_seg = (int)((n_tiles + st - 1) / st);
+        if (sp.n_seg >= 2) {
+            sp.prefill = true;
+            sp.state_bytes = (size_t)(nbh * sp.n_seg * g.P * g.S) * sizeof(float);
+            sp.count_bytes = 0;
+            sp.gd_bytes = 2 * (size_t)(nbh * g.L) * sizeof(float);
+            return sp;
+        }
     }
     int64_t want = (8LL * sm_count_pair() + units - 1) / units;
     want = want < 1 ? 1 : want;
@@ -1027,7 +1058,8 @@ size_t pair_tc_scratch_bytes(const Geom &g)
     const PairSegPlan sp = pair_seg_plan(g);
     if (!sp.wrap && sp.n_seg <= 1)
         return 0;
-    return (sp.state_bytes + 255) / 256 * 256 + (sp.count_bytes + 255) / 256 * 256;
+    return (sp.state_bytes + 255) / 256 * 256 + (sp.count_bytes + 255) / 256 * 256 +
+           (sp.gd_bytes + 511) / 512 * 512;
 }
 
 cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dt,
@@ -1055,17 +1087,28 @@ cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, 
     prm.seg_tiles = sp.seg_tiles;
     prm.n_seg = sp.n_seg;
     prm.wrap = sp.wrap ? 1 : 0;
+    prm.prefilled = sp.prefill ? 1 : 0;
     prm.wrap_units = (long long)(g.B * (g.H / 2)) * prm.n_tiles;
     prm.n_items = (int)(g.B * (g.H / 2) * (sp.wrap ? 1 : sp.n_seg));
     if (sp.wrap || sp.n_seg > 1) {
         const size_t off = (sp.state_bytes + 255) / 256 * 256;
-        if (!scratch || scratch_bytes < off + sp.count_bytes)
+        const size_t off_gd = off + (sp.count_bytes + 255) / 256 * 256;
+        if (!scratch || scratch_bytes < off_gd + sp.gd_bytes)
             return cudaErrorInvalidValue;
         prm.seg_state = static_cast<float *>(scratch);
         prm.seg_count = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + off);
-        cudaError_t e = cudaMemsetAsync(prm.seg_count, 0, sp.count_bytes, st);
-        if (e != cudaSuccess)
+        cudaError_t e;
+        if (sp.prefill) {
+            // every segment's start state: G, then the segmented state pass
+            float *Gc = reinterpret_cast<float *>(static_cast<char *>(scratch) + off_gd);
+            float *dtT = Gc + g.B * g.H * g.L;
+            if ((e = launch_chunk_cumsum(dt, A, Gc, dtT, g, st)) != cudaSuccess ||
+                (e = launch_segment_starts_tc(x, Bm, dtT, Gc, init, prm.seg_state, sp.seg_tiles,
+                                              sp.n_seg, g, st)) != cudaSuccess)
+                return e;
+        } else if ((e = cudaMemsetAsync(prm.seg_count, 0, sp.count_bytes, st)) != cudaSuccess) {
             return e;
+        }
     }
     prm.status = device_status_word();
     if (!prm.status)

@@ -612,4 +612,40 @@ cudaError_t launch_state_pass_tc_segmented(const void *x, const void *Bm, const 
                      : launch_p<128, false>(tx, tb, dtT, Gc, init, states, final_state, g, status, st, sg);
 }
 
+// Start states of n_seg segments of seg_tiles tiles each (a whole number of
+// chunks): pass 1 and the combine of the segmented pass, with
+// slots[(bh * n_seg + k) * P * S ..] receiving the state at the start of
+// segment k + 1 (k < n_seg - 1).  For kernels that then run every segment at
+// once from these states.
+cudaError_t launch_segment_starts_tc(const void *x, const void *Bm, const float *dtT,
+                                     const float *Gc, const float *init, float *slots,
+                                     int seg_tiles, int n_seg, const Geom &g, cudaStream_t st)
+{
+    if (!state_pass_tc_supported(g) || n_seg < 2 || n_seg > kMaxSeg ||
+        (seg_tiles * kTile) % g.T != 0)
+        return cudaErrorNotSupported;
+    unsigned int *status = device_status_word();
+    if (!status)
+        return cudaErrorUnknown;
+    CUtensorMap tx, tb;
+    if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g))
+        return cudaErrorInvalidValue;
+    SpSeg sg{};
+    sg.mode = 1;
+    sg.seg_tiles = seg_tiles;
+    sg.n_seg = n_seg;
+    sg.slot_base = slots;
+    sg.slot_k = g.P * g.S;
+    sg.slot_bh = (int64_t)n_seg * sg.slot_k;
+    cudaError_t e =
+        g.P == 64 ? launch_p<64, false>(tx, tb, dtT, Gc, nullptr, nullptr, nullptr, g, status, st, sg)
+                  : launch_p<128, false>(tx, tb, dtT, Gc, nullptr, nullptr, nullptr, g, status, st, sg);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 cgrid((unsigned)((g.P * g.S + 255) / 256), (unsigned)(g.B * g.H));
+    seg_combine_kernel<<<cgrid, 256, 0, st>>>(Gc, init, g, sg);
+    note_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace ssd

@@ -58,6 +58,9 @@ cudaError_t launch_state_pass_tc(const void *x, const void *Bm, const float *dtT
 // start states), for long sequences with few (batch, head) units; needs the
 // chunk-state array.  cudaErrorNotSupported: too few tiles to split.
 void state_pass_seg_plan(const Geom &g, int sms, int *seg_tiles, int *n_seg);
+cudaError_t launch_segment_starts_tc(const void *x, const void *Bm, const float *dtT,
+                                     const float *Gc, const float *init, float *slots,
+                                     int seg_tiles, int n_seg, const Geom &g, cudaStream_t st);
 cudaError_t launch_state_pass_tc_segmented(const void *x, const void *Bm, const float *dtT,
                                            const float *Gc, const float *init, float *states,
                                            float *final_state, const Geom &g, cudaStream_t st);

@@ -188,10 +188,36 @@ def test_fused_kernels_every_decay_mode(kernel, monkeypatch):
 
 
 @pytest.mark.parametrize("S", [64, 128])
-def test_pair_kernel_many_segments(S):
+@pytest.mark.parametrize("prefill", ["1", "0"])
+def test_pair_kernel_many_segments(S, prefill, monkeypatch):
     """One batch row and four heads over 4095 tokens: the fused pass splits
-    each sequence into many segments handed off through global memory."""
+    each sequence into many segments, their start states either computed
+    beforehand by the segmented state pass (prefill) or handed off through
+    global memory from segment to segment."""
+    monkeypatch.setenv("SSD_PAIR_PREFILL", prefill)
     check_case(1, 4095, 4, 64, S, 1, 128, torch.bfloat16, init="randn", seed=43 + S)
+
+
+@pytest.mark.parametrize("T", [128, 256])
+@pytest.mark.parametrize("init", ["zero", "randn"])
+def test_pair_prefilled_segments_match_handoff(T, init, monkeypatch):
+    """Few head pairs (one wave of (pair, segment) items): segments run at
+    once from start states of the segmented state pass ("Kernel 2:
+    fwd_pass_state" over parallel segments plus a serial combine).  The
+    result matches the hand-off plan and the oracle, chunk states included,
+    over a ragged last segment and two tiles per chunk at T = 256."""
+    inp = case_inputs(2, 3001, 4, 64, 128, 2, T, init=init, seed=T + 5)
+    ref = oracle_run(inp, T, want_states=True)
+    out = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("SSD_PAIR_PREFILL", mode)
+        out[mode] = run_fwd(inp, T)
+        y, fin, st = out[mode]
+        assert_parity(y, ref["y"], torch.bfloat16, "y")
+        assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
+        assert_parity(st, ref["chunk_states"], torch.bfloat16, "chunk_states")
+    scale = max(1.0, out["0"][1].abs().max().item())
+    assert (out["1"][1] - out["0"][1]).abs().max().item() <= 1e-3 * scale
 
 
 def test_pair_and_single_kernels_agree(monkeypatch):
