@@ -474,20 +474,26 @@ cudaError_t launch_state_pass_tc(const void *x, const void *Bm, const float *dtT
 // Start states of the segments from their local end states (mode 1):
 // slot(k) <- exp2(D_k) slot(k-1) + slot(k), slot(-1) = init (or 0), where D_k
 // is segment k's total log2 decay, the sum of G at each of its chunks' last
-// valid tokens.  One thread per state element; the first n_seg - 1 threads
-// of each block form the decay factors.  The slot loads are independent of
-// the carried state, so they are issued eight at a time ahead of the chain.
+// valid tokens.  One thread per state element; each warp of the block sums
+// the decays of some segments, its lanes striding over the segment's chunks.
+// The slot loads are independent of the carried state, so they are issued
+// eight at a time ahead of the chain.
 __global__ void __launch_bounds__(256)
 seg_combine_kernel(const float *__restrict__ Gc, const float *__restrict__ init, Geom g, SpSeg sg)
 {
     __shared__ float sdec[kMaxSeg];
     const int64_t bh = blockIdx.y;
     const int chunks_per_seg = sg.seg_tiles * kTile / g.T;
-    for (int k = threadIdx.x; k < sg.n_seg - 1; k += blockDim.x) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int k = warp; k < sg.n_seg - 1; k += blockDim.x >> 5) {
         float d = 0.f;
-        for (int c = k * chunks_per_seg; c < (k + 1) * chunks_per_seg && c < g.nc; ++c)
+        for (int c = k * chunks_per_seg + lane; c < (k + 1) * chunks_per_seg && c < g.nc; c += 32)
             d += Gc[bh * g.L + min64(g.L, (int64_t)(c + 1) * g.T) - 1];
-        sdec[k] = exp2f(d);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            d += __shfl_xor_sync(0xffffffffu, d, o);
+        if (lane == 0)
+            sdec[k] = exp2f(d);
     }
     __syncthreads();
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
