@@ -36,7 +36,9 @@
 //   * Roles: warps 0-7, two warpgroups over the same 128 rows, each with half
 //     of every row, build X_hat (thread = token row), fold the jumps in and
 //     store chunk states (thread = state row); one thread of warp 8 issues
-//     the MMAs, one thread of warp 9 the TMA loads.  Every mbarrier
+//     the MMAs; warp 9 issues the TMA loads (one lane) and forms each tile's
+//     per-token weights and decay from G and dt (loaded a tile ahead) into
+//     the stage, off the compute warps' path.  Every mbarrier
 //     wait is bounded; a timeout sets the kernel status word and the role
 //     leaves its loop.
 #include "common.cuh"
@@ -69,7 +71,7 @@ struct SpLayout {
     // (P = 64; P = 128 has no room and stores from registers)
     static constexpr bool kTmaEmit = P <= 64;
     static constexpr uint32_t off_stg = off_lo + 2 * kX;
-    // G and dt of each stage's tile (128 + 128 f32), staged by the load warp
+    // weights of each stage's tile (128 f32) and its decay, by the load warp
     static constexpr uint32_t off_gd = off_stg + (kTmaEmit ? P * 128 * 4 : 0);
     static constexpr uint32_t bytes = off_gd + kStages * 1024;
     static constexpr uint32_t kTmemCols = 2 * P;         // two jump buffers
@@ -153,9 +155,13 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int seg = blockIdx.z;
     const int64_t t_begin = sg.mode ? (int64_t)seg * sg.seg_tiles : 0;
     const int64_t t_end = sg.mode ? min64(n_all, t_begin + sg.seg_tiles) : n_all;
-    const int64_t n_tiles = t_end - t_begin;  // tiles of this CTA
+    const int n_tiles = (int)(t_end - t_begin);  // tiles of this CTA
     // first token of the i-th tile this CTA walks
-    auto tile_tau = [&](int64_t i) -> int64_t { return (REV ? t_end - 1 - i : t_begin + i) * kTile; };
+    auto tile_tau = [&](int i) -> int64_t { return (REV ? t_end - 1 - i : t_begin + i) * kTile; };
+    // chunks are one or two tiles (T = 128 or 256): chunk index and chunk
+    // start by shift and mask, no 64-bit division in the tile loop
+    const int tpc_shift = g.T == 2 * kTile ? 1 : 0;
+    auto tile_index = [&](int i) -> int { return (int)(REV ? t_end - 1 - i : t_begin + i); };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -181,19 +187,26 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     if (warp == kCompute / 32 + 1) {
         // ---------------- load warp: x and B by TMA (lane 0); G and dt of the
         // tile by the whole warp, loaded a tile ahead into registers so their
-        // latency overlaps the wait for a free stage
+        // latency overlaps the wait for a free stage, turned into the tile's
+        // weights here
         const float *grow = Gc + bh * g.L;
         const float *drow = dtT + bh * g.L;
-        float pg[4], pd[4];
-        auto gload = [&](int64_t i) {
+        float pg0 = 0.f, pg1 = 0.f, pg2 = 0.f, pg3 = 0.f;  // G of tokens 4 lane + 0..3
+        float pd0 = 0.f, pd1 = 0.f, pd2 = 0.f, pd3 = 0.f;  // dt of the same tokens
+        float gl_prev = 0.f;  // G at the previous tile's last token (forward walk)
+        auto gload = [&](int i) {
             const int64_t tau = tile_tau(i);
             const int n = (int)min64(kTile, g.L - tau);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int t = 4 * lane + k;
-                pg[k] = t < n ? grow[tau + t] : 0.f;
-                pd[k] = (!REV && t < n) ? drow[tau + t] : 0.f;
-            }
+            const int t = 4 * lane;
+            const float *gp = grow + tau + t, *dp = drow + tau + t;
+            pg0 = t < n ? gp[0] : 0.f;
+            pg1 = t + 1 < n ? gp[1] : 0.f;
+            pg2 = t + 2 < n ? gp[2] : 0.f;
+            pg3 = t + 3 < n ? gp[3] : 0.f;
+            pd0 = (!REV && t < n) ? dp[0] : 0.f;
+            pd1 = (!REV && t + 1 < n) ? dp[1] : 0.f;
+            pd2 = (!REV && t + 2 < n) ? dp[2] : 0.f;
+            pd3 = (!REV && t + 3 < n) ? dp[3] : 0.f;
         };
         if (lane == 0) {
             prefetch_tmap(&tm_x);
@@ -201,7 +214,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
         if (n_tiles > 0)
             gload(0);
-        for (int64_t i = 0; i < n_tiles; ++i) {
+        for (int i = 0; i < n_tiles; ++i) {
             const int s = (int)(i % kStages);
             if (i >= kStages &&
                 !__all_sync(0xffffffffu, mbar_wait(&bar_empty[s], (uint32_t)((i / kStages - 1) & 1)))) {
@@ -209,15 +222,31 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                     atomicOr(status, 1u);
                 break;
             }
-            float *sgd = reinterpret_cast<float *>(smem + Lay::off_gd + s * 1024);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                sgd[4 * lane + k] = pg[k];
-                sgd[128 + 4 * lane + k] = pd[k];
+            // the tile's per-token weights and its decay, into the stage's
+            // slot: forward w = dt_t exp2(G_last - G_t), reverse exp2(G_t),
+            // with G relative to the tile start (G restarts at chunk starts; a
+            // tile in the middle of a chunk subtracts G before it)
+            {
+                const int n = (int)min64(kTile, g.L - tile_tau(i));
+                const float gb = (tile_index(i) & tpc_shift) == 0 ? 0.f : gl_prev;
+                const int e = (n - 1) & 3;
+                const float mine = e == 0 ? pg0 : (e == 1 ? pg1 : (e == 2 ? pg2 : pg3));
+                const float gl = __shfl_sync(0xffffffffu, mine, (n - 1) >> 2);
+                const float gL = gl - gb;
+                float *sw = reinterpret_cast<float *>(smem + Lay::off_gd + s * 1024);
+                auto wt = [&](int t, float gv, float dv) {
+                    return t < n ? (REV ? exp2f(gv - gb) : dv * exp2f(gL - (gv - gb))) : 0.f;
+                };
+                const int t = 4 * lane;
+                *reinterpret_cast<float4 *>(sw + t) =
+                    make_float4(wt(t, pg0, pd0), wt(t + 1, pg1, pd1), wt(t + 2, pg2, pd2), wt(t + 3, pg3, pd3));
+                if (lane == 0)
+                    sw[128] = exp2f(gL);
+                gl_prev = gl;
             }
             if (i + 1 < n_tiles)
                 gload(i + 1);
-            __syncwarp();  // the warp's G / dt stores precede lane 0's arrival
+            __syncwarp();  // the warp's weight stores precede lane 0's arrival
             if (lane == 0) {
                 uint8_t *stage = smem + s * Lay::kStage;
                 mbar_arrive_expect_tx(&bar_full[s], Lay::kTxBytes);
@@ -233,7 +262,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // ---------------- MMA issuer: J[i & 1] = B^T (X_hat hi + X_hat lo)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(128, P, true, true);
-            for (int64_t i = 0; i < n_tiles; ++i) {
+            for (int i = 0; i < n_tiles; ++i) {
                 const int s = (int)(i % kStages), jb = (int)(i & 1);
                 if (!mbar_wait(&bar_xready[s], (uint32_t)((i / kStages) & 1)) ||
                     (i >= 2 && !mbar_wait(&bar_jfree[jb], (uint32_t)(((i - 2) >> 1) & 1)))) {
@@ -284,26 +313,15 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             hs[p] = v;
         }
 
-        // G at the previous tile's last token: the base of a tile in the
-        // middle of a chunk (forward walk; the reverse walk has tile = chunk)
-        float gl_prev = 0.f;
-        // weight of this thread's token row and decay of tile i, from the
-        // stage's G / dt: forward w = dt_t exp2(G_last - G_t), reverse exp2(G_t)
-        auto weights = [&](int64_t i, float &w, float &decay) {
-            const float *sgd = reinterpret_cast<const float *>(smem + Lay::off_gd + (i % kStages) * 1024);
-            const int64_t tau = tile_tau(i);
-            const int n = (int)min64(kTile, g.L - tau);
-            // tile-local log2 decay: G restarts at chunk starts
-            const float gb = (tau % g.T == 0) ? 0.f : gl_prev;
-            const float gl = sgd[n - 1];
-            const float gr = sgd[row];
-            const float gL = gl - gb;
-            w = row < n ? (REV ? exp2f(gr - gb) : sgd[128 + row] * exp2f(gL - (gr - gb))) : 0.f;
-            decay = exp2f(gL);
-            gl_prev = gl;
+        // weight of this thread's token row and decay of tile i, formed by the
+        // load warp in the stage's slot
+        auto weights = [&](int i, float &w, float &decay) {
+            const float *sw = reinterpret_cast<const float *>(smem + Lay::off_gd + (i % kStages) * 1024);
+            w = sw[row];
+            decay = sw[128];
         };
         // this warpgroup's half of X_hat of tile i: hi over x, lo in buffer i & 1
-        auto build = [&](int64_t i, float &decay) -> bool {
+        auto build = [&](int i, float &decay) -> bool {
             const int s = (int)(i % kStages);
             if (!__all_sync(0xffffffffu, mbar_wait(&bar_full[s], (uint32_t)((i / kStages) & 1))))
                 return false;
@@ -314,18 +332,26 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             const uint32_t wlo = pack_bf16x2(w_lo, w_lo);
             uint8_t *stage = smem + s * Lay::kStage;
             uint8_t *slo = smem + Lay::off_lo + (uint32_t)(i & 1) * Lay::kX;
+            // every load before the first store: the stores go over the same
+            // buffer, so the compiler would otherwise keep each chunk's load
+            // behind the previous chunk's store
+            uint32_t off[NQ];
+            uint4 v[NQ];
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
                 const int qq = wg * NQ + q;
-                const uint32_t off = (qq >> 3) * kRegion + sw128_offset(row, qq & 7);
-                const uint4 v = *reinterpret_cast<const uint4 *>(stage + off);
+                off[q] = (qq >> 3) * kRegion + sw128_offset(row, qq & 7);
+                v[q] = *reinterpret_cast<const uint4 *>(stage + off[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
                 uint4 hi, lo;
-                split_scaled(v.x, whi, wlo, hi.x, lo.x);
-                split_scaled(v.y, whi, wlo, hi.y, lo.y);
-                split_scaled(v.z, whi, wlo, hi.z, lo.z);
-                split_scaled(v.w, whi, wlo, hi.w, lo.w);
-                *reinterpret_cast<uint4 *>(stage + off) = hi;
-                *reinterpret_cast<uint4 *>(slo + off) = lo;
+                split_scaled(v[q].x, whi, wlo, hi.x, lo.x);
+                split_scaled(v[q].y, whi, wlo, hi.y, lo.y);
+                split_scaled(v[q].z, whi, wlo, hi.z, lo.z);
+                split_scaled(v[q].w, whi, wlo, hi.w, lo.w);
+                *reinterpret_cast<uint4 *>(stage + off[q]) = hi;
+                *reinterpret_cast<uint4 *>(slo + off[q]) = lo;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -338,11 +364,11 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         float d_cur = 1.f, d_next = 1.f;
         if (n_tiles > 0)
             ok = build(0, d_cur);
-        for (int64_t i = 0; ok && i < n_tiles; ++i) {
+        for (int i = 0; ok && i < n_tiles; ++i) {
             // chunk start: store h, the state before this chunk
-            const int64_t tau = tile_tau(i);
-            if (states && sg.mode != 1 && tau % g.T == 0) {
-                const int64_t row0 = (bh * g.nc + tau / g.T) * g.P;  // row of p = 0 in [.., S]
+            const int ti = tile_index(i);
+            if (states && sg.mode != 1 && (ti & tpc_shift) == 0) {
+                const int64_t row0 = (bh * g.nc + (ti >> tpc_shift)) * g.P;  // row of p = 0 in [.., S]
                 if (Lay::kTmaEmit && tma_emit) {
                     // the staging box is free once the previous store has read it
                     if (tid == 0)
