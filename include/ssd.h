@@ -268,6 +268,34 @@ ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, con
                              float *final_state, float *chunk_states, ssd_dims_t dims,
                              ssd_dtype_t dtype, int chunk_size, void *stream);
 
+/*
+ * ssd_fwd from host memory to host memory.  x, dt, A, Bm, Cm, D, init_state
+ * (optional) and the outputs y and final_state (optional) are HOST buffers
+ * in ssd_fwd's layouts; page-locked (pinned) host memory lets the copies run
+ * asynchronously.  workspace is DEVICE memory of at least
+ * ssd_fwd_host_workspace_size(dims, dtype, chunk_size) bytes, 256-byte
+ * aligned.  Chunk states are not returned (use ssd_fwd for those).
+ *
+ * The sequence is cut into up to four parts of whole chunks (at least 512
+ * tokens each); part k runs ssd_fwd on its tokens from the state part k-1
+ * ended with -- "Kernel 2: fwd_pass_state" carries the state across chunk
+ * boundaries, so this computes ssd_fwd's function, up to the rounding of the
+ * carried state.  Part k's inputs are copied up on one internal stream while
+ * part k-1 computes on `stream` and part k-2's y is copied down on a second
+ * internal stream, so both copy directions overlap the kernels.  The call is
+ * asynchronous and stream-ordered: it starts after the work already on
+ * `stream`, and `stream` waits for all of it (synchronize `stream` before
+ * reading y).  The internal streams and events of each device are created
+ * on first use and kept; calls are serialized by a mutex while they issue
+ * work (not while it runs).  Errors: as ssd_fwd, plus SSD_ERR_WORKSPACE for
+ * a short or unaligned workspace and SSD_ERR_CUDA for a failed copy.
+ */
+size_t ssd_fwd_host_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size);
+ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const void *Bm,
+                          const void *Cm, const float *D, const float *init_state, void *y,
+                          float *final_state, ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
 /* Chunk size ssd_fwd uses for chunk_size == 0 with these dims and dtype. */
 int ssd_fwd_chosen_chunk_size(ssd_dims_t dims, ssd_dtype_t dtype);
 

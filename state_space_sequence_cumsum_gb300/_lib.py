@@ -26,6 +26,7 @@ SSD_F32 = 1
 EXPORTS = ("ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out",
            "ssd_state_out_workspace_size",
            "ssd_fwd_path", "ssd_fwd_workspace_size", "ssd_fwd", "ssd_fwd_noalloc",
+           "ssd_fwd_host", "ssd_fwd_host_workspace_size",
            "ssd_fwd_chosen_chunk_size", "ssd_decode_step", "ssd_bwd", "ssd_bwd_workspace_size",
            "ssd_gated_rmsnorm",
            "ssd_launch_count", "ssd_status_string", "ssd_stream_status")
@@ -78,6 +79,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "ssd_fwd": ([vp, fp, fp, vp, vp, fp, fp, vp, fp, fp, D, i32, i32, vp,
                          ctypes.c_size_t, vp], st),
             "ssd_fwd_noalloc": ([vp, fp, fp, vp, vp, fp, fp, vp, fp, fp, D, i32, i32, vp], st),
+            "ssd_fwd_host": ([vp, fp, fp, vp, vp, fp, fp, vp, fp, D, i32, i32, vp,
+                              ctypes.c_size_t, vp], st),
+            "ssd_fwd_host_workspace_size": ([D, i32, i32], ctypes.c_size_t),
             "ssd_fwd_chosen_chunk_size": ([D, i32], ctypes.c_int),
             "ssd_decode_step": ([vp, fp, fp, vp, vp, fp, fp, fp, vp, D, i32, vp], st),
             "ssd_bwd_workspace_size": ([D, i32], ctypes.c_size_t),

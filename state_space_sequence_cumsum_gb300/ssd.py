@@ -17,6 +17,7 @@ from ._lib import SsdError, check, dims as _dims
 __all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out", "ssd_fwd",
            "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd_staged",
            "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_stream_status",
+           "ssd_fwd_host",
            "ssd_status_string", "ssd_decode_step", "ssd_bwd", "ssd_gated_rmsnorm",
            "SsdFunction", "SsdError",
            "Workspace"]
@@ -272,6 +273,50 @@ def ssd_fwd(x, dt, A, B, C, D, chunk_size=0, initial_state=None, return_final_st
                       _ptr(initial_state), _ptr(y), _ptr(final_state), _ptr(chunk_states), d,
                       code, T, _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream)), "ssd_fwd")
     return y, final_state, chunk_states
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("ssd_fwd_host takes host (CPU) tensors")
+    if not t.is_contiguous():
+        raise ValueError("SSD tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else None
+
+
+def ssd_fwd_host(x, dt, A, B, C, D, chunk_size=0, initial_state=None, y=None,
+                 final_state=True, workspace: Workspace | None = None, device=None, stream=None):
+    """Whole SSD forward from host tensors to host tensors (ssd_fwd_host: the
+    copies overlap the kernels).  Inputs and outputs are CPU tensors, pinned
+    for asynchronous copies; the call returns before the work ends --
+    synchronize `stream` (default: the current stream of `device`) before
+    reading y.  Returns (y, final_state or None)."""
+    d = _geom(x, B)
+    for t, n in ((dt, "dt"), (A, "A"), (D, "D"), (initial_state, "initial_state")):
+        _f32(t, n)
+    code = _dtype_code(x)
+    lib = _lib.load()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if y is None:
+        y = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    if final_state is True:
+        final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate),
+                                  dtype=torch.float32).pin_memory()
+    elif final_state is False:
+        final_state = None
+    nbytes = int(lib.ssd_fwd_host_workspace_size(d, code, int(chunk_size)))
+    if nbytes == 0:
+        raise SsdError(_lib.SSD_ERR_INVALID_ARG, "ssd_fwd_host")
+    ws = (workspace or Workspace()).get(nbytes, dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        check(lib.ssd_fwd_host(_host_ptr(x), _host_ptr(dt), _host_ptr(A), _host_ptr(B),
+                               _host_ptr(C), _host_ptr(D), _host_ptr(initial_state), _host_ptr(y),
+                               _host_ptr(final_state), d, code, int(chunk_size), _ptr(ws),
+                               ctypes.c_size_t(ws.numel()), ctypes.c_void_p(s.cuda_stream)),
+              "ssd_fwd_host")
+    return y, final_state
 
 
 def ssd_state_out(x, B, C, dt_t, G_cum, D, chunk_size, initial_state=None, y=None,
