@@ -77,10 +77,14 @@ struct BtParams {
 // lane-0-only block); the aligned bar.sync would be undefined there.
 __device__ __forceinline__ void compute_sync() { asm volatile("barrier.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+// TMA reduce-add of a [128 rows][32 f32] swizzled shared-memory box into
+// global f32 (rows past the tensor's end are not touched).
+__device__ __forceinline__ void tma4_reduce_add(const void *tmap, const void *src, int c0, int c1,
+                                                int c2, int c3)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
+    asm volatile("cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.bulk_group"
+                 " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(tmap),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
                  : "memory");
 }
 
@@ -88,7 +92,8 @@ template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
                     const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
-                    const __grid_constant__ CUtensorMap tm_dx, BtParams prm)
+                    const __grid_constant__ CUtensorMap tm_dx, const __grid_constant__ CUtensorMap tm_db,
+                    const __grid_constant__ CUtensorMap tm_dc, BtParams prm)
 {
     using Lay = BtLayout<S>;
     extern __shared__ uint8_t smem_raw[];
@@ -227,18 +232,32 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const float *ds_g = prm.dstates + (bh * g.nc + c) * 64 * S;
             constexpr int kLanesPerRow = S / 4;           // 32 (S 128) or 16 (S 64)
             constexpr int kRowsPerPass = 32 / kLanesPerRow;
+            constexpr int kIters = 64 / (4 * kRowsPerPass);  // rows per lane: 16 or 8
+            constexpr int kBatch = 8;                         // rows whose loads are in flight together
             const int sub = lane % kLanesPerRow, rsub = lane / kLanesPerRow;
-            for (int p = warp * kRowsPerPass + rsub; p < 64; p += 4 * kRowsPerPass) {
-                const int s = 4 * sub;
-                const float4 hv = *reinterpret_cast<const float4 *>(hin_g + p * S + s);
-                const float4 dv = *reinterpret_cast<const float4 *>(ds_g + p * S + s);
-                dshin += hv.x * dv.x + hv.y * dv.y + hv.z * dv.z + hv.w * dv.w;
-                const uint32_t reg = (uint32_t)(s / 64), col = (uint32_t)(s % 64);
-                const uint32_t off = reg * Lay::kStateRegion + sw128_offset((uint32_t)p, col / 8) + (col % 8) * 2;
-                *reinterpret_cast<uint2 *>(smem + Lay::off_hin + off) =
-                    make_uint2(pack_bf16x2(hv.x, hv.y), pack_bf16x2(hv.z, hv.w));
-                *reinterpret_cast<uint2 *>(smem + Lay::off_ds + off) =
-                    make_uint2(pack_bf16x2(dv.x, dv.y), pack_bf16x2(dv.z, dv.w));
+            const int s = 4 * sub;
+            const uint32_t reg = (uint32_t)(s / 64), col = (uint32_t)(s % 64);
+#pragma unroll
+            for (int k0 = 0; k0 < kIters; k0 += kBatch) {
+                // a batch of rows' loads first: each is an HBM round trip
+                float4 hv[kBatch], dv[kBatch];
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int p = warp * kRowsPerPass + rsub + (k0 + k) * 4 * kRowsPerPass;
+                    hv[k] = *reinterpret_cast<const float4 *>(hin_g + p * S + s);
+                    dv[k] = *reinterpret_cast<const float4 *>(ds_g + p * S + s);
+                }
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int p = warp * kRowsPerPass + rsub + (k0 + k) * 4 * kRowsPerPass;
+                    dshin += hv[k].x * dv[k].x + hv[k].y * dv[k].y + hv[k].z * dv[k].z + hv[k].w * dv[k].w;
+                    const uint32_t off =
+                        reg * Lay::kStateRegion + sw128_offset((uint32_t)p, col / 8) + (col % 8) * 2;
+                    *reinterpret_cast<uint2 *>(smem + Lay::off_hin + off) =
+                        make_uint2(pack_bf16x2(hv[k].x, hv[k].y), pack_bf16x2(hv[k].z, hv[k].w));
+                    *reinterpret_cast<uint2 *>(smem + Lay::off_ds + off) =
+                        make_uint2(pack_bf16x2(dv[k].x, dv[k].y), pack_bf16x2(dv[k].z, dv[k].w));
+                }
             }
         }
         fence_proxy_async_smem();
@@ -366,30 +385,40 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             ddt_direct = colq + eT * xb;
             rj = eT * dti * xb;
             fence_proxy_async_smem();
-            // dB and dC rows of this chunk's tokens.  The TMEM loads are
-            // warp-collective (.sync.aligned): every lane runs them, and only the
-            // rows of valid tokens are added.
+            // dB and dC rows of this chunk's tokens, added into the f32
+            // accumulators by TMA reductions: each row goes to shared memory in
+            // [128 rows][32 f32] swizzled boxes (dB over Q1 / Q2, dC over B / C:
+            // phase B has read them all), then one thread issues the bulk adds.
+            // The TMEM loads are warp-collective, so every lane runs them; rows
+            // past the sequence end are clipped by the tensor map.
             {
-                const int64_t row = (b * g.L + tau + (valid ? i : 0)) * g.G + grp;
-                float *dbrow = prm.dBacc + row * S;
-                float *dcrow = prm.dCacc + row * S;
+                uint8_t *stg_db = smem + Lay::off_q1, *stg_dc = smem + Lay::off_b;
 #pragma unroll
                 for (int s0 = 0; s0 < S; s0 += 16) {
                     uint32_t vb[16], vc[16];
                     tmem_ld16(tl + Lay::t_db + s0, vb);
                     tmem_ld16(tl + Lay::t_dc + s0, vc);
                     tmem_ld_wait();
-                    if (valid) {
+                    const uint32_t box = (uint32_t)(s0 / 32) * kRegion;
 #pragma unroll
-                        for (int q = 0; q < 16; q += 4) {
-                            red_add_v4(dbrow + s0 + q, __uint_as_float(vb[q]), __uint_as_float(vb[q + 1]),
-                                       __uint_as_float(vb[q + 2]), __uint_as_float(vb[q + 3]));
-                            red_add_v4(dcrow + s0 + q, __uint_as_float(vc[q]), __uint_as_float(vc[q + 1]),
-                                       __uint_as_float(vc[q + 2]), __uint_as_float(vc[q + 3]));
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t off = box + sw128_offset((uint32_t)i, (uint32_t)((s0 % 32) / 4 + q));
+                        *reinterpret_cast<uint4 *>(stg_db + off) =
+                            make_uint4(vb[4 * q], vb[4 * q + 1], vb[4 * q + 2], vb[4 * q + 3]);
+                        *reinterpret_cast<uint4 *>(stg_dc + off) =
+                            make_uint4(vc[4 * q], vc[4 * q + 1], vc[4 * q + 2], vc[4 * q + 3]);
                     }
                 }
             }
+        }
+        fence_proxy_async_smem();
+        compute_sync();  // every row of the dB / dC boxes and of the dx tile is in shared memory
+        if (ok && i == 0) {
+            for (int r = 0; r < S / 32; ++r) {
+                tma4_reduce_add(&tm_db, smem + Lay::off_q1 + r * kRegion, 32 * r, (int)grp, (int)tau, (int)b);
+                tma4_reduce_add(&tm_dc, smem + Lay::off_b + r * kRegion, 32 * r, (int)grp, (int)tau, (int)b);
+            }
+            bulk_commit();
         }
         // dL_i (the column part and the end-state part come from the other rows)
         sdl[i] = valid ? rowq - colq * dti + ei * yst - rj : 0.f;
@@ -406,24 +435,43 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             red[2][warp] = v2;
         }
         compute_sync();
-        if (ok && i == 0) {
+        // suffix sums of dL, da_i = sum_{k >= i} dL_k, as a scan over the 128
+        // rows (shuffles within a warp, then the later warps' totals); the
+        // last valid row also takes the end-state terms
+        float da = valid ? sdl[i] : 0.f;
+        if (i == n - 1) {
             const float rsum = red[0][0] + red[0][1] + red[0][2] + red[0][3];
             const float dsh = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-            const float dd = red[2][0] + red[2][1] + red[2][2] + red[2][3];
-            sdl[n - 1] += rsum + exp2f(glast) * dsh;
-            // suffix sums of dL: da_k; dA gets sum dt_k da_k (stored in sdl as da)
-            float da = 0.f, dasum = 0.f;
-            for (int k = n - 1; k >= 0; --k) {
-                da += sdl[k];
-                sdl[k] = da;
-                dasum = fmaf(sdt[k], da, dasum);
-            }
-            atomicAdd(prm.dA + h, dasum);
+            da += rsum + exp2f(glast) * dsh;
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_down_sync(0xffffffffu, da, o);
+            if (lane + o < 32)
+                da += u;
+        }
+        const float dd = red[2][0] + red[2][1] + red[2][2] + red[2][3];
+        compute_sync();  // every thread has read red[][]
+        if (lane == 0)
+            red[3][warp] = da;  // warp total (lane 0 holds the whole warp's suffix)
+        compute_sync();
+        for (int w2 = warp + 1; w2 < 4; ++w2)
+            da += red[3][w2];
+        // dA gets sum dt_k da_k
+        float dasum = valid ? sdt[i] * da : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            dasum += __shfl_xor_sync(0xffffffffu, dasum, o);
+        compute_sync();  // every thread has read red[3][]
+        if (lane == 0)
+            red[0][warp] = dasum;
+        compute_sync();
+        if (ok && i == 0) {
+            atomicAdd(prm.dA + h, red[0][0] + red[0][1] + red[0][2] + red[0][3]);
             atomicAdd(prm.dD + h, dd);
         }
-        compute_sync();
         if (ok && valid)
-            prm.ddt[(b * g.L + tau + i) * g.H + h] = ddt_direct + prm.A[h] * sdl[i];
+            prm.ddt[(b * g.L + tau + i) * g.H + h] = ddt_direct + prm.A[h] * da;
         // dx rows out by TMA (rows past the sequence end are not written)
         if (ok && i == 0) {
             prefetch_tmap(&tm_dx);
@@ -444,7 +492,8 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 
 template <int S>
 cudaError_t launch_bt(const CUtensorMap &tx, const CUtensorMap &tdy, const CUtensorMap &tb,
-                      const CUtensorMap &tc_, const CUtensorMap &tdx, const BtParams &p, cudaStream_t st)
+                      const CUtensorMap &tc_, const CUtensorMap &tdx, const CUtensorMap &tdb,
+                      const CUtensorMap &tdc, const BtParams &p, cudaStream_t st)
 {
     const size_t smem = BtLayout<S>::bytes + 1024;
     auto k = bwd_chunk_tc_kernel<S>;
@@ -452,7 +501,7 @@ cudaError_t launch_bt(const CUtensorMap &tx, const CUtensorMap &tdy, const CUten
     if (e != cudaSuccess)
         return e;
     const dim3 grid((unsigned)p.g.nc, (unsigned)(p.g.B * p.g.H));
-    k<<<grid, kThreads, smem, st>>>(tx, tdy, tb, tc_, tdx, p);
+    k<<<grid, kThreads, smem, st>>>(tx, tdy, tb, tc_, tdx, tdb, tdc, p);
     note_launch();
     return cudaGetLastError();
 }
@@ -476,15 +525,16 @@ cudaError_t launch_bwd_chunk_tc(const void *x, const void *Bm, const void *Cm, c
     unsigned int *status = device_status_word();
     if (!status)
         return cudaErrorUnknown;
-    CUtensorMap tx, tdy, tb, tc_, tdx;
+    CUtensorMap tx, tdy, tb, tc_, tdx, tdb, tdc;
     if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_heads(&tdy, dy, g) ||
         !make_tmap_tokens_groups(&tb, Bm, g) || !make_tmap_tokens_groups(&tc_, Cm, g) ||
-        !make_tmap_tokens_heads(&tdx, dx, g))
+        !make_tmap_tokens_heads(&tdx, dx, g) || !make_tmap_f32_tokens_groups(&tdb, dBacc, g) ||
+        !make_tmap_f32_tokens_groups(&tdc, dCacc, g))
         return cudaErrorInvalidValue;
     BtParams p{Gc, dtT, A, D, states, dstates, ddt, dA, dD, dBacc, dCacc, g, status};
     if (g.S == 64)
-        return launch_bt<64>(tx, tdy, tb, tc_, tdx, p, st);
-    return launch_bt<128>(tx, tdy, tb, tc_, tdx, p, st);
+        return launch_bt<64>(tx, tdy, tb, tc_, tdx, tdb, tdc, p, st);
+    return launch_bt<128>(tx, tdy, tb, tc_, tdx, tdb, tdc, p, st);
 }
 
 }  // namespace ssd

@@ -45,6 +45,7 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t
 bool make_tmap_f32_rows(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
                         uint32_t box_cols, uint32_t box_rows);
 bool make_tmap_tokens_heads(CUtensorMap *map, const void *base, const Geom &g);
+bool make_tmap_f32_tokens_groups(CUtensorMap *map, const void *base, const Geom &g);
 bool make_tmap_tokens_groups(CUtensorMap *map, const void *base, const Geom &g);
 
 // Tensor-core (tcgen05) state pass; bf16 inputs.  Returns cudaErrorNotSupported

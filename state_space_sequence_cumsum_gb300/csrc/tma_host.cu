@@ -84,4 +84,16 @@ bool make_tmap_tokens_groups(CUtensorMap *map, const void *base, const Geom &g)
     return make_tmap_bf16(map, base, 4, dims, st, box);
 }
 
+// f32 [B, L, G, S] (the dB / dC accumulators) viewed as 4-D {S, G, L, B};
+// box {32, 1, 128, 1}: 128 token rows of 32 f32 (128 bytes), 128-byte swizzle.
+bool make_tmap_f32_tokens_groups(CUtensorMap *map, const void *base, const Geom &g)
+{
+    const uint64_t dims[4] = {(uint64_t)g.S, (uint64_t)g.G, (uint64_t)g.L, (uint64_t)g.B};
+    const uint64_t st[3] = {(uint64_t)g.S * 4, (uint64_t)(g.G * g.S) * 4,
+                            (uint64_t)(g.L * g.G * g.S) * 4};
+    const uint32_t box[4] = {32, 1, 128, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, 4, dims, st, box,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 }  // namespace ssd
