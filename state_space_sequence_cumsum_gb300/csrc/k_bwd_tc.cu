@@ -32,6 +32,8 @@
 // TMA store.  Roles: warps 0-3 compute (thread i = row / TMEM lane i), one
 // thread of warp 4 issues TMA and MMA.  Every wait is bounded; a timeout sets
 // the status word and the CTA leaves after freeing TMEM.
+#include <type_traits>
+
 #include "common.cuh"
 #include "ssd_internal.h"
 #include "tc05.cuh"
@@ -266,6 +268,21 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         const float glast = sg[n - 1];
         const float gi = sg[i], dti = sdt[i];
         const float eT = valid ? exp2f(glast - gi) : 0.f, ei = valid ? exp2f(gi) : 0.f;
+        // Score weights exp2(g_i - g_j) = r_i c_j with a reference g_m in the
+        // middle of the chunk's range, while that range stays within 200
+        // (both factors within 2^100): c_j and c_j dt_j go to shared memory
+        // (over dl and dt: this row's dt is already in a register), and the
+        // Q loop needs no exponent.  Wider ranges take exp2 per element.
+        const float g0 = sg[0];
+        const bool fact = fabsf(g0 - glast) <= 200.f;  // the same for the whole CTA
+        const float gm = 0.5f * (g0 + glast);
+        const float ri = (fact && valid) ? exp2f(gi - gm) : 0.f;
+        if (fact) {
+            const float cj = valid ? exp2f(gm - gi) : 0.f;
+            sdl[i] = cj;
+            sdt[i] = cj * dti;
+        }
+        compute_sync();  // the column factors are visible
 
         // ok is made warp-uniform: the TMEM loads below are warp-collective
         bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_in, 0) && mbar_wait(&bar_a, 0));
@@ -308,30 +325,53 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
             }
             // Q1 = W * CB and Q2 = W * dyx * dt_j, row i, 16 keys at a time
-#pragma unroll 1
-            for (int j0 = 0; j0 < kT; j0 += 16) {
+            // one loop per weight form (the CTA-uniform branch stays out of
+            // the unrolled body)
+            auto q_block = [&](auto fact_c, int j0, uint32_t (&q1)[8], uint32_t (&q2)[8]) {
+                constexpr bool kFact = decltype(fact_c)::value;
                 uint32_t cb[16], dx[16];
                 tmem_ld16(tl + Lay::t_cb + j0, cb);
                 tmem_ld16(tl + Lay::t_dyx + j0, dx);
                 tmem_ld_wait();
-                uint32_t q1[8], q2[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     float a[2], bq[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int j = j0 + 2 * e + u;
-                        const float w = (valid && j <= i) ? exp2f(gi - sg[j]) : 0.f;
                         const float cbv = __uint_as_float(cb[2 * e + u]);
                         const float dyxv = __uint_as_float(dx[2 * e + u]);
-                        a[u] = w * cbv;
-                        bq[u] = w * dyxv * sdt[j];
-                        rowq = fmaf(a[u], dyxv * sdt[j], rowq);
+                        if (kFact) {
+                            const float m = (valid && j <= i) ? ri : 0.f;
+                            a[u] = m * sdl[j] * cbv;
+                            bq[u] = m * sdt[j] * dyxv;  // w dt_j dyx
+                            rowq = fmaf(cbv, bq[u], rowq);
+                        } else {
+                            const float w = (valid && j <= i) ? exp2f(gi - sg[j]) : 0.f;
+                            a[u] = w * cbv;
+                            bq[u] = w * dyxv * sdt[j];
+                            rowq = fmaf(a[u], dyxv * sdt[j], rowq);
+                        }
                         if (j == i)
                             dyx_ii = dyxv;
                     }
                     q1[e] = pack_bf16x2(a[0], a[1]);
                     q2[e] = pack_bf16x2(bq[0], bq[1]);
+                }
+            };
+#pragma unroll 1
+            for (int j0 = 0; j0 < kT; j0 += 16) {
+                // keys past every row of this warp: zero weights, nothing to load
+                const bool none = j0 > warp * 32 + 31;  // warp-uniform
+                uint32_t q1[8], q2[8];
+                if (none) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        q1[e] = q2[e] = 0u;
+                } else if (fact) {
+                    q_block(std::true_type{}, j0, q1, q2);
+                } else {
+                    q_block(std::false_type{}, j0, q1, q2);
                 }
                 const int reg = j0 / 64, ch0 = (j0 % 64) / 8;
 #pragma unroll
@@ -458,7 +498,7 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         for (int w2 = warp + 1; w2 < 4; ++w2)
             da += red[3][w2];
         // dA gets sum dt_k da_k
-        float dasum = valid ? sdt[i] * da : 0.f;
+        float dasum = valid ? dti * da : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             dasum += __shfl_xor_sync(0xffffffffu, dasum, o);
