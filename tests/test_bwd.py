@@ -110,6 +110,37 @@ def test_bwd_tensor_core_path(B, L, H, P, S, G):
     check_tc(out, ref)
 
 
+def test_bwd_tensor_core_fast_decay_chunks():
+    """Heads whose decay over a 128-token chunk exceeds 200 (log2 units): the
+    tensor-core chunk kernel forms exp2(g_i - g_j) per element there, and
+    with the factorized weights r_i c_j elsewhere; dt of alternate heads is
+    scaled by 40, so one call has chunks of both kinds (log2 ranges of the
+    first chunk: 133 and 364 on the scaled heads).  Larger dt stresses the
+    bf16 operand rounding itself: at 100x the bound is exceeded (dB 4.95e-2,
+    dA 0.196 beyond 2^-5 |ref|) identically by the kernel before the
+    factorized weights existed."""
+    B, L, H, P, S, G = 1, 400, 4, 64, 128, 1
+    inp = make_inputs(Shape(B, L, H, P, S, G, 64), dtype=torch.bfloat16, init="randn", seed=21,
+                      init_std=0.5)
+    dt = inp["dt"].clone()
+    dt[:, :, 0::2] *= 40.0
+    inp["dt"] = dt
+    ranges = (-inp["A"][None, None, :].double() * dt.double()).reshape(B, -1, H)
+    per_chunk = ranges[:, :128].sum(1)[0] * np.log2(np.e)
+    assert per_chunk.max() > 200 and per_chunk.min() < 200
+    rng = np.random.default_rng(28)
+    dy = torch.from_numpy(rng.standard_normal((B, L, H, P)).astype(np.float32)).to(torch.bfloat16)
+    df = torch.from_numpy(rng.standard_normal((B, H, P, S)).astype(np.float32))
+    g = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    out = ssd.ssd_bwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], dy.cuda(),
+                      initial_state=g["init"], dfinal=df.cuda())
+    torch.cuda.synchronize()
+    assert ssd.ssd_stream_status() == 0
+    ref = oracle.bwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], dy,
+                     init=inp["init"], dfinal=df)
+    check_tc(out, ref)
+
+
 def test_bwd_without_initial_state_or_final_gradient():
     out, ref = run_case(2, 150, 4, 32, 64, 1, torch.float32, init=False, dfinal=False, seed=4)
     check(out, ref, torch.float32)
