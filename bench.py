@@ -293,6 +293,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest of every rank's x: the job's step time is its slowest
+    replica's.  One rank: x itself (no process group needed)."""
+    if ws <= 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ws: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job units per second: every replica processes units_per_rank
+    units in the (max-over-ranks) time ms."""
+    return ws * units_per_rank / (ms / 1e3)
+
+
 def run_ours(args):
     import state_space_sequence_cumsum_gb300 as ssd
     from state_space_sequence_cumsum_gb300 import _lib
@@ -352,12 +368,9 @@ def run_ours(args):
                   for i in range(nk)]
     step_ms = [sum(per_kernel[i][k] for i in range(nk)) for k in range(args.steps)]
     ms = statistics.mean(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, ws, dev)
     tokens = shape.tokens
-    value = ws * tokens / (ms / 1e3)
+    value = job_throughput(ws, tokens, ms)
 
     # dominant kernel and its roofline
     means = [statistics.mean(v) for v in per_kernel]
@@ -423,10 +436,7 @@ def run_ours(args):
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
     e_ms_mean = statistics.mean(e_ms)
-    if ws > 1:
-        t = torch.tensor([e_ms_mean], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms_mean = float(t.item())
+    e_ms_mean = max_over_ranks(e_ms_mean, ws, dev)
     st = ssd.ssd_stream_status()
     if st != 0:
         raise RuntimeError(f"kernel status {st} in the timed region")
@@ -445,7 +455,7 @@ def run_ours(args):
         "roofline": roofline, "step_roofline": step_roof,
         "per_kernel_ms": {n: round(m, 5) for n, m in zip(plan["kernels"], means)},
         "wall_s_timed_loop": round(t_wall, 4),
-        "e2e": {"value": round(ws * tokens / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(ws, tokens, e_ms_mean), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e_ms_mean, 4), "api": e2e_api},
         "gpu_launches": int(launches),
@@ -527,10 +537,7 @@ def run_decode(args):
         torch.distributed.barrier()
     launches = lib.ssd_launch_count() - launches0
     ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, ws, dev)
     peaks, peak_src = load_peaks()
     kb = decode_bytes(b, H, P, S, G, dtype)
     achieved = kb / (ms / 1e3) / 1e9
@@ -565,11 +572,11 @@ def run_decode(args):
         c.record(stream)
         c.synchronize()
         e_ms.append(a.elapsed_time(c))
-    e_ms_mean = statistics.mean(e_ms)
+    e_ms_mean = max_over_ranks(statistics.mean(e_ms), ws, dev)
     if ssd.ssd_stream_status() != 0:
         raise RuntimeError("kernel status in the timed region")
     line = {
-        "metric": DECODE_METRIC, "value": round(ws * b / (ms / 1e3), 1), "unit": "tokens/s",
+        "metric": DECODE_METRIC, "value": round(job_throughput(ws, b, ms), 1), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
@@ -579,7 +586,7 @@ def run_decode(args):
                    "parallelism": f"replicas{ws}",
                    "l2": "flushed before every timed step (512 MB write, outside the events)"},
         "roofline": roofline,
-        "e2e": {"value": round(ws * b / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(ws, b, e_ms_mean), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e_ms_mean, 4)},
         "gpu_launches": int(launches),
@@ -660,10 +667,7 @@ def run_norm(args):
         clk.mark_end()
     launches = lib.ssd_launch_count() - launches0
     ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, ws, dev)
     peaks, peak_src = load_peaks()
     kb = 3 * ntok * dim * elem_bytes(dtype) + dim * 4
     achieved = kb / (ms / 1e3) / 1e9
@@ -686,9 +690,9 @@ def run_norm(args):
         c.synchronize()
         if k:
             e_ms.append(a.elapsed_time(c))
-    e_ms_mean = statistics.mean(e_ms)
+    e_ms_mean = max_over_ranks(statistics.mean(e_ms), ws, dev)
     line = {
-        "metric": NORM_METRIC, "value": round(ws * ntok / (ms / 1e3), 1), "unit": "tokens/s",
+        "metric": NORM_METRIC, "value": round(job_throughput(ws, ntok, ms), 1), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
@@ -696,7 +700,7 @@ def run_norm(args):
                    "parallelism": f"replicas{ws}",
                    "l2": "flushed before every timed step (512 MB write, outside the events)"},
         "roofline": roofline,
-        "e2e": {"value": round(ws * ntok / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(ws, ntok, e_ms_mean), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * ntok * dim * elem_bytes(dtype),
                 "d2h_bytes_per_step": ntok * dim * elem_bytes(dtype), "ms_per_step": round(e_ms_mean, 4)},
         "gpu_launches": int(launches),
@@ -802,10 +806,7 @@ def run_bwd(args):
         clk.mark_end()
     launches = lib.ssd_launch_count() - launches0
     ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, ws, dev)
     peaks, peak_src = load_peaks()
     cb = bwd_compulsory_bytes(shape, dtype, init)
     fl = bwd_flops(shape)
@@ -853,12 +854,12 @@ def run_bwd(args):
         c.record(stream)
         c.synchronize()
         e_ms.append(a.elapsed_time(c))
-    e_ms_mean = statistics.mean(e_ms)
+    e_ms_mean = max_over_ranks(statistics.mean(e_ms), ws, dev)
     if ssd.ssd_stream_status() != 0:
         raise RuntimeError("kernel status in the timed region")
     tokens = shape.tokens
     line = {
-        "metric": BWD_METRIC, "value": round(ws * tokens / (ms / 1e3), 1), "unit": "tokens/s",
+        "metric": BWD_METRIC, "value": round(job_throughput(ws, tokens, ms), 1), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if dtype == torch.bfloat16 else "f32",
@@ -869,7 +870,7 @@ def run_bwd(args):
                    "parallelism": f"replicas{ws}",
                    "l2": "flushed before every timed step (512 MB write, outside the events)"},
         "roofline": roofline,
-        "e2e": {"value": round(ws * tokens / (e_ms_mean / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(ws, tokens, e_ms_mean), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e_ms_mean, 4)},
         "gpu_launches": int(launches),
