@@ -28,7 +28,8 @@
 // warps), so each contraction is one tcgen05.mma chain with f32 accumulators
 // in TMEM: dyx cols [0,128), CB [128,256), Chin [256,320), BdS [384,448); in
 // phase B dX1 [0,64), dB [128,128+S), dC [256,256+S).  dB and dC are summed
-// over the heads of a group with vector f32 atomics; dx goes out through a
+// over the heads of a group in f32 by TMA bulk reductions (the rows staged in
+// shared memory as swizzled [128 x 32] f32 boxes); dx goes out through a
 // TMA store.  Roles: warps 0-3 compute (thread i = row / TMEM lane i), one
 // thread of warp 4 issues TMA and MMA.  Every wait is bounded; a timeout sets
 // the status word and the CTA leaves after freeing TMEM.
