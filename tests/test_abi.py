@@ -157,3 +157,32 @@ def test_gated_rmsnorm_validation(lib):
         _lib.SSD_ERR_ALIGNMENT
     assert f(FAKE, FAKE, FAKE, FAKE, 4, 96, 32, 1e-5, 9, None) == _lib.SSD_ERR_INVALID_ARG
     assert lib.ssd_launch_count() == before
+
+
+def test_fwd_host_validation(lib):
+    """ssd_fwd_host checks its arguments and workspace on the host before any
+    copy or launch (a rejected call launches nothing)."""
+    before = lib.ssd_launch_count()
+    d = _lib.dims(2, 3000, 4, 64, 128, 2)
+    need = lib.ssd_fwd_host_workspace_size(d, 0, 128)
+    assert need > 0 and need % 256 == 0
+    # the parts and the slots grow with the sequence
+    assert lib.ssd_fwd_host_workspace_size(_lib.dims(2, 30000, 4, 64, 128, 2), 0, 128) > need
+    # invalid dims / dtype / chunk size: no size
+    assert lib.ssd_fwd_host_workspace_size(_lib.dims(0, 3000, 4, 64, 128, 2), 0, 128) == 0
+    assert lib.ssd_fwd_host_workspace_size(d, 7, 128) == 0
+    assert lib.ssd_fwd_host_workspace_size(d, 0, 512) == 0
+    host = [FAKE] * 6  # x, dt, A, B, C, D
+    ok_tail = [None, FAKE, None, d, 0, 128]
+    # a required input missing
+    for k in range(6):
+        args = list(host)
+        args[k] = None
+        assert lib.ssd_fwd_host(*args, *ok_tail, FAKE, need, None) == _lib.SSD_ERR_INVALID_ARG
+    # no y for a non-empty sequence
+    assert lib.ssd_fwd_host(*host, None, None, None, d, 0, 128, FAKE, need, None) == _lib.SSD_ERR_INVALID_ARG
+    # workspace missing, short or not 256-byte aligned
+    assert lib.ssd_fwd_host(*host, *ok_tail, None, need, None) == _lib.SSD_ERR_WORKSPACE
+    assert lib.ssd_fwd_host(*host, *ok_tail, FAKE, need - 256, None) == _lib.SSD_ERR_WORKSPACE
+    assert lib.ssd_fwd_host(*host, *ok_tail, ctypes.c_void_p(0x10010), need, None) == _lib.SSD_ERR_WORKSPACE
+    assert lib.ssd_launch_count() == before
