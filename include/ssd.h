@@ -284,8 +284,9 @@ ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const float *A, con
  * part k-1 computes on `stream` and part k-2's y is copied down on a second
  * internal stream, so both copy directions overlap the kernels.  The call is
  * asynchronous and stream-ordered: it starts after the work already on
- * `stream`, and `stream` waits for all of it (synchronize `stream` before
- * reading y).  The internal streams and events of each device are created
+ * `stream`, and `stream` waits for all of it -- also when an error is
+ * returned after some copies started -- so the host buffers must stay
+ * untouched until `stream` has completed (synchronize it before reading y).  The internal streams and events of each device are created
  * on first use and kept; calls are serialized by a mutex while they issue
  * work (not while it runs).  Errors: as ssd_fwd, plus SSD_ERR_WORKSPACE for
  * a short or unaligned workspace and SSD_ERR_CUDA for a failed copy.

@@ -201,10 +201,21 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
     cudaError_t e = pipe_for_device(&pp);
     if (e != cudaSuccess)
         return SSD_ERR_CUDA;
+    // On a failure after work was issued, `stream` still waits for the copy
+    // streams before the error is returned, so the caller's stream order
+    // covers every copy that did start.
+    auto join = [&]() {
+        if (cudaEventRecord(pp->done, pp->up) == cudaSuccess)
+            cudaStreamWaitEvent(st, pp->done, 0);
+        if (cudaEventRecord(pp->done, pp->down) == cudaSuccess)
+            cudaStreamWaitEvent(st, pp->done, 0);
+    };
 #define HOST_TRY(expr)                  \
     do {                                \
-        if ((expr) != cudaSuccess)      \
+        if ((expr) != cudaSuccess) {    \
+            join();                     \
             return SSD_ERR_CUDA;        \
+        }                               \
     } while (0)
     // everything already on `stream` comes first
     HOST_TRY(cudaEventRecord(pp->entry, st));
@@ -248,8 +259,10 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
             ssd_fwd(slot + pl.off_x, reinterpret_cast<const float *>(slot + pl.off_dt), A_d,
                     slot + pl.off_b, slot + pl.off_c, D_d, init_k, slot + pl.off_y, st_d[k & 1],
                     nullptr, dp, dtype, pl.T, ws + pl.off_fws, pl.fws_bytes, st);
-        if (sk != SSD_OK)
+        if (sk != SSD_OK) {
+            join();
             return sk;
+        }
         HOST_TRY(cudaEventRecord(pp->comp[s], st));
         HOST_TRY(cudaStreamWaitEvent(pp->down, pp->comp[s], 0));
         HOST_TRY(copy_rows(yh + l0 * rx, L * rx, slot + pl.off_y, lk * rx, lk * rx, B,
@@ -268,10 +281,11 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
                                  cudaMemcpyDeviceToHost, pp->down));
     }
     // the caller's stream waits for both copy streams
-    HOST_TRY(cudaEventRecord(pp->done, pp->up));
-    HOST_TRY(cudaStreamWaitEvent(st, pp->done, 0));
-    HOST_TRY(cudaEventRecord(pp->done, pp->down));
-    HOST_TRY(cudaStreamWaitEvent(st, pp->done, 0));
+    if (cudaEventRecord(pp->done, pp->up) != cudaSuccess ||
+        cudaStreamWaitEvent(st, pp->done, 0) != cudaSuccess ||
+        cudaEventRecord(pp->done, pp->down) != cudaSuccess ||
+        cudaStreamWaitEvent(st, pp->done, 0) != cudaSuccess)
+        return SSD_ERR_CUDA;
 #undef HOST_TRY
     return SSD_OK;
 }
