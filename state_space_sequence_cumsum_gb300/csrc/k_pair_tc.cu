@@ -967,7 +967,7 @@ struct PairSegPlan {
     size_t state_bytes, count_bytes, gd_bytes;  // gd: G and dt^T for the prefill
 };
 
-PairSegPlan pair_seg_plan(const Geom &g)
+PairSegPlan pair_seg_plan(const Geom &g, bool allow_prefill = true)
 {
     PairSegPlan sp;
     const int64_t n_tiles = (g.L + kTile - 1) / kTile;
@@ -990,7 +990,7 @@ PairSegPlan pair_seg_plan(const Geom &g)
         want1 = kMaxPrefillSeg;
     if (want1 * 2 * tpc > n_tiles)
         want1 = n_tiles / (2 * tpc);
-    if (want1 >= 2 && state_pass_tc_supported(g) && !(env && strcmp(env, "0") == 0)) {
+    if (allow_prefill && want1 >= 2 && state_pass_tc_supported(g) && !(env && strcmp(env, "0") == 0)) {
         int64_t st = (n_tiles + want1 - 1) / want1;
         st = (st + tpc - 1) / tpc * tpc;
         sp.seg_tiles = (int)st;
@@ -1053,9 +1053,9 @@ bool pair_tc_supported(const Geom &g)
            g.G <= 65535 && g.B <= 65535 && g.B * g.H * n_tiles < (1LL << 31);
 }
 
-size_t pair_tc_scratch_bytes(const Geom &g)
+size_t pair_tc_scratch_bytes(const Geom &g, bool allow_prefill)
 {
-    const PairSegPlan sp = pair_seg_plan(g);
+    const PairSegPlan sp = pair_seg_plan(g, allow_prefill);
     if (!sp.wrap && sp.n_seg <= 1)
         return 0;
     return (sp.state_bytes + 255) / 256 * 256 + (sp.count_bytes + 255) / 256 * 256 +
@@ -1083,7 +1083,10 @@ cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, 
     prm.H = (int)g.H;
     prm.npairs = (int)(g.H / 2);
     prm.hpg = g.hpg;
-    const PairSegPlan sp = pair_seg_plan(g);
+    // the prefilled plan when the scratch holds it, else the hand-off plan
+    PairSegPlan sp = pair_seg_plan(g);
+    if (sp.prefill && scratch_bytes < pair_tc_scratch_bytes(g, true))
+        sp = pair_seg_plan(g, false);
     prm.seg_tiles = sp.seg_tiles;
     prm.n_seg = sp.n_seg;
     prm.wrap = sp.wrap ? 1 : 0;

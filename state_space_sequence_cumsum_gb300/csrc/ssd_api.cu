@@ -169,7 +169,8 @@ struct Workspace {
     float *Gc, *dtT, *states;
     char *fused_scratch;
     size_t fused_scratch_bytes;
-    size_t bytes;
+    size_t bytes;      // what ssd_fwd_workspace_size reports
+    size_t min_bytes;  // the least the call runs with (head pairs: the hand-off plan)
 };
 
 // ssd_fwd's workspace: G_cum and dt_t, then either the chunk states the
@@ -185,6 +186,7 @@ Workspace layout(const Geom &g, ssd_path_t path, bool caller_states, char *base)
         w.fused_scratch_bytes = pair_tc_scratch_bytes(g);
         w.fused_scratch = base;
         w.bytes = round_up(w.fused_scratch_bytes, 256);
+        w.min_bytes = round_up(pair_tc_scratch_bytes(g, false), 256);
         if (!base)
             w.fused_scratch = nullptr;
         return w;
@@ -203,6 +205,7 @@ Workspace layout(const Geom &g, ssd_path_t path, bool caller_states, char *base)
         off = round_up(off + (size_t)(g.B * g.H * g.nc * g.P * g.S) * sizeof(float), 256);
     }
     w.bytes = off;
+    w.min_bytes = off;
     if (!base) {
         w.Gc = w.dtT = w.states = nullptr;
         w.fused_scratch = nullptr;
@@ -235,6 +238,25 @@ BwdWs bwd_layout(const Geom &g, char *base)
     return w;
 }
 }  // namespace
+
+// The least workspace ssd_fwd runs with for these arguments (0: invalid).
+size_t fwd_workspace_min_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
+                              int want_chunk_states)
+{
+    Geom g;
+    if (make_geom(dims, chunk_size, true, &g) != SSD_OK)
+        return 0;
+    if (dtype != SSD_BF16 && dtype != SSD_F32)
+        return 0;
+    if (g.T == 0) {
+        g.T = choose_chunk_size(g, dtype);
+        g.nc = (g.L + g.T - 1) / g.T;
+    }
+    const size_t b = layout(g, choose_path(g, dtype, want_chunk_states != 0),
+                            want_chunk_states != 0, nullptr).min_bytes;
+    return b ? b : 256;
+}
+
 }  // namespace ssd
 
 using namespace ssd;
@@ -438,14 +460,15 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
     const ssd_path_t path = choose_path(g, dtype, chunk_states != nullptr);
     const bool fused = path == SSD_PATH_FUSED_TENSOR_CORES;
     const Workspace need_ws = layout(g, path, chunk_states != nullptr, nullptr);
-    if (need_ws.bytes && (!workspace || workspace_bytes < need_ws.bytes ||
-                          (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    if (need_ws.min_bytes && (!workspace || workspace_bytes < need_ws.min_bytes ||
+                              (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return SSD_ERR_WORKSPACE;
     const Workspace w = layout(g, path, chunk_states != nullptr, static_cast<char *>(workspace));
+    // the head-pair kernel takes the plan the whole workspace holds
     if (path == SSD_PATH_FUSED_PAIR_TENSOR_CORES)
         return cuda_status(launch_fused_pair_tc(x, Bm, Cm, dt, A, D, init_state, chunk_states,
                                                 final_state, y, g, w.fused_scratch,
-                                                w.fused_scratch_bytes, st));
+                                                workspace ? workspace_bytes : 0, st));
     float *states = chunk_states ? chunk_states : w.states;
     const bool bf16 = dtype == SSD_BF16;
 

@@ -126,7 +126,15 @@ cudaError_t launch_fused_tc(const void *x, const void *Bm, const void *Cm, const
 // SSD_FUSED_KERNEL=single asks for the cumsum + one-head fused pair.
 bool pair_tc_supported(const Geom &g);
 bool fused_pair_enabled(const Geom &g);
-size_t pair_tc_scratch_bytes(const Geom &g);
+// The least workspace ssd_fwd runs with for these arguments (its own
+// ssd_fwd_workspace_size reports the preferred size; the head-pair kernel
+// also runs with the smaller hand-off plan's).  0: invalid arguments.
+size_t fwd_workspace_min_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
+                              int want_chunk_states);
+// Scratch of the head-pair kernel: with allow_prefill, that of the plan it
+// prefers (the prefilled segments where they apply, which also hold G and
+// dt^T); without, that of the hand-off plan, the least it runs with.
+size_t pair_tc_scratch_bytes(const Geom &g, bool allow_prefill = true);
 cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dt,
                                  const float *A, const float *D, const float *init, float *states,
                                  float *final_state, void *y, const Geom &g, void *scratch,

@@ -56,8 +56,10 @@ extern "C" ssd_status_t ssd_fwd_noalloc(const void *x, const float *dt, const fl
                                         float *chunk_states, ssd_dims_t dims, ssd_dtype_t dtype,
                                         int chunk_size, void *stream)
 {
+    // the least the call runs with: the head-pair kernel falls back to its
+    // hand-off plan when the scratch cannot hold the prefilled one
     const size_t need =
-        ssd_fwd_workspace_size(dims, dtype, chunk_size, chunk_states != nullptr ? 1 : 0);
+        ssd::fwd_workspace_min_size(dims, dtype, chunk_size, chunk_states != nullptr ? 1 : 0);
     if (need == 0)
         return SSD_ERR_INVALID_ARG;
     if (need > ssd::kNoAllocScratchBytes)

@@ -248,3 +248,46 @@ def test_pair_kernel_fast_decay_with_noise():
     ref = oracle_run(inp, 128)
     assert_parity(y, ref["y"], torch.bfloat16, "y")
     assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
+
+
+def test_pair_kernel_runs_with_the_hand_off_workspace():
+    """ssd_fwd_workspace_size reports the prefilled plan's workspace (it also
+    holds G and dt^T); the head-pair path accepts less -- down to the
+    hand-off plan's -- and then runs that plan.  Found by bisection on the
+    host-side check (a short workspace returns SSD_ERR_WORKSPACE before any
+    launch), then run at exactly that size against the oracle."""
+    import ctypes
+    from state_space_sequence_cumsum_gb300 import _lib
+    B, L, H, P, S, G, T = 1, 4095, 4, 64, 128, 1, 128
+    inp = case_inputs(B, L, H, P, S, G, T, init="randn", seed=77)
+    g = to_gpu(inp)
+    lib = _lib.load()
+    d = _lib.dims(B, L, H, P, S, G)
+    pref = int(lib.ssd_fwd_workspace_size(d, 0, T, 0))
+    big = torch.empty(pref, dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(g["x"])
+    fin = torch.empty((B, H, P, S), device="cuda")
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call(nbytes):
+        return lib.ssd_fwd(ptr(g["x"]), ptr(g["dt"]), ptr(g["A"]), ptr(g["B"]), ptr(g["C"]),
+                           ptr(g["D"]), ptr(g["init"]), ptr(y), ptr(fin), None, d, 0, T,
+                           ptr(big), ctypes.c_size_t(nbytes), stream)
+    lo, hi = 0, pref // 256  # in 256-byte units: lo fails, hi works
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        st = call(mid * 256) if mid else _lib.SSD_ERR_WORKSPACE
+        if st == _lib.SSD_OK:
+            hi = mid
+        else:
+            assert st == _lib.SSD_ERR_WORKSPACE
+            lo = mid
+    least = hi * 256
+    assert least < pref  # the hand-off plan needs no G / dt^T copy
+    assert call(least) == _lib.SSD_OK
+    torch.cuda.synchronize()
+    assert ssd.ssd_stream_status() == 0
+    ref = oracle_run(inp, T)
+    assert_parity(y, ref["y"], torch.bfloat16, "y")
+    assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
