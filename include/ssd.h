@@ -165,9 +165,9 @@ size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size
  * chunk_states != NULL) bytes, 256-byte aligned; its contents on entry do
  * not matter.  On the head-pair path (SSD_PATH_FUSED_PAIR_TENSOR_CORES) with
  * few head pairs, that size covers the prefilled-segment plan, which also
- * holds G and dt_t; a smaller workspace that still holds the plan whose
- * segments hand their states to one another is accepted, and that plan
- * runs (SSD_ERR_WORKSPACE below it).
+ * holds G and dt_t; a workspace too small for it that still holds the plan
+ * whose segments hand their states to one another is accepted, and that
+ * plan runs (SSD_ERR_WORKSPACE below both).
  */
 ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void *Bm,
                      const void *Cm, const float *D, const float *init_state, void *y,

@@ -1084,6 +1084,7 @@ cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, 
     prm.npairs = (int)(g.H / 2);
     prm.hpg = g.hpg;
     // the prefilled plan when the scratch holds it, else the hand-off plan
+    // (the caller checked that one of the two fits)
     PairSegPlan sp = pair_seg_plan(g);
     if (sp.prefill && scratch_bytes < pair_tc_scratch_bytes(g, true))
         sp = pair_seg_plan(g, false);

@@ -1,6 +1,7 @@
 // C ABI of the SSD forward library: argument validation, workspace layout,
 // stage orchestration and the kernel status word.  See include/ssd.h for the
 // contract of every entry point.
+#include <algorithm>
 #include <atomic>
 #include <initializer_list>
 #include <cstdlib>
@@ -186,7 +187,9 @@ Workspace layout(const Geom &g, ssd_path_t path, bool caller_states, char *base)
         w.fused_scratch_bytes = pair_tc_scratch_bytes(g);
         w.fused_scratch = base;
         w.bytes = round_up(w.fused_scratch_bytes, 256);
-        w.min_bytes = round_up(pair_tc_scratch_bytes(g, false), 256);
+        // the hand-off plan's scratch may be the smaller one or not (it has
+        // more segments, but no G / dt^T)
+        w.min_bytes = std::min(w.bytes, round_up(pair_tc_scratch_bytes(g, false), 256));
         if (!base)
             w.fused_scratch = nullptr;
         return w;
