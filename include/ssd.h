@@ -254,10 +254,12 @@ ssd_status_t ssd_decode_step(const void *x, const float *dt, const float *A, con
  * The workspace is a fixed scratch array inside the library: 160 MiB
  * (167772160 bytes) per device, reserved on a device when the library's code
  * for this entry point is first loaded there and kept until the process
- * exits.  A call whose ssd_fwd_workspace_size(...) exceeds it returns
- * SSD_ERR_UNSUPPORTED before launching anything (roughly: the fused path
- * needs 8 bytes per batch x head x token; the staged paths also hold the
- * chunk states when chunk_states is NULL).  Inputs, outputs and their
+ * exits.  A call whose least workspace exceeds it returns
+ * SSD_ERR_UNSUPPORTED before launching anything: ssd_fwd_workspace_size(...),
+ * or on the head-pair path the smaller of its two plans' scratch (see
+ * ssd_fwd).  Roughly: the one-head fused path needs 8 bytes per batch x
+ * head x token; the staged paths also hold the chunk states when
+ * chunk_states is NULL.  Inputs, outputs and their
  * conventions are exactly those of ssd_fwd, and nothing is allocated.
  *
  * The first call on each device looks up the array's device address (with
