@@ -30,6 +30,7 @@ between explicit copies instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -61,11 +62,14 @@ WORKLOADS = {
     "extreme-B1-L262144-H32-P64-S512-T128-states": (EXTREME_256K, torch.bfloat16, "zero", True),
     "pages-example-B4-L16384-H8-P64-S128-T128": (PAGES_EXAMPLE, torch.bfloat16, "zero", False),
 }
+# the length x dstate sweep with the chunk size chosen by the library's tuner
+# (chunk_size 0: it times {64, 128, 256} once per shape before the warm-up)
 for _L in (1024, 4096, 16384, 65536, 262144, 4095):
     for _S in (64, 128, 256, 512):
-        _sh = sweep_shape(_L, _S, 128)
-        WORKLOADS[f"sweep-B{_sh.batch}-L{_L}-H64-P64-S{_S}-T128"] = (_sh, torch.bfloat16, "zero",
-                                                                     False)
+        _sh = sweep_shape(_L, _S, 0)
+        WORKLOADS[f"sweep-B{_sh.batch}-L{_L}-H64-P64-S{_S}-Tauto"] = (_sh, torch.bfloat16, "zero",
+                                                                      False)
+TUNE_CANDIDATES = (64, 128, 256)
 DEFAULT = "mamba2-2.7b-layer-B4-L4096-H80-P64-S128-T256"
 # single-token decode steps on a carried state: name -> (batch, H, P, S, G, dtype)
 DECODE = {
@@ -259,8 +263,11 @@ def oracle_row(inp, s: Shape, b: int, threads: int):
     args = [oracle._f64(v) for v in (inp["x"][sl], inp["dt"][sl], inp["A"], inp["B"][sl],
                                      inp["C"][sl], inp["D"])]
     init = oracle._f64(None if inp["init"] is None else inp["init"][sl])
+    # y and the final state do not depend on the chunk size (no chunk states
+    # are asked for here), so a library-chosen one is timed at 128
+    T = s.chunk_size or 128
     t0 = time.perf_counter()
-    oracle.fwd(*args, s.chunk_size, init=init, nthreads=threads)
+    oracle.fwd(*args, T, init=init, nthreads=threads)
     return time.perf_counter() - t0, s.seqlen
 
 
@@ -321,19 +328,34 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     shape, dtype, init, want_states = WORKLOADS[args.workload]
     T = shape.chunk_size
+    auto = T == 0
     inp = make_inputs(shape, dtype=dtype, init=init, seed=rank)
     lib = _lib.load()
 
     g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     y = torch.empty_like(g["x"])
     fin = torch.empty((shape.batch, shape.nheads, shape.headdim, shape.dstate), device=dev)
-    states = (torch.empty((shape.batch, shape.nheads, shape.nchunks, shape.headdim,
-                           shape.dstate), device=dev) if want_states else None)
     wsp = ssd.Workspace()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    tuned = None
+    if auto:
+        # the library's per-shape choice: the first chunk_size=0 call times the
+        # candidates and fixes the fastest (before the warm-up, untimed)
+        ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=0,
+                    initial_state=g["init"], y=y, final_state=fin, workspace=wsp)
+        torch.cuda.synchronize(dev)
+        dims = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                shape.ngroups, dtype)
+        T = ssd.ssd_fwd_chosen_chunk_size(*dims)
+        tuned = ssd.ssd_fwd_chunk_size_was_timed(*dims)
+        shape = dataclasses.replace(shape, chunk_size=T)
+    states = (torch.empty((shape.batch, shape.nheads, shape.nchunks, shape.headdim,
+                           shape.dstate), device=dev) if want_states else None)
 
     plan = ssd.ssd_fwd_plan(g["x"], g["B"], T, want_states=want_states)
+    # the one-call path passes chunk_size 0 so the tuned plan choice applies
+    plan["call_chunk_size"] = 0 if auto else T
 
     def step(events=None):
         return ssd.ssd_fwd_staged(plan, g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"],
@@ -388,10 +410,21 @@ def run_ours(args):
     cb = compulsory_bytes(shape, dtype, init, want_states)
     fl = algorithmic_flops(shape)
     t_roof = max(cb / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+    if auto:
+        # a library-chosen chunk size: the roofline is the least over the
+        # candidates, so a larger chunk cannot loosen it
+        fls = {c: algorithmic_flops(dataclasses.replace(shape, chunk_size=c))
+               for c in TUNE_CANDIDATES}
+        c_min = min(fls, key=lambda c: max(cb / (peaks["hbm_gbs"] * 1e9),
+                                           fls[c] / (peaks["bf16_tflops"] * 1e12)))
+        fl = fls[c_min]
+        t_roof = max(cb / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
     step_roof = {"compulsory_bytes": cb, "algorithmic_flops": fl,
                  "t_roof_us": round(t_roof * 1e6, 2), "frac": round(t_roof / (ms / 1e3), 4),
                  "bound": "hbm" if cb / peaks["hbm_gbs"] >= fl / (peaks["bf16_tflops"] * 1e3)
                  else "tensor"}
+    if auto:
+        step_roof["flops_at_chunk_size"] = c_min
 
     # e2e: public ssd_fwd call, pinned host inputs in, y + final out, per step
     host_in = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
@@ -410,7 +443,7 @@ def run_ours(args):
     def e2e_step():
         if not want_states:
             ssd.ssd_fwd_host(host_in["x"], host_in["dt"], host_in["A"], host_in["B"],
-                             host_in["C"], host_in["D"], chunk_size=T,
+                             host_in["C"], host_in["D"], chunk_size=plan["call_chunk_size"],
                              initial_state=host_in["init"], y=y_host, final_state=fin_host,
                              workspace=wsp_host, device=dev, stream=stream)
             return
@@ -419,7 +452,7 @@ def run_ours(args):
                 g[k].copy_(v, non_blocking=True)
         ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=T,
                     initial_state=g["init"], y=y, final_state=fin, chunk_states=states,
-                    return_chunk_states=want_states, workspace=wsp)
+                    return_chunk_states=want_states, workspace=wsp)  # explicit-T copy path
         y_host.copy_(y, non_blocking=True)
         fin_host.copy_(fin, non_blocking=True)
 
@@ -448,7 +481,10 @@ def run_ours(args):
         "dtype": "bf16" if dtype == torch.bfloat16 else "f32", "data": "synthetic",
         "config": {"workload": args.workload, "batch": shape.batch, "seqlen": shape.seqlen,
                    "nheads": shape.nheads, "headdim": shape.headdim, "dstate": shape.dstate,
-                   "ngroups": shape.ngroups, "chunk_size": T, "init": init,
+                   "ngroups": shape.ngroups, "chunk_size": T,
+                   "chunk_size_choice": ("timed by the library over {64, 128, 256}" if tuned else
+                                         "the library's static choice") if auto else "fixed",
+                   "init": init,
                    "chunk_states": want_states, "parallelism": f"replicas{ws}",
                    "l2": "flushed before every timed step (512 MB write, outside the events)",
                    "path": plan["path"]},
@@ -999,6 +1035,23 @@ def run_bwd_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def spawn_ranks(n: int) -> int:
+    """--gpus N outside torchrun: relaunch this command as N ranks of one node
+    (one per GPU) under torch.distributed.run, rendezvous on 127.0.0.1."""
+    if torch.cuda.device_count() < n:
+        print(f"bench.py: --gpus {n} but only {torch.cuda.device_count()} GPU(s) visible",
+              file=sys.stderr)
+        return 2
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1009,6 +1062,14 @@ def main():
                     choices=sorted(WORKLOADS) + sorted(DECODE) + sorted(BACKWARD) + sorted(NORM))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if args.gpus != ws:
+        if ws == 1 and "LOCAL_RANK" not in os.environ:
+            sys.exit(spawn_ranks(args.gpus))
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {ws}", file=sys.stderr)
+        sys.exit(2)
     if args.workload in NORM:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the gated norm's reference arm is "

@@ -45,8 +45,11 @@
  *   L >= 0 (L == 0 copies init_state to final_state and launches nothing
  *   else).  The tensor-core (tcgen05) kernels serve bf16 with T a multiple
  *   of 128: the state pass for P in {64, 128} and S % 64 == 0; the chunk
- *   output and the fused pass for P == 64 and S in {64, 128, 256}.  Other
- *   shapes and all f32 calls run f32-arithmetic CUDA-core kernels.
+ *   output for P == 64 and S in {64, 128, 256}, and for S in {384, 512}
+ *   with T == 128; the one-head fused pass for P == 64 and S in
+ *   {64, 128, 256}; the head-pair fused pass for P == 64, S in {64, 128}
+ *   and an even number of heads per group.  Other shapes and all f32 calls
+ *   run f32-arithmetic CUDA-core kernels.
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H
@@ -149,8 +152,12 @@ ssd_path_t ssd_fwd_path(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, int 
  * Bytes of device workspace ssd_fwd needs for these arguments (the G_cum,
  * dt_t and, when the caller does not want them, the chunk states the
  * three-stage path keeps between stages, plus the chain buffers of the fused
- * path).  chunk_size 0 means "let the library choose", as in ssd_fwd.
- * Returns 0 for invalid arguments.
+ * path).  chunk_size 0 means "let the library choose", as in ssd_fwd: once
+ * the choice for the shape is fixed (ssd_fwd_chosen_chunk_size), that
+ * choice's size; before, without chunk states, the largest size among the
+ * candidates the tuner may time (candidates on CUDA cores are left out where
+ * another candidate runs on tensor cores: the tuner skips a candidate whose
+ * workspace does not fit).  Returns 0 for invalid arguments.
  */
 size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
                               int want_chunk_states);
@@ -160,7 +167,9 @@ size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size
  * single-pass kernel (state carried on chip / in L2 between chunks) when the
  * shape allows it.  y receives the output; final_state and chunk_states are
  * optional outputs (NULL = not wanted); init_state may be NULL (zeros).
- * chunk_size 0 lets the library choose among {64, 128, 256}.
+ * chunk_size 0 lets the library choose among {64, 128, 256} (see
+ * ssd_fwd_chosen_chunk_size: the first such call for a shape may time the
+ * candidates on the caller's buffers and stream).
  * workspace must hold ssd_fwd_workspace_size(dims, dtype, chunk_size,
  * chunk_states != NULL) bytes, 256-byte aligned; its contents on entry do
  * not matter.  On the head-pair path (SSD_PATH_FUSED_PAIR_TENSOR_CORES) with
@@ -193,7 +202,9 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
  *   f32, dinit [B, H, P, S] f32 (may be NULL: not wanted; the gradient with
  *   respect to init_state, or to the zero initial state when init_state is
  *   NULL).
- * Arithmetic is f32 on CUDA cores (bf16 inputs widened).  Supported: P <= 64
+ * Arithmetic: bf16 calls with P == 64 and S in {64, 128} run tcgen05 kernels
+ * (128-token chunks, bf16 operands, f32 accumulation); every other call runs
+ * f32 arithmetic on CUDA cores (bf16 inputs widened).  Supported: P <= 64
  * and the sizes of ssd_fwd; other headdims return SSD_ERR_UNSUPPORTED.
  * workspace: ssd_bwd_workspace_size(dims, dtype) bytes, 256-byte aligned;
  * contents on entry do not matter.
@@ -303,8 +314,65 @@ ssd_status_t ssd_fwd_host(const void *x, const float *dt, const float *A, const 
                           float *final_state, ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
                           void *workspace, size_t workspace_bytes, void *stream);
 
-/* Chunk size ssd_fwd uses for chunk_size == 0 with these dims and dtype. */
+/*
+ * Chunk size ssd_fwd uses for chunk_size == 0 with these dims and dtype
+ * (0 for invalid arguments).  The pages search the best configuration per
+ * shape ("Accelerating Mamba-2 forward-pass kernels with CUDA Tile
+ * (cuTile)", section "Mamba-2 性能优化"); here the choice among {64, 128, 256}
+ * -- and, on the head-pair path, between its prefilled-segment and hand-off
+ * plans -- is fixed once per (batch, seqlen, nheads, headdim, dstate,
+ * ngroups, dtype) and process, by whichever comes first:
+ *   - the first ssd_fwd(chunk_size = 0) call without chunk_states, outside
+ *     stream capture, whose y and final_state overlap no input: it runs
+ *     every candidate whose workspace fits the one passed, once untimed and
+ *     twice between CUDA events on the caller's stream, synchronizing that
+ *     stream (so that first call blocks the host and takes a few times a
+ *     forward), keeps the fastest, then runs the call itself;
+ *   - this function, or any other ssd_fwd(chunk_size = 0) call: the static
+ *     choice (128 for bf16; for f32 64 when seqlen <= 64, else 128).
+ * A fixed choice never changes in the process, so chunk_states can be sized
+ * from this function.  Make the first chunk_size = 0 call for a shape
+ * before any stream capture that could be active in another thread (the
+ * tuner records and waits on events).
+ */
 int ssd_fwd_chosen_chunk_size(ssd_dims_t dims, ssd_dtype_t dtype);
+
+/* 1 if the choice above was fixed by timing the candidates, else 0. */
+int ssd_fwd_chunk_size_was_timed(ssd_dims_t dims, ssd_dtype_t dtype);
+
+/*
+ * Sequence-sharded (context-parallel) forward, one segment of the sequence
+ * per rank, ranks in sequence order.  Section "Kernel 2: fwd_pass_state"
+ * makes the state at the end of one call the initial state of the next, and
+ * the state update is linear in the state, so the segments need one
+ * exchange of a per-segment summary:
+ *   1. ssd_segment_summary on every rank: seg_state [B, H, P, S] f32 = the
+ *      segment's end state when run from a zero state, and seg_decay [B, H]
+ *      f32 = the segment's total decay sum_t A[h] dt[b,t,h] in log2 units
+ *      (log2(e) times the natural-log sum; the pages keep G in log2 units).
+ *      Inputs as for ssd_fwd (x, dt, A, Bm of the segment).  workspace:
+ *      ssd_segment_summary_workspace_size(dims, dtype, chunk_size) bytes,
+ *      256-byte aligned (G and dt^T of the segment).
+ *   2. the caller all-gathers (seg_state, seg_decay) of every segment.
+ *   3. ssd_carry_in on rank r: h_in = exp2(D_{r-1}) h_{r-1} + s_{r-1} with
+ *      h_0 = init_state (NULL: zeros); seg_states [n_segments, B, H, P, S]
+ *      and seg_decays [n_segments, B, H] hold the gathered summaries (only
+ *      the first `upto` segments are read; upto = r).  h_in [B, H, P, S]
+ *      f32 may be init_state itself, but may not overlap anything else.
+ *      Only batch, nheads, headdim and dstate of dims are used.
+ *   4. ssd_fwd of the segment with init_state = h_in: y, final state and
+ *      chunk states of that segment (chunk states match the unsharded run's
+ *      when every segment but the last is a whole number of chunks).
+ * Errors as ssd_fwd; every call is asynchronous on `stream`.
+ */
+size_t ssd_segment_summary_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size);
+ssd_status_t ssd_segment_summary(const void *x, const float *dt, const float *A, const void *Bm,
+                                 float *seg_state, float *seg_decay, ssd_dims_t dims,
+                                 ssd_dtype_t dtype, int chunk_size, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+ssd_status_t ssd_carry_in(const float *seg_states, const float *seg_decays,
+                          const float *init_state, int n_segments, int upto, float *h_in,
+                          ssd_dims_t dims, void *stream);
 
 /*
  * Number of kernel launches this library has issued in this process (all
@@ -321,6 +389,11 @@ const char *ssd_status_string(ssd_status_t status);
  * device's kernel status word.  Returns SSD_ERR_TIMEOUT if any kernel since
  * the last read gave up a bounded wait, SSD_ERR_CUDA if the stream reports
  * an error, else SSD_OK.
+ * Fault injection (debug only): with SSD_FAULT_SKIP_ARRIVE=1 in the
+ * environment when the head-pair kernel is launched, one compute warp per
+ * CTA skips a barrier arrival on the CTA's first tile and every wait of that
+ * launch gives up after 20 ms; the launch then records the timeout here,
+ * leaves with nothing in flight, and its outputs are undefined.
  */
 ssd_status_t ssd_stream_status(void *stream);
 

@@ -7,7 +7,8 @@ built or loaded (there is no CPU fallback).
 """
 from .ssd import (SsdError, SsdFunction, Workspace, ssd_bwd, ssd_chunk_cumsum,  # noqa: F401
                   ssd_chunk_out, ssd_decode_step, ssd_fwd, ssd_fwd_host, ssd_gated_rmsnorm,
-                  ssd_fwd_chosen_chunk_size, ssd_fwd_path, ssd_fwd_plan, ssd_fwd_staged,
-                  ssd_fwd_workspace_size, ssd_state_out, ssd_state_pass,
-                  ssd_status_string, ssd_stream_status)
+                  ssd_fwd_chosen_chunk_size, ssd_fwd_chunk_size_was_timed, ssd_fwd_path,
+                  ssd_fwd_plan, ssd_fwd_staged, ssd_fwd_workspace_size, ssd_state_out,
+                  ssd_state_pass, ssd_status_string, ssd_stream_status, ssd_segment_summary,
+                  ssd_carry_in, ssd_fwd_context_parallel)
 from ._build import build  # noqa: F401

@@ -27,8 +27,10 @@ EXPORTS = ("ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out
            "ssd_state_out_workspace_size",
            "ssd_fwd_path", "ssd_fwd_workspace_size", "ssd_fwd", "ssd_fwd_noalloc",
            "ssd_fwd_host", "ssd_fwd_host_workspace_size",
-           "ssd_fwd_chosen_chunk_size", "ssd_decode_step", "ssd_bwd", "ssd_bwd_workspace_size",
-           "ssd_gated_rmsnorm",
+           "ssd_fwd_chosen_chunk_size", "ssd_fwd_chunk_size_was_timed", "ssd_decode_step",
+           "ssd_bwd", "ssd_bwd_workspace_size",
+           "ssd_gated_rmsnorm", "ssd_segment_summary", "ssd_segment_summary_workspace_size",
+           "ssd_carry_in",
            "ssd_launch_count", "ssd_status_string", "ssd_stream_status")
 PATH_NAMES = {0: "staged-cuda-cores", 1: "staged-tensor-cores", 2: "fused-tensor-cores",
               3: "fused-pair-tensor-cores"}
@@ -83,12 +85,17 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                               ctypes.c_size_t, vp], st),
             "ssd_fwd_host_workspace_size": ([D, i32, i32], ctypes.c_size_t),
             "ssd_fwd_chosen_chunk_size": ([D, i32], ctypes.c_int),
+            "ssd_fwd_chunk_size_was_timed": ([D, i32], ctypes.c_int),
             "ssd_decode_step": ([vp, fp, fp, vp, vp, fp, fp, fp, vp, D, i32, vp], st),
             "ssd_bwd_workspace_size": ([D, i32], ctypes.c_size_t),
             "ssd_gated_rmsnorm": ([vp, vp, fp, vp, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int64, ctypes.c_float, i32, vp], st),
             "ssd_bwd": ([vp, fp, fp, vp, vp, fp, fp, vp, fp, vp, fp, fp, vp, vp, fp, fp, D, i32,
                          vp, ctypes.c_size_t, vp], st),
+            "ssd_segment_summary_workspace_size": ([D, i32, i32], ctypes.c_size_t),
+            "ssd_segment_summary": ([vp, fp, fp, vp, fp, fp, D, i32, i32, vp, ctypes.c_size_t,
+                                     vp], st),
+            "ssd_carry_in": ([fp, fp, fp, i32, i32, fp, D, vp], st),
             "ssd_launch_count": ([], ctypes.c_uint64),
             "ssd_status_string": ([st], ctypes.c_char_p),
             "ssd_stream_status": ([vp], st),

@@ -109,6 +109,13 @@ struct PairParams {
     float *seg_state;         // [B*H*n_seg][P][S]
     unsigned int *seg_count;  // [B*H*n_seg], zero at launch
     unsigned int *status;
+    // Bounded waits give up after wait_ns.  Fault injection (a host-set debug
+    // parameter, off by default): with fault_skip_arrive, compute warp 0 of
+    // every CTA skips its X_hat-barrier arrival on the CTA's first tile, so
+    // the waits on that barrier run out and every role leaves its loop with
+    // no copy or MMA in flight (see the launcher).
+    unsigned long long wait_ns;
+    int fault_skip_arrive;
 };
 
 struct PItem {
@@ -220,6 +227,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
     const Geom &g = prm.g;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const uint64_t wait_ns = prm.wait_ns;
 
     if (tid == 0) {
         mbar_init(&bar_bc, 1);
@@ -281,7 +289,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         continue;
                     }
                     const uint32_t pp = (it - 1) & 1;
-                    if (!mbar_wait(&bar_xh, pp)) {
+                    if (!mbar_wait(&bar_xh, pp, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -290,13 +298,13 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         load_x(0);
                     if (m1)
                         load_x(1);
-                    if (!mbar_wait(&bar_ds, pp)) {
+                    if (!mbar_wait(&bar_ds, pp, wait_ns)) {
                         ok = false;
                         break;
                     }
                     load_bc();
                     if (!m0 || !m1) {
-                        if (!mbar_wait(&bar_y, pp)) {
+                        if (!mbar_wait(&bar_y, pp, wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -338,7 +346,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const uint32_t par = it & 1;
                     // CB overwrites the previous tile's CB, whose conversion
                     // ended before that tile's Y1 was issued
-                    if (!mbar_wait(&bar_bc, par)) {
+                    if (!mbar_wait(&bar_bc, par, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -348,7 +356,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
                                id_cb, ks > 0);
                     mma_commit(&bar_cb);
-                    if (!mbar_wait(&bar_xh, par) || !mbar_wait(&bar_h, par)) {
+                    if (!mbar_wait(&bar_xh, par, wait_ns) || !mbar_wait(&bar_h, par, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -399,7 +407,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         if (!y1_sent) {
                             bool ready = grp > 0 && mbar_test(&bar_sc, par);
                             if (grp == n_grp && !ready) {
-                                if (!mbar_wait(&bar_sc, par)) {
+                                if (!mbar_wait(&bar_sc, par, wait_ns)) {
                                     ok = false;
                                     break;
                                 }
@@ -435,7 +443,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             for (int j = 0; j < n_my && ok; ++j) {
                 const PItem w = my_item(prm, s_plan, j);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
-                    if (!mbar_wait(&bar_ys, it & 1)) {
+                    if (!mbar_wait(&bar_ys, it & 1, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -589,7 +597,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 if (i == 0)
                     s_mode[par][k] = narrow ? 1 : 0;
                 // x landed; the previous tile's state jump and Y1 are done
-                if (!mbar_wait(&bar_x[k], par) || (it > 0 && !mbar_wait(&bar_ds, par ^ 1u))) {
+                if (!mbar_wait(&bar_x[k], par, wait_ns) || (it > 0 && !mbar_wait(&bar_ds, par ^ 1u, wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -637,7 +645,8 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 tmem_st_wait();
                 tc_fence_before();
                 cp_async_wait_all();  // the next tile's dt (see prefetch_dt)
-                warp_arrive(&bar_xh);
+                if (!(prm.fault_skip_arrive && it == 0 && warp == 0))
+                    warp_arrive(&bar_xh);
 
                 // ---- a later segment waits until its predecessor published its state
                 if (first && w.seg > 0 && !prm.prefilled) {
@@ -645,7 +654,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     bool ready = ld_acquire_gpu(cnt) >= 4u;
                     const uint64_t t_start = globaltimer_ns();
                     while (!ready) {
-                        if (globaltimer_ns() - t_start > 2000000000ull)
+                        if (globaltimer_ns() - t_start > wait_ns)
                             break;
                         __nanosleep(256);
                         ready = ld_acquire_gpu(cnt) >= 4u;
@@ -656,7 +665,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     }
                 }
                 // the previous tile's y store has read the H buffers
-                if (it > 0 && !mbar_wait(&bar_hfree, par ^ 1u)) {
+                if (it > 0 && !mbar_wait(&bar_hfree, par ^ 1u, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -749,7 +758,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
 
                 // ---- scores.  Shared masked CB (keys [64k, 64k + 64) here) when a
                 // head is factorized; the exact per-element scores of a wide head.
-                if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_xh, par)) {
+                if (!mbar_wait(&bar_cb, par, wait_ns) || !mbar_wait(&bar_xh, par, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -821,7 +830,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                             tmem_st8(tl + region + j0 / 2, pk);
                         }
                         // Y = exp2(g_i) (C H^T) + D x, before the score product adds on
-                        if (!mbar_wait(&bar_y2, par)) {
+                        if (!mbar_wait(&bar_y2, par, wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -858,7 +867,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     nxt_g = tile_g((it + 1) & 1, kLog2e * a_next);
 
                 // ---- epilogue: y = r Y, staged in this head's H buffer
-                if (!mbar_wait(&bar_y, par)) {
+                if (!mbar_wait(&bar_y, par, wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -897,7 +906,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                                          : ((last_seq && want_final) ? prm.final_state + bh * g.P * g.S
                                                                      : nullptr);
                     if (dst) {
-                        if (!mbar_wait(&bar_ds, par)) {
+                        if (!mbar_wait(&bar_ds, par, wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -1062,10 +1071,12 @@ size_t pair_tc_scratch_bytes(const Geom &g, bool allow_prefill)
            (sp.gd_bytes + 511) / 512 * 512;
 }
 
+bool pair_tc_prefers_prefill(const Geom &g) { return pair_tc_supported(g) && pair_seg_plan(g).prefill; }
+
 cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dt,
                                  const float *A, const float *D, const float *init, float *states,
                                  float *final_state, void *y, const Geom &g, void *scratch,
-                                 size_t scratch_bytes, cudaStream_t st)
+                                 size_t scratch_bytes, cudaStream_t st, bool allow_prefill)
 {
     if (!pair_tc_supported(g))
         return cudaErrorNotSupported;
@@ -1085,7 +1096,7 @@ cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, 
     prm.hpg = g.hpg;
     // the prefilled plan when the scratch holds it, else the hand-off plan
     // (the caller checked that one of the two fits)
-    PairSegPlan sp = pair_seg_plan(g);
+    PairSegPlan sp = pair_seg_plan(g, allow_prefill);
     if (sp.prefill && scratch_bytes < pair_tc_scratch_bytes(g, true))
         sp = pair_seg_plan(g, false);
     prm.seg_tiles = sp.seg_tiles;
@@ -1117,6 +1128,16 @@ cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, 
     prm.status = device_status_word();
     if (!prm.status)
         return cudaErrorUnknown;
+    // SSD_FAULT_SKIP_ARRIVE=1 (debug only) injects a lost barrier arrival on
+    // every CTA's first tile and shortens every wait to 20 ms, so a test can
+    // see the timeout path report SSD_ERR_TIMEOUT through ssd_stream_status.
+    // What is in flight when the waits run out: the first tile's TMA loads
+    // (each already waited for by its consumer) and its C B^T MMA (waited for
+    // by the compute warps through its commit barrier before the wait that
+    // runs out), so every role leaves with nothing outstanding.
+    const char *fault = getenv("SSD_FAULT_SKIP_ARRIVE");
+    prm.fault_skip_arrive = (fault && strcmp(fault, "1") == 0) ? 1 : 0;
+    prm.wait_ns = prm.fault_skip_arrive ? 20000000ull : 2000000000ull;
     CUtensorMap tx, tb, tcm, ty;
     if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g) ||
         !make_tmap_tokens_groups(&tcm, Cm, g) || !make_tmap_tokens_heads(&ty, y, g))

@@ -6,6 +6,7 @@
 #include <initializer_list>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -156,14 +157,86 @@ cudaError_t run_state_pass(const void *x, const void *Bm, const float *dtT, cons
     return launch_state_pass_simt(x, Bm, dtT, Gc, init, states, final_state, g, bf16, st);
 }
 
-int choose_chunk_size(const Geom &g, ssd_dtype_t t)
+// The chunk size used for chunk_size == 0 before (or instead of) timing.
+// bf16: the tensor-core kernels walk 128-token tiles; 128 keeps the chunk
+// states (when requested) as fine as the tiles.  f32: short chunks keep the
+// CUDA-core score tile small.
+int static_chunk_size(const Geom &g, ssd_dtype_t t)
 {
-    // bf16: the tensor-core kernels walk 128-token tiles; 128 keeps the chunk
-    // states (when requested) as fine as the tiles.  f32: short chunks keep
-    // the CUDA-core score tile small.
     if (t == SSD_BF16)
         return 128;
     return g.L <= 64 ? 64 : 128;
+}
+
+// ---------------------------------------------------------------------------
+// chunk_size == 0: the per-shape choice ("Accelerating Mamba-2 forward-pass
+// kernels with CUDA Tile (cuTile)", section "Mamba-2 性能优化": the best
+// configuration is searched per shape).  The candidates are the chunk sizes
+// {64, 128, 256} and, on the head-pair path where the prefilled-segment plan
+// applies, that plan or the hand-off plan.  A choice is fixed once per
+// (B, L, H, P, S, G, dtype) and process, by whichever comes first:
+//   * the first ssd_fwd(chunk_size = 0) call without chunk states, outside
+//     stream capture and with no output overlapping an input: it runs every
+//     candidate whose workspace fits the one passed (once untimed, then twice
+//     between CUDA events on the caller's stream, keeping the faster time) and
+//     keeps the fastest; a candidate must beat the current best by 2% to
+//     replace it, so near-ties keep the static choice;
+//   * ssd_fwd_chosen_chunk_size, or any other ssd_fwd(chunk_size = 0) call:
+//     the static choice above.
+// The choice never changes afterwards, so a caller can size chunk_states from
+// ssd_fwd_chosen_chunk_size.  The cache is guarded by a mutex; two threads
+// tuning one shape at once both time it and the first to finish wins.
+struct TuneKey {
+    int64_t B, L, H, P, S, G;
+    int dtype;
+    bool operator<(const TuneKey &o) const
+    {
+        const int64_t a[7] = {B, L, H, P, S, G, dtype}, b[7] = {o.B, o.L, o.H, o.P, o.S, o.G, o.dtype};
+        return std::lexicographical_compare(a, a + 7, b, b + 7);
+    }
+};
+struct TuneChoice {
+    int T;
+    bool allow_prefill;  // head-pair path: the prefilled plan where it applies
+    bool timed;
+};
+std::mutex g_tune_mu;
+std::map<TuneKey, TuneChoice> g_tune;
+
+TuneKey tune_key(const Geom &g, ssd_dtype_t t) { return TuneKey{g.B, g.L, g.H, g.P, g.S, g.G, (int)t}; }
+
+bool tune_lookup(const Geom &g, ssd_dtype_t t, TuneChoice *c)
+{
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    const auto it = g_tune.find(tune_key(g, t));
+    if (it == g_tune.end())
+        return false;
+    *c = it->second;
+    return true;
+}
+
+// Fixes c unless a choice is already there; returns the one that stands.
+TuneChoice tune_fix(const Geom &g, ssd_dtype_t t, const TuneChoice &c)
+{
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    return g_tune.emplace(tune_key(g, t), c).first->second;
+}
+
+// The current choice without fixing it: the cached one, else the static one.
+TuneChoice tune_peek(const Geom &g, ssd_dtype_t t)
+{
+    TuneChoice c;
+    if (tune_lookup(g, t, &c))
+        return c;
+    return TuneChoice{static_chunk_size(g, t), true, false};
+}
+
+Geom with_chunk(const Geom &g0, int T)
+{
+    Geom g = g0;
+    g.T = T;
+    g.nc = (g.L + T - 1) / T;
+    return g;
 }
 
 struct Workspace {
@@ -251,13 +324,19 @@ size_t fwd_workspace_min_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size
         return 0;
     if (dtype != SSD_BF16 && dtype != SSD_F32)
         return 0;
-    if (g.T == 0) {
-        g.T = choose_chunk_size(g, dtype);
-        g.nc = (g.L + g.T - 1) / g.T;
-    }
+    if (g.T == 0)
+        g = with_chunk(g, tune_peek(g, dtype).T);
     const size_t b = layout(g, choose_path(g, dtype, want_chunk_states != 0),
                             want_chunk_states != 0, nullptr).min_bytes;
     return b ? b : 256;
+}
+
+int chunk_size_peek(ssd_dims_t dims, ssd_dtype_t dtype)
+{
+    Geom g;
+    if (make_geom(dims, 0, true, &g) != SSD_OK || (dtype != SSD_BF16 && dtype != SSD_F32))
+        return 0;
+    return tune_peek(g, dtype).T;
 }
 
 }  // namespace ssd
@@ -398,19 +477,27 @@ ssd_path_t ssd_fwd_path(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size, int 
     if (make_geom(dims, chunk_size, true, &g) != SSD_OK ||
         (dtype != SSD_BF16 && dtype != SSD_F32))
         return SSD_PATH_INVALID;
-    if (g.T == 0) {
-        g.T = choose_chunk_size(g, dtype);
-        g.nc = (g.L + g.T - 1) / g.T;
-    }
+    if (g.T == 0)
+        g = with_chunk(g, tune_peek(g, dtype).T);
     return choose_path(g, dtype, want_chunk_states != 0);
 }
 
 int ssd_fwd_chosen_chunk_size(ssd_dims_t dims, ssd_dtype_t dtype)
 {
     Geom g;
-    if (make_geom(dims, 0, true, &g) != SSD_OK)
+    if (make_geom(dims, 0, true, &g) != SSD_OK || (dtype != SSD_BF16 && dtype != SSD_F32))
         return 0;
-    return choose_chunk_size(g, dtype);
+    return tune_fix(g, dtype, tune_peek(g, dtype)).T;
+}
+
+int ssd_fwd_chunk_size_was_timed(ssd_dims_t dims, ssd_dtype_t dtype)
+{
+    Geom g;
+    TuneChoice c;
+    if (make_geom(dims, 0, true, &g) != SSD_OK || (dtype != SSD_BF16 && dtype != SSD_F32) ||
+        !tune_lookup(g, dtype, &c))
+        return 0;
+    return c.timed ? 1 : 0;
 }
 
 size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
@@ -421,14 +508,184 @@ size_t ssd_fwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size
         return 0;
     if (dtype != SSD_BF16 && dtype != SSD_F32)
         return 0;
-    if (g.T == 0) {
-        g.T = choose_chunk_size(g, dtype);
-        g.nc = (g.L + g.T - 1) / g.T;
+    const bool ws = want_chunk_states != 0;
+    TuneChoice c;
+    if (g.T == 0 && !ws && !tune_lookup(g, dtype, &c)) {
+        // not fixed yet: room for every candidate the tuner may time, leaving
+        // out CUDA-core candidates where another candidate runs on tensor cores
+        // (they cannot win, and the staged CUDA-core path keeps every chunk
+        // state in the workspace)
+        size_t b_tc = 0, b_all = 0;
+        for (int T : {64, 128, 256}) {
+            Geom gt;
+            if (make_geom(dims, T, false, &gt) != SSD_OK)
+                continue;
+            const ssd_path_t p = choose_path(gt, dtype, false);
+            const size_t b = layout(gt, p, false, nullptr).bytes;
+            b_all = std::max(b_all, b);
+            if (p != SSD_PATH_STAGED_CUDA_CORES)
+                b_tc = std::max(b_tc, b);
+        }
+        const size_t b = b_tc ? b_tc : b_all;
+        return b ? b : 256;
     }
-    const size_t b = layout(g, choose_path(g, dtype, want_chunk_states != 0),
-                            want_chunk_states != 0, nullptr).bytes;
+    if (g.T == 0)
+        g = with_chunk(g, tune_peek(g, dtype).T);
+    const size_t b = layout(g, choose_path(g, dtype, ws), ws, nullptr).bytes;
     return b ? b : 256;
 }
+
+}  // extern "C"
+
+namespace ssd {
+namespace {
+
+struct FwdArgs {
+    const void *x;
+    const float *dt, *A;
+    const void *Bm, *Cm;
+    const float *D, *init_state;
+    void *y;
+    float *final_state, *chunk_states;
+    ssd_dims_t dims;
+    ssd_dtype_t dtype;
+    void *workspace;
+    size_t workspace_bytes;
+    cudaStream_t st;
+};
+
+// The forward with the chunk size fixed (g.T > 0); pointers already validated.
+ssd_status_t fwd_impl(const FwdArgs &a, const Geom &g, bool allow_prefill)
+{
+    const bool ne = g.L > 0;
+    if (!ne)
+        return ssd_state_pass(a.x, a.Bm, nullptr, nullptr, a.init_state, a.chunk_states,
+                              a.final_state, a.dims, a.dtype, g.T, a.st);
+    const ssd_path_t path = choose_path(g, a.dtype, a.chunk_states != nullptr);
+    const bool fused = path == SSD_PATH_FUSED_TENSOR_CORES;
+    const Workspace need_ws = layout(g, path, a.chunk_states != nullptr, nullptr);
+    if (need_ws.min_bytes && (!a.workspace || a.workspace_bytes < need_ws.min_bytes ||
+                              (reinterpret_cast<uintptr_t>(a.workspace) & 255u)))
+        return SSD_ERR_WORKSPACE;
+    const Workspace w = layout(g, path, a.chunk_states != nullptr, static_cast<char *>(a.workspace));
+    // the head-pair kernel takes the plan the whole workspace holds
+    if (path == SSD_PATH_FUSED_PAIR_TENSOR_CORES)
+        return cuda_status(launch_fused_pair_tc(a.x, a.Bm, a.Cm, a.dt, a.A, a.D, a.init_state,
+                                                a.chunk_states, a.final_state, a.y, g,
+                                                w.fused_scratch,
+                                                a.workspace ? a.workspace_bytes : 0, a.st,
+                                                allow_prefill));
+    float *states = a.chunk_states ? a.chunk_states : w.states;
+    const bool bf16 = a.dtype == SSD_BF16;
+
+    SSD_TRY(cuda_status(launch_chunk_cumsum(a.dt, a.A, w.Gc, w.dtT, g, a.st)));
+    if (fused)
+        return cuda_status(launch_fused_tc(a.x, a.Bm, a.Cm, w.dtT, w.Gc, a.D, a.init_state,
+                                           a.chunk_states, a.final_state, a.y, g, w.fused_scratch,
+                                           w.fused_scratch_bytes, a.st));
+    SSD_TRY(cuda_status(run_state_pass(a.x, a.Bm, w.dtT, w.Gc, a.init_state, states,
+                                       a.final_state, g, bf16, a.st)));
+    return cuda_status(run_chunk_out(a.x, a.Bm, a.Cm, w.dtT, w.Gc, states, a.D, a.y, g, bf16, a.st));
+}
+
+bool overlaps(const void *p, size_t np, const void *q, size_t nq)
+{
+    if (!p || !q || !np || !nq)
+        return false;
+    const char *a = static_cast<const char *>(p), *b = static_cast<const char *>(q);
+    return a < b + nq && b < a + np;
+}
+
+// Repeated runs are harmless only when no output overlaps an input.
+bool outputs_disjoint(const FwdArgs &a, const Geom &g)
+{
+    const size_t e = a.dtype == SSD_BF16 ? 2 : 4;
+    const size_t nx = (size_t)(g.B * g.L * g.H * g.P) * e, nbc = (size_t)(g.B * g.L * g.G * g.S) * e;
+    const size_t ndt = (size_t)(g.B * g.L * g.H) * 4, nh = (size_t)g.H * 4;
+    const size_t nst = (size_t)(g.B * g.H * g.P * g.S) * 4;
+    const void *in[7] = {a.x, a.dt, a.A, a.Bm, a.Cm, a.D, a.init_state};
+    const size_t nin[7] = {nx, ndt, nh, nbc, nbc, nh, nst};
+    const void *out[2] = {a.y, a.final_state};
+    const size_t nout[2] = {nx, nst};
+    for (int o = 0; o < 2; ++o)
+        for (int i = 0; i < 7; ++i)
+            if (overlaps(out[o], nout[o], in[i], nin[i]))
+                return false;
+    return !overlaps(a.y, nx, a.final_state, nst);
+}
+
+// Times every candidate (see the note at tune_key) and fixes the fastest.
+TuneChoice tune_and_fix(const FwdArgs &a, const Geom &g0)
+{
+    const TuneChoice fallback{static_chunk_size(g0, a.dtype), true, false};
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0)
+            cudaEventDestroy(e0);
+        cudaGetLastError();
+        return tune_fix(g0, a.dtype, fallback);
+    }
+    // the static choice first, so that near-ties keep it
+    int order[3] = {fallback.T, 0, 0}, n_order = 1;
+    for (int T : {64, 128, 256})
+        if (T != fallback.T)
+            order[n_order++] = T;
+    float best = 0.f;
+    TuneChoice best_c = fallback;
+    bool have = false, failed = false;
+    auto run_once = [&](const Geom &g, bool pre, float *ms) {
+        if (cudaEventRecord(e0, a.st) != cudaSuccess)
+            return false;
+        if (fwd_impl(a, g, pre) != SSD_OK)
+            return false;
+        if (cudaEventRecord(e1, a.st) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess)
+            return false;
+        return cudaEventElapsedTime(ms, e0, e1) == cudaSuccess;
+    };
+    for (int k = 0; k < n_order && !failed; ++k) {
+        Geom g;
+        if (make_geom(a.dims, order[k], false, &g) != SSD_OK)
+            continue;
+        const ssd_path_t path = choose_path(g, a.dtype, false);
+        if (layout(g, path, false, nullptr).min_bytes > (a.workspace ? a.workspace_bytes : 0))
+            continue;
+        // the hand-off plan as a second candidate where the prefilled one runs
+        const bool two_plans = path == SSD_PATH_FUSED_PAIR_TENSOR_CORES &&
+                               pair_tc_prefers_prefill(g) &&
+                               a.workspace_bytes >= pair_tc_scratch_bytes(g, true) &&
+                               a.workspace_bytes >= pair_tc_scratch_bytes(g, false);
+        for (int pl = 0; pl < (two_plans ? 2 : 1); ++pl) {
+            const bool pre = pl == 0;
+            float t_warm = 0.f, t1 = 0.f, t2 = 0.f;
+            if (!run_once(g, pre, &t_warm)) {
+                failed = true;  // a launch failed: stop timing, keep what stands
+                break;
+            }
+            if (have && t_warm > 1.5f * best)
+                continue;  // far behind: not worth timing
+            if (!run_once(g, pre, &t1) || !run_once(g, pre, &t2)) {
+                failed = true;
+                break;
+            }
+            const float t = std::min(t1, t2);
+            if (!have || t < 0.98f * best) {
+                best = t;
+                best_c = TuneChoice{order[k], pre, true};
+                have = true;
+            }
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (failed)
+        cudaGetLastError();  // the caller's own run reports any sticky error
+    return tune_fix(g0, a.dtype, have ? best_c : fallback);
+}
+
+}  // namespace
+}  // namespace ssd
+
+extern "C" {
 
 ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void *Bm,
                      const void *Cm, const float *D, const float *init_state, void *y,
@@ -440,10 +697,6 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
     SSD_TRY(make_geom(dims, chunk_size, true, &g));
     if (dtype != SSD_BF16 && dtype != SSD_F32)
         return SSD_ERR_INVALID_ARG;
-    if (g.T == 0) {
-        g.T = choose_chunk_size(g, dtype);
-        g.nc = (g.L + g.T - 1) / g.T;
-    }
     const bool ne = g.L > 0;
     SSD_TRY(need(x, ne));
     SSD_TRY(need(dt, ne));
@@ -455,34 +708,25 @@ ssd_status_t ssd_fwd(const void *x, const float *dt, const float *A, const void 
     SSD_TRY(opt(init_state));
     SSD_TRY(opt(final_state));
     SSD_TRY(opt(chunk_states));
-    cudaStream_t st = (cudaStream_t)stream;
-    if (!ne)
-        return ssd_state_pass(x, Bm, nullptr, nullptr, init_state, chunk_states, final_state,
-                              dims, dtype, g.T, stream);
-
-    const ssd_path_t path = choose_path(g, dtype, chunk_states != nullptr);
-    const bool fused = path == SSD_PATH_FUSED_TENSOR_CORES;
-    const Workspace need_ws = layout(g, path, chunk_states != nullptr, nullptr);
-    if (need_ws.min_bytes && (!workspace || workspace_bytes < need_ws.min_bytes ||
-                              (reinterpret_cast<uintptr_t>(workspace) & 255u)))
-        return SSD_ERR_WORKSPACE;
-    const Workspace w = layout(g, path, chunk_states != nullptr, static_cast<char *>(workspace));
-    // the head-pair kernel takes the plan the whole workspace holds
-    if (path == SSD_PATH_FUSED_PAIR_TENSOR_CORES)
-        return cuda_status(launch_fused_pair_tc(x, Bm, Cm, dt, A, D, init_state, chunk_states,
-                                                final_state, y, g, w.fused_scratch,
-                                                workspace ? workspace_bytes : 0, st));
-    float *states = chunk_states ? chunk_states : w.states;
-    const bool bf16 = dtype == SSD_BF16;
-
-    SSD_TRY(cuda_status(launch_chunk_cumsum(dt, A, w.Gc, w.dtT, g, st)));
-    if (fused)
-        return cuda_status(launch_fused_tc(x, Bm, Cm, w.dtT, w.Gc, D, init_state, chunk_states,
-                                           final_state, y, g, w.fused_scratch,
-                                           w.fused_scratch_bytes, st));
-    SSD_TRY(cuda_status(
-        run_state_pass(x, Bm, w.dtT, w.Gc, init_state, states, final_state, g, bf16, st)));
-    return cuda_status(run_chunk_out(x, Bm, Cm, w.dtT, w.Gc, states, D, y, g, bf16, st));
+    const FwdArgs a{x, dt, A, Bm, Cm, D, init_state, y, final_state, chunk_states, dims, dtype,
+                    workspace, workspace_bytes, (cudaStream_t)stream};
+    bool allow_prefill = true;
+    if (g.T == 0) {
+        TuneChoice c;
+        if (!tune_lookup(g, dtype, &c)) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            const bool capturing =
+                cudaStreamIsCapturing(a.st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone;
+            if (capturing)
+                cudaGetLastError();
+            c = (!ne || chunk_states || capturing || !outputs_disjoint(a, g))
+                    ? tune_fix(g, dtype, tune_peek(g, dtype))
+                    : tune_and_fix(a, g);
+        }
+        g = with_chunk(g, c.T);
+        allow_prefill = c.allow_prefill;
+    }
+    return fwd_impl(a, g, allow_prefill);
 }
 
 size_t ssd_bwd_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype)

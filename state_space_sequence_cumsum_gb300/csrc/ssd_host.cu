@@ -81,7 +81,7 @@ ssd_status_t make_host_plan(const ssd_dims_t &d, ssd_dtype_t dtype, int chunk_si
         return SSD_ERR_INVALID_ARG;
     HostPlan p;
     p.esz = dtype == SSD_BF16 ? 2 : 4;
-    p.T = chunk_size ? chunk_size : ssd_fwd_chosen_chunk_size(d, dtype);
+    p.T = chunk_size ? chunk_size : chunk_size_peek(d, dtype);
     if (p.T <= 0)
         return SSD_ERR_INVALID_ARG;
     const int64_t L = d.seqlen;

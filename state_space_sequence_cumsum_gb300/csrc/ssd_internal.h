@@ -131,13 +131,20 @@ bool fused_pair_enabled(const Geom &g);
 // also runs with the smaller hand-off plan's).  0: invalid arguments.
 size_t fwd_workspace_min_size(ssd_dims_t dims, ssd_dtype_t dtype, int chunk_size,
                               int want_chunk_states);
+// The chunk size ssd_fwd(chunk_size = 0) would use now, without fixing the
+// choice (the cached one, else the static rule); 0 for invalid arguments.
+int chunk_size_peek(ssd_dims_t dims, ssd_dtype_t dtype);
 // Scratch of the head-pair kernel: with allow_prefill, that of the plan it
 // prefers (the prefilled segments where they apply, which also hold G and
 // dt^T); without, that of the hand-off plan, the least it runs with.
 size_t pair_tc_scratch_bytes(const Geom &g, bool allow_prefill = true);
+// True when the head-pair kernel would run the prefilled-segment plan for g.
+bool pair_tc_prefers_prefill(const Geom &g);
+// allow_prefill = false keeps the hand-off plan even where the prefilled one
+// applies and fits (the chunk-size tuner times both).
 cudaError_t launch_fused_pair_tc(const void *x, const void *Bm, const void *Cm, const float *dt,
                                  const float *A, const float *D, const float *init, float *states,
                                  float *final_state, void *y, const Geom &g, void *scratch,
-                                 size_t scratch_bytes, cudaStream_t st);
+                                 size_t scratch_bytes, cudaStream_t st, bool allow_prefill = true);
 
 }  // namespace ssd

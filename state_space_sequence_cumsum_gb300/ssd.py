@@ -16,8 +16,9 @@ from ._lib import SsdError, check, dims as _dims
 
 __all__ = ["ssd_chunk_cumsum", "ssd_state_pass", "ssd_chunk_out", "ssd_state_out", "ssd_fwd",
            "ssd_fwd_path", "ssd_fwd_plan", "ssd_fwd_staged",
-           "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_stream_status",
-           "ssd_fwd_host",
+           "ssd_fwd_workspace_size", "ssd_fwd_chosen_chunk_size", "ssd_fwd_chunk_size_was_timed",
+           "ssd_stream_status",
+           "ssd_fwd_host", "ssd_segment_summary", "ssd_carry_in", "ssd_fwd_context_parallel",
            "ssd_status_string", "ssd_decode_step", "ssd_bwd", "ssd_gated_rmsnorm",
            "SsdFunction", "SsdError",
            "Workspace"]
@@ -218,8 +219,17 @@ def ssd_fwd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, dtyp
 
 
 def ssd_fwd_chosen_chunk_size(batch, seqlen, nheads, headdim, dstate, ngroups, dtype) -> int:
+    """The chunk size ssd_fwd(chunk_size=0) uses for this shape; fixes the
+    choice if no call has fixed it yet (see include/ssd.h)."""
     code = _lib.SSD_BF16 if dtype == torch.bfloat16 else _lib.SSD_F32
     return int(_lib.load().ssd_fwd_chosen_chunk_size(
+        _dims(batch, seqlen, nheads, headdim, dstate, ngroups), code))
+
+
+def ssd_fwd_chunk_size_was_timed(batch, seqlen, nheads, headdim, dstate, ngroups, dtype) -> bool:
+    """True if this shape's chunk size was fixed by timing the candidates."""
+    code = _lib.SSD_BF16 if dtype == torch.bfloat16 else _lib.SSD_F32
+    return bool(_lib.load().ssd_fwd_chunk_size_was_timed(
         _dims(batch, seqlen, nheads, headdim, dstate, ngroups), code))
 
 
@@ -254,10 +264,13 @@ def ssd_fwd(x, dt, A, B, C, D, chunk_size=0, initial_state=None, return_final_st
         _f32(t, n)
     code = _dtype_code(x)
     lib = _lib.load()
-    T = int(chunk_size) or int(lib.ssd_fwd_chosen_chunk_size(d, code))
-    if T <= 0:
-        raise SsdError(_lib.SSD_ERR_INVALID_ARG, "ssd_fwd")
-    nc = (d.seqlen + T - 1) // T
+    T = int(chunk_size)
+    want_states = chunk_states is not None or return_chunk_states
+    if T == 0 and want_states:
+        # the chunk states' count depends on the chunk size: fix the choice now
+        T = int(lib.ssd_fwd_chosen_chunk_size(d, code))
+        if T <= 0:
+            raise SsdError(_lib.SSD_ERR_INVALID_ARG, "ssd_fwd")
     dev = x.device
     if y is None:
         y = torch.empty_like(x)
@@ -265,8 +278,11 @@ def ssd_fwd(x, dt, A, B, C, D, chunk_size=0, initial_state=None, return_final_st
         final_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate), device=dev,
                                   dtype=torch.float32)
     if chunk_states is None and return_chunk_states:
+        nc = (d.seqlen + T - 1) // T
         chunk_states = torch.empty((d.batch, d.nheads, nc, d.headdim, d.dstate), device=dev,
                                    dtype=torch.float32)
+    # chunk_size 0 without chunk states: the library chooses (and the first
+    # such call for a shape times the candidates on these buffers)
     nbytes = int(lib.ssd_fwd_workspace_size(d, code, T, int(chunk_states is not None)))
     ws = (workspace or Workspace()).get(nbytes, dev)
     check(lib.ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
@@ -384,7 +400,8 @@ def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk
 
     if plan["kernels"] == ["fused_pair"]:
         mark(0)
-        ssd_fwd(x, dt, A, B, C, D, chunk_size=T, initial_state=initial_state, y=y,
+        ssd_fwd(x, dt, A, B, C, D, chunk_size=plan.get("call_chunk_size", T),
+                initial_state=initial_state, y=y,
                 final_state=final_state, chunk_states=chunk_states,
                 return_final_state=final_state is not None,
                 return_chunk_states=chunk_states is not None, workspace=workspace, stream=s)
@@ -412,6 +429,88 @@ def ssd_fwd_staged(plan, x, dt, A, B, C, D, initial_state, y, final_state, chunk
     ssd_chunk_out(x, B, C, dtT, Gc, states, D, T, y=y, stream=s)
     mark(3)
     return y, final_state, chunk_states
+
+
+def ssd_segment_summary(x, dt, A, B, chunk_size, workspace: "Workspace | None" = None,
+                        stream=None):
+    """Step 1 of the sequence-sharded forward: this segment's end state from a
+    zero state [batch, H, P, S] f32 and its total decay [batch, H] f32 (log2
+    units).  Returns (seg_state, seg_decay)."""
+    d = _geom(x, B)
+    code = _dtype_code(x)
+    lib = _lib.load()
+    dev = x.device
+    seg_state = torch.empty((d.batch, d.nheads, d.headdim, d.dstate), device=dev,
+                            dtype=torch.float32)
+    seg_decay = torch.empty((d.batch, d.nheads), device=dev, dtype=torch.float32)
+    nbytes = int(lib.ssd_segment_summary_workspace_size(d, code, int(chunk_size)))
+    if nbytes == 0:
+        raise SsdError(_lib.SSD_ERR_INVALID_ARG, "ssd_segment_summary")
+    ws = (workspace or Workspace()).get(nbytes, dev)
+    check(lib.ssd_segment_summary(_ptr(x), _ptr(_f32(dt, "dt")), _ptr(_f32(A, "A")), _ptr(B),
+                                  _ptr(seg_state), _ptr(seg_decay), d, code, int(chunk_size),
+                                  _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream)),
+          "ssd_segment_summary")
+    return seg_state, seg_decay
+
+
+def ssd_carry_in(seg_states, seg_decays, upto, initial_state=None, out=None, stream=None):
+    """Step 3 of the sequence-sharded forward: the state carried into segment
+    `upto` from the gathered summaries seg_states [R, batch, H, P, S] and
+    seg_decays [R, batch, H] (f32, one entry per segment in sequence order)
+    and the sequence's initial state (None: zeros).  Returns h_in."""
+    R, b, H, P, S = seg_states.shape
+    if tuple(seg_decays.shape) != (R, b, H):
+        raise ValueError("seg_decays must be [segments, batch, nheads]")
+    if out is None:
+        out = torch.empty((b, H, P, S), device=seg_states.device, dtype=torch.float32)
+    d = _dims(b, 1, H, P, S, 1)
+    check(_lib.load().ssd_carry_in(_ptr(_f32(seg_states, "seg_states")),
+                                   _ptr(_f32(seg_decays, "seg_decays")),
+                                   _ptr(_f32(initial_state, "initial_state")), int(R), int(upto),
+                                   _ptr(out), d, _stream(stream)),
+          "ssd_carry_in")
+    return out
+
+
+def ssd_fwd_context_parallel(x, dt, A, B, C, D, chunk_size, initial_state=None, group=None,
+                             return_chunk_states=False, workspace: "Workspace | None" = None,
+                             stream=None):
+    """Sequence-sharded forward over the ranks of a torch.distributed group:
+    rank r holds the r-th contiguous segment of every sequence (x, dt, B, C
+    of its tokens; A, D and the sequence's initial state are the same on
+    every rank).  One all-gather of the per-segment summaries, then each rank
+    runs its segment from its carried-in state.  Returns this segment's
+    (y, final_state, chunk_states or None); the last rank's final state is the
+    sequence's.  With chunk states, every segment but the last must be a
+    whole number of chunks for them to line up with the unsharded run's."""
+    import torch.distributed as dist
+    R = dist.get_world_size(group)
+    r = dist.get_rank(group)
+    b, _, H, P = x.shape
+    Sd = B.shape[3]
+    n_state = b * H * P * Sd
+    if r < R - 1:
+        s_r, d_r = ssd_segment_summary(x, dt, A, B, chunk_size, workspace=workspace,
+                                       stream=stream)
+        payload = torch.cat([s_r.reshape(-1), d_r.reshape(-1)])
+    else:  # no later segment needs the last one's summary
+        payload = torch.zeros(n_state + b * H, device=x.device, dtype=torch.float32)
+    # the exchange: CUDA tensors for NCCL, host tensors for other backends
+    on_dev = dist.get_backend(group) == "nccl"
+    if not on_dev and payload.is_cuda:
+        s = stream if stream is not None else torch.cuda.current_stream(x.device)
+        s.synchronize()
+        payload = payload.cpu()
+    parts = [torch.empty_like(payload) for _ in range(R)]
+    dist.all_gather(parts, payload, group=group)
+    allp = torch.stack(parts).to(x.device, non_blocking=False)
+    seg_states = allp[:, :n_state].reshape(R, b, H, P, Sd).contiguous()
+    seg_decays = allp[:, n_state:].reshape(R, b, H).contiguous()
+    h_in = ssd_carry_in(seg_states, seg_decays, r, initial_state=initial_state, stream=stream)
+    return ssd_fwd(x, dt, A, B, C, D, chunk_size=chunk_size, initial_state=h_in,
+                   return_final_state=True, return_chunk_states=return_chunk_states,
+                   workspace=workspace, stream=stream)
 
 
 def ssd_stream_status(stream=None) -> int:

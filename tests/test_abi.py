@@ -111,6 +111,29 @@ def test_auto_chunk_size_is_supported(lib):
         assert T in (64, 128, 256)
 
 
+def test_auto_chunk_size_is_fixed_by_the_first_query(lib):
+    """Without a timed call, the first query fixes the static choice; it then
+    never changes, and the chunk_size-0 workspace becomes that choice's."""
+    for code, want in ((0, 128), (1, 128)):
+        d = _lib.dims(3, 777, 6, 64, 128, 3)  # a shape no other test uses
+        before = lib.ssd_fwd_workspace_size(d, code, 0, 0)
+        assert lib.ssd_fwd_chunk_size_was_timed(d, code) == 0
+        T = lib.ssd_fwd_chosen_chunk_size(d, code)
+        assert T == want
+        assert lib.ssd_fwd_chosen_chunk_size(d, code) == T
+        assert lib.ssd_fwd_chunk_size_was_timed(d, code) == 0
+        after = lib.ssd_fwd_workspace_size(d, code, 0, 0)
+        assert after == lib.ssd_fwd_workspace_size(d, code, T, 0)
+        # before the choice was fixed the size covered every candidate
+        assert before >= after
+        assert lib.ssd_fwd_path(d, code, 0, 0) == lib.ssd_fwd_path(d, code, T, 0)
+    # f32 sequences of at most 64 tokens take 64
+    assert lib.ssd_fwd_chosen_chunk_size(_lib.dims(1, 50, 2, 16, 16, 1), 1) == 64
+    # invalid arguments
+    assert lib.ssd_fwd_chosen_chunk_size(_lib.dims(0, 50, 2, 16, 16, 1), 0) == 0
+    assert lib.ssd_fwd_chosen_chunk_size(_lib.dims(1, 50, 2, 16, 16, 1), 7) == 0
+
+
 def test_decode_step_validation(lib):
     before = lib.ssd_launch_count()
     d1 = _lib.dims(2, 1, 4, 16, 32, 2)

@@ -113,6 +113,64 @@ def test_auto_chunk_size_and_no_states():
     assert_parity(fin, ref["final_state"], torch.bfloat16, "final")
 
 
+def test_auto_chunk_size_is_timed_then_fixed():
+    """chunk_size 0: the first call without chunk states times the candidates
+    {64, 128, 256} (section "Mamba-2 性能优化": the best configuration is
+    searched per shape) and fixes the fastest; later calls, and calls that
+    return chunk states, use that choice."""
+    shape = (2, 1500, 6, 64, 128, 1, torch.bfloat16)  # a shape no other test uses
+    inp = case_inputs(*shape[:6], 128, seed=23)
+    g = to_gpu(inp)
+    args = (g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"])
+    assert not ssd.ssd_fwd_chunk_size_was_timed(*shape)
+    y, fin, _ = ssd.ssd_fwd(*args, chunk_size=0)
+    torch.cuda.synchronize()
+    assert ssd.ssd_stream_status() == 0
+    assert ssd.ssd_fwd_chunk_size_was_timed(*shape)
+    T = ssd.ssd_fwd_chosen_chunk_size(*shape)
+    assert T in (64, 128, 256)
+    ref = oracle_run(inp, T, want_states=True)
+    assert_parity(y, ref["y"], torch.bfloat16, "y")
+    assert_parity(fin, ref["final_state"], torch.bfloat16, "final")
+    y2, fin2, st = ssd.ssd_fwd(*args, chunk_size=0, return_chunk_states=True)
+    assert ssd.ssd_fwd_chosen_chunk_size(*shape) == T
+    assert st.shape[2] == (1500 + T - 1) // T
+    assert_parity(y2, ref["y"], torch.bfloat16, "y (second call)")
+    assert_parity(st, ref["chunk_states"], torch.bfloat16, "chunk_states")
+
+
+def test_auto_chunk_size_with_chunk_states_first_keeps_the_static_choice():
+    shape = (1, 900, 4, 64, 64, 2, torch.bfloat16)  # a shape no other test uses
+    inp = case_inputs(*shape[:6], 128, init="randn", seed=29)
+    g = to_gpu(inp)
+    y, fin, st = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=0,
+                             initial_state=g["init"], return_chunk_states=True)
+    assert not ssd.ssd_fwd_chunk_size_was_timed(*shape)
+    T = ssd.ssd_fwd_chosen_chunk_size(*shape)
+    assert T == 128 and st.shape[2] == (900 + T - 1) // T
+    ref = oracle_run(inp, T, want_states=True)
+    assert_parity(y, ref["y"], torch.bfloat16, "y")
+    assert_parity(st, ref["chunk_states"], torch.bfloat16, "chunk_states")
+    # a later call without states does not re-time a fixed choice
+    ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=0,
+                initial_state=g["init"])
+    assert not ssd.ssd_fwd_chunk_size_was_timed(*shape)
+
+
+def test_auto_chunk_size_f32_timed():
+    shape = (1, 333, 3, 32, 48, 1, torch.float32)  # a shape no other test uses
+    inp = case_inputs(*shape[:6], 64, dtype=torch.float32, init="randn", seed=31)
+    g = to_gpu(inp)
+    y, fin, _ = ssd.ssd_fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=0,
+                            initial_state=g["init"])
+    assert ssd.ssd_fwd_chunk_size_was_timed(*shape)
+    T = ssd.ssd_fwd_chosen_chunk_size(*shape)
+    assert T in (64, 128, 256)
+    ref = oracle_run(inp, T)
+    assert_parity(y, ref["y"], torch.float32, "y")
+    assert_parity(fin, ref["final_state"], torch.float32, "final")
+
+
 def test_two_halves_with_carried_state_equal_one_run():
     """final_state of call 1 fed as init of call 2 reproduces the single run
     (section "Kernel 2": the final state is the next call's init_state)."""

@@ -12,8 +12,9 @@ every sampled head keeps its own B and C.
 Workloads: the 2.7B-layer shape (B 4, L 4096, H 80, P 64, S 128, chunk 256),
 the long grouped shape with an initial state (B 2, L 32768, H 64, S 256,
 G 8), the extreme length with every chunk state (B 1, L 262144, H 32,
-S 512, chunk 128) and points of the length x dstate sweep with the chunk
-size left to the library, including the ragged L = 4095.
+S 512, chunk 128) and every point of the length x dstate sweep (L 1K-256K
+x S 64-512, 256K tokens) with the chunk size left to the library's tuner,
+plus the ragged L = 4095.
 """
 import pytest
 import torch
@@ -73,6 +74,7 @@ def run_full(shape: Shape, dtype, init, want_states, chunk_size, batches, heads_
     if want_states:
         assert_parity(st.index_select(0, bd).index_select(1, hd), ref["chunk_states"], dtype,
                       "chunk_states")
+    return T
 
 
 def test_layer_2p7b_shape():
@@ -92,14 +94,29 @@ def test_extreme_length_all_chunk_states():
     run_full(EXTREME_256K, torch.bfloat16, "zero", True, 128, [0], {0: [0, 15, 31]})
 
 
-@pytest.mark.parametrize("L,S,batches,heads", [
-    (4095, 128, [0, 63], [0, 31, 63]),      # ragged last chunk, B 64
-    (1024, 64, [0, 255], [7, 42]),          # short sequences, B 256
-    (16384, 256, [5], [1, 62]),
-    (65536, 512, [1], [5, 50]),             # S 512: tensor-core bound on the roofline
-    (262144, 128, [0], [3, 60]),
-])
-def test_length_dstate_sweep(L, S, batches, heads):
-    """batch x L = 256K tokens, 64 heads, P 64, G 1, chunk size chosen by the library."""
-    shape = sweep_shape(L, S, 128)
-    run_full(shape, torch.bfloat16, "zero", False, 0, batches, {0: heads})
+def sweep_sample(L: int, batch: int):
+    """Sampled (batch rows, heads) of one sweep point: about 256K-512K
+    sampled token-heads per point, first and last rows included."""
+    if L >= 65536:
+        return [batch - 1], [3, 60]
+    if L >= 16384:
+        return [1, batch - 1], [5, 50]
+    if L >= 4095:
+        return [0, batch // 2, batch - 1], [0, 31, 63]
+    return [0, 100, batch - 1], [7, 42, 63]
+
+
+SWEEP = [(L, S) for L in (1024, 4096, 16384, 65536, 262144) for S in (64, 128, 256, 512)]
+SWEEP.append((4095, 128))  # ragged last chunk, B 64
+
+
+@pytest.mark.parametrize("L,S", SWEEP, ids=[f"L{L}-S{S}" for L, S in SWEEP])
+def test_length_dstate_sweep(L, S):
+    """batch x L = 256K tokens, 64 heads, P 64, G 1, bf16; chunk size left to
+    the library (chunk_size 0), which times {64, 128, 256} on this very call
+    and keeps the fastest -- the launch configuration the benchmark times."""
+    shape = sweep_shape(L, S, 0)
+    batches, heads = sweep_sample(L, shape.batch)
+    T = run_full(shape, torch.bfloat16, "zero", False, 0, batches, {0: heads})
+    assert T in (64, 128, 256)
+    assert ssd.ssd_fwd_chunk_size_was_timed(shape.batch, L, 64, 64, S, 1, torch.bfloat16)
