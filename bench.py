@@ -61,6 +61,10 @@ WORKLOADS = {
     "long-B2-L32768-H64-P64-S256-G8-T256": (LONG_S256_G8, torch.bfloat16, "randn", False),
     "extreme-B1-L262144-H32-P64-S512-T128-states": (EXTREME_256K, torch.bfloat16, "zero", True),
     "pages-example-B4-L16384-H8-P64-S128-T128": (PAGES_EXAMPLE, torch.bfloat16, "zero", False),
+    # an eighth of the extreme-length shape (same kernels, 1.2 GB of chunk
+    # states): the size the profiles of its kernels are captured on
+    "extreme-slice-B1-L32768-H32-P64-S512-T128-states": (
+        Shape(1, 32768, 32, 64, 512, 1, 128), torch.bfloat16, "zero", True),
 }
 # the length x dstate sweep with the chunk size chosen by the library's tuner
 # (chunk_size 0: it times {64, 128, 256} once per shape before the warm-up)

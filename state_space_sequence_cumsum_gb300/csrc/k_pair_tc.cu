@@ -346,7 +346,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const uint32_t par = it & 1;
                     // CB overwrites the previous tile's CB, whose conversion
                     // ended before that tile's Y1 was issued
-                    if (!mbar_wait(&bar_bc, par, wait_ns)) {
+                    if (!mbar_spin(&bar_bc, par, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -356,7 +356,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
                                id_cb, ks > 0);
                     mma_commit(&bar_cb);
-                    if (!mbar_wait(&bar_xh, par, wait_ns) || !mbar_wait(&bar_h, par, wait_ns)) {
+                    if (!mbar_spin(&bar_xh, par, wait_ns) || !mbar_spin(&bar_h, par, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -366,6 +366,20 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     for (int ks = 0; ks < S / 16; ++ks)
                         mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2, 1u);
                     mma_commit(&bar_y2);
+                    // The state jump (hi, then lo) right after Y2, in one straight
+                    // run of MMAs: with Y2 it is the last reader of the B / C tiles,
+                    // the H buffers and the X_hat lo buffers, so their reuse for the
+                    // next tile can start as soon as it completes; the compute warps
+                    // build the next tile's H from its result while Y1 runs.
+                    if (do_state) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            mma_ss(tmem + Lay::t_st, desc_mn(d_bmn, u), desc_mn(d_hi, u), id_ds, 1u);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            mma_ss(tmem + Lay::t_st, desc_mn(d_bmn, u), desc_mn(d_lo, u), id_ds, 1u);
+                    }
+                    mma_commit(&bar_ds);
                     // Y1 once the scores are ready: both heads in one N = 128 MMA
                     // when both are factorized, else per head.
                     auto issue_y1 = [&]() {
@@ -392,40 +406,11 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         }
                         mma_commit(&bar_y);
                     };
-                    // The state jump (hi, lo) next: with Y2 it is the last reader of
-                    // the B / C tiles, so their reload for the next tile can start as
-                    // soon as it completes.  It goes in four groups of four MMAs;
-                    // between groups Y1 overtakes the rest of the jump as soon as the
-                    // scores are ready, since the tensor pipe runs in issue order and
-                    // the epilogue waits only for Y1.
-                    bool y1_sent = false;
-                    const int n_grp = do_state ? 4 : 0;
-#pragma unroll 1
-                    for (int grp = 0; grp <= n_grp; ++grp) {
-                        if (grp == n_grp)
-                            mma_commit(&bar_ds);
-                        if (!y1_sent) {
-                            bool ready = grp > 0 && mbar_test(&bar_sc, par);
-                            if (grp == n_grp && !ready) {
-                                if (!mbar_wait(&bar_sc, par, wait_ns)) {
-                                    ok = false;
-                                    break;
-                                }
-                                ready = true;
-                            }
-                            if (ready) {
-                                issue_y1();
-                                y1_sent = true;
-                            }
-                        }
-                        if (grp < n_grp) {
-                            const uint64_t db = d_bmn + (grp & 1) * (4 * 128);
-                            const uint64_t dxh = ((grp >> 1) ? d_lo : d_hi) + (grp & 1) * (4 * 128);
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                mma_ss(tmem + Lay::t_st, desc_mn(db, u), desc_mn(dxh, u), id_ds, 1u);
-                        }
+                    if (!mbar_spin(&bar_sc, par, wait_ns)) {
+                        ok = false;
+                        break;
                     }
+                    issue_y1();
                     if (!ok)
                         break;
                 }
@@ -434,7 +419,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 atomicOr(prm.status, 1u);
         }
     } else if (warp == 10) {
-        // ---------------- y store from the H buffers
+        // ---------------- y store from the X_hat lo buffers (its staging)
         if ((tid & 31) == 0) {
             prefetch_tmap(&tm_y);
             uint32_t it = 0;
@@ -447,8 +432,8 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                         ok = false;
                         break;
                     }
-                    tma4_store(&tm_y, smem + Lay::off_h, 0, w.h0, t * kTile, w.b);
-                    tma4_store(&tm_y, smem + Lay::off_h + kRegion, 0, w.h0 + 1, t * kTile, w.b);
+                    tma4_store(&tm_y, smem + Lay::off_xh + 2 * kRegion, 0, w.h0, t * kTile, w.b);
+                    tma4_store(&tm_y, smem + Lay::off_xh + 3 * kRegion, 0, w.h0 + 1, t * kTile, w.b);
                     bulk_commit();
                     bulk_wait_read();
                     mbar_arrive(&bar_hfree);
@@ -460,6 +445,13 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
     } else if (warp < kWarps) {
         // ---------------- compute: warpgroup k owns head h0 + k
+        //
+        // Order per tile `it` (the next tile is it + 1):
+        //   scores(it) -> G of it + 1 -> [state leaving the item] -> H(it + 1)
+        //   -> epilogue(it) -> X_hat(it + 1)
+        // so the next tile's H is built while Y1(it) runs on the tensor cores,
+        // and y(it) is staged in the X_hat lo buffers (free once the state
+        // jump of `it` is done), which leaves the H buffers to H(it + 1).
         const int k = warp >> 2, q = warp & 3;
         const int i = q * 32 + (tid & 31);
         const int row_lo = q * 32, row_hi = q * 32 + 31;
@@ -474,12 +466,12 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         const int tpc_mask = (1 << prm.tpc_shift) - 1;
 
         // dt of a tile for both heads (adjacent in the [B, L, H] input), copied
-        // one tile ahead by cp.async: thread i of warpgroup 0 copies row i's
+        // two tiles ahead by cp.async: thread i of warpgroup 0 copies row i's
         // pair of words into slot [parity][i][2].  Each thread waits for its
-        // copy before arriving at the X_hat barrier, so every compute thread
-        // may read the whole tile once it has passed that barrier.  G within
-        // the tile is then a prefix sum each warp computes with shuffles, so
-        // no separate cumsum pass is needed.
+        // copy before arriving at the X_hat barrier of the tile before it, so
+        // every compute thread may read the whole tile once it has passed that
+        // barrier.  G within the tile is then a prefix sum each warp computes
+        // with shuffles, so no separate cumsum pass is needed.
         float *raw_all = reinterpret_cast<float *>(smem + Lay::off_raw);
         const int lane_id = tid & 31;
         auto prefetch_dt = [&](const PItem &w, int t, uint32_t buf) {
@@ -534,405 +526,476 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tg.gL = pre;  // rows past the end add nothing
             return tg;
         };
-        const int n_my = s_plan.count;
-        PItem w_next{};
-        float a_next = 0.f, d_next = 0.f;  // A and D of the next item's head, loaded early
-        TileG nxt_g{};  // G of the tile about to start, formed during the previous tile
-        if (n_my > 0) {
-            w_next = my_item(prm, s_plan, 0);
-            prefetch_dt(w_next, w_next.t0, 0);
-            a_next = ld_early(prm.A + w_next.h0 + k);
-            d_next = ld_early(prm.D + w_next.h0 + k);
-            cp_async_wait_all();
-        }
-        // the first tile's dt is visible to all 256 compute threads
-        // (non-aligned form: the copies above leave lanes diverged)
-        asm volatile("barrier.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
-        if (n_my > 0)
-            nxt_g = tile_g(0, kLog2e * a_next);
-        uint32_t it = 0;
-        bool ok = true;
-        for (int j = 0; j < n_my && ok; ++j) {
-            const PItem w = w_next;
-            const int h = w.h0 + k;
-            const int64_t bh = (int64_t)w.b * prm.H + h;
-            const float Dh = d_next, a_l2 = kLog2e * a_next;
-            const bool more = j + 1 < n_my;
-            if (more) {
-                w_next = my_item(prm, s_plan, j + 1);
-                a_next = ld_early(prm.A + w_next.h0 + k);
-                d_next = ld_early(prm.D + w_next.h0 + k);
-            }
-            // true state = exp2(lp) * stored state: the per-tile decay is kept as
-            // this scalar instead of rescaling the state in TMEM every tile
-            float lp = 0.f;
-            for (int t = w.t0; t < w.t1; ++t, ++it) {
-                const int tau = t * kTile;
-                const int n = min(kTile, (int)g.L - tau);
-                const bool first = t == w.t0, last_item = t + 1 == w.t1;
-                const bool last_seq = t + 1 == prm.n_tiles;
-                const bool do_state = !last_seq || want_final;
-                const TileG cur = nxt_g;
-                const float gL = cur.gL, g0 = cur.g0, gi = cur.gi, dti = cur.dti;
-                // the next tile's dt, for its G formed while this tile's Y1 runs
-                if (!last_item)
-                    prefetch_dt(w, t + 1, (it + 1) & 1);
-                else if (more)
-                    prefetch_dt(w_next, w_next.t0, (it + 1) & 1);
-                // Reference gref of the factorized form: keep the stored state's
-                // scale (gref = -lp) while every exponent gref - g_j, g_i - gref
-                // stays within kRefRange; else fold the scale into the state with
-                // gref at the middle of the tile's range; beyond 2 kRefRange the
-                // exact per-element form for this head (gref = g_L).
-                const float gmin = fminf(g0, gL), gmax = fmaxf(g0, gL);
-                const bool keep = !first && -lp - gmin <= kRefRange && gmax + lp <= kRefRange;
-                const bool narrow = keep || gmax - gmin <= 2.f * kRefRange;
-                const float gref = keep ? -lp : (narrow ? 0.5f * (gmin + gmax) : gL);
-                const uint32_t par = it & 1;
 
-                // ---- per-head g / dt table (wide scores), mode
-                float *gtab = gtab_all + (par * 2 + k) * 256;
-                gtab[i] = gi;
-                gtab[128 + i] = dti;
-                if (i == 0)
-                    s_mode[par][k] = narrow ? 1 : 0;
-                // x landed; the previous tile's state jump and Y1 are done
-                if (!mbar_wait(&bar_x[k], par, wait_ns) || (it > 0 && !mbar_wait(&bar_ds, par ^ 1u, wait_ns))) {
+        // Position of a tile in this CTA's work: item j, tile t, and the
+        // item's head's A and D.
+        struct Pos {
+            PItem w;
+            int j, t;
+            float a, d;
+            bool valid;
+        };
+        const int n_my = s_plan.count;
+        auto first_pos = [&]() {
+            Pos p{};
+            p.valid = n_my > 0;
+            if (p.valid) {
+                p.j = 0;
+                p.w = my_item(prm, s_plan, 0);
+                p.t = p.w.t0;
+                p.a = ld_early(prm.A + p.w.h0 + k);
+                p.d = ld_early(prm.D + p.w.h0 + k);
+            }
+            return p;
+        };
+        auto next_pos = [&](const Pos &p) {
+            Pos n = p;
+            if (!p.valid)
+                return n;
+            if (p.t + 1 < p.w.t1) {
+                n.t = p.t + 1;
+                return n;
+            }
+            if (p.j + 1 >= n_my) {
+                n.valid = false;
+                return n;
+            }
+            n.j = p.j + 1;
+            n.w = my_item(prm, s_plan, n.j);
+            n.t = n.w.t0;
+            n.a = ld_early(prm.A + n.w.h0 + k);
+            n.d = ld_early(prm.D + n.w.h0 + k);
+            return n;
+        };
+
+        // One tile: its place, its G, and the decay reference chosen for it.
+        // Reference gref of the factorized form: keep the stored state's scale
+        // (gref = -lp) while every exponent gref - g_j, g_i - gref stays within
+        // kRefRange; else fold the scale into the state with gref at the middle
+        // of the tile's range; beyond 2 kRefRange the exact per-element form
+        // for this head (gref = g_L).
+        struct Tile {
+            PItem w;
+            int t, n;
+            uint32_t it;
+            bool first, last_item, last_seq, do_state, keep, narrow;
+            float gi, dti, gL, gref, Dh, lp;  // lp: the stored state's scale on entry
+            int64_t bh;
+        };
+        auto make_tile = [&](const Pos &p, uint32_t it, const TileG &tg, float lp) {
+            Tile c;
+            c.w = p.w;
+            c.t = p.t;
+            c.it = it;
+            c.n = min(kTile, (int)g.L - p.t * kTile);
+            c.first = p.t == p.w.t0;
+            c.last_item = p.t + 1 == p.w.t1;
+            c.last_seq = p.t + 1 == prm.n_tiles;
+            c.do_state = !c.last_seq || want_final;
+            c.gi = tg.gi;
+            c.dti = tg.dti;
+            c.gL = tg.gL;
+            const float gmin = fminf(tg.g0, tg.gL), gmax = fmaxf(tg.g0, tg.gL);
+            c.keep = !c.first && -lp - gmin <= kRefRange && gmax + lp <= kRefRange;
+            c.narrow = c.keep || gmax - gmin <= 2.f * kRefRange;
+            c.gref = c.keep ? -lp : (c.narrow ? 0.5f * (gmin + gmax) : tg.gL);
+            c.Dh = p.d;
+            c.lp = c.first ? 0.f : lp;
+            c.bh = (int64_t)p.w.b * prm.H + p.w.h0 + k;
+            return c;
+        };
+
+        // ---- X_hat = dt exp2(gref - g) x (hi, lo) and Y = D x / r (0 if wide).
+        // Packed bf16 arithmetic with the weight w split as w_hi + w_lo:
+        // hi = bf16(x w_hi); the rounding residual x w_hi - hi is exact in
+        // bf16 (x and w_hi carry 8 significant bits each), so
+        // lo = bf16(x w_lo + residual) leaves hi + lo within ~2^-16 of x w.
+        // hi and Y go out first; lo is held in registers until the previous
+        // tile's y store has read the lo buffers (its staging area).
+        auto build_xhat = [&](const Tile &c) -> bool {
+            const uint32_t par = c.it & 1;
+            float *gtab = gtab_all + (par * 2 + k) * 256;
+            gtab[i] = c.gi;
+            gtab[128 + i] = c.dti;
+            if (i == 0)
+                s_mode[par][k] = c.narrow ? 1 : 0;
+            if (!mbar_wait(&bar_x[k], par, wait_ns))
+                return false;
+            tc_fence_after();
+            const float e = ex2_approx(c.gref - c.gi);
+            const float wv = i < c.n ? c.dti * e : 0.f;
+            const float dsc = c.narrow ? c.Dh * e : 0.f;
+            const uint32_t whi = pack_bf16x2(wv, wv);
+            const float wv_lo = wv - bf_lo(whi);
+            const uint32_t wlo = pack_bf16x2(wv_lo, wv_lo);
+            const uint64_t dsc2 = f2_pack(__float_as_uint(dsc), __float_as_uint(dsc));
+            uint32_t lo_keep[8][4];
+#pragma unroll
+            for (int c2 = 0; c2 < 4; ++c2) {
+                uint32_t dx[16];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int ch = 2 * c2 + cc;
+                    const uint32_t off = sw128_offset(i, ch);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
+                    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t hi[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        hi[e2] = bf2_mul(vv[e2], whi);
+                        lo_keep[ch][e2] = bf2_fma(vv[e2], wlo, bf2_fma(vv[e2], whi, hi[e2] ^ 0x80008000u));
+                        f2_unpack(f2_mul(bf2_to_f2(vv[e2]), dsc2), dx[8 * cc + 2 * e2],
+                                  dx[8 * cc + 2 * e2 + 1]);
+                    }
+                    *reinterpret_cast<uint4 *>(s_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
+                tmem_st16(ty + 16 * c2, dx);
+            }
+            // the previous tile's y store has read the lo buffers
+            if (c.it > 0 && !mbar_wait(&bar_hfree, par ^ 1u, wait_ns))
+                return false;
+            if (c.do_state) {
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(s_lo + sw128_offset(i, ch)) =
+                        make_uint4(lo_keep[ch][0], lo_keep[ch][1], lo_keep[ch][2], lo_keep[ch][3]);
+            }
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            cp_async_wait_all();  // the dt copied for the tile after this one
+            if (!(prm.fault_skip_arrive && c.it == 0 && warp == 0))
+                warp_arrive(&bar_xh);
+            return true;
+        };
+
+        // ---- H = bf16(exp2(gref) h) for the factorized form, bf16(h) for the
+        // exact one (MN-major [s][p]).  The stored state is rewritten only
+        // when its scale is folded in: S <- exp2(lp) S, times exp2(g_L) if
+        // exact.  A non-first tile reads the state the previous tile's jump
+        // left (the caller waited for that jump); an item's first tile loads
+        // its start state (a later segment waits until its predecessor has
+        // published it).
+        auto build_h = [&](const Tile &c) -> bool {
+            if (c.first && c.w.seg > 0 && !prm.prefilled) {
+                const unsigned int *cnt = prm.seg_count + c.bh * prm.n_seg + c.w.seg - 1;
+                bool ready = ld_acquire_gpu(cnt) >= 4u;
+                const uint64_t t_start = globaltimer_ns();
+                while (!ready) {
+                    if (globaltimer_ns() - t_start > wait_ns)
+                        break;
+                    __nanosleep(256);
+                    ready = ld_acquire_gpu(cnt) >= 4u;
+                }
+                if (!ready)
+                    return false;
+            }
+            const bool fold = !c.keep;
+            const bool emit = prm.states_out && (c.t & tpc_mask) == 0;
+            if (srow) {
+                const float *src = nullptr;
+                if (c.first) {
+                    if (c.w.seg > 0)
+                        src = prm.seg_state + ((c.bh * prm.n_seg + c.w.seg - 1) * g.P) * g.S;
+                    else if (prm.init)
+                        src = prm.init + c.bh * g.P * g.S;
+                }
+                float *emit_dst =
+                    emit ? prm.states_out + ((c.bh * g.nc + (c.t >> prm.tpc_shift)) * g.P) * g.S
+                         : nullptr;
+                // The pending scale and the new reference scale are applied one
+                // after the other: their product can fall below the f32 range
+                // even though each scaled value does not.
+                const float pv = c.first ? 1.f : ex2_approx(c.lp);
+                const float eref = ex2_approx(c.gref);
+                const float hsc = c.narrow ? eref : 1.f;
+                // the whole 64-column state row in one TMEM round trip
+                uint32_t r[64];
+                if (c.first) {
+#pragma unroll
+                    for (int jj = 0; jj < 64; ++jj)
+                        r[jj] = __float_as_uint(src ? __ldcg(src + (int64_t)jj * S + i) : 0.f);
+                } else {
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq)
+                        tmem_ld16(tst + 16 * qq, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * qq));
+                    tmem_ld_wait();
+                }
+                if (emit_dst) {
+#pragma unroll
+                    for (int jj = 0; jj < 64; ++jj)
+                        emit_dst[(int64_t)jj * S + i] = pv * __uint_as_float(r[jj]);
+                }
+                // scaling runs on f32 pairs
+                auto scaled = [&](int jj, uint64_t s2, uint32_t &a, uint32_t &b) {
+                    f2_unpack(f2_mul(f2_pack(r[jj], r[jj + 1]), s2), a, b);
+                };
+                if (fold) {  // r <- the true state h
+                    const uint64_t pv2 = f2_pack(__float_as_uint(pv), __float_as_uint(pv));
+#pragma unroll
+                    for (int jj = 0; jj < 64; jj += 2)
+                        scaled(jj, pv2, r[jj], r[jj + 1]);
+                }
+                // keep: H = bf16(S); fold: H = bf16(hsc h)
+                const uint64_t hs2 = f2_pack(__float_as_uint(hsc), __float_as_uint(hsc));
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    uint32_t hp[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const int jj = 8 * cc + 2 * e2;
+                        uint32_t a = r[jj], b = r[jj + 1];
+                        if (!c.keep)
+                            scaled(jj, hs2, a, b);
+                        hp[e2] = pack_bf16x2(__uint_as_float(a), __uint_as_float(b));
+                    }
+                    *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, cc)) =
+                        make_uint4(hp[0], hp[1], hp[2], hp[3]);
+                }
+                if (fold && c.do_state) {  // stored state <- exp2(gref) h
+                    const uint64_t er2 = f2_pack(__float_as_uint(eref), __float_as_uint(eref));
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        uint32_t o[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 2)
+                            scaled(16 * qq + jj, er2, o[jj], o[jj + 1]);
+                        tmem_st16(tst + 16 * qq, o);
+                    }
+                }
+                if (fold && c.do_state)
+                    tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bar_h);
+            return true;
+        };
+
+        // ---- scores.  Shared masked CB (keys [64k, 64k + 64) here) when a
+        // head is factorized; the exact per-element scores of a wide head.
+        auto build_scores = [&](const Tile &c, const Pos &p_after_next) -> bool {
+            const uint32_t par = c.it & 1;
+            if (!mbar_wait(&bar_cb, par, wait_ns) || !mbar_wait(&bar_xh, par, wait_ns))
+                return false;
+            tc_fence_after();
+            // dt two tiles ahead, into this tile's buffer: every compute warp
+            // has formed this tile's G (it arrived at this tile's X_hat
+            // barrier after doing so)
+            if (p_after_next.valid)
+                prefetch_dt(p_after_next.w, p_after_next.t, par);
+            const int m0 = s_mode[par][0], m1 = s_mode[par][1];
+            if (m0 || m1) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t cbv[2][16];
+#pragma unroll
+                    for (int gq = 0; gq < 2; ++gq) {
+                        const int j0 = 64 * k + 32 * half + 16 * gq;
+                        if (j0 <= row_hi)
+                            tmem_ld16(tl + Lay::t_cb + j0, cbv[gq]);
+                    }
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int gq = 0; gq < 2; ++gq) {
+                        const int j0 = 64 * k + 32 * half + 16 * gq;
+                        uint32_t pk[8];
+                        if (j0 > row_hi) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                pk[e] = 0u;
+                        } else if (j0 + 15 < row_lo) {  // whole group below the diagonal
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                pk[e] = pack_bf16x2(__uint_as_float(cbv[gq][2 * e]),
+                                                    __uint_as_float(cbv[gq][2 * e + 1]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int jk = j0 + 2 * e;
+                                pk[e] = pack_bf16x2(jk <= i ? __uint_as_float(cbv[gq][2 * e]) : 0.f,
+                                                    jk + 1 <= i ? __uint_as_float(cbv[gq][2 * e + 1]) : 0.f);
+                            }
+                        }
+                        tmem_st8(tl + Lay::t_sc + j0 / 2, pk);
+                    }
+                }
+            }
+            if (!c.narrow) {
+                // exact scores CB_ij exp2(g_i - g_j) dt_j of this head, all keys
+                const float *gtab = gtab_all + (par * 2 + k) * 256;
+                const uint32_t region = (k == 0 && !m1) ? Lay::t_sc : Lay::t_wide;
+#pragma unroll 1
+                for (int j0 = 0; j0 < kTile; j0 += 16) {
+                    uint32_t cbv[16], pk[8];
+                    if (j0 <= row_hi) {  // warp-uniform
+                        tmem_ld16(tl + Lay::t_cb + j0, cbv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            float v2[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int jk = j0 + 2 * e + u;
+                                v2[u] = jk <= i ? __uint_as_float(cbv[2 * e + u]) *
+                                                      ex2_approx(c.gi - gtab[jk]) * gtab[128 + jk]
+                                                : 0.f;
+                            }
+                            pk[e] = pack_bf16x2(v2[0], v2[1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pk[e] = 0u;
+                    }
+                    tmem_st8(tl + region + j0 / 2, pk);
+                }
+                // Y = exp2(g_i) (C H^T) + D x, before the score product adds on
+                if (!mbar_wait(&bar_y2, par, wait_ns))
+                    return false;
+                tc_fence_after();
+                const float er = ex2_approx(c.gi);
+#pragma unroll
+                for (int c2 = 0; c2 < 4; ++c2) {
+                    uint32_t yv[16];
+                    tmem_ld16(ty + 16 * c2, yv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(sx + sw128_offset(i, 2 * c2 + cc));
+                        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const int o = 8 * cc + 2 * e2;
+                            yv[o] = __float_as_uint(er * __uint_as_float(yv[o]) + c.Dh * bf_lo(vv[e2]));
+                            yv[o + 1] =
+                                __float_as_uint(er * __uint_as_float(yv[o + 1]) + c.Dh * bf_hi(vv[e2]));
+                        }
+                    }
+                    tmem_st16(ty + 16 * c2, yv);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&bar_sc);
+            return true;
+        };
+
+        // ---- the state leaving an item: the next segment's start, or the
+        // final state (the caller waited for the item's last jump)
+        auto leave_state = [&](const Tile &c) {
+            const bool handoff = !c.last_seq && !prm.prefilled;
+            float *dst = handoff ? prm.seg_state + ((c.bh * prm.n_seg + c.w.seg) * g.P) * g.S
+                                 : ((c.last_seq && want_final) ? prm.final_state + c.bh * g.P * g.S
+                                                               : nullptr);
+            if (dst && srow) {
+                const float pscale = ex2_approx(c.gL - c.gref);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[32];
+                    tmem_ld16(tst + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(r));
+                    tmem_ld16(tst + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        __stcg(dst + (int64_t)(32 * half + jj) * S + i, pscale * __uint_as_float(r[jj]));
+                }
+            }
+            if (dst && handoff) {
+                __threadfence();
+                __syncwarp();
+                if ((tid & 31) == 0)
+                    atomicAdd(prm.seg_count + c.bh * prm.n_seg + c.w.seg, 1u);
+            }
+        };
+
+        // ---- epilogue: y = r Y, staged in this head's lo buffer (free once
+        // the tile's state jump is done; the caller waited for it)
+        auto epilogue = [&](const Tile &c) -> bool {
+            const uint32_t par = c.it & 1;
+            if (!mbar_wait(&bar_y, par, wait_ns))
+                return false;
+            tc_fence_after();
+            const float r = c.narrow ? ex2_approx(c.gi - c.gref) : 1.f;
+            const uint64_t r2 = f2_pack(__float_as_uint(r), __float_as_uint(r));
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t yv[32];
+                tmem_ld16(ty + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(yv));
+                tmem_ld16(ty + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(yv + 16));
+                tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        uint32_t a, b;
+                        f2_unpack(f2_mul(f2_pack(yv[8 * cc + 2 * e2], yv[8 * cc + 2 * e2 + 1]), r2), a, b);
+                        o[e2] = pack_bf16x2(__uint_as_float(a), __uint_as_float(b));
+                    }
+                    *reinterpret_cast<uint4 *>(s_lo + sw128_offset(i, 4 * half + cc)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bar_ys);
+            return true;
+        };
+
+        bool ok = true;
+        Pos p0 = first_pos();
+        if (p0.valid) {
+            Pos p1 = next_pos(p0);
+            Pos p2 = next_pos(p1);
+            prefetch_dt(p0.w, p0.t, 0);
+            cp_async_wait_all();
+            // the first tile's dt is visible to all 256 compute threads
+            // (non-aligned form: the copies above leave lanes diverged)
+            asm volatile("barrier.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+            Tile cur = make_tile(p0, 0, tile_g(0, kLog2e * p0.a), 0.f);
+            if (p1.valid)
+                prefetch_dt(p1.w, p1.t, 1);
+            ok = build_xhat(cur) && build_h(cur);
+            for (uint32_t it = 0; ok; ++it) {
+                if (!build_scores(cur, p2)) {
+                    ok = false;
+                    break;
+                }
+                TileG tg1{};
+                if (p1.valid)  // the next tile's G while the jump runs on the tensor cores
+                    tg1 = tile_g((it + 1) & 1, kLog2e * p1.a);
+
+                // this tile's state jump is done: the state, the H buffers and
+                // the lo buffers are free
+                if (!mbar_wait(&bar_ds, it & 1, wait_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-
-                // ---- X_hat = dt exp2(gref - g) x (hi, lo) and Y = D x / r (0 if wide).
-                // Packed bf16 arithmetic with the weight w split as w_hi + w_lo:
-                // hi = bf16(x w_hi); the rounding residual x w_hi - hi is exact in
-                // bf16 (x and w_hi carry 8 significant bits each), so
-                // lo = bf16(x w_lo + residual) leaves hi + lo within ~2^-16 of x w.
-                {
-                    const float e = ex2_approx(gref - gi);
-                    const float wv = i < n ? dti * e : 0.f;
-                    const float dsc = narrow ? Dh * e : 0.f;
-                    const uint32_t whi = pack_bf16x2(wv, wv);
-                    const float wv_lo = wv - bf_lo(whi);
-                    const uint32_t wlo = pack_bf16x2(wv_lo, wv_lo);
-                    const uint64_t dsc2 = f2_pack(__float_as_uint(dsc), __float_as_uint(dsc));
-#pragma unroll
-                    for (int c2 = 0; c2 < 4; ++c2) {
-                        uint32_t dx[16];
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            const int c = 2 * c2 + cc;
-                            const uint32_t off = sw128_offset(i, c);
-                            const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
-                            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-                            uint32_t hi[4], lo[4];
-#pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                hi[e2] = bf2_mul(vv[e2], whi);
-                                lo[e2] = bf2_fma(vv[e2], wlo, bf2_fma(vv[e2], whi, hi[e2] ^ 0x80008000u));
-                                f2_unpack(f2_mul(bf2_to_f2(vv[e2]), dsc2), dx[8 * cc + 2 * e2],
-                                          dx[8 * cc + 2 * e2 + 1]);
-                            }
-                            *reinterpret_cast<uint4 *>(s_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            if (do_state)
-                                *reinterpret_cast<uint4 *>(s_lo + off) =
-                                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        }
-                        tmem_st16(ty + 16 * c2, dx);
-                    }
-                }
-                fence_proxy_async_smem();
-                tmem_st_wait();
-                tc_fence_before();
-                cp_async_wait_all();  // the next tile's dt (see prefetch_dt)
-                if (!(prm.fault_skip_arrive && it == 0 && warp == 0))
-                    warp_arrive(&bar_xh);
-
-                // ---- a later segment waits until its predecessor published its state
-                if (first && w.seg > 0 && !prm.prefilled) {
-                    const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + w.seg - 1;
-                    bool ready = ld_acquire_gpu(cnt) >= 4u;
-                    const uint64_t t_start = globaltimer_ns();
-                    while (!ready) {
-                        if (globaltimer_ns() - t_start > wait_ns)
-                            break;
-                        __nanosleep(256);
-                        ready = ld_acquire_gpu(cnt) >= 4u;
-                    }
-                    if (!ready) {
+                if (cur.last_item && cur.do_state)
+                    leave_state(cur);
+                Tile nxt{};
+                if (p1.valid) {
+                    nxt = make_tile(p1, it + 1, tg1, cur.gL - cur.gref);
+                    if (!build_h(nxt)) {
                         ok = false;
                         break;
                     }
                 }
-                // the previous tile's y store has read the H buffers
-                if (it > 0 && !mbar_wait(&bar_hfree, par ^ 1u, wait_ns)) {
+                if (!epilogue(cur)) {
                     ok = false;
                     break;
                 }
-
-                // ---- H = bf16(exp2(gref) h) for the factorized form, bf16(h) for the
-                // exact one (MN-major [s][p]).  The stored state is rewritten only
-                // when its scale is folded in: S <- exp2(lp) S, times exp2(g_L) if exact.
-                {
-                    const bool fold = !keep;
-                    const bool emit = prm.states_out && (t & tpc_mask) == 0;
-                    if (srow) {
-                        const float *src = nullptr;
-                        if (first) {
-                            if (w.seg > 0)
-                                src = prm.seg_state + ((bh * prm.n_seg + w.seg - 1) * g.P) * g.S;
-                            else if (prm.init)
-                                src = prm.init + bh * g.P * g.S;
-                        }
-                        float *emit_dst =
-                            emit ? prm.states_out + ((bh * g.nc + (t >> prm.tpc_shift)) * g.P) * g.S
-                                 : nullptr;
-                        // The pending scale and the new reference scale are applied one
-                        // after the other: their product can fall below the f32 range
-                        // even though each scaled value does not.
-                        const float pv = first ? 1.f : ex2_approx(lp);
-                        const float eref = ex2_approx(gref);
-                        const float hsc = narrow ? eref : 1.f;
-                        // the whole 64-column state row in one TMEM round trip
-                        uint32_t r[64];
-                        if (first) {
-#pragma unroll
-                            for (int j = 0; j < 64; ++j)
-                                r[j] = __float_as_uint(src ? __ldcg(src + (int64_t)j * S + i) : 0.f);
-                        } else {
-#pragma unroll
-                            for (int qq = 0; qq < 4; ++qq)
-                                tmem_ld16(tst + 16 * qq, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * qq));
-                            tmem_ld_wait();
-                        }
-                        if (emit_dst) {
-#pragma unroll
-                            for (int j = 0; j < 64; ++j)
-                                emit_dst[(int64_t)j * S + i] = pv * __uint_as_float(r[j]);
-                        }
-                        // scaling runs on f32 pairs
-                        auto scaled = [&](int j, uint64_t s2, uint32_t &a, uint32_t &b) {
-                            f2_unpack(f2_mul(f2_pack(r[j], r[j + 1]), s2), a, b);
-                        };
-                        if (fold) {  // r <- the true state h
-                            const uint64_t pv2 = f2_pack(__float_as_uint(pv), __float_as_uint(pv));
-#pragma unroll
-                            for (int j = 0; j < 64; j += 2)
-                                scaled(j, pv2, r[j], r[j + 1]);
-                        }
-                        // keep: H = bf16(S); fold: H = bf16(hsc h)
-                        const uint64_t hs2 = f2_pack(__float_as_uint(hsc), __float_as_uint(hsc));
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint32_t hp[4];
-#pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                const int j = 8 * c + 2 * e2;
-                                uint32_t a = r[j], b = r[j + 1];
-                                if (!keep)
-                                    scaled(j, hs2, a, b);
-                                hp[e2] = pack_bf16x2(__uint_as_float(a), __uint_as_float(b));
-                            }
-                            *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, c)) =
-                                make_uint4(hp[0], hp[1], hp[2], hp[3]);
-                        }
-                        if (fold && do_state) {  // stored state <- exp2(gref) h
-                            const uint64_t er2 = f2_pack(__float_as_uint(eref), __float_as_uint(eref));
-#pragma unroll
-                            for (int qq = 0; qq < 4; ++qq) {
-                                uint32_t o[16];
-#pragma unroll
-                                for (int j = 0; j < 16; j += 2)
-                                    scaled(16 * qq + j, er2, o[j], o[j + 1]);
-                                tmem_st16(tst + 16 * qq, o);
-                            }
-                        }
-                    }
-                    lp = gL - gref;
-                    if (fold && do_state)
-                        tmem_st_wait();
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                warp_arrive(&bar_h);
-
-                // ---- scores.  Shared masked CB (keys [64k, 64k + 64) here) when a
-                // head is factorized; the exact per-element scores of a wide head.
-                if (!mbar_wait(&bar_cb, par, wait_ns) || !mbar_wait(&bar_xh, par, wait_ns)) {
+                if (!p1.valid)
+                    break;
+                if (!build_xhat(nxt)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                {
-                    const int m0 = s_mode[par][0], m1 = s_mode[par][1];
-                    if (m0 || m1) {
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            uint32_t cbv[2][16];
-#pragma unroll
-                            for (int gq = 0; gq < 2; ++gq) {
-                                const int j0 = 64 * k + 32 * half + 16 * gq;
-                                if (j0 <= row_hi)
-                                    tmem_ld16(tl + Lay::t_cb + j0, cbv[gq]);
-                            }
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int gq = 0; gq < 2; ++gq) {
-                                const int j0 = 64 * k + 32 * half + 16 * gq;
-                                uint32_t pk[8];
-                                if (j0 > row_hi) {
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e)
-                                        pk[e] = 0u;
-                                } else if (j0 + 15 < row_lo) {  // whole group below the diagonal
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e)
-                                        pk[e] = pack_bf16x2(__uint_as_float(cbv[gq][2 * e]),
-                                                            __uint_as_float(cbv[gq][2 * e + 1]));
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        const int j = j0 + 2 * e;
-                                        pk[e] = pack_bf16x2(j <= i ? __uint_as_float(cbv[gq][2 * e]) : 0.f,
-                                                            j + 1 <= i ? __uint_as_float(cbv[gq][2 * e + 1]) : 0.f);
-                                    }
-                                }
-                                tmem_st8(tl + Lay::t_sc + j0 / 2, pk);
-                            }
-                        }
-                    }
-                    if (!narrow) {
-                        // exact scores CB_ij exp2(g_i - g_j) dt_j of this head, all keys
-                        const uint32_t region = (k == 0 && !m1) ? Lay::t_sc : Lay::t_wide;
-#pragma unroll 1
-                        for (int j0 = 0; j0 < kTile; j0 += 16) {
-                            uint32_t cbv[16], pk[8];
-                            if (j0 <= row_hi) {  // warp-uniform
-                                tmem_ld16(tl + Lay::t_cb + j0, cbv);
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    float v2[2];
-#pragma unroll
-                                    for (int u = 0; u < 2; ++u) {
-                                        const int j = j0 + 2 * e + u;
-                                        v2[u] = j <= i ? __uint_as_float(cbv[2 * e + u]) *
-                                                             ex2_approx(gi - gtab[j]) * gtab[128 + j]
-                                                       : 0.f;
-                                    }
-                                    pk[e] = pack_bf16x2(v2[0], v2[1]);
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    pk[e] = 0u;
-                            }
-                            tmem_st8(tl + region + j0 / 2, pk);
-                        }
-                        // Y = exp2(g_i) (C H^T) + D x, before the score product adds on
-                        if (!mbar_wait(&bar_y2, par, wait_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const float er = ex2_approx(gi);
-#pragma unroll
-                        for (int c2 = 0; c2 < 4; ++c2) {
-                            uint32_t yv[16];
-                            tmem_ld16(ty + 16 * c2, yv);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int cc = 0; cc < 2; ++cc) {
-                                const uint4 v = *reinterpret_cast<const uint4 *>(sx + sw128_offset(i, 2 * c2 + cc));
-                                const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                                for (int e2 = 0; e2 < 4; ++e2) {
-                                    const int o = 8 * cc + 2 * e2;
-                                    yv[o] = __float_as_uint(er * __uint_as_float(yv[o]) + Dh * bf_lo(vv[e2]));
-                                    yv[o + 1] =
-                                        __float_as_uint(er * __uint_as_float(yv[o + 1]) + Dh * bf_hi(vv[e2]));
-                                }
-                            }
-                            tmem_st16(ty + 16 * c2, yv);
-                        }
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                warp_arrive(&bar_sc);
-                // the next tile's G while Y1 runs on the tensor cores
-                if (!last_item)
-                    nxt_g = tile_g((it + 1) & 1, a_l2);
-                else if (more)
-                    nxt_g = tile_g((it + 1) & 1, kLog2e * a_next);
-
-                // ---- epilogue: y = r Y, staged in this head's H buffer
-                if (!mbar_wait(&bar_y, par, wait_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                {
-                    const float r = narrow ? ex2_approx(gi - gref) : 1.f;
-                    const uint64_t r2 = f2_pack(__float_as_uint(r), __float_as_uint(r));
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t yv[32];
-                        tmem_ld16(ty + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(yv));
-                        tmem_ld16(ty + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(yv + 16));
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t o[4];
-#pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                uint32_t a, b;
-                                f2_unpack(f2_mul(f2_pack(yv[8 * c + 2 * e2], yv[8 * c + 2 * e2 + 1]), r2), a, b);
-                                o[e2] = pack_bf16x2(__uint_as_float(a), __uint_as_float(b));
-                            }
-                            *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, 4 * half + c)) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                warp_arrive(&bar_ys);
-
-                // ---- state leaving the item: the next segment's start, or the final state
-                if (do_state && last_item) {
-                    const bool handoff = !last_seq && !prm.prefilled;
-                    float *dst = handoff ? prm.seg_state + ((bh * prm.n_seg + w.seg) * g.P) * g.S
-                                         : ((last_seq && want_final) ? prm.final_state + bh * g.P * g.S
-                                                                     : nullptr);
-                    if (dst) {
-                        if (!mbar_wait(&bar_ds, par, wait_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        if (srow) {
-                            const float pscale = ex2_approx(lp);
-#pragma unroll
-                            for (int half = 0; half < 2; ++half) {
-                                uint32_t r[32];
-                                tmem_ld16(tst + 32 * half, *reinterpret_cast<uint32_t(*)[16]>(r));
-                                tmem_ld16(tst + 32 * half + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    __stcg(dst + (int64_t)(32 * half + j) * S + i,
-                                           pscale * __uint_as_float(r[j]));
-                            }
-                        }
-                    }
-                    if (handoff) {
-                        __threadfence();
-                        __syncwarp();
-                        if ((tid & 31) == 0)
-                            atomicAdd(prm.seg_count + bh * prm.n_seg + w.seg, 1u);
-                    }
-                }
+                cur = nxt;
+                p1 = p2;
+                p2 = next_pos(p2);
             }
         }
         if (!ok)

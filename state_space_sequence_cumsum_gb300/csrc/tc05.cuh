@@ -105,6 +105,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Bounded wait that never parks the thread: polls with test_wait, so the
+// waiter resumes as soon as the phase completes (try_wait may suspend the
+// thread for a while after the phase has completed).  For a lone issuing
+// thread on the critical path, whose polling costs the other warps little.
+__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = 2000000000ull)
+{
+    if (mbar_test(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity))
+            return true;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
 // ------------------------------------------------------------------ fences
 
 __device__ __forceinline__ void fence_proxy_async_smem()
