@@ -94,9 +94,9 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     __shared__ uint64_t bar_full[2], bar_empty[2], bar_x[2], bar_xfree[2];
     // MMA completions: CB complete; Y1 (and everything before) complete
     __shared__ uint64_t bar_cb, bar_y;
-    // compute warps (8 arrivals): H and the g / dt table written; scores
-    // written; y staged (per x buffer)
-    __shared__ uint64_t bar_h, bar_sc, bar_ys[2];
+    // compute warps (8 arrivals): H's rows of dstate block k written (block 0
+    // also the g / dt table); scores written; y staged (per x buffer)
+    __shared__ uint64_t bar_h[Lay::kSB], bar_sc, bar_ys[2];
     __shared__ uint32_t tmem_slot;
 
     const Geom &g = prm.g;
@@ -111,7 +111,8 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         mbar_init(&bar_cb, 1);
         mbar_init(&bar_y, 1);
-        mbar_init(&bar_h, kWarps);
+        for (int k = 0; k < Lay::kSB; ++k)
+            mbar_init(&bar_h[k], kWarps);
         mbar_init(&bar_sc, kWarps);
         fence_barrier_init();
     }
@@ -132,10 +133,22 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             prefetch_tmap(&tm_c);
             uint32_t it = 0, u = 0;
             bool ok = true;
+            // the f32 chunk state of an item (P x S, contiguous) into L2 ahead
+            // of the compute warps' loads of it: the first item's now, then
+            // each next item's as the current one starts
+            const uint32_t st_bytes = (uint32_t)(g.P * S) * 4u;
+            auto prefetch_state = [&](int item) {
+                if (item < prm.n_items) {
+                    const BItem v = big_item(prm, item);
+                    bulk_prefetch_l2(prm.states + ((v.bh * prm.nc + v.c) * g.P) * g.S, st_bytes);
+                }
+            };
+            prefetch_state(blockIdx.x);
             for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x, ++it) {
                 const BItem w = big_item(prm, item);
                 const int grp = w.h / g.hpg;
                 const uint32_t xs = it & 1;
+                prefetch_state(item + gridDim.x);
                 if (it >= 2 && !mbar_wait(&bar_xfree[xs], ((it >> 1) - 1) & 1)) {
                     ok = false;
                     break;
@@ -185,13 +198,12 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     for (int ks = 0; ks < 8; ++ks)
                         mma_ss(tmem + Lay::t_cb, desc_k(d_c, kRegion, ks), desc_k(d_b, kRegion, ks),
                                id_cb, (sb | ks) != 0);
-                    if (sb == 0) {  // H of this item written (and Y2 of the last one read)
-                        if (!mbar_wait(&bar_h, par)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                    // this block's rows of H written (and Y2 of the last item read H)
+                    if (!mbar_wait(&bar_h[sb], par)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
                     const uint64_t d_hb = d_h + ((uint32_t)(sb * 128 * 128) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
@@ -270,32 +282,34 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 gtab[i] = gi;
             else
                 gtab[128 + i] = dti;
+            // H one 128-row dstate block at a time, published per block so
+            // that block k's C H^T starts while the next rows are written: both
+            // warpgroups take every block, thread i its row 128 k + i and
+            // warpgroup wg the headdim columns [32 wg, 32 wg + 32)
             const float *src = prm.states + ((w.bh * prm.nc + w.c) * g.P) * g.S;
 #pragma unroll 1
-            for (int m = 0; m < Lay::kSB / 2 + (Lay::kSB & 1); ++m) {
-                const int s_row = wg * (Lay::kSB / 2 + (Lay::kSB & 1)) * 128 + m * 128 + i;
-                if (s_row < S) {
-                    float v[64];
+            for (int sb = 0; sb < Lay::kSB; ++sb) {
+                const int s_row = sb * 128 + i;
+                float v[32];
 #pragma unroll
-                    for (int p = 0; p < 64; ++p)
-                        v[p] = __ldcs(src + (int64_t)p * S + s_row);
+                for (int p = 0; p < 32; ++p)
+                    v[p] = __ldcs(src + (int64_t)(32 * wg + p) * S + s_row);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 o = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
-                                                   pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
-                                                   pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
-                                                   pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
-                        *reinterpret_cast<uint4 *>(s_h + sw128_offset(s_row, c)) = o;
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 o = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]),
+                                               pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                               pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                               pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+                    *reinterpret_cast<uint4 *>(s_h + sw128_offset(s_row, 4 * wg + c)) = o;
                 }
+                fence_proxy_async_smem();
+                warp_arrive(&bar_h[sb]);
             }
-            fence_proxy_async_smem();
-            warp_arrive(&bar_h);
 
             // ---- exact scores CB_ij exp2(g_i - g_j) dt_j (j <= i); warpgroup wg
             // converts keys [64 wg, 64 wg + 64).  The table is complete once all
-            // eight warps have arrived at bar_h.
-            if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_h, par)) {
+            // eight warps have arrived at bar_h[0].
+            if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_h[0], par)) {
                 ok = false;
                 break;
             }

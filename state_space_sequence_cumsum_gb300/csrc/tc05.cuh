@@ -414,6 +414,14 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
         "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// Prefetch of a contiguous global range into L2 (a bulk copy engine
+// operation; nothing lands in shared memory and nothing waits for it).
+// The address must be 16-byte aligned and the size a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gmem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the shared-memory source of every committed store has been read
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
