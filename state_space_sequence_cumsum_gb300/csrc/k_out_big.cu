@@ -47,7 +47,9 @@ struct BigLayout {
     static constexpr uint32_t off_h = off_x + 2 * kRegion;  // H [S][P] bf16, MN-major
     static constexpr uint32_t off_g = off_h + S * 128;       // g 128 | dt 128, f32
     static constexpr uint32_t bytes = off_g + 256 * 4;
-    // TMEM columns: CB (f32), bf16 scores (two per column), Y1, Y2
+    // TMEM columns: CB (f32), bf16 scores (two per column), Y1, Y2 (two
+    // buffers by item parity: the next item's C H^T may start before this
+    // item's epilogue has read its Y2)
     static constexpr uint32_t t_cb = 0, t_sc = 128, t_y1 = 192, t_y2 = 256;
     static_assert(S % 128 == 0 && S >= 256 && S <= 512, "dstate blocks");
     static_assert(bytes + 1024 + 512 <= 232448, "shared memory budget");
@@ -207,7 +209,7 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                     const uint64_t d_hb = d_h + ((uint32_t)(sb * 128 * 128) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma_ss(tmem + Lay::t_y2, desc_k(d_c, kRegion, ks), desc_mn(d_hb, ks), id_y2,
+                        mma_ss(tmem + Lay::t_y2 + 64 * par, desc_k(d_c, kRegion, ks), desc_mn(d_hb, ks), id_y2,
                                (sb | ks) != 0);
                     mma_commit(&bar_empty[s]);
                 }
@@ -265,27 +267,17 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             g_nx = i < w.n ? ld_early(prm.Gc + o) : 0.f;
             d_nx = i < w.n ? ld_early(prm.dtT + o) : 0.f;
         };
-        if ((int)blockIdx.x < prm.n_items)
-            load_gd(big_item(prm, blockIdx.x));
-        uint32_t it = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x, ++it) {
-            const BItem w = big_item(prm, item);
-            const uint32_t par = it & 1, xs = it & 1;
-            const float gi = g_nx, dti = d_nx;
-            if (item + (int)gridDim.x < prm.n_items)
-                load_gd(big_item(prm, item + gridDim.x));
-
-            // ---- g / dt table; H = bf16(h_c), MN-major [s][p].  The previous
-            // item's MMAs (Y2 reading H) are done: its epilogue waited for Y1.
+        // ---- g / dt table; H = bf16(h_c), MN-major [s][p], one 128-row dstate
+        // block at a time, published per block so that block k's C H^T starts
+        // while the next rows are written: both warpgroups take every block,
+        // thread i its row 128 k + i and warpgroup wg the headdim columns
+        // [32 wg, 32 wg + 32).  The caller has seen the previous item's C B^T
+        // and C H^T complete (bar_cb) and every warp's scores of it done.
+        auto build_h = [&](const BItem &w, float gi, float dti) {
             if (wg == 0)
                 gtab[i] = gi;
             else
                 gtab[128 + i] = dti;
-            // H one 128-row dstate block at a time, published per block so
-            // that block k's C H^T starts while the next rows are written: both
-            // warpgroups take every block, thread i its row 128 k + i and
-            // warpgroup wg the headdim columns [32 wg, 32 wg + 32)
             const float *src = prm.states + ((w.bh * prm.nc + w.c) * g.P) * g.S;
 #pragma unroll 1
             for (int sb = 0; sb < Lay::kSB; ++sb) {
@@ -305,6 +297,25 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 fence_proxy_async_smem();
                 warp_arrive(&bar_h[sb]);
             }
+        };
+        // Order per item k: scores(k), then the next item's table and H (they
+        // overlap Y1(k) and the next item's C B^T), then the epilogue of k.
+        float gi_cur = 0.f, dti_cur = 0.f;
+        if ((int)blockIdx.x < prm.n_items) {
+            load_gd(big_item(prm, blockIdx.x));
+            gi_cur = g_nx;
+            dti_cur = d_nx;
+            if ((int)(blockIdx.x + gridDim.x) < prm.n_items)
+                load_gd(big_item(prm, blockIdx.x + gridDim.x));
+            build_h(big_item(prm, blockIdx.x), gi_cur, dti_cur);
+        }
+        uint32_t it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x, ++it) {
+            const BItem w = big_item(prm, item);
+            const uint32_t par = it & 1, xs = it & 1;
+            const float gi = gi_cur;
+            const bool more = item + (int)gridDim.x < prm.n_items;
 
             // ---- exact scores CB_ij exp2(g_i - g_j) dt_j (j <= i); warpgroup wg
             // converts keys [64 wg, 64 wg + 64).  The table is complete once all
@@ -353,6 +364,21 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             tc_fence_before();
             warp_arrive(&bar_sc);
 
+            // ---- the next item's table and H: every warp is done with this
+            // item's table once bar_sc completes, and bar_cb covered this
+            // item's C H^T (the last reader of H)
+            if (more) {
+                if (!mbar_wait(&bar_sc, par)) {
+                    ok = false;
+                    break;
+                }
+                gi_cur = g_nx;
+                dti_cur = d_nx;
+                if (item + 2 * (int)gridDim.x < prm.n_items)
+                    load_gd(big_item(prm, item + 2 * gridDim.x));
+                build_h(big_item(prm, item + gridDim.x), gi_cur, dti_cur);
+            }
+
             // ---- epilogue: y = Y1 + exp2(g_i) Y2 + D x, written over x
             if (!mbar_wait(&bar_y, par) || !mbar_wait(&bar_x[xs], (it >> 1) & 1)) {
                 ok = false;
@@ -367,7 +393,7 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 for (int c16 = 0; c16 < 32; c16 += 16) {
                     uint32_t ra[16], rb[16];
                     tmem_ld16(tl + Lay::t_y1 + c0w + c16, ra);
-                    tmem_ld16(tl + Lay::t_y2 + c0w + c16, rb);
+                    tmem_ld16(tl + Lay::t_y2 + 64 * par + c0w + c16, rb);
                     tmem_ld_wait();
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
