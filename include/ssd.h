@@ -41,6 +41,10 @@
  *   ssd_stream_status() reads.
  * Threads: calls are thread-safe; the only shared host state is a
  *   mutex-guarded cache of TMA descriptors and tuning choices.
+ * Device lifetime: the library caches, per device, the device addresses of
+ *   its own __device__ arrays (the status word, the scratch array of
+ *   ssd_fwd_noalloc) for the life of the process; do not use it on a device
+ *   after cudaDeviceReset has been called there.
  * Supported sizes: 1 <= P <= 256, 1 <= S <= 512, 1 <= T <= 256, H % G == 0,
  *   L >= 0 (L == 0 copies init_state to final_state and launches nothing
  *   else).  The tensor-core (tcgen05) kernels serve bf16 with T a multiple
