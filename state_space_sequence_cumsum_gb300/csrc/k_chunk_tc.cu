@@ -112,6 +112,9 @@ struct Params {
     int n_seg;
     float *seg_state;          // [B*H*n_seg][P][S]
     unsigned int *seg_count;   // [B*H*n_seg], zero at launch
+    // prefilled: a state pass has already put every segment's start state in
+    // seg_state, so no segment waits for another and none hands off
+    int prefilled;
     unsigned int *status;
 };
 
@@ -462,7 +465,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 warp_arrive(&bar_xh);
 
                 // ---- a later segment waits until its predecessor published its state
-                if (MODE == kModeFused && first && chunk > 0) {
+                if (MODE == kModeFused && first && chunk > 0 && !prm.prefilled) {
                     const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + chunk - 1;
                     bool ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
                     const uint64_t t_start = globaltimer_ns();
@@ -654,7 +657,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 // ---- state leaving the item: the next segment's start, or the final state
                 if (do_state && last_item) {
                     float *dst = nullptr;
-                    const bool handoff = MODE == kModeFused && !last_seq;
+                    const bool handoff = MODE == kModeFused && !last_seq && !prm.prefilled;
                     if (handoff)
                         dst = prm.seg_state + ((bh * prm.n_seg + chunk) * g.P) * g.S;
                     else if (last_seq && want_final)
@@ -751,14 +754,49 @@ cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtenso
 struct SegPlan {
     int seg_tiles;
     int n_seg;
+    bool prefill;
     size_t state_bytes, count_bytes;
 };
+
+// Segments of the fused pass.  With at most half as many (batch, head)
+// sequences as SMs, segments that hand their states to one another run as a
+// wavefront (at most one segment of each sequence makes progress at a time),
+// so the sequences are cut into up to kMaxPrefillSeg segments of whole chunks
+// -- about eight items per SM, at least two chunks each -- whose start states
+// a segmented state pass computes first (the prefilled plan): every item is
+// then independent.  (With more sequences the extra state pass costs more
+// than the wavefront: B 2, L 32768, H 64, S 256 took 1.74 ms prefilled
+// against 1.39 ms with hand-offs; B 1, L 262144, H 64, S 256 took 6.17 ms
+// against 10.66 ms.)  Otherwise: enough hand-off segments for about eight
+// items per SM, none shorter than two tiles.
+constexpr int kMaxPrefillSeg = 64;  // segments the state pass's combine handles
 
 SegPlan seg_plan(const Geom &g)
 {
     SegPlan sp;
+    sp.prefill = false;
     const int64_t n_tiles = (g.L + kTile - 1) / kTile;
     const int64_t nbh = g.B * g.H;
+    const int tpc = g.T / kTile;
+    if (2 * nbh <= sm_count() && state_pass_tc_supported(g)) {
+        int64_t want = (8LL * sm_count() + nbh - 1) / nbh;
+        if (want > kMaxPrefillSeg)
+            want = kMaxPrefillSeg;
+        if (want * 2 * tpc > n_tiles)
+            want = n_tiles / (2 * tpc);
+        if (want >= 2) {
+            int64_t st = (n_tiles + want - 1) / want;
+            st = (st + tpc - 1) / tpc * tpc;
+            sp.seg_tiles = (int)st;
+            sp.n_seg = (int)((n_tiles + st - 1) / st);
+            if (sp.n_seg >= 2) {
+                sp.prefill = true;
+                sp.state_bytes = (size_t)(nbh * sp.n_seg * g.P * g.S) * sizeof(float);
+                sp.count_bytes = 0;
+                return sp;
+            }
+        }
+    }
     int64_t want = (8LL * sm_count() + nbh - 1) / nbh;
     want = want < 1 ? 1 : want;
     if (want > (n_tiles + 1) / 2)
@@ -798,13 +836,21 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
         prm.seg_tiles = sp.seg_tiles;
         prm.n_seg = sp.n_seg;
         prm.n_items = (int)(g.B * g.H * sp.n_seg);
+        prm.prefilled = sp.prefill ? 1 : 0;
         if (sp.n_seg > 1) {
             const size_t off = (sp.state_bytes + 255) / 256 * 256;
             if (!scratch || scratch_bytes < off + sp.count_bytes)
                 return cudaErrorInvalidValue;
             prm.seg_state = static_cast<float *>(scratch);
-            prm.seg_count = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + off);
-            cudaError_t e = cudaMemsetAsync(prm.seg_count, 0, sp.count_bytes, st);
+            cudaError_t e;
+            if (sp.prefill) {
+                // every segment's start state (segment 0's is the initial state)
+                e = launch_segment_starts_tc(x, Bm, dtT, Gc, h_src, prm.seg_state, sp.seg_tiles,
+                                             sp.n_seg, g, st);
+            } else {
+                prm.seg_count = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch) + off);
+                e = cudaMemsetAsync(prm.seg_count, 0, sp.count_bytes, st);
+            }
             if (e != cudaSuccess)
                 return e;
         }
