@@ -38,10 +38,11 @@
 //              TMEM lane i = 32 q + lane, warpgroup wg owns half of the
 //              columns of every per-tile step;
 //   warp 8     TMA loads of B, C and x tiles into a STAGES-deep ring
-//              (128-byte swizzle);
+//              (128-byte swizzle); a stage's B / C are reloaded as soon as
+//              the tile's state jump is done, its x once its y is stored;
 //   warp 9     MMA issue;
 //   warp 10    TMA store of y: the epilogue writes y over the x tile it has
-//              consumed, this warp stores it and then frees the stage.
+//              consumed, this warp stores it and then frees the x slot.
 // Every wait is bounded; a timeout sets the kernel status word and the role
 // leaves its loop.
 #include <cstdlib>
@@ -163,7 +164,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     // full: TMA landed; empty: stage free (MMA reads done + y store read);
     // ys: y of the stage's tile written to shared memory.
-    __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES], bar_ys[STAGES];
+    // per stage: B / C landed, x landed; B / C free (the tile's C B^T, C H^T
+    // and state jump done), x free (its y, staged over it, stored)
+    __shared__ uint64_t bar_full[STAGES], bar_full_x[STAGES], bar_empty[STAGES],
+        bar_empty_x[STAGES], bar_ys[STAGES];
     // MMA completions: cb (CB), y (Y1 and Y2), ds (state jump and all before)
     __shared__ uint64_t bar_cb, bar_y, bar_ds;
     // compute warps done with: X_hat and the g / dt table, H and the state
@@ -178,7 +182,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 2);
+            mbar_init(&bar_full_x[s], 1);
+            mbar_init(&bar_empty[s], 1);
+            mbar_init(&bar_empty_x[s], 1);
             mbar_init(&bar_ys[s], kComputeWarps);
         }
         mbar_init(&bar_cb, 1);
@@ -212,20 +218,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const int grp = w.h / g.hpg;
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     const int s = (int)(it % STAGES);
+                    // B / C as soon as the stage's previous tile no longer reads
+                    // them (its state jump done), x once that tile's y is stored
                     if (it >= STAGES &&
                         !mbar_wait(&bar_empty[s], ((it / STAGES) - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     uint8_t *st = smem + s * Lay::kStage;
-                    mbar_arrive_expect_tx(&bar_full[s], Lay::kStage);
+                    mbar_arrive_expect_tx(&bar_full[s], 2 * Lay::kB);
                     const int tok = t * kTile;
                     for (int r = 0; r < Lay::kSReg; ++r) {
                         tma4(st + r * kRegion, &tm_b, &bar_full[s], r * 64, grp, tok, w.b);
                         tma4(st + Lay::kB + r * kRegion, &tm_c, &bar_full[s], r * 64, grp, tok, w.b);
                     }
+                    if (it >= STAGES &&
+                        !mbar_wait(&bar_empty_x[s], ((it / STAGES) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bar_full_x[s], Lay::kX);
                     for (int r = 0; r < Lay::kPReg; ++r)
-                        tma4(st + 2 * Lay::kB + r * kRegion, &tm_x, &bar_full[s], r * 64, w.h, tok,
+                        tma4(st + 2 * Lay::kB + r * kRegion, &tm_x, &bar_full_x[s], r * 64, w.h, tok,
                              w.b);
                 }
             }
@@ -299,9 +313,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                                desc_mn(d_xh + ((part * Lay::kX) >> 4), ks), id_ds, 1u);
                         }
                         mma_commit(&bar_ds);
+                        // the last readers of this stage's B / C: its reload may start
+                        mma_commit(&bar_empty[s]);
                     };
-                    // X_hat is published before H, so it is ready here
-                    if (!mbar_wait(&bar_xh, par)) {
+                    // X_hat is published before H, so it is ready here; x itself
+                    // has landed too (Y1 reads raw x for a wide tile)
+                    if (!mbar_wait(&bar_xh, par) || !mbar_wait(&bar_full_x[s], (it / STAGES) & 1)) {
                         ok = false;
                         break;
                     }
@@ -319,7 +336,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         tc_fence_after();
                         issue_y1();
                     }
-                    mma_commit(&bar_empty[s]);
+                    if (!ok)
+                        break;
                 }
             }
             if (!ok)
@@ -344,7 +362,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         tma4_store(&tm_y, sy + r * kRegion, r * 64, w.h, t * kTile, w.b);
                     bulk_commit();
                     bulk_wait_read();
-                    mbar_arrive(&bar_empty[s]);
+                    mbar_arrive(&bar_empty_x[s]);
                 }
             }
             bulk_wait_all();
@@ -429,7 +447,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     s_mode[it & 1] = narrow ? 1 : 0;
                 // x landed; the previous tile's state jump (and everything
                 // before it: Y1 and Y2 reading X_hat and H) has completed
-                if (!mbar_wait(&bar_full[s], (it / STAGES) & 1) ||
+                if (!mbar_wait(&bar_full_x[s], (it / STAGES) & 1) ||
                     (it > 0 && !mbar_wait(&bar_ds, (it - 1) & 1))) {
                     ok = false;
                     break;
