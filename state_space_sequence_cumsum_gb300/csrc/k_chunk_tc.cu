@@ -24,7 +24,8 @@
 //               to zero without evaluating the exponent), bf16 into TMEM
 //   Y1  = scores X              N = P, K = 128, A operand from TMEM
 //   Y2  = C H^T, H = bf16(h_c)  N = P, K = S
-//   y   = Y1 + exp2(g_i) Y2 + D x      (f32 epilogue, bf16)
+//   y   = Y1 + exp2(g_i) Y2 + D x      (f32 epilogue, bf16; D x is written
+//                                       into Y1's accumulator before its MMAs)
 //   and, when a later tile needs the state: h <- exp2(g_L) h + B^T X_hat with
 //   X_hat = dt exp2(g_L - g) X split into bf16 hi + lo (two MMA passes); the
 //   state h^T [S, P] is an f32 TMEM accumulator.
@@ -162,12 +163,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    // full: TMA landed; empty: stage free (MMA reads done + y store read);
-    // ys: y of the stage's tile written to shared memory.
     // per stage: B / C landed, x landed; B / C free (the tile's C B^T, C H^T
-    // and state jump done), x free (its y, staged over it, stored)
+    // and state jump done), x free (X_hat built; for an exact tile, Y1 done)
     __shared__ uint64_t bar_full[STAGES], bar_full_x[STAGES], bar_empty[STAGES],
-        bar_empty_x[STAGES], bar_ys[STAGES];
+        bar_empty_x[STAGES];
+    // y staged in the X_hat lo buffer (compute warps); that buffer read by
+    // the y store
+    __shared__ uint64_t bar_ys, bar_lofree;
     // MMA completions: cb (CB), y (Y1 and Y2), ds (state jump and all before)
     __shared__ uint64_t bar_cb, bar_y, bar_ds;
     // compute warps done with: X_hat and the g / dt table, H and the state
@@ -184,9 +186,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_full_x[s], 1);
             mbar_init(&bar_empty[s], 1);
-            mbar_init(&bar_empty_x[s], 1);
-            mbar_init(&bar_ys[s], kComputeWarps);
+            mbar_init(&bar_empty_x[s], kComputeWarps);
         }
+        mbar_init(&bar_ys, kComputeWarps);
+        mbar_init(&bar_lofree, 1);
         mbar_init(&bar_cb, 1);
         mbar_init(&bar_y, 1);
         mbar_init(&bar_ds, 1);
@@ -247,9 +250,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 atomicOr(prm.status, 1u);
         }
     } else if (warp == 9) {
-        // ---------------- MMA issuer.  Per tile: CB; Y2 once H is ready; then
-        // Y1 (scores ready) and the state jump (X_hat ready) in whichever
-        // order their inputs arrive.
+        // ---------------- MMA issuer.  Per tile: CB; Y2 and the state jump as
+        // one straight run once H and X_hat are ready; Y1 once the scores are.
+        // The waits poll with test_wait (never parked).
         if ((tid & 31) == 0) {
             const uint32_t id_cb = idesc_bf16(128, 128, false, false);
             const uint32_t id_y1 = idesc_bf16(128, P, false, true);  // A (scores) from TMEM
@@ -283,7 +286,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
                                id_cb, ks > 0);
                     mma_commit(&bar_cb);
-                    if (!mbar_wait(&bar_h, par)) {
+                    // Y2 once H is built and X_hat too (X_hat comes after the
+                    // previous tile's epilogue has read Y2).  An exact tile's Y1
+                    // reads raw x: wait for it to have landed (its slot is held
+                    // until that Y1 is done; a factorized tile's slot may already
+                    // be reloading, and its MMAs never read raw x).
+                    if (!mbar_spin(&bar_h, par) || !mbar_spin(&bar_xh, par) ||
+                        (!s_mode[par] && !mbar_spin(&bar_full_x[s], (it / STAGES) & 1))) {
                         ok = false;
                         break;
                     }
@@ -292,49 +301,34 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int ks = 0; ks < S / 16; ++ks)
                         mma_ss(tmem + Lay::t_y2, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2,
                                ks > 0);
-                    auto issue_y1 = [&]() {
-                        const uint64_t d_y1b = s_mode[it & 1] ? d_xh : d_x;  // X_hat or raw x
+                    // the state jump right after Y2, in one straight run: with
+                    // them the tile's B / C are done with, so their reload starts
+                    if (do_state) {
 #pragma unroll
-                        for (int ks = 0; ks < kTile / 16; ++ks)
-                            mma_ts(tmem + Lay::t_y1, tmem + Lay::t_sc + ks * 8, desc_mn(d_y1b, ks),
-                                   id_y1, ks > 0);
-                        mma_commit(&bar_y);
-                    };
-                    auto issue_ds = [&]() {
-                        if (do_state) {
+                        for (int mb = 0; mb < Lay::kSBlk; ++mb)
 #pragma unroll
-                            for (int mb = 0; mb < Lay::kSBlk; ++mb)
+                            for (int part = 0; part < 2; ++part)
 #pragma unroll
-                                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                                    for (int ks = 0; ks < kTile / 16; ++ks)
-                                        mma_ss(tmem + Lay::t_st + mb * P,
-                                               desc_mn(d_bmn + ((2 * mb * kRegion) >> 4), ks),
-                                               desc_mn(d_xh + ((part * Lay::kX) >> 4), ks), id_ds, 1u);
-                        }
-                        mma_commit(&bar_ds);
-                        // the last readers of this stage's B / C: its reload may start
-                        mma_commit(&bar_empty[s]);
-                    };
-                    // X_hat is published before H, so it is ready here; x itself
-                    // has landed too (Y1 reads raw x for a wide tile)
-                    if (!mbar_wait(&bar_xh, par) || !mbar_wait(&bar_full_x[s], (it / STAGES) & 1)) {
+                                for (int ks = 0; ks < kTile / 16; ++ks)
+                                    mma_ss(tmem + Lay::t_st + mb * P,
+                                           desc_mn(d_bmn + ((2 * mb * kRegion) >> 4), ks),
+                                           desc_mn(d_xh + ((part * Lay::kX) >> 4), ks), id_ds, 1u);
+                    }
+                    mma_commit(&bar_ds);
+                    mma_commit(&bar_empty[s]);
+                    // Y1 (adding onto D x / r1) once the scores are converted
+                    if (!mbar_spin(&bar_scores, par)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (mbar_test(&bar_scores, par)) {
-                        tc_fence_after();
-                        issue_y1();
-                        issue_ds();
-                    } else {
-                        issue_ds();
-                        if (!mbar_wait(&bar_scores, par)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_y1();
+                    {
+                        const uint64_t d_y1b = s_mode[par] ? d_xh : d_x;  // X_hat or raw x
+#pragma unroll
+                        for (int ks = 0; ks < kTile / 16; ++ks)
+                            mma_ts(tmem + Lay::t_y1, tmem + Lay::t_sc + ks * 8, desc_mn(d_y1b, ks),
+                                   id_y1, 1u);
+                        mma_commit(&bar_y);
                     }
                     if (!ok)
                         break;
@@ -344,7 +338,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 atomicOr(prm.status, 1u);
         }
     } else if (warp == 10) {
-        // ---------------- y store: the epilogue left y in the stage's x region
+        // ---------------- y store: the epilogue left y in the X_hat lo buffer
         if ((tid & 31) == 0) {
             prefetch_tmap(&tm_y);
             uint32_t it = 0;
@@ -352,17 +346,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
                 const Item w = decode_item<MODE>(prm, item);
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
-                    const int s = (int)(it % STAGES);
-                    if (!mbar_wait(&bar_ys[s], (it / STAGES) & 1)) {
+                    if (!mbar_wait(&bar_ys, it & 1)) {
                         ok = false;
                         break;
                     }
-                    const uint8_t *sy = smem + s * Lay::kStage + 2 * Lay::kB;
+                    const uint8_t *sy = smem + Lay::off_xh + Lay::kX;  // the X_hat lo buffer
                     for (int r = 0; r < Lay::kPReg; ++r)
                         tma4_store(&tm_y, sy + r * kRegion, r * 64, w.h, t * kTile, w.b);
                     bulk_commit();
                     bulk_wait_read();
-                    mbar_arrive(&bar_empty_x[s]);
+                    mbar_arrive(&bar_lofree);
                 }
             }
             bulk_wait_all();
@@ -370,19 +363,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 atomicOr(prm.status, 1u);
         }
     } else if (warp < kComputeWarps) {
-        // ---------------- two compute warpgroups.  Per tile: g / dt table,
-        // X_hat, H (publishing the state for the jump), scores, epilogue.
+        // ---------------- two compute warpgroups.  Order per tile `it`:
+        //   scores(it) -> [state leaving the item] -> H(it + 1) -> epilogue(it)
+        //   -> X_hat(it + 1)
+        // so the next tile's H is built from the state the jump of `it` left
+        // while Y1(it) runs on the tensor cores.  y is staged in the X_hat lo
+        // buffer (free once the jump of `it` is done) and D x goes into the Y1
+        // accumulator when X_hat is built, so x is free as soon as X_hat is
+        // (Y1 of a wide tile, which reads raw x, keeps it until Y1 is done).
         const int wg = warp >> 2, q = warp & 3;
         const int i = q * 32 + (tid & 31);
         const int row_lo = q * 32, row_hi = q * 32 + 31;  // this warp's rows
         const uint32_t lane = tmem_at(tmem, (uint32_t)(q * 32), 0);
         float *gtab_all = reinterpret_cast<float *>(smem + Lay::off_g);
         uint8_t *s_xh = smem + Lay::off_xh;
+        uint8_t *s_lo = s_xh + Lay::kX;
         uint8_t *s_h = smem + Lay::off_h;
         constexpr int kPHalf = P / 2;
         const int c0w = wg * kPHalf;  // this warpgroup's first headdim column
 
-        // raw G / dt words of a tile, loaded one tile ahead
+        // raw G / dt words of a tile, loaded two tiles ahead
         struct Raw {
             float base, g0, gL, gi, dti;
         };
@@ -399,317 +399,414 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             r.dti = i < n ? ld_early(prm.dtT + (int64_t)w.bh * g.L + tau + i) : 0.f;
             return r;
         };
-        Raw nxt{};
-        Item w_next{};
-        if ((int)blockIdx.x < prm.n_items) {
-            w_next = decode_item<MODE>(prm, blockIdx.x);
-            nxt = load_raw(w_next, w_next.t0);
-        }
-        uint32_t it = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
-            const Item w = w_next;
-            const int64_t bh = w.bh;
-            const int chunk = w.chunk;
-            const float Dh = prm.D[w.h];
-            const bool more = item + (int)gridDim.x < prm.n_items;
-            if (more)
-                w_next = decode_item<MODE>(prm, item + gridDim.x);
-            for (int t = w.t0; t < w.t1; ++t, ++it) {
-                const int tau = t * kTile;
-                const int n = min(kTile, (int)g.L - tau);
-                const bool first = t == w.t0, last_item = t + 1 == w.t1;
-                const bool last_seq = MODE == kModeOut ? last_item : t + 1 == prm.n_tiles;
-                const bool do_state = !last_seq || want_final;
-                const Raw cur = nxt;
-                // prefetch the next tile's G / dt while this one is processed
-                if (!last_item)
-                    nxt = load_raw(w, t + 1);
-                else if (more)
-                    nxt = load_raw(w_next, w_next.t0);
-                const float gL = cur.gL - cur.base;
-                const float range = (cur.g0 - cur.base) - gL;
-                const bool narrow = range <= kNarrow && range >= -kNarrow;
-                const float gi = cur.gi - cur.base;
-                const float dti = cur.dti;
-                const int s = (int)(it % STAGES);
-                uint8_t *sx = smem + s * Lay::kStage + 2 * Lay::kB;
-                const uint32_t par = it & 1;
+        // Position of a tile in this CTA's work: item, tile, the head's D.
+        struct Pos {
+            Item w;
+            int item, t;
+            float Dh;
+            bool valid;
+        };
+        auto first_pos = [&]() {
+            Pos p{};
+            p.item = blockIdx.x;
+            p.valid = p.item < prm.n_items;
+            if (p.valid) {
+                p.w = decode_item<MODE>(prm, p.item);
+                p.t = p.w.t0;
+                p.Dh = prm.D[p.w.h];
+            }
+            return p;
+        };
+        // next_pos past the last tile returns valid = false with the last
+        // tile's place unchanged
+        auto next_pos = [&](const Pos &p) {
+            Pos n = p;
+            if (!p.valid)
+                return n;
+            if (p.t + 1 < p.w.t1) {
+                n.t = p.t + 1;
+                return n;
+            }
+            n.item = p.item + (int)gridDim.x;
+            n.valid = n.item < prm.n_items;
+            if (n.valid) {
+                n.w = decode_item<MODE>(prm, n.item);
+                n.t = n.w.t0;
+                n.Dh = prm.D[n.w.h];
+            }
+            return n;
+        };
+        struct Tile {
+            Item w;
+            int t, n, s;
+            uint32_t it;
+            bool first, last_item, last_seq, do_state, narrow;
+            float gi, dti, gL, Dh;
+        };
+        auto make_tile = [&](const Pos &p, uint32_t it, const Raw &raw) {
+            Tile c;
+            c.w = p.w;
+            c.t = p.t;
+            c.it = it;
+            c.s = (int)(it % STAGES);
+            c.n = min(kTile, (int)g.L - p.t * kTile);
+            c.first = p.t == p.w.t0;
+            c.last_item = p.t + 1 == p.w.t1;
+            c.last_seq = MODE == kModeOut ? c.last_item : p.t + 1 == prm.n_tiles;
+            c.do_state = !c.last_seq || want_final;
+            c.gL = raw.gL - raw.base;
+            const float range = (raw.g0 - raw.base) - c.gL;
+            c.narrow = range <= kNarrow && range >= -kNarrow;
+            c.gi = raw.gi - raw.base;
+            c.dti = raw.dti;
+            c.Dh = p.Dh;
+            return c;
+        };
 
-                // ---- per-tile g / dt table (double-buffered by tile parity),
-                // published with X_hat
-                float *gtab = gtab_all + (it & 1) * 256;
-                if (wg == 0)
-                    gtab[i] = gi;
-                else
-                    gtab[128 + i] = dti;
-                if (tid == 0)
-                    s_mode[it & 1] = narrow ? 1 : 0;
-                // x landed; the previous tile's state jump (and everything
-                // before it: Y1 and Y2 reading X_hat and H) has completed
-                if (!mbar_wait(&bar_full_x[s], (it / STAGES) & 1) ||
-                    (it > 0 && !mbar_wait(&bar_ds, (it - 1) & 1))) {
+        // ---- X_hat = dt exp2(g_L - g) x as bf16 hi (+ lo for the state jump),
+        // and Y1 <- D x / r1 (r1 = exp2(g_i - g_L) factorized, 1 exact), which
+        // Y1's MMAs add onto.  lo goes in once the previous tile's y store has
+        // read the lo buffer.
+        auto build_xhat = [&](const Tile &c) -> bool {
+            const uint32_t par = c.it & 1;
+            float *gtab = gtab_all + par * 256;
+            if (wg == 0)
+                gtab[i] = c.gi;
+            else
+                gtab[128 + i] = c.dti;
+            if (tid == 0)
+                s_mode[par] = c.narrow ? 1 : 0;
+            if (!mbar_wait(&bar_full_x[c.s], (c.it / STAGES) & 1))
+                return false;
+            tc_fence_after();
+            const uint8_t *sx = smem + c.s * Lay::kStage + 2 * Lay::kB;
+            const bool build = c.narrow || c.do_state;
+            const float e = ex2_approx(c.gL - c.gi);
+            const float w = (build && i < c.n) ? c.dti * e : 0.f;
+            const float dsc = c.narrow ? c.Dh * e : c.Dh;
+            uint32_t lo_keep[4][4];
+            uint32_t dx[32];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int ch = wg * 4 + k;
+                const uint32_t off = sw128_offset(i, ch);
+                const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
+                const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+                uint32_t hi[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const float x0 = bf_lo(vv[e2]), x1 = bf_hi(vv[e2]);
+                    const float a = x0 * w, bb = x1 * w;
+                    hi[e2] = pack_bf16x2(a, bb);
+                    lo_keep[k][e2] = pack_bf16x2(a - bf_lo(hi[e2]), bb - bf_hi(hi[e2]));
+                    dx[8 * k + 2 * e2] = __float_as_uint(dsc * x0);
+                    dx[8 * k + 2 * e2 + 1] = __float_as_uint(dsc * x1);
+                }
+                if (build)
+                    *reinterpret_cast<uint4 *>(s_xh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            }
+            tmem_st16(lane + Lay::t_y1 + c0w, *reinterpret_cast<uint32_t(*)[16]>(dx));
+            tmem_st16(lane + Lay::t_y1 + c0w + 16, *reinterpret_cast<uint32_t(*)[16]>(dx + 16));
+            // a factorized tile no longer needs raw x: its slot may be reloaded
+            if (c.narrow)
+                warp_arrive(&bar_empty_x[c.s]);
+            // the previous tile's y store has read the lo buffer
+            if (c.it > 0 && !mbar_wait(&bar_lofree, par ^ 1u))
+                return false;
+            if (c.do_state) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint4 *>(s_lo + sw128_offset(i, wg * 4 + k)) =
+                        make_uint4(lo_keep[k][0], lo_keep[k][1], lo_keep[k][2], lo_keep[k][3]);
+            }
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&bar_xh);
+            return true;
+        };
+
+        // ---- H = bf16(hscale * h), MN-major [s][p]; emit and decay the state.
+        // A non-first tile reads the state the previous tile's jump left (the
+        // caller waited for it); an item's first tile loads its start state (a
+        // later segment waits until its predecessor has published it).
+        auto build_h = [&](const Tile &c) -> bool {
+            const int64_t bh = c.w.bh;
+            const int chunk = c.w.chunk;
+            if (MODE == kModeFused && c.first && chunk > 0 && !prm.prefilled) {
+                const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + chunk - 1;
+                bool ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
+                const uint64_t t_start = globaltimer_ns();
+                while (!ready) {
+                    if (globaltimer_ns() - t_start > 2000000000ull)
+                        break;
+                    __nanosleep(256);
+                    ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
+                }
+                if (!ready)
+                    return false;
+            }
+            const float decay = ex2_approx(c.gL);
+            const float hscale = c.narrow ? decay : 1.f;
+            const bool emit = MODE == kModeFused && prm.states_out && (c.t & tpc_mask) == 0;
+#pragma unroll
+            for (int mb = 0; mb < Lay::kSBlk; ++mb) {
+                const int sidx = mb * 128 + i;
+                const bool s_ok = sidx < S;
+                const uint32_t acc = lane + Lay::t_st + mb * P + c0w;
+                uint32_t r[kPHalf];
+                if (c.first) {
+                    const float *src = nullptr;
+                    if (MODE == kModeOut)
+                        src = prm.h_src + ((bh * g.nc + chunk) * g.P) * g.S;
+                    else if (chunk > 0)  // later segment: the predecessor's state
+                        src = prm.seg_state + ((bh * prm.n_seg + chunk - 1) * g.P) * g.S;
+                    else if (prm.h_src)
+                        src = prm.h_src + bh * g.P * g.S;
+#pragma unroll
+                    for (int j = 0; j < kPHalf; ++j)
+                        r[j] = __float_as_uint(
+                            (src && s_ok) ? __ldcg(src + (int64_t)(c0w + j) * S + sidx) : 0.f);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < kPHalf; cc += 16)
+                        tmem_ld16(acc + cc, *reinterpret_cast<uint32_t(*)[16]>(r + cc));
+                    tmem_ld_wait();
+                }
+                float *emit_dst =
+                    emit ? prm.states_out + ((bh * g.nc + (c.t >> prm.tpc_shift)) * g.P) * g.S
+                         : nullptr;
+                uint32_t hp[kPHalf / 2];
+#pragma unroll
+                for (int j = 0; j < kPHalf; j += 2) {
+                    const float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
+                    if (emit_dst && s_ok) {
+                        emit_dst[(int64_t)(c0w + j) * S + sidx] = v0;
+                        emit_dst[(int64_t)(c0w + j + 1) * S + sidx] = v1;
+                    }
+                    hp[j / 2] = pack_bf16x2(v0 * hscale, v1 * hscale);
+                    r[j] = __float_as_uint(v0 * decay);
+                    r[j + 1] = __float_as_uint(v1 * decay);
+                }
+                if (s_ok) {  // row sidx, columns c0w .. c0w + 31: four 16-byte chunks
+#pragma unroll
+                    for (int k = 0; k < kPHalf / 8; ++k)
+                        *reinterpret_cast<uint4 *>(s_h + sw128_offset(sidx, c0w / 8 + k)) =
+                            make_uint4(hp[4 * k], hp[4 * k + 1], hp[4 * k + 2], hp[4 * k + 3]);
+                }
+                if (c.do_state) {
+#pragma unroll
+                    for (int cc = 0; cc < kPHalf; cc += 16)
+                        tmem_st16(acc + cc, *reinterpret_cast<uint32_t(*)[16]>(r + cc));
+                }
+            }
+            if (c.do_state)
+                tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bar_h);
+            return true;
+        };
+
+        // ---- scores: CB (f32) -> masked, decayed bf16 A operand in TMEM.
+        // Warpgroup wg converts keys [64 wg, 64 wg + 64): one TMEM round trip
+        // for all of them.  The g / dt table is complete once every warp has
+        // published X_hat.
+        auto build_scores = [&](const Tile &c) -> bool {
+            const uint32_t par = c.it & 1;
+            if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_xh, par))
+                return false;
+            tc_fence_after();
+            const float *gtab = gtab_all + par * 256;
+            const bool full = c.n == kTile;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t cbv[2][16];
+#pragma unroll
+                for (int gq = 0; gq < 2; ++gq) {
+                    const int j0 = wg * 64 + half * 32 + gq * 16;
+                    if (j0 <= row_hi)  // warp-uniform: keys above the diagonal stay zero
+                        tmem_ld16(lane + Lay::t_cb + j0, cbv[gq]);
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int gq = 0; gq < 2; ++gq) {
+                    const int j0 = wg * 64 + half * 32 + gq * 16;
+                    uint32_t pk[8];
+                    if (j0 > row_hi) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pk[e] = 0u;
+                    } else if (c.narrow) {
+                        if (full && j0 + 15 < row_lo) {  // whole group below the diagonal
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                pk[e] = pack_bf16x2(__uint_as_float(cbv[gq][2 * e]),
+                                                    __uint_as_float(cbv[gq][2 * e + 1]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = j0 + 2 * e;
+                                const float a =
+                                    (j <= i && j < c.n) ? __uint_as_float(cbv[gq][2 * e]) : 0.f;
+                                const float bb = (j + 1 <= i && j + 1 < c.n)
+                                                     ? __uint_as_float(cbv[gq][2 * e + 1])
+                                                     : 0.f;
+                                pk[e] = pack_bf16x2(a, bb);
+                            }
+                        }
+                    } else {
+                        const float4 *g4 = reinterpret_cast<const float4 *>(gtab + j0);
+                        const float4 *d4 = reinterpret_cast<const float4 *>(gtab + 128 + j0);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const float4 gg = g4[v4], dd = d4[v4];
+                            const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
+                            const float dj[4] = {dd.x, dd.y, dd.z, dd.w};
+                            float val[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = j0 + 4 * v4 + e;
+                                val[e] = (j <= i && j < c.n)
+                                             ? __uint_as_float(cbv[gq][4 * v4 + e]) *
+                                                   ex2_approx(c.gi - gj[e]) * dj[e]
+                                             : 0.f;
+                            }
+                            pk[2 * v4] = pack_bf16x2(val[0], val[1]);
+                            pk[2 * v4 + 1] = pack_bf16x2(val[2], val[3]);
+                        }
+                    }
+                    tmem_st8(lane + Lay::t_sc + j0 / 2, pk);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&bar_scores);
+            return true;
+        };
+
+        // ---- the state leaving an item: the next segment's start, or the
+        // final state (the caller waited for the item's last jump)
+        auto leave_state = [&](const Tile &c) {
+            const int64_t bh = c.w.bh;
+            float *dst = nullptr;
+            const bool handoff = MODE == kModeFused && !c.last_seq && !prm.prefilled;
+            if (handoff)
+                dst = prm.seg_state + ((bh * prm.n_seg + c.w.chunk) * g.P) * g.S;
+            else if (c.last_seq && want_final)
+                dst = prm.final_state + bh * g.P * g.S;
+            if (dst) {
+#pragma unroll
+                for (int mb = 0; mb < Lay::kSBlk; ++mb) {
+                    const int sidx = mb * 128 + i;
+                    uint32_t r[kPHalf];
+#pragma unroll
+                    for (int cc = 0; cc < kPHalf; cc += 16)
+                        tmem_ld16(lane + Lay::t_st + mb * P + c0w + cc,
+                                  *reinterpret_cast<uint32_t(*)[16]>(r + cc));
+                    tmem_ld_wait();
+                    if (sidx < S) {
+#pragma unroll
+                        for (int j = 0; j < kPHalf; ++j)
+                            __stcg(dst + (int64_t)(c0w + j) * S + sidx, __uint_as_float(r[j]));
+                    }
+                }
+            }
+            if (handoff) {
+                __threadfence();
+                __syncwarp();
+                if ((tid & 31) == 0)
+                    atomicAdd(prm.seg_count + bh * prm.n_seg + c.w.chunk, 1u);
+            }
+        };
+
+        // ---- epilogue: y = r1 Y1 + r2 Y2 (Y1 holds D x / r1), staged in the
+        // lo buffer (free: the caller waited for this tile's jump)
+        auto epilogue = [&](const Tile &c) -> bool {
+            const uint32_t par = c.it & 1;
+            if (!mbar_wait(&bar_y, par))
+                return false;
+            tc_fence_after();
+            // an exact tile's Y1 read raw x: its slot may be reloaded now
+            if (!c.narrow)
+                warp_arrive(&bar_empty_x[c.s]);
+            const float r1 = c.narrow ? ex2_approx(c.gi - c.gL) : 1.f;
+            const float r2 = c.narrow ? r1 : ex2_approx(c.gi);
+#pragma unroll
+            for (int c16 = 0; c16 < kPHalf; c16 += 16) {
+                uint32_t ra[16], rb[16];
+                tmem_ld16(lane + Lay::t_y1 + c0w + c16, ra);
+                tmem_ld16(lane + Lay::t_y2 + c0w + c16, rb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int cc = 8 * k + 2 * e;
+                        o[e] = pack_bf16x2(r1 * __uint_as_float(ra[cc]) + r2 * __uint_as_float(rb[cc]),
+                                           r1 * __uint_as_float(ra[cc + 1]) +
+                                               r2 * __uint_as_float(rb[cc + 1]));
+                    }
+                    *reinterpret_cast<uint4 *>(s_lo + sw128_offset(i, (c0w + c16) / 8 + k)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bar_ys);
+            return true;
+        };
+
+        bool ok = true;
+        Pos p1 = first_pos();
+        if (p1.valid) {
+            const Raw raw0 = load_raw(p1.w, p1.t);
+            Tile cur = make_tile(p1, 0, raw0);
+            p1 = next_pos(p1);
+            // (a position past the CTA's last tile keeps that tile's place, so
+            // these loads are always in bounds; selecting between a load and
+            // a default would make the thread wait for the load right here)
+            Raw raw1 = load_raw(p1.w, p1.t);
+            ok = build_xhat(cur) && build_h(cur);
+            for (uint32_t it = 0; ok; ++it) {
+                // the tile after the next one, its G / dt in flight
+                const Pos p2 = next_pos(p1);
+                const Raw raw2 = load_raw(p2.w, p2.t);
+                if (!build_scores(cur)) {
+                    ok = false;
+                    break;
+                }
+                // this tile's jump (and Y2, CB before it) is done: the state, the
+                // H buffer and the lo buffer are free
+                if (!mbar_wait(&bar_ds, it & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-
-                // ---- X_hat = dt exp2(g_L - g) x as bf16 hi (+ lo for the state jump)
-                if (narrow || do_state) {
-                    const float w = i < n ? dti * ex2_approx(gL - gi) : 0.f;
-#pragma unroll
-                    for (int r = 0; r < Lay::kPReg; ++r) {
-#pragma unroll
-                        for (int c = wg * 4; c < wg * 4 + 4; ++c) {
-                            const uint32_t off = r * kRegion + sw128_offset(i, c);
-                            const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
-                            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-                            uint32_t hi[4], lo[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float a = bf_lo(vv[e]) * w, bb = bf_hi(vv[e]) * w;
-                                hi[e] = pack_bf16x2(a, bb);
-                                lo[e] = pack_bf16x2(a - bf_lo(hi[e]), bb - bf_hi(hi[e]));
-                            }
-                            *reinterpret_cast<uint4 *>(s_xh + off) =
-                                make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            if (do_state)
-                                *reinterpret_cast<uint4 *>(s_xh + Lay::kX + off) =
-                                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                        }
-                    }
-                    fence_proxy_async_smem();
-                }
-                warp_arrive(&bar_xh);
-
-                // ---- a later segment waits until its predecessor published its state
-                if (MODE == kModeFused && first && chunk > 0 && !prm.prefilled) {
-                    const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + chunk - 1;
-                    bool ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
-                    const uint64_t t_start = globaltimer_ns();
-                    while (!ready) {
-                        if (globaltimer_ns() - t_start > 2000000000ull)
-                            break;
-                        __nanosleep(256);
-                        ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
-                    }
-                    if (!ready) {
+                if (cur.last_item && cur.do_state)
+                    leave_state(cur);
+                Tile nxt{};
+                if (p1.valid) {
+                    nxt = make_tile(p1, it + 1, raw1);
+                    if (!build_h(nxt)) {
                         ok = false;
                         break;
                     }
                 }
-
-                // ---- H = bf16(hscale * h), MN-major [s][p]; emit and decay the state
-                const float decay = ex2_approx(gL);
-                const float hscale = narrow ? decay : 1.f;
-                const bool emit = MODE == kModeFused && prm.states_out && (t & tpc_mask) == 0;
-#pragma unroll
-                for (int mb = 0; mb < Lay::kSBlk; ++mb) {
-                    const int sidx = mb * 128 + i;
-                    const bool s_ok = sidx < S;
-                    const uint32_t acc = lane + Lay::t_st + mb * P + c0w;
-                    uint32_t r[kPHalf];
-                    if (first) {
-                        const float *src = nullptr;
-                        if (MODE == kModeOut)
-                            src = prm.h_src + ((bh * g.nc + chunk) * g.P) * g.S;
-                        else if (chunk > 0)  // later segment: the predecessor's state
-                            src = prm.seg_state + ((bh * prm.n_seg + chunk - 1) * g.P) * g.S;
-                        else if (prm.h_src)
-                            src = prm.h_src + bh * g.P * g.S;
-#pragma unroll
-                        for (int j = 0; j < kPHalf; ++j)
-                            r[j] = __float_as_uint(
-                                (src && s_ok) ? __ldcg(src + (int64_t)(c0w + j) * S + sidx) : 0.f);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < kPHalf; c += 16)
-                            tmem_ld16(acc + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
-                        tmem_ld_wait();
-                    }
-                    float *emit_dst =
-                        emit ? prm.states_out + ((bh * g.nc + (t >> prm.tpc_shift)) * g.P) * g.S
-                             : nullptr;
-                    uint32_t hp[kPHalf / 2];
-#pragma unroll
-                    for (int j = 0; j < kPHalf; j += 2) {
-                        const float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
-                        if (emit_dst && s_ok) {
-                            emit_dst[(int64_t)(c0w + j) * S + sidx] = v0;
-                            emit_dst[(int64_t)(c0w + j + 1) * S + sidx] = v1;
-                        }
-                        hp[j / 2] = pack_bf16x2(v0 * hscale, v1 * hscale);
-                        r[j] = __float_as_uint(v0 * decay);
-                        r[j + 1] = __float_as_uint(v1 * decay);
-                    }
-                    if (s_ok) {  // row sidx, columns c0w .. c0w + 31: four 16-byte chunks
-#pragma unroll
-                        for (int k = 0; k < kPHalf / 8; ++k)
-                            *reinterpret_cast<uint4 *>(s_h + sw128_offset(sidx, c0w / 8 + k)) =
-                                make_uint4(hp[4 * k], hp[4 * k + 1], hp[4 * k + 2], hp[4 * k + 3]);
-                    }
-                    if (do_state) {
-#pragma unroll
-                        for (int c = 0; c < kPHalf; c += 16)
-                            tmem_st16(acc + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
-                    }
-                }
-                if (do_state)
-                    tmem_st_wait();
-                fence_proxy_async_smem();
-                tc_fence_before();
-                warp_arrive(&bar_h);
-
-                // ---- scores: CB (f32) -> masked, decayed bf16 A operand in TMEM.
-                // Warpgroup wg converts keys [64 wg, 64 wg + 64): one TMEM round
-                // trip for all of them.  The g / dt table is complete once every
-                // warp has published X_hat.
-                if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_xh, par)) {
+                if (!epilogue(cur)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const bool full = n == kTile;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t cbv[2][16];
-#pragma unroll
-                    for (int gq = 0; gq < 2; ++gq) {
-                        const int j0 = wg * 64 + half * 32 + gq * 16;
-                        if (j0 <= row_hi)  // warp-uniform: keys above the diagonal stay zero
-                            tmem_ld16(lane + Lay::t_cb + j0, cbv[gq]);
-                    }
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int gq = 0; gq < 2; ++gq) {
-                        const int j0 = wg * 64 + half * 32 + gq * 16;
-                        uint32_t pk[8];
-                        if (j0 > row_hi) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                pk[e] = 0u;
-                        } else if (narrow) {
-                            if (full && j0 + 15 < row_lo) {  // whole group below the diagonal
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    pk[e] = pack_bf16x2(__uint_as_float(cbv[gq][2 * e]),
-                                                        __uint_as_float(cbv[gq][2 * e + 1]));
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const int j = j0 + 2 * e;
-                                    const float a =
-                                        (j <= i && j < n) ? __uint_as_float(cbv[gq][2 * e]) : 0.f;
-                                    const float bb = (j + 1 <= i && j + 1 < n)
-                                                         ? __uint_as_float(cbv[gq][2 * e + 1])
-                                                         : 0.f;
-                                    pk[e] = pack_bf16x2(a, bb);
-                                }
-                            }
-                        } else {
-                            const float4 *g4 = reinterpret_cast<const float4 *>(gtab + j0);
-                            const float4 *d4 = reinterpret_cast<const float4 *>(gtab + 128 + j0);
-#pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4) {
-                                const float4 gg = g4[v4], dd = d4[v4];
-                                const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
-                                const float dj[4] = {dd.x, dd.y, dd.z, dd.w};
-                                float val[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int j = j0 + 4 * v4 + e;
-                                    val[e] = (j <= i && j < n)
-                                                 ? __uint_as_float(cbv[gq][4 * v4 + e]) *
-                                                       ex2_approx(gi - gj[e]) * dj[e]
-                                                 : 0.f;
-                                }
-                                pk[2 * v4] = pack_bf16x2(val[0], val[1]);
-                                pk[2 * v4 + 1] = pack_bf16x2(val[2], val[3]);
-                            }
-                        }
-                        tmem_st8(lane + Lay::t_sc + j0 / 2, pk);
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                warp_arrive(&bar_scores);
-
-                // ---- epilogue: y = r1 Y1 + r2 Y2 + D x, written over x in the stage
-                if (!mbar_wait(&bar_y, par)) {
+                if (!p1.valid)
+                    break;
+                if (!build_xhat(nxt)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                {
-                    const float r1 = narrow ? ex2_approx(gi - gL) : 1.f;
-                    const float r2 = narrow ? r1 : ex2_approx(gi);
-#pragma unroll
-                    for (int c16 = 0; c16 < kPHalf; c16 += 16) {
-                        uint32_t ra[16], rb[16];
-                        tmem_ld16(lane + Lay::t_y1 + c0w + c16, ra);
-                        tmem_ld16(lane + Lay::t_y2 + c0w + c16, rb);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int k = 0; k < 2; ++k) {
-                            uint8_t *xp = sx + sw128_offset(i, (c0w + c16) / 8 + k);
-                            const uint4 xv4 = *reinterpret_cast<const uint4 *>(xp);
-                            const uint32_t xv[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
-                            uint32_t o[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int c = 8 * k + 2 * e;
-                                const float a = r1 * __uint_as_float(ra[c]) +
-                                                r2 * __uint_as_float(rb[c]) + Dh * bf_lo(xv[e]);
-                                const float bb = r1 * __uint_as_float(ra[c + 1]) +
-                                                 r2 * __uint_as_float(rb[c + 1]) + Dh * bf_hi(xv[e]);
-                                o[e] = pack_bf16x2(a, bb);
-                            }
-                            *reinterpret_cast<uint4 *>(xp) = make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                warp_arrive(&bar_ys[s]);
-
-                // ---- state leaving the item: the next segment's start, or the final state
-                if (do_state && last_item) {
-                    float *dst = nullptr;
-                    const bool handoff = MODE == kModeFused && !last_seq && !prm.prefilled;
-                    if (handoff)
-                        dst = prm.seg_state + ((bh * prm.n_seg + chunk) * g.P) * g.S;
-                    else if (last_seq && want_final)
-                        dst = prm.final_state + bh * g.P * g.S;
-                    if (dst) {
-                        if (!mbar_wait(&bar_ds, par)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int mb = 0; mb < Lay::kSBlk; ++mb) {
-                            const int sidx = mb * 128 + i;
-                            uint32_t r[kPHalf];
-#pragma unroll
-                            for (int c = 0; c < kPHalf; c += 16)
-                                tmem_ld16(lane + Lay::t_st + mb * P + c0w + c,
-                                          *reinterpret_cast<uint32_t(*)[16]>(r + c));
-                            tmem_ld_wait();
-                            if (sidx < S) {
-#pragma unroll
-                                for (int j = 0; j < kPHalf; ++j)
-                                    __stcg(dst + (int64_t)(c0w + j) * S + sidx,
-                                           __uint_as_float(r[j]));
-                            }
-                        }
-                    }
-                    if (handoff) {
-                        __threadfence();
-                        __syncwarp();
-                        if ((tid & 31) == 0)
-                            atomicAdd(prm.seg_count + bh * prm.n_seg + chunk, 1u);
-                    }
-                }
+                cur = nxt;
+                p1 = p2;
+                raw1 = raw2;
             }
         }
         if (!ok)
@@ -766,9 +863,6 @@ cudaError_t dispatch(const CUtensorMap &tx, const CUtensorMap &tb, const CUtenso
     return cudaErrorNotSupported;
 }
 
-// Segmentation of the fused pass: enough (batch, head, segment) items for
-// about eight per SM, so the persistent CTAs end within one item of each
-// other; no segment shorter than two tiles.
 struct SegPlan {
     int seg_tiles;
     int n_seg;
@@ -785,8 +879,15 @@ struct SegPlan {
 // then independent.  (With more sequences the extra state pass costs more
 // than the wavefront: B 2, L 32768, H 64, S 256 took 1.74 ms prefilled
 // against 1.39 ms with hand-offs; B 1, L 262144, H 64, S 256 took 6.17 ms
-// against 10.66 ms.)  Otherwise: enough hand-off segments for about eight
-// items per SM, none shorter than two tiles.
+// against 10.66 ms.)  With at most one sequence per SM: one segment each, a
+// CTA runs its sequence end to end (only one segment of a sequence can run at
+// a time, so cutting it adds hand-offs and lets one late segment hold up the
+// others queued behind it on the same CTA: B 2, L 32768, H 64, S 256 took
+// 1.22 ms against 1.32 ms with ten segments each).  With more sequences than
+// SMs: enough hand-off segments for about sixteen items per SM, none shorter
+// than two tiles, so that CTAs whose tiles run slower (their share of L2
+// bandwidth differs) end near the others (B 4, L 65536, H 64, S 256: 3.94 ms
+// against 4.05 ms with about eight).
 constexpr int kMaxPrefillSeg = 64;  // segments the state pass's combine handles
 
 SegPlan seg_plan(const Geom &g)
@@ -815,7 +916,8 @@ SegPlan seg_plan(const Geom &g)
             }
         }
     }
-    int64_t want = (8LL * sm_count() + nbh - 1) / nbh;
+    // one segment per sequence while every sequence has an SM of its own
+    int64_t want = nbh <= sm_count() ? 1 : (16LL * sm_count() + nbh - 1) / nbh;
     want = want < 1 ? 1 : want;
     if (want > (n_tiles + 1) / 2)
         want = (n_tiles + 1) / 2 < 1 ? 1 : (n_tiles + 1) / 2;

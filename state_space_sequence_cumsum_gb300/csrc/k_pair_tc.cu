@@ -1027,10 +1027,12 @@ int sm_count_pair()
 // hand-off slot per sequence).  With at most half as many head pairs as SMs:
 // prefilled segments -- one wave of (pair, segment) items, every segment's
 // start state computed beforehand by the segmented tensor-core state pass, so
-// no item waits for another.  Otherwise segmentation with hand-offs: enough
-// (batch, head pair, segment) items for about eight per SM, no segment
-// shorter than two tiles.  SSD_PAIR_PREFILL=0 turns the prefilled plan off (a
-// test and measurement switch).
+// no item waits for another.  Otherwise one item per head pair, run end to
+// end by one CTA: only one segment of a sequence can run at a time, so
+// cutting the sequences into segments that hand their states on adds waits
+// and no parallelism (B 4, L 65536, H 64, S 128 took 1.75 ms against 1.87 ms
+// with about eight hand-off segments per SM).  SSD_PAIR_PREFILL=0 turns the
+// prefilled plan off (a test and measurement switch).
 constexpr int kMaxPrefillSeg = 64;  // segments the state pass's combine handles
 
 struct PairSegPlan {
@@ -1075,14 +1077,10 @@ PairSegPlan pair_seg_plan(const Geom &g, bool allow_prefill = true)
             return sp;
         }
     }
-    int64_t want = (8LL * sm_count_pair() + units - 1) / units;
-    want = want < 1 ? 1 : want;
-    if (want > (n_tiles + 1) / 2)
-        want = (n_tiles + 1) / 2 < 1 ? 1 : (n_tiles + 1) / 2;
-    sp.seg_tiles = (int)((n_tiles + want - 1) / want);
-    sp.n_seg = (int)((n_tiles + sp.seg_tiles - 1) / sp.seg_tiles);
-    sp.state_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg * g.P * g.S) * sizeof(float) : 0;
-    sp.count_bytes = sp.n_seg > 1 ? (size_t)(nbh * sp.n_seg) * sizeof(unsigned int) : 0;
+    sp.seg_tiles = (int)n_tiles;
+    sp.n_seg = 1;
+    sp.state_bytes = 0;
+    sp.count_bytes = 0;
     return sp;
 }
 

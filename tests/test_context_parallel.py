@@ -118,7 +118,9 @@ def test_host_logic_under_gloo_ranks_equals_one_run(ws):
     shape = (2, 200, 4, 8, 8, 2, 16)  # B, L, H, P, S, G, T
     cuts = _segments(shape[1], ws, shape[6])
     port = _free_port()
-    with mp.Manager() as m:
+    # the manager process is started by spawn too: never fork a process
+    # that may hold a CUDA context
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_cpu_worker, args=(ws, port, shape, cuts, out), nprocs=ws, join=True)
         res = dict(out)
@@ -231,7 +233,9 @@ def test_two_processes_on_one_gpu_over_gloo():
     ws = 2
     cuts = _segments(shape[1], ws, shape[6])
     port = _free_port()
-    with mp.Manager() as m:
+    # the manager process is started by spawn too: never fork a process
+    # that may hold a CUDA context
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_gpu_worker, args=(ws, port, shape, cuts, out), nprocs=ws, join=True)
         res = dict(out)

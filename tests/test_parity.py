@@ -249,21 +249,22 @@ def test_fused_kernels_every_decay_mode(kernel, monkeypatch):
 @pytest.mark.parametrize("prefill", ["1", "0"])
 def test_pair_kernel_many_segments(S, prefill, monkeypatch):
     """One batch row and four heads over 4095 tokens: the fused pass splits
-    each sequence into many segments, their start states either computed
-    beforehand by the segmented state pass (prefill) or handed off through
-    global memory from segment to segment."""
+    each sequence into many segments whose start states the segmented state
+    pass computes beforehand (prefill), or, with that plan off, one CTA runs
+    each head pair end to end."""
     monkeypatch.setenv("SSD_PAIR_PREFILL", prefill)
     check_case(1, 4095, 4, 64, S, 1, 128, torch.bfloat16, init="randn", seed=43 + S)
 
 
 @pytest.mark.parametrize("T", [128, 256])
 @pytest.mark.parametrize("init", ["zero", "randn"])
-def test_pair_prefilled_segments_match_handoff(T, init, monkeypatch):
+def test_pair_prefilled_segments_match_unsegmented(T, init, monkeypatch):
     """Few head pairs (one wave of (pair, segment) items): segments run at
     once from start states of the segmented state pass ("Kernel 2:
     fwd_pass_state" over parallel segments plus a serial combine).  The
-    result matches the hand-off plan and the oracle, chunk states included,
-    over a ragged last segment and two tiles per chunk at T = 256."""
+    result matches the plan without segments (one CTA per head pair) and the
+    oracle, chunk states included, over a ragged last segment and two tiles
+    per chunk at T = 256."""
     inp = case_inputs(2, 3001, 4, 64, 128, 2, T, init=init, seed=T + 5)
     ref = oracle_run(inp, T, want_states=True)
     out = {}
@@ -308,12 +309,13 @@ def test_pair_kernel_fast_decay_with_noise():
     assert_parity(fin, ref["final_state"], torch.bfloat16, "final_state")
 
 
-def test_pair_kernel_runs_with_the_hand_off_workspace():
+def test_pair_kernel_runs_with_the_smaller_workspace():
     """ssd_fwd_workspace_size reports the prefilled plan's workspace (it also
-    holds G and dt^T); the head-pair path accepts less -- down to the
-    hand-off plan's -- and then runs that plan.  Found by bisection on the
-    host-side check (a short workspace returns SSD_ERR_WORKSPACE before any
-    launch), then run at exactly that size against the oracle."""
+    holds G and dt^T); the head-pair path accepts less -- down to what the
+    plan without segments needs -- and then runs that plan.  Found by
+    bisection on the host-side check (a short workspace returns
+    SSD_ERR_WORKSPACE before any launch), then run at exactly that size
+    against the oracle."""
     import ctypes
     from state_space_sequence_cumsum_gb300 import _lib
     B, L, H, P, S, G, T = 1, 4095, 4, 64, 128, 1, 128
@@ -342,7 +344,7 @@ def test_pair_kernel_runs_with_the_hand_off_workspace():
             assert st == _lib.SSD_ERR_WORKSPACE
             lo = mid
     least = hi * 256
-    assert least < pref  # the hand-off plan needs no G / dt^T copy
+    assert least < pref  # the plan without segments needs no G / dt^T copy
     assert call(least) == _lib.SSD_OK
     torch.cuda.synchronize()
     assert ssd.ssd_stream_status() == 0

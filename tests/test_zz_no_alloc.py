@@ -10,9 +10,11 @@ by every GPU test (2e-2 of the output's rms for bf16 inputs, 1e-4 for f32)
 sizes beyond the scratch array are refused before any launch.  Before the
 calls that are checked, a call on other inputs leaves its own values in the
 scratch array, so a kernel that read scratch before writing it would show.
-The cases cover the head-pair path (its hand-off plan and its prefilled
-plan), the one-head fused path at dstate 256, the staged dstate-512 path with
-chunk states, and the f32 path.
+The cases cover the head-pair path (one CTA per pair, prefilled segments,
+and the wrap plan whose sequences hand states from CTA to CTA), the one-head
+fused path at dstate 256 (prefilled segments, and hand-off segments when there
+are more sequences than SMs), the staged dstate-512 path with chunk states,
+and the f32 path.
 
 The file is named so pytest collects it last.
 """
@@ -49,9 +51,11 @@ def _max_rel(a, b):
 
 
 @pytest.mark.parametrize("shape,dtype,want_states", [
-    ((2, 777, 8, 64, 128, 2, 256), torch.bfloat16, False),   # head pairs, hand-off plan
+    ((2, 777, 8, 64, 128, 2, 256), torch.bfloat16, False),   # head pairs, one CTA per pair
     ((1, 4096, 2, 64, 128, 1, 128), torch.bfloat16, False),  # head pairs, prefilled segments
-    ((1, 1000, 3, 64, 256, 1, 128), torch.bfloat16, False),  # one-head fused, dstate 256
+    ((1, 300, 320, 64, 64, 1, 128), torch.bfloat16, False),  # head pairs, wrap plan (160 pairs)
+    ((1, 1000, 3, 64, 256, 1, 128), torch.bfloat16, False),  # one-head fused, dstate 256, prefilled
+    ((1, 600, 160, 64, 256, 1, 128), torch.bfloat16, False),  # one-head fused, hand-off segments
     ((1, 600, 2, 64, 512, 1, 128), torch.bfloat16, True),    # staged, dstate 512, chunk states
     ((1, 300, 3, 32, 48, 1, 64), torch.float32, False),      # f32 CUDA cores
 ])
