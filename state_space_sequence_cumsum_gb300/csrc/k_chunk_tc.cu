@@ -382,7 +382,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         constexpr int kPHalf = P / 2;
         const int c0w = wg * kPHalf;  // this warpgroup's first headdim column
 
-        // raw G / dt words of a tile, loaded two tiles ahead
+        // raw G / dt words of a tile, loaded two tiles ahead.  Every load is
+        // unconditional (addresses clamped into the row) and the choices
+        // between a loaded word and a default are made in make_tile, a tile
+        // later: a select on a load still in flight would hold the thread
+        // until the load returns.
         struct Raw {
             float base, g0, gL, gi, dti;
         };
@@ -391,12 +395,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const float *grow = prm.Gc + (int64_t)w.bh * g.L;
             const int tau = t * kTile;
             const int n = min(kTile, (int)g.L - tau);
+            const int ic = i < n ? i : n - 1;
             Raw r;
-            r.base = (t & tpc_mask) == 0 ? 0.f : ld_early(grow + tau - 1);
+            r.base = ld_early(grow + (tau > 0 ? tau - 1 : 0));
             r.g0 = ld_early(grow + tau);
             r.gL = ld_early(grow + tau + n - 1);
-            r.gi = i < n ? ld_early(grow + tau + i) : r.base;
-            r.dti = i < n ? ld_early(prm.dtT + (int64_t)w.bh * g.L + tau + i) : 0.f;
+            r.gi = ld_early(grow + tau + ic);
+            r.dti = ld_early(prm.dtT + (int64_t)w.bh * g.L + tau + ic);
             return r;
         };
         // Position of a tile in this CTA's work: item, tile, the head's D.
@@ -454,11 +459,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             c.last_item = p.t + 1 == p.w.t1;
             c.last_seq = MODE == kModeOut ? c.last_item : p.t + 1 == prm.n_tiles;
             c.do_state = !c.last_seq || want_final;
-            c.gL = raw.gL - raw.base;
-            const float range = (raw.g0 - raw.base) - c.gL;
+            // G restarts at chunk starts; a tile inside a chunk is relative to
+            // G just before it
+            const float base = (p.t & tpc_mask) == 0 ? 0.f : raw.base;
+            c.gL = raw.gL - base;
+            const float range = (raw.g0 - base) - c.gL;
             c.narrow = range <= kNarrow && range >= -kNarrow;
-            c.gi = raw.gi - raw.base;
-            c.dti = raw.dti;
+            c.gi = i < c.n ? raw.gi - base : 0.f;
+            c.dti = i < c.n ? raw.dti : 0.f;
             c.Dh = p.Dh;
             return c;
         };
