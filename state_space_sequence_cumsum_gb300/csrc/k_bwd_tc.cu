@@ -27,7 +27,14 @@
 // layout (x, dy, B, C by TMA; h_in, dS, Q1, Q2, Xs, Ys written by the compute
 // warps), so each contraction is one tcgen05.mma chain with f32 accumulators
 // in TMEM: dyx cols [0,128), CB [128,256), Chin [256,320), BdS [384,448); in
-// phase B dX1 [0,64), dB [128,128+S), dC [256,256+S).  dB and dC are summed
+// phase B dX1 [0,64), dB [128,128+S), dC [256,256+S).  h_in, dS, Xs and Ys
+// enter the contractions as bf16 hi + lo pairs (h_in, dS in phase A; all four
+// in a second phase-B step that adds Xs dS_lo + Xs_lo dS to dB and Ys h_lo +
+// Ys_lo h_in to dC, once the lo tiles are over Q1 / Q2): with single bf16
+// roundings the state terms cancel badly at long sequences (dC 6e-2 of its
+// rms beyond 2^-5 of each element at 4000 tokens; 1e-3 with the split).
+// The lo halves of h_in and dS wait in TMEM [448, 448 + S/2) between the
+// two uses.  dB and dC are summed
 // over the heads of a group in f32 by TMA bulk reductions (the rows staged in
 // shared memory as swizzled [128 x 32] f32 boxes); dx goes out through a
 // TMA store.  Roles: warps 0-3 compute (thread i = row / TMEM lane i), one
@@ -51,7 +58,7 @@ template <int S>
 struct BtLayout {
     static constexpr uint32_t kSR = S / 64;                   // 64-wide dstate regions
     static constexpr uint32_t kStateRegion = 64 * 128;        // 64 rows (p) x 128 bytes
-    static constexpr uint32_t off_x = 0;                      // x [t][p]
+    static constexpr uint32_t off_x = 0;                      // x [t][p] (then dx staging)
     static constexpr uint32_t off_dy = off_x + kRegion;       // dy [t][p]
     static constexpr uint32_t off_b = off_dy + kRegion;       // B [t][s], kSR regions
     static constexpr uint32_t off_c = off_b + kSR * kRegion;  // C [t][s]
@@ -59,13 +66,17 @@ struct BtLayout {
     static constexpr uint32_t off_ds = off_hin + kSR * kStateRegion;  // dS [p][s] bf16
     static constexpr uint32_t off_q1 = off_ds + kSR * kStateRegion;   // Q1 [i][j], 2 regions
     static constexpr uint32_t off_q2 = off_q1 + 2 * kRegion;          // Q2 [i][j], 2 regions
-    static constexpr uint32_t off_xs = off_q2 + 2 * kRegion;          // Xs [t][p] (then dx staging)
-    static constexpr uint32_t off_ys = off_xs + kRegion;              // Ys [t][p]
+    static constexpr uint32_t off_xs = off_q2 + 2 * kRegion;          // h_in lo (phase A), then Xs [t][p]
+    static constexpr uint32_t off_ys = off_xs + kRegion;              // dS lo (phase A), then Ys [t][p]
     static constexpr uint32_t off_vec = off_ys + kRegion;             // g, dt, dl: 3 x 128 f32
     static constexpr uint32_t bytes = off_vec + 3 * 128 * 4;
     static_assert(bytes + 1024 + 256 <= 232448, "shared memory budget");
     static constexpr uint32_t t_dyx = 0, t_cb = 128, t_chin = 256, t_bds = 384;
     static constexpr uint32_t t_dx = 0, t_db = 128, t_dc = 256;
+    // the lo halves of h_in and dS (bf16 pairs), kept from the conversion
+    // at the item's start until the second phase-B step
+    static constexpr uint32_t t_lo = 448;
+    static_assert(t_lo + S / 2 <= 512, "TMEM budget");
 };
 
 struct BtParams {
@@ -139,7 +150,7 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_in, bar_sld, bar_st, bar_a, bar_q, bar_b, bar_stg, bar_end;
+    __shared__ uint64_t bar_in, bar_sld, bar_st, bar_a, bar_q, bar_b1, bar_q2, bar_b, bar_stg, bar_end;
     __shared__ uint32_t tmem_slot;
     __shared__ float red[4][4];
     __shared__ int s_fail;
@@ -153,6 +164,8 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         mbar_init(&bar_st, 4);
         mbar_init(&bar_a, 1);
         mbar_init(&bar_q, 4);
+        mbar_init(&bar_b1, 1);
+        mbar_init(&bar_q2, 4);
         mbar_init(&bar_b, 1);
         mbar_init(&bar_sld, 1);
         mbar_init(&bar_stg, 4);
@@ -199,8 +212,14 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const uint64_t d_hm = desc_mn0(base + Lay::off_hin, Lay::kStateRegion);
             const uint64_t d_xs = desc_k0(base + Lay::off_xs), d_ys = desc_k0(base + Lay::off_ys);
             const uint64_t d_q2k = desc_k0(base + Lay::off_q2);
+            // the lo halves: of h_in and dS over Xs / Ys for phase A, over Q1
+            // for phase B; of Xs and Ys over Q2
+            const uint64_t d_hlo_a = desc_k0(base + Lay::off_xs), d_slo_a = desc_k0(base + Lay::off_ys);
+            const uint64_t d_hlo_b = desc_mn0(base + Lay::off_q1, Lay::kStateRegion);
+            const uint64_t d_slo_b = desc_mn0(base + Lay::off_q1 + Lay::kSR * Lay::kStateRegion, Lay::kStateRegion);
+            const uint64_t d_xslo = desc_k0(base + Lay::off_q2), d_yslo = desc_k0(base + Lay::off_q2 + kRegion);
             // an item's staged rows out: dB (over Q1) and dC (over B / C) added
-            // into the f32 accumulators, dx (over Xs) stored; rows past the
+            // into the f32 accumulators, dx (over x) stored; rows past the
             // sequence end are clipped by the tensor maps
             auto send_out = [&](const BtItem &w) {
                 for (int r = 0; r < S / 32; ++r) {
@@ -209,7 +228,7 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     tma4_reduce_add(&tm_dc, smem + Lay::off_b + r * kRegion, 32 * r, (int)w.grp, (int)w.tau,
                                     (int)w.b);
                 }
-                tma4_store(&tm_dx, smem + Lay::off_xs, 0, (int)w.h, (int)w.tau, (int)w.b);
+                tma4_store(&tm_dx, smem + Lay::off_x, 0, (int)w.h, (int)w.tau, (int)w.b);
                 bulk_commit();
             };
             prefetch_tmap(&tm_dx);
@@ -273,13 +292,22 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     break;
                 }
                 tc_fence_after();
-                // Chin = C h_in^T and BdS = B dS^T: N = p (64 rows of the state tiles), K = s
+                // Chin = C h_in^T and BdS = B dS^T: N = p (64 rows of the state
+                // tiles), K = s; h_in and dS as hi + lo (the lo halves over the
+                // Xs / Ys regions until the compute warps build Xs and Ys)
 #pragma unroll
                 for (int ks = 0; ks < S / 16; ++ks) {
                     mma_ss(tmem + Lay::t_chin, desc_k(d_c, kRegion, ks), desc_k(d_hk, Lay::kStateRegion, ks),
                            id_tp, ks > 0);
                     mma_ss(tmem + Lay::t_bds, desc_k(d_b, kRegion, ks), desc_k(d_sk, Lay::kStateRegion, ks),
                            id_tp, ks > 0);
+                }
+#pragma unroll
+                for (int ks = 0; ks < S / 16; ++ks) {
+                    mma_ss(tmem + Lay::t_chin, desc_k(d_c, kRegion, ks), desc_k(d_hlo_a, Lay::kStateRegion, ks),
+                           id_tp, 1u);
+                    mma_ss(tmem + Lay::t_bds, desc_k(d_b, kRegion, ks), desc_k(d_slo_a, Lay::kStateRegion, ks),
+                           id_tp, 1u);
                 }
                 mma_commit(&bar_a);
                 if (!mbar_wait(&bar_q, par)) {
@@ -305,6 +333,22 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_ss(tmem + Lay::t_dc, desc_k(d_ys, kRegion, ks), desc_mn(d_hm, ks), id_ks, 1u);
+                mma_commit(&bar_b1);
+                // the state terms' lo parts, once the compute warps have put
+                // h_in lo, dS lo (over Q1) and Xs lo, Ys lo (over Q2) in place:
+                // dB += Xs dS_lo + Xs_lo dS, dC += Ys h_lo + Ys_lo h_in
+                if (!mbar_wait(&bar_q2, par)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    mma_ss(tmem + Lay::t_db, desc_k(d_xs, kRegion, ks), desc_mn(d_slo_b, ks), id_ks, 1u);
+                    mma_ss(tmem + Lay::t_db, desc_k(d_xslo, kRegion, ks), desc_mn(d_dsm, ks), id_ks, 1u);
+                    mma_ss(tmem + Lay::t_dc, desc_k(d_ys, kRegion, ks), desc_mn(d_hlo_b, ks), id_ks, 1u);
+                    mma_ss(tmem + Lay::t_dc, desc_k(d_yslo, kRegion, ks), desc_mn(d_hm, ks), id_ks, 1u);
+                }
                 mma_commit(&bar_b);
                 prev = w;
             }
@@ -338,31 +382,52 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             sg[i] = valid ? grow[i] : 0.f;
             sdt[i] = valid ? prm.dtT[bh * g.L + tau + i] : 0.f;
             // h_in and dS: f32 [P][S], brought into the Q1 / Q2 regions by the
-            // issuing thread's bulk copies -> bf16 [p][s], swizzled rows of 64 s.
+            // issuing thread's bulk copies -> bf16 hi + lo [p][s], swizzled rows
+            // of 64 s: hi into the h_in / dS tiles, lo over the Xs / Ys regions
+            // (for phase A) and into TMEM (for the second phase-B step), as
+            // the contractions with the states cancel strongly at long
+            // sequences and a single bf16 rounding of the state showed there.
             // Warp w takes rows p = w, w + 4, ...; lane l four consecutive s.
+            constexpr int kLanesPerRow = S / 4;           // 32 (S 128) or 16 (S 64)
+            constexpr int kRowsPerPass = 32 / kLanesPerRow;
+            constexpr int kIters = 64 / (4 * kRowsPerPass);  // rows per lane: 16 or 8
+            const int st_sub = lane % kLanesPerRow, st_rsub = lane / kLanesPerRow;
+            const int st_s = 4 * st_sub;
+            const uint32_t st_reg = (uint32_t)(st_s / 64), st_col = (uint32_t)(st_s % 64);
+            auto st_off = [&](int r, int &p) {
+                p = warp * kRowsPerPass + st_rsub + r * 4 * kRowsPerPass;
+                return st_reg * Lay::kStateRegion + sw128_offset((uint32_t)p, st_col / 8) + (st_col % 8) * 2;
+            };
             float dshin = 0.f;
             bool ok = __all_sync(0xffffffffu, mbar_wait(&bar_sld, par));
             if (ok) {
                 const float *hin_s = reinterpret_cast<const float *>(smem + Lay::off_q1);
                 const float *ds_s = reinterpret_cast<const float *>(smem + Lay::off_q2);
-                constexpr int kLanesPerRow = S / 4;           // 32 (S 128) or 16 (S 64)
-                constexpr int kRowsPerPass = 32 / kLanesPerRow;
-                constexpr int kIters = 64 / (4 * kRowsPerPass);  // rows per lane: 16 or 8
-                const int sub = lane % kLanesPerRow, rsub = lane / kLanesPerRow;
-                const int s = 4 * sub;
-                const uint32_t reg = (uint32_t)(s / 64), col = (uint32_t)(s % 64);
-#pragma unroll 4
-                for (int r = 0; r < kIters; ++r) {
-                    const int p = warp * kRowsPerPass + rsub + r * 4 * kRowsPerPass;
-                    const float4 hv = *reinterpret_cast<const float4 *>(hin_s + p * S + s);
-                    const float4 dv = *reinterpret_cast<const float4 *>(ds_s + p * S + s);
-                    dshin += hv.x * dv.x + hv.y * dv.y + hv.z * dv.z + hv.w * dv.w;
-                    const uint32_t off = reg * Lay::kStateRegion + sw128_offset((uint32_t)p, col / 8) + (col % 8) * 2;
-                    *reinterpret_cast<uint2 *>(smem + Lay::off_hin + off) =
-                        make_uint2(pack_bf16x2(hv.x, hv.y), pack_bf16x2(hv.z, hv.w));
-                    *reinterpret_cast<uint2 *>(smem + Lay::off_ds + off) =
-                        make_uint2(pack_bf16x2(dv.x, dv.y), pack_bf16x2(dv.z, dv.w));
+#pragma unroll 1
+                for (int r0 = 0; r0 < kIters; r0 += 4) {
+                    uint32_t lw[16];  // lo words of four rows: h (2), dS (2) each
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        int p;
+                        const uint32_t off = st_off(r0 + q, p);
+                        const float4 hv = *reinterpret_cast<const float4 *>(hin_s + p * S + st_s);
+                        const float4 dv = *reinterpret_cast<const float4 *>(ds_s + p * S + st_s);
+                        dshin += hv.x * dv.x + hv.y * dv.y + hv.z * dv.z + hv.w * dv.w;
+                        const uint32_t h0 = pack_bf16x2(hv.x, hv.y), h1 = pack_bf16x2(hv.z, hv.w);
+                        const uint32_t d0 = pack_bf16x2(dv.x, dv.y), d1 = pack_bf16x2(dv.z, dv.w);
+                        lw[4 * q] = pack_bf16x2(hv.x - bf_lo(h0), hv.y - bf_hi(h0));
+                        lw[4 * q + 1] = pack_bf16x2(hv.z - bf_lo(h1), hv.w - bf_hi(h1));
+                        lw[4 * q + 2] = pack_bf16x2(dv.x - bf_lo(d0), dv.y - bf_hi(d0));
+                        lw[4 * q + 3] = pack_bf16x2(dv.z - bf_lo(d1), dv.w - bf_hi(d1));
+                        *reinterpret_cast<uint2 *>(smem + Lay::off_hin + off) = make_uint2(h0, h1);
+                        *reinterpret_cast<uint2 *>(smem + Lay::off_ds + off) = make_uint2(d0, d1);
+                        *reinterpret_cast<uint2 *>(smem + Lay::off_xs + off) = make_uint2(lw[4 * q], lw[4 * q + 1]);
+                        *reinterpret_cast<uint2 *>(smem + Lay::off_ys + off) =
+                            make_uint2(lw[4 * q + 2], lw[4 * q + 3]);
+                    }
+                    tmem_st16(tl + Lay::t_lo + 4 * r0, lw);
                 }
+                tmem_st_wait();
             }
             fence_proxy_async_smem();
             warp_arrive(&bar_st);
@@ -490,14 +555,71 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             tc_fence_before();
             warp_arrive(&bar_q);
 
-            // ---------------- epilogue
-            ok = __all_sync(0xffffffffu, ok && mbar_wait(&bar_b, par));
+            // ---------------- the lo halves for the second phase-B step, over
+            // Q1 (h_in lo, dS lo) and Q2 (Xs lo, Ys lo).  They are read from
+            // TMEM and formed in registers while phase B runs, and stored once
+            // phase B has read Q1 and Q2.
+            {
+                constexpr int kLoWords = kIters * 4;  // 64 (S 128) or 32 (S 64)
+                uint32_t lw[kLoWords];
+#pragma unroll
+                for (int c16 = 0; c16 < kLoWords; c16 += 16)
+                    tmem_ld16(tl + Lay::t_lo + c16, *reinterpret_cast<uint32_t(*)[16]>(lw + c16));
+                uint32_t xl[32], yl[32];
+                {
+                    const uint8_t *sxr = smem + Lay::off_x, *sdyr = smem + Lay::off_dy;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)ch);
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(sxr + off);
+                        const uint4 dv = *reinterpret_cast<const uint4 *>(sdyr + off);
+                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const float a0 = dti * eT * bf_lo(xw[e2]), a1 = dti * eT * bf_hi(xw[e2]);
+                            const float b0 = ei * bf_lo(dw[e2]), b1 = ei * bf_hi(dw[e2]);
+                            const uint32_t ah = pack_bf16x2(a0, a1), bh = pack_bf16x2(b0, b1);
+                            xl[4 * ch + e2] = pack_bf16x2(a0 - bf_lo(ah), a1 - bf_hi(ah));
+                            yl[4 * ch + e2] = pack_bf16x2(b0 - bf_lo(bh), b1 - bf_hi(bh));
+                        }
+                    }
+                }
+                tmem_ld_wait();
+                ok = __all_sync(0xffffffffu, ok && mbar_wait(&bar_b1, par));
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int r = 0; r < kIters; ++r) {
+                        int p;
+                        const uint32_t off = st_off(r, p);
+                        *reinterpret_cast<uint2 *>(smem + Lay::off_q1 + off) = make_uint2(lw[4 * r], lw[4 * r + 1]);
+                        *reinterpret_cast<uint2 *>(smem + Lay::off_q1 + Lay::kSR * Lay::kStateRegion + off) =
+                            make_uint2(lw[4 * r + 2], lw[4 * r + 3]);
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint32_t off = sw128_offset((uint32_t)i, (uint32_t)ch);
+                        *reinterpret_cast<uint4 *>(smem + Lay::off_q2 + off) =
+                            make_uint4(xl[4 * ch], xl[4 * ch + 1], xl[4 * ch + 2], xl[4 * ch + 3]);
+                        *reinterpret_cast<uint4 *>(smem + Lay::off_q2 + kRegion + off) =
+                            make_uint4(yl[4 * ch], yl[4 * ch + 1], yl[4 * ch + 2], yl[4 * ch + 3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bar_q2);
+
+            // ---------------- epilogue.  dx first: its inputs (dX1, BdS, x, dy)
+            // are complete after phase B's first step, so it runs while the
+            // second step is in flight, and its rows go over the x tile (each
+            // thread reads its row of x before writing dx there; no MMA reads
+            // x any more)
             float colq = 0.f, ddt_direct = 0.f, rj = 0.f;
             if (ok) {
-                tc_fence_after();
                 const float Dh = prm.D[h];
                 const uint8_t *sxr = smem + Lay::off_x, *sdyr = smem + Lay::off_dy;
-                uint8_t *stage = smem + Lay::off_xs;  // Xs was read by phase B: dx staging
+                uint8_t *stage = smem + Lay::off_x;
 #pragma unroll
                 for (int c2 = 0; c2 < 4; ++c2) {
                     uint32_t d1[16], bd[16];
@@ -526,7 +648,10 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
                 ddt_direct = colq + eT * xb;
                 rj = eT * dti * xb;
-                fence_proxy_async_smem();
+            }
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(&bar_b, par));
+            if (ok) {
+                tc_fence_after();
                 // dB and dC rows of this chunk's tokens, added into the f32
                 // accumulators by TMA reductions: each row goes to shared memory in
                 // [128 rows][32 f32] swizzled boxes (dB over Q1 / Q2, dC over B / C:

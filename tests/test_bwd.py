@@ -104,6 +104,11 @@ def test_bwd_matches_oracle(B, L, H, P, S, G, dtype, monkeypatch):
     (2, 300, 4, 64, 64, 1),     # ragged last chunk, dstate 64
     (1, 128, 2, 64, 128, 1),    # exactly one chunk
     (2, 520, 6, 64, 128, 3),    # grouped, ragged
+    # more (batch, chunk, head) items than a GB300 has SMs three times over:
+    # each persistent CTA runs several items, so every barrier phase turns
+    # over and each item's outputs leave while the next one loads
+    (2, 4000, 8, 64, 128, 2),   # 512 items, ragged last chunk
+    (2, 4096, 8, 64, 64, 1),    # 512 items, dstate 64, one group
 ])
 def test_bwd_tensor_core_path(B, L, H, P, S, G):
     out, ref = run_case(B, L, H, P, S, G, torch.bfloat16, seed=6)
