@@ -437,9 +437,9 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const float eT = valid ? exp2f(glast - gi) : 0.f, ei = valid ? exp2f(gi) : 0.f;
             // Score weights exp2(g_i - g_j) = r_i c_j with a reference g_m in the
             // middle of the chunk's range, while that range stays within 200
-            // (both factors within 2^100): c_j and c_j dt_j go to shared memory
-            // (over dl and dt: this row's dt is already in a register), and the
-            // Q loop needs no exponent.  Wider ranges take exp2 per element.
+            // (both factors within 2^100): c_j goes to shared memory (over dl),
+            // and the Q loop needs no exponent.  Wider ranges take exp2 per
+            // element.
             const float g0 = sg[0];
             const bool fact = fabsf(g0 - glast) <= 200.f;  // the same for the whole CTA
             const float gm = 0.5f * (g0 + glast);
@@ -447,7 +447,6 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             if (fact) {
                 const float cj = valid ? exp2f(gm - gi) : 0.f;
                 sdl[i] = cj;
-                sdt[i] = cj * dti;
             }
             compute_sync();  // the column factors are visible
 
@@ -502,28 +501,30 @@ bwd_chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        float a[2], bq[2];
+                        float a[2], bq[2], dxt[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const int j = j0 + 2 * e + u;
                             const float cbv = __uint_as_float(cb[2 * e + u]);
                             const float dyxv = __uint_as_float(dx[2 * e + u]);
-                            if (kFact) {
-                                const float m = (valid && j <= i) ? ri : 0.f;
-                                a[u] = m * sdl[j] * cbv;
-                                bq[u] = m * sdt[j] * dyxv;  // w dt_j dyx
-                                rowq = fmaf(cbv, bq[u], rowq);
-                            } else {
-                                const float w = (valid && j <= i) ? exp2f(gi - sg[j]) : 0.f;
-                                a[u] = w * cbv;
-                                bq[u] = w * dyxv * sdt[j];
-                                rowq = fmaf(a[u], dyxv * sdt[j], rowq);
-                            }
+                            float w;
+                            if (kFact)
+                                w = (valid && j <= i) ? ri * sdl[j] : 0.f;
+                            else
+                                w = (valid && j <= i) ? exp2f(gi - sg[j]) : 0.f;
+                            a[u] = w * cbv;              // Q1 = W CB
+                            dxt[u] = dyxv * sdt[j];
+                            bq[u] = w * dxt[u];          // Q2 = W dyx dt_j
                             if (j == i)
                                 dyx_ii = dyxv;
                         }
                         q1[e] = pack_bf16x2(a[0], a[1]);
                         q2[e] = pack_bf16x2(bq[0], bq[1]);
+                        // the row sum of Q1 dyx dt from the bf16 Q1 that dX1 (and
+                        // with it the column sums x . dX1) is formed from: the two
+                        // enter dL with opposite signs and their chunk totals are
+                        // equal, so they must carry the same rounding
+                        rowq = fmaf(bf_lo(q1[e]), dxt[0], fmaf(bf_hi(q1[e]), dxt[1], rowq));
                     }
                 };
 #pragma unroll 1

@@ -58,12 +58,16 @@ def uses_tensor_cores(P, S, dtype):
 
 
 def check_tc(out, ref):
+    """The tensor-core backward: every gradient within 2^-5 |ref| + 2e-2 rms
+    element by element -- the forward's 2e-2 rms plus a relative term for the
+    bf16 rounding of the decay-weighted score matrices (Q1, Q2), whose
+    products reach the largest elements of dB and dC."""
     for k in ("dx", "dB", "dC", "ddt", "dA", "dD", "dinit"):
         g = out[k].detach().to("cpu", torch.float64).numpy()
         r = ref[k]
         rms = float(np.sqrt(np.mean(r * r)))
         excess = np.max(np.abs(g - r) - 2.0 ** -5 * np.abs(r)) / rms
-        assert excess <= 4e-2, f"{k}: error beyond 2^-5 |ref| is {excess:.3e} * rms"
+        assert excess <= 2e-2, f"{k}: error beyond 2^-5 |ref| is {excess:.3e} * rms"
 
 
 def check(out, ref, dtype):
