@@ -1025,15 +1025,16 @@ int sm_count_pair()
 // Work plan.  With at least one head pair per SM: the wrap schedule (one
 // contiguous piece of the pair-major tile sequence per CTA, at most one
 // hand-off slot per sequence).  With at most half as many head pairs as SMs:
-// prefilled segments -- one wave of (pair, segment) items, every segment's
-// start state computed beforehand by the segmented tensor-core state pass, so
-// no item waits for another.  Otherwise one item per head pair, run end to
+// prefilled segments -- one to four waves of (pair, segment) items, every
+// segment's start state computed beforehand by the segmented tensor-core
+// state pass, so no item waits for another.  Otherwise one item per head pair, run end to
 // end by one CTA: only one segment of a sequence can run at a time, so
 // cutting the sequences into segments that hand their states on adds waits
 // and no parallelism (B 4, L 65536, H 64, S 128 took 1.75 ms against 1.87 ms
 // with about eight hand-off segments per SM).  SSD_PAIR_PREFILL=0 turns the
 // prefilled plan off (a test and measurement switch).
 constexpr int kMaxPrefillSeg = 64;  // segments the state pass's combine handles
+constexpr int64_t kMinWaveSeg = 96;  // tiles of a prefilled segment past the first wave
 
 struct PairSegPlan {
     bool wrap, prefill;
@@ -1059,7 +1060,14 @@ PairSegPlan pair_seg_plan(const Geom &g, bool allow_prefill = true)
     }
     const char *env = getenv("SSD_PAIR_PREFILL");
     const int tpc = g.T / kTile;
-    int64_t want1 = sm_count_pair() / units;
+    // one wave of items, or two or four while the segments stay at least
+    // kMinWaveSeg tiles long (B 1, L 262144, H 64: S 128 2.80 -> 2.51 ms and
+    // S 64 2.68 -> 2.35 ms at four waves, eight were slower; B 4, L 16384,
+    // H 8 is fastest with one)
+    int64_t waves = 1;
+    while (waves < 4 && n_tiles * units / (2 * waves * sm_count_pair()) >= kMinWaveSeg)
+        waves *= 2;
+    int64_t want1 = waves * sm_count_pair() / units;
     if (want1 > kMaxPrefillSeg)
         want1 = kMaxPrefillSeg;
     if (want1 * 2 * tpc > n_tiles)
