@@ -145,7 +145,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_full[kStages], bar_xready[kStages], bar_empty[kStages];
-    __shared__ uint64_t bar_jfull[2], bar_jfree[2];
+    __shared__ uint64_t bar_jfull[2], bar_jfree[2], bar_end;
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -173,6 +173,7 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             mbar_init(&bar_jfull[j], 1);
             mbar_init(&bar_jfree[j], kCompute / 32);
         }
+        mbar_init(&bar_end, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -283,6 +284,11 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 mma_commit(&bar_jfull[jb]);
                 mma_commit(&bar_empty[s]);
             }
+            // every MMA this thread issued has completed before TMEM is freed
+            // (the compute warps wait for each jump only while nothing failed)
+            mma_commit(&bar_end);
+            if (!mbar_wait(&bar_end, 0))
+                atomicOr(status, 1u);
         }
     } else {
         // ---------------- compute threads: token row `row` for X_hat, state row
@@ -360,11 +366,14 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             return true;
         };
 
+        // A warp whose wait gives up (ok false) keeps walking the tiles without
+        // work: the chunk-state stores below synchronise all compute warps, so
+        // leaving the loop early would hold the others at that barrier.
         bool ok = true;
         float d_cur = 1.f, d_next = 1.f;
         if (n_tiles > 0)
             ok = build(0, d_cur);
-        for (int i = 0; ok && i < n_tiles; ++i) {
+        for (int i = 0; i < n_tiles; ++i) {
             // chunk start: store h, the state before this chunk
             const int ti = tile_index(i);
             if (states && sg.mode != 1 && (ti & tpc_shift) == 0) {
@@ -392,12 +401,14 @@ state_pass_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                         dst[(int64_t)p * g.S] = hs[p];
                 }
             }
-            if (i + 1 < n_tiles && !(ok = build(i + 1, d_next)))
-                break;
+            if (ok && i + 1 < n_tiles)
+                ok = build(i + 1, d_next);
             // fold in this warpgroup's columns of the jump of tile i
             const int jb = (int)(i & 1);
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bar_jfull[jb], (uint32_t)((i >> 1) & 1)))))
-                break;
+            if (ok)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar_jfull[jb], (uint32_t)((i >> 1) & 1)));
+            if (!ok)
+                continue;
             tc_fence_after();
             constexpr int kQ = PH / 16 < 4 ? PH / 16 : 4;  // 16-column loads in flight
 #pragma unroll
