@@ -171,7 +171,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     // the y store
     __shared__ uint64_t bar_ys, bar_lofree;
     // MMA completions: cb (CB), y (Y1 and Y2), ds (state jump and all before)
-    __shared__ uint64_t bar_cb, bar_y, bar_ds;
+    __shared__ uint64_t bar_cb, bar_y, bar_ds, bar_end;
     // compute warps done with: X_hat and the g / dt table, H and the state
     // decay, the score operand
     __shared__ uint64_t bar_xh, bar_h, bar_scores;
@@ -192,6 +192,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         mbar_init(&bar_lofree, 1);
         mbar_init(&bar_cb, 1);
         mbar_init(&bar_y, 1);
+        mbar_init(&bar_end, 1);
         mbar_init(&bar_ds, 1);
         mbar_init(&bar_xh, kComputeWarps);
         mbar_init(&bar_h, kComputeWarps);
@@ -335,6 +336,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
             }
             if (!ok)
+                atomicOr(prm.status, 1u);
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&bar_end);
+            if (!mbar_wait(&bar_end, 0))
                 atomicOr(prm.status, 1u);
         }
     } else if (warp == 10) {

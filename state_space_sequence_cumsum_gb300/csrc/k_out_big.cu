@@ -95,7 +95,7 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     // (the y written over it has been stored)
     __shared__ uint64_t bar_full[2], bar_empty[2], bar_x[2], bar_xfree[2];
     // MMA completions: CB complete; Y1 (and everything before) complete
-    __shared__ uint64_t bar_cb, bar_y;
+    __shared__ uint64_t bar_cb, bar_y, bar_end;
     // compute warps (8 arrivals): H's rows of dstate block k written (block 0
     // also the g / dt table); scores written; y staged (per x buffer)
     __shared__ uint64_t bar_h[Lay::kSB], bar_sc, bar_ys[2];
@@ -113,6 +113,7 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         }
         mbar_init(&bar_cb, 1);
         mbar_init(&bar_y, 1);
+        mbar_init(&bar_end, 1);
         for (int k = 0; k < Lay::kSB; ++k)
             mbar_init(&bar_h[k], kWarps);
         mbar_init(&bar_sc, kWarps);
@@ -228,6 +229,10 @@ out_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 mma_commit(&bar_y);
             }
             if (!ok)
+                atomicOr(prm.status, 1u);
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&bar_end);
+            if (!mbar_wait(&bar_end, 0))
                 atomicOr(prm.status, 1u);
         }
     } else if (warp == 10) {

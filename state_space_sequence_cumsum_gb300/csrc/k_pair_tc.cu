@@ -215,7 +215,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
     // TMA landed: B and C; x of head k
     __shared__ uint64_t bar_bc, bar_x[2];
     // MMA completions: CB; Y2; Y2 + state jump (B / C / X_hat free); Y1 (Y complete)
-    __shared__ uint64_t bar_cb, bar_y2, bar_ds, bar_y;
+    __shared__ uint64_t bar_cb, bar_y2, bar_ds, bar_y, bar_end;
     // compute warps (8 arrivals): X_hat + D x + modes; H + decayed state;
     // scores (+ wide rescale); y staged
     __shared__ uint64_t bar_xh, bar_h, bar_sc, bar_ys;
@@ -237,6 +237,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
         mbar_init(&bar_y2, 1);
         mbar_init(&bar_ds, 1);
         mbar_init(&bar_y, 1);
+        mbar_init(&bar_end, 1);
         mbar_init(&bar_xh, kWarps);
         mbar_init(&bar_h, kWarps);
         mbar_init(&bar_sc, kWarps);
@@ -416,6 +417,10 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 }
             }
             if (!ok)
+                atomicOr(prm.status, 1u);
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&bar_end);
+            if (!mbar_wait(&bar_end, 0, wait_ns))
                 atomicOr(prm.status, 1u);
         }
     } else if (warp == 10) {
