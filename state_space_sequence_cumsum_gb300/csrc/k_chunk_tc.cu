@@ -74,13 +74,20 @@ struct CoLayout {
     static constexpr int kSBlk = (S + 127) / 128;  // 128-row blocks of the state
     static constexpr uint32_t kB = kSReg * kRegion;
     static constexpr uint32_t kX = kPReg * kRegion;
-    static constexpr uint32_t kStage = 2 * kB + kX;  // B, C, x (then y)
-    static constexpr uint32_t off_xh = STAGES * kStage;  // X_hat hi, then lo
+    static constexpr uint32_t kStage = 2 * kB;  // B, C
+    // x has a ring of its own, at least two slots deep: the next tile's x
+    // lands while an exact tile's Y1 still reads its own x
+    static constexpr int kXSt = STAGES < 2 ? 2 : STAGES;
+    static constexpr uint32_t off_x = STAGES * kStage;
+    static constexpr uint32_t off_xh = off_x + kXSt * kX;  // X_hat hi, then lo (then y)
     static constexpr uint32_t off_h = off_xh + 2 * kX;
     // H is stored MN-major: one 128-byte row of P bf16 per state index s
     static constexpr uint32_t kH = S * 128;
-    static constexpr uint32_t off_g = off_h + kH;  // [2 tiles][g 128 | dt 128] f32
-    static constexpr uint32_t bytes = off_g + 2 * 256 * 4;
+    // [g 128 | dt 128] f32 of the tile whose X_hat was built last (every
+    // warp has converted the previous tile's scores by then: its epilogue
+    // waited for Y1, which waited for the scores)
+    static constexpr uint32_t off_g = off_h + kH;
+    static constexpr uint32_t bytes = off_g + 256 * 4;
     // TMEM columns: CB (f32), the bf16 score operand (two per column), Y1, Y2,
     // and the f32 state accumulator
     static constexpr uint32_t t_cb = 0, t_sc = 128, t_y1 = 192, t_y2 = 192 + P,
@@ -163,10 +170,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    // per stage: B / C landed, x landed; B / C free (the tile's C B^T, C H^T
-    // and state jump done), x free (X_hat built; for an exact tile, Y1 done)
-    __shared__ uint64_t bar_full[STAGES], bar_full_x[STAGES], bar_empty[STAGES],
-        bar_empty_x[STAGES];
+    // per B / C stage: landed; free (the tile's C B^T, C H^T and state jump
+    // done).  Per x slot: landed; free (X_hat built; for an exact tile, Y1 done)
+    __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES], bar_full_x[Lay::kXSt],
+        bar_empty_x[Lay::kXSt];
     // y staged in the X_hat lo buffer (compute warps); that buffer read by
     // the y store
     __shared__ uint64_t bar_ys, bar_lofree;
@@ -184,8 +191,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_full_x[s], 1);
             mbar_init(&bar_empty[s], 1);
+        }
+        for (int s = 0; s < Lay::kXSt; ++s) {
+            mbar_init(&bar_full_x[s], 1);
             mbar_init(&bar_empty_x[s], kComputeWarps);
         }
         mbar_init(&bar_ys, kComputeWarps);
@@ -221,9 +230,23 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const Item w = decode_item<MODE>(prm, item);
                 const int grp = w.h / g.hpg;
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
-                    const int s = (int)(it % STAGES);
-                    // B / C as soon as the stage's previous tile no longer reads
-                    // them (its state jump done), x once that tile's y is stored
+                    const int s = (int)(it % STAGES), sx = (int)(it % Lay::kXSt);
+                    const int tok = t * kTile;
+                    // x once its slot's previous tile no longer reads it (X_hat
+                    // built, or for an exact tile Y1 done); then B / C once the
+                    // stage's previous tile no longer reads them (its state
+                    // jump and Y2 done).  x never waits behind B / C: its slot
+                    // frees no later than the epilogue before the next X_hat,
+                    // which the state jump that frees B / C waits for.
+                    if (it >= Lay::kXSt &&
+                        !mbar_wait(&bar_empty_x[sx], ((it / Lay::kXSt) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sxp = smem + Lay::off_x + sx * Lay::kX;
+                    mbar_arrive_expect_tx(&bar_full_x[sx], Lay::kX);
+                    for (int r = 0; r < Lay::kPReg; ++r)
+                        tma4(sxp + r * kRegion, &tm_x, &bar_full_x[sx], r * 64, w.h, tok, w.b);
                     if (it >= STAGES &&
                         !mbar_wait(&bar_empty[s], ((it / STAGES) - 1) & 1)) {
                         ok = false;
@@ -231,20 +254,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     uint8_t *st = smem + s * Lay::kStage;
                     mbar_arrive_expect_tx(&bar_full[s], 2 * Lay::kB);
-                    const int tok = t * kTile;
                     for (int r = 0; r < Lay::kSReg; ++r) {
                         tma4(st + r * kRegion, &tm_b, &bar_full[s], r * 64, grp, tok, w.b);
                         tma4(st + Lay::kB + r * kRegion, &tm_c, &bar_full[s], r * 64, grp, tok, w.b);
                     }
-                    if (it >= STAGES &&
-                        !mbar_wait(&bar_empty_x[s], ((it / STAGES) - 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&bar_full_x[s], Lay::kX);
-                    for (int r = 0; r < Lay::kPReg; ++r)
-                        tma4(st + 2 * Lay::kB + r * kRegion, &tm_x, &bar_full_x[s], r * 64, w.h, tok,
-                             w.b);
                 }
             }
             if (!ok)
@@ -270,10 +283,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 for (int t = w.t0; t < w.t1; ++t, ++it) {
                     const bool last_seq = MODE == kModeOut ? t + 1 == w.t1 : t + 1 == prm.n_tiles;
                     const bool do_state = !last_seq || want_final;
-                    const int s = (int)(it % STAGES);
+                    const int s = (int)(it % STAGES), sx = (int)(it % Lay::kXSt);
                     const uint32_t sb = smem_u32(smem + s * Lay::kStage);
                     const uint64_t d_bk = desc_k0(sb), d_ck = desc_k0(sb + Lay::kB);
-                    const uint64_t d_bmn = desc_mn0(sb), d_x = desc_mn0(sb + 2 * Lay::kB);
+                    const uint64_t d_bmn = desc_mn0(sb);
+                    const uint64_t d_x = desc_mn0(smem_u32(smem + Lay::off_x + sx * Lay::kX));
                     const uint32_t par = it & 1;
                     // CB overwrites the previous tile's CB, whose conversion
                     // ended before that tile's Y1 was issued
@@ -293,7 +307,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     // until that Y1 is done; a factorized tile's slot may already
                     // be reloading, and its MMAs never read raw x).
                     if (!mbar_spin(&bar_h, par) || !mbar_spin(&bar_xh, par) ||
-                        (!s_mode[par] && !mbar_spin(&bar_full_x[s], (it / STAGES) & 1))) {
+                        (!s_mode[par] && !mbar_spin(&bar_full_x[sx], (it / Lay::kXSt) & 1))) {
                         ok = false;
                         break;
                     }
@@ -448,7 +462,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         };
         struct Tile {
             Item w;
-            int t, n, s;
+            int t, n, sx;  // sx: x slot
             uint32_t it;
             bool first, last_item, last_seq, do_state, narrow;
             float gi, dti, gL, Dh;
@@ -458,7 +472,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             c.w = p.w;
             c.t = p.t;
             c.it = it;
-            c.s = (int)(it % STAGES);
+            c.sx = (int)(it % Lay::kXSt);
             c.n = min(kTile, (int)g.L - p.t * kTile);
             c.first = p.t == p.w.t0;
             c.last_item = p.t + 1 == p.w.t1;
@@ -482,17 +496,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // read the lo buffer.
         auto build_xhat = [&](const Tile &c) -> bool {
             const uint32_t par = c.it & 1;
-            float *gtab = gtab_all + par * 256;
+            float *gtab = gtab_all;
             if (wg == 0)
                 gtab[i] = c.gi;
             else
                 gtab[128 + i] = c.dti;
             if (tid == 0)
                 s_mode[par] = c.narrow ? 1 : 0;
-            if (!mbar_wait(&bar_full_x[c.s], (c.it / STAGES) & 1))
+            if (!mbar_wait(&bar_full_x[c.sx], (c.it / Lay::kXSt) & 1))
                 return false;
             tc_fence_after();
-            const uint8_t *sx = smem + c.s * Lay::kStage + 2 * Lay::kB;
+            const uint8_t *sx = smem + Lay::off_x + c.sx * Lay::kX;
             const bool build = c.narrow || c.do_state;
             const float e = ex2_approx(c.gL - c.gi);
             const float w = (build && i < c.n) ? c.dti * e : 0.f;
@@ -522,7 +536,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tmem_st16(lane + Lay::t_y1 + c0w + 16, *reinterpret_cast<uint32_t(*)[16]>(dx + 16));
             // a factorized tile no longer needs raw x: its slot may be reloaded
             if (c.narrow)
-                warp_arrive(&bar_empty_x[c.s]);
+                warp_arrive(&bar_empty_x[c.sx]);
             // the previous tile's y store has read the lo buffer
             if (c.it > 0 && !mbar_wait(&bar_lofree, par ^ 1u))
                 return false;
@@ -630,7 +644,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_xh, par))
                 return false;
             tc_fence_after();
-            const float *gtab = gtab_all + par * 256;
+            const float *gtab = gtab_all;
             const bool full = c.n == kTile;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -742,7 +756,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             tc_fence_after();
             // an exact tile's Y1 read raw x: its slot may be reloaded now
             if (!c.narrow)
-                warp_arrive(&bar_empty_x[c.s]);
+                warp_arrive(&bar_empty_x[c.sx]);
             const float r1 = c.narrow ? ex2_approx(c.gi - c.gL) : 1.f;
             const float r2 = c.narrow ? r1 : ex2_approx(c.gi);
 #pragma unroll
