@@ -635,6 +635,12 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
             const uint32_t wlo = pack_bf16x2(wv_lo, wv_lo);
             const uint64_t dsc2 = f2_pack(__float_as_uint(dsc), __float_as_uint(dsc));
             uint32_t lo_keep[8][4];
+            // every x load before the first store (the stores go to other
+            // buffers, which the compiler cannot tell)
+            uint4 xv[8];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                xv[ch] = *reinterpret_cast<const uint4 *>(sx + sw128_offset(i, ch));
 #pragma unroll
             for (int c2 = 0; c2 < 4; ++c2) {
                 uint32_t dx[16];
@@ -642,7 +648,7 @@ pair_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__
                 for (int cc = 0; cc < 2; ++cc) {
                     const int ch = 2 * c2 + cc;
                     const uint32_t off = sw128_offset(i, ch);
-                    const uint4 v = *reinterpret_cast<const uint4 *>(sx + off);
+                    const uint4 v = xv[ch];
                     const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
                     uint32_t hi[4];
 #pragma unroll
