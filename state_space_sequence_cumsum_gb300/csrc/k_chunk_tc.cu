@@ -847,6 +847,701 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     }
 }
 
+// ---------------------------------------------------------------- dstate 384 / 512
+// The fused forward for dstate 384 and 512, one head per CTA item.  One
+// tile's B and C (128 KB each at S = 512) do not fit in shared memory next to
+// x, X_hat and H, so they stream through a two-slot ring in 128-row dstate
+// blocks and every contraction over S runs block by block: per block b,
+//   CB += C_b B_b^T,  state_b += B_b^T (X_hat hi + lo),  Y += C_b H_b^T,
+// where H_b = bf16 of the tile's start state rows of block b, built by the
+// compute warps into one of two 16 KB buffers just before the block's jump.
+// CB is complete only after the last block, so the score conversion and Y1
+// follow the block loop.  Y holds C H^T and, for a factorized tile, Y1 on top
+// (y = exp2(g_i - g_L) Y + D x); an exact tile's Y1 goes to the CB columns
+// (y = exp2(g_i) Y + Y1 + D x).  D x is added in the epilogue from the x tile,
+// which stays in its slot until then; y is written over it and stored.
+//
+// Per tile `it`, compute warps: scores(it) -> [state leaving the item] ->
+// H blocks 0, 1 of it + 1 -> (Y1 done) X_hat(it + 1) -> epilogue(it) -> the
+// remaining H blocks of it + 1.  MMA thread, per block: C B^T, the jump (after
+// the block's H and, for block 0, X_hat), C H^T (block 0 after the previous
+// epilogue has read Y); then Y1 once the scores are converted.
+//
+// Shared memory (P 64, S 512): B / C ring 2 x 64 KB, x ring 2 x 16 KB, X_hat
+// hi / lo 32 KB, H 2 x 16 KB, g / dt 1 KB = 225 KB.  TMEM: CB 128 columns,
+// scores 64, Y 64, state S / 128 blocks of 64.
+template <int P, int S>
+struct BigLayout {
+    static constexpr int kSBlk = S / 128;            // 128-row dstate blocks
+    static constexpr uint32_t kBlk = 2 * kRegion;    // one block of B or C: 128 tokens x 128 s
+    static constexpr uint32_t kSlot = 2 * kBlk;      // B block, then C block
+    static constexpr uint32_t kX = kRegion;          // x / y tile (P = 64)
+    static constexpr uint32_t kH = kRegion;          // H block: 128 rows s x 64 p bf16
+    static constexpr uint32_t off_x = 2 * kSlot;     // two x slots (y is staged over x)
+    static constexpr uint32_t off_xh = off_x + 2 * kX;  // X_hat hi, then lo
+    static constexpr uint32_t off_h = off_xh + 2 * kX;  // two H buffers, MN-major [s][p]
+    static constexpr uint32_t off_g = off_h + 2 * kH;   // [g 128 | dt 128] f32
+    static constexpr uint32_t bytes = off_g + 256 * 4;
+    static constexpr uint32_t t_cb = 0, t_sc = 128, t_y = 192, t_st = 256;
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(P == 64, "one 128-byte row of x / y / H per token or state index");
+    static_assert(S % 128 == 0 && S >= 384 && t_st + kSBlk * P <= 512, "TMEM budget");
+    static_assert(bytes + 1024 + 256 <= 232448, "shared memory budget");
+};
+
+template <int P, int S>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                 const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_y,
+                 const Params prm)
+{
+    using Lay = BigLayout<P, S>;
+    constexpr int kSBlk = Lay::kSBlk;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // B / C slots: landed, free (the block's C B^T, jump and C H^T done)
+    __shared__ uint64_t bar_full[2], bar_empty[2];
+    // x slots: landed, free (y stored from it); y staged in the slot
+    __shared__ uint64_t bar_full_x[2], bar_empty_x[2], bar_ys[2];
+    // H buffers: built (compute warps), free (the block's C H^T done)
+    __shared__ uint64_t bar_hr[2], bar_hf[2];
+    // X_hat built; the block loop done (CB complete, state jumped); scores
+    // converted; Y complete (Y1 done); the epilogue has read Y; teardown
+    __shared__ uint64_t bar_xh, bar_blk, bar_sc, bar_y, bar_ep, bar_end;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_mode[2];  // per tile parity: 1 = factorized (narrow) decay
+
+    const Geom &g = prm.g;
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+            mbar_init(&bar_full_x[s], 1);
+            mbar_init(&bar_empty_x[s], 1);
+            mbar_init(&bar_ys[s], kComputeWarps);
+            mbar_init(&bar_hr[s], kComputeWarps);
+            mbar_init(&bar_hf[s], 1);
+        }
+        mbar_init(&bar_xh, kComputeWarps);
+        mbar_init(&bar_blk, 1);
+        mbar_init(&bar_sc, kComputeWarps);
+        mbar_init(&bar_y, 1);
+        mbar_init(&bar_ep, kComputeWarps);
+        mbar_init(&bar_end, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, Lay::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const bool want_final = prm.final_state != nullptr;
+
+    if (warp == 8) {
+        // ---------------- TMA loads: per tile, x into slot it & 1 once the
+        // y stored from that slot two tiles back has been read, then B / C
+        // block by block into the ring
+        if ((tid & 31) == 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_b);
+            prefetch_tmap(&tm_c);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const Item w = decode_item<kModeFused>(prm, item);
+                const int grp = w.h / g.hpg;
+                for (int t = w.t0; t < w.t1 && ok; ++t, ++it) {
+                    const int tok = t * kTile;
+                    const int sx = (int)(it & 1);
+                    if (it >= 2 && !mbar_wait(&bar_empty_x[sx], ((it >> 1) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bar_full_x[sx], Lay::kX);
+                    tma4(smem + Lay::off_x + sx * Lay::kX, &tm_x, &bar_full_x[sx], 0, w.h, tok, w.b);
+                    for (int k = 0; k < kSBlk; ++k) {
+                        const uint32_t gb = it * kSBlk + k;
+                        const int slot = (int)(gb & 1);
+                        if (gb >= 2 && !mbar_wait(&bar_empty[slot], ((gb >> 1) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *sb = smem + slot * Lay::kSlot;
+                        mbar_arrive_expect_tx(&bar_full[slot], 2 * Lay::kBlk);
+                        for (int r = 0; r < 2; ++r) {
+                            tma4(sb + r * kRegion, &tm_b, &bar_full[slot], (2 * k + r) * 64, grp, tok, w.b);
+                            tma4(sb + Lay::kBlk + r * kRegion, &tm_c, &bar_full[slot], (2 * k + r) * 64, grp,
+                                 tok, w.b);
+                        }
+                    }
+                }
+            }
+            if (!ok)
+                atomicOr(prm.status, 1u);
+        }
+    } else if (warp == 9) {
+        // ---------------- MMA issuer (waits poll with test_wait)
+        if ((tid & 31) == 0) {
+            const uint32_t id_cb = idesc_bf16(128, 128, false, false);
+            const uint32_t id_y1 = idesc_bf16(128, P, false, true);  // A (scores) from TMEM
+            const uint32_t id_y2 = idesc_bf16(128, P, false, true);  // H is MN-major
+            const uint32_t id_ds = idesc_bf16(128, P, true, true);
+            const uint64_t d_xh = desc_mn0(smem_u32(smem + Lay::off_xh));
+            const uint64_t d_lo = desc_mn0(smem_u32(smem + Lay::off_xh + Lay::kX));
+            uint32_t it = 0;
+            bool ok = true, prev_exact = false;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const Item w = decode_item<kModeFused>(prm, item);
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
+                    const bool do_state = t + 1 != prm.n_tiles || want_final;
+                    const uint32_t par = it & 1;
+                    // the previous tile's epilogue reads Y (and, for an exact
+                    // tile, Y1 in the CB columns): wait for it once per tile,
+                    // before the first MMA that overwrites what it reads
+                    bool ep_done = it == 0;
+                    if (prev_exact && !ep_done) {
+                        if (!mbar_spin(&bar_ep, (it - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        ep_done = true;
+                    }
+                    for (int k = 0; k < kSBlk && ok; ++k) {
+                        const uint32_t gb = it * kSBlk + k;
+                        const int slot = (int)(gb & 1);
+                        if (!mbar_spin(&bar_full[slot], (gb >> 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sb = smem_u32(smem + slot * Lay::kSlot);
+                        const uint64_t d_bk = desc_k0(sb), d_ck = desc_k0(sb + Lay::kBlk);
+                        const uint64_t d_bmn = desc_mn0(sb);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
+                                   id_cb, (k > 0 || ks > 0) ? 1u : 0u);
+                        // the jump once the block's H has read the state (and
+                        // X_hat is built)
+                        if (!mbar_spin(&bar_hr[slot], (gb >> 1) & 1) ||
+                            (k == 0 && !mbar_spin(&bar_xh, par))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (do_state) {
+#pragma unroll
+                            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                                for (int ks = 0; ks < 8; ++ks)
+                                    mma_ss(tmem + Lay::t_st + k * P, desc_mn(d_bmn, ks),
+                                           desc_mn(part ? d_lo : d_xh, ks), id_ds, 1u);
+                        }
+                        if (!ep_done) {
+                            if (!mbar_spin(&bar_ep, (it - 1) & 1)) {
+                                ok = false;
+                                break;
+                            }
+                            ep_done = true;
+                            tc_fence_after();
+                        }
+                        const uint64_t d_h = desc_mn0(smem_u32(smem + Lay::off_h + slot * Lay::kH));
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2,
+                                   (k > 0 || ks > 0) ? 1u : 0u);
+                        mma_commit(&bar_hf[slot]);
+                        mma_commit(&bar_empty[slot]);
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(&bar_blk);
+                    if (!mbar_spin(&bar_sc, par)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const bool narrow = s_mode[par] != 0;
+                    if (narrow) {
+#pragma unroll
+                        for (int ks = 0; ks < kTile / 16; ++ks)
+                            mma_ts(tmem + Lay::t_y, tmem + Lay::t_sc + ks * 8, desc_mn(d_xh, ks), id_y1, 1u);
+                    } else {
+                        const uint64_t d_x = desc_mn0(smem_u32(smem + Lay::off_x + (it & 1) * Lay::kX));
+#pragma unroll
+                        for (int ks = 0; ks < kTile / 16; ++ks)
+                            mma_ts(tmem + Lay::t_cb, tmem + Lay::t_sc + ks * 8, desc_mn(d_x, ks), id_y1,
+                                   ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bar_y);
+                    prev_exact = !narrow;
+                }
+            }
+            if (!ok)
+                atomicOr(prm.status, 1u);
+            // every MMA this thread issued has completed before TMEM is freed
+            mma_commit(&bar_end);
+            if (!mbar_wait(&bar_end, 0))
+                atomicOr(prm.status, 1u);
+        }
+    } else if (warp == 10) {
+        // ---------------- y store: the epilogue wrote y over its tile's x
+        if ((tid & 31) == 0) {
+            prefetch_tmap(&tm_y);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < prm.n_items && ok; item += gridDim.x) {
+                const Item w = decode_item<kModeFused>(prm, item);
+                for (int t = w.t0; t < w.t1; ++t, ++it) {
+                    const int sx = (int)(it & 1);
+                    if (!mbar_wait(&bar_ys[sx], (it >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tma4_store(&tm_y, smem + Lay::off_x + sx * Lay::kX, 0, w.h, t * kTile, w.b);
+                    bulk_commit();
+                    bulk_wait_read();
+                    mbar_arrive(&bar_empty_x[sx]);
+                }
+            }
+            bulk_wait_all();
+            if (!ok)
+                atomicOr(prm.status, 1u);
+        }
+    } else if (warp < kComputeWarps) {
+        // ---------------- two compute warpgroups; thread (wg, q, lane) owns
+        // tile row / TMEM lane i = 32 q + lane, warpgroup wg half of the
+        // columns of every step
+        const int wg = warp >> 2, q = warp & 3;
+        const int i = q * 32 + (tid & 31);
+        const int row_lo = q * 32, row_hi = q * 32 + 31;
+        const uint32_t lane = tmem_at(tmem, (uint32_t)(q * 32), 0);
+        float *gtab = reinterpret_cast<float *>(smem + Lay::off_g);
+        uint8_t *s_xh = smem + Lay::off_xh;
+        uint8_t *s_lo = s_xh + Lay::kX;
+        constexpr int kPHalf = P / 2;
+        const int c0w = wg * kPHalf;
+        const int tpc_mask = (1 << prm.tpc_shift) - 1;
+
+        // raw G / dt words of a tile, loaded two tiles ahead, unconditionally
+        // (addresses clamped into the row; defaults chosen a tile later)
+        struct Raw {
+            float base, g0, gL, gi, dti;
+        };
+        auto load_raw = [&](const Item &w, int t) {
+            const float *grow = prm.Gc + (int64_t)w.bh * g.L;
+            const int tau = t * kTile;
+            const int n = min(kTile, (int)g.L - tau);
+            const int ic = i < n ? i : n - 1;
+            Raw r;
+            r.base = ld_early(grow + (tau > 0 ? tau - 1 : 0));
+            r.g0 = ld_early(grow + tau);
+            r.gL = ld_early(grow + tau + n - 1);
+            r.gi = ld_early(grow + tau + ic);
+            r.dti = ld_early(prm.dtT + (int64_t)w.bh * g.L + tau + ic);
+            return r;
+        };
+        struct Pos {
+            Item w;
+            int item, t;
+            float Dh;
+            bool valid;
+        };
+        auto first_pos = [&]() {
+            Pos p{};
+            p.item = blockIdx.x;
+            p.valid = p.item < prm.n_items;
+            if (p.valid) {
+                p.w = decode_item<kModeFused>(prm, p.item);
+                p.t = p.w.t0;
+                p.Dh = prm.D[p.w.h];
+            }
+            return p;
+        };
+        // past the last tile: valid = false, the last tile's place kept
+        auto next_pos = [&](const Pos &p) {
+            Pos n = p;
+            if (!p.valid)
+                return n;
+            if (p.t + 1 < p.w.t1) {
+                n.t = p.t + 1;
+                return n;
+            }
+            n.item = p.item + (int)gridDim.x;
+            n.valid = n.item < prm.n_items;
+            if (n.valid) {
+                n.w = decode_item<kModeFused>(prm, n.item);
+                n.t = n.w.t0;
+                n.Dh = prm.D[n.w.h];
+            }
+            return n;
+        };
+        // a tile of sequence bh, segment seg
+        struct Tile {
+            int bh, seg, t, n, sx;
+            uint32_t it;
+            bool first, last_item, last_seq, do_state, narrow;
+            float gi, dti, gL, Dh;
+        };
+        auto make_tile = [&](const Pos &p, uint32_t it, const Raw &raw) {
+            Tile c;
+            c.bh = p.w.bh;
+            c.seg = p.w.chunk;
+            c.t = p.t;
+            c.it = it;
+            c.sx = (int)(it & 1);
+            c.n = min(kTile, (int)g.L - p.t * kTile);
+            c.first = p.t == p.w.t0;
+            c.last_item = p.t + 1 == p.w.t1;
+            c.last_seq = p.t + 1 == prm.n_tiles;
+            c.do_state = !c.last_seq || want_final;
+            const float base = (p.t & tpc_mask) == 0 ? 0.f : raw.base;
+            c.gL = raw.gL - base;
+            const float range = (raw.g0 - base) - c.gL;
+            c.narrow = range <= kNarrow && range >= -kNarrow;
+            c.gi = i < c.n ? raw.gi - base : 0.f;
+            c.dti = i < c.n ? raw.dti : 0.f;
+            c.Dh = p.Dh;
+            return c;
+        };
+
+        // ---- X_hat = dt exp2(g_L - g) x, bf16 hi (+ lo for the jump).  The
+        // caller waited for the previous tile's Y1 (the last reader of hi, of
+        // the table and, through the jumps before it, of lo).
+        auto build_xhat = [&](const Tile &c) -> bool {
+            const uint32_t par = c.it & 1;
+            if (wg == 0)
+                gtab[i] = c.gi;
+            else
+                gtab[128 + i] = c.dti;
+            if (tid == 0)
+                s_mode[par] = c.narrow ? 1 : 0;
+            if (!mbar_wait(&bar_full_x[c.sx], (c.it >> 1) & 1))
+                return false;
+            const uint8_t *sx = smem + Lay::off_x + c.sx * Lay::kX;
+            const bool build = c.narrow || c.do_state;
+            const float e = ex2_approx(c.gL - c.gi);
+            const float w = (build && i < c.n) ? c.dti * e : 0.f;
+            uint4 xv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                xv[k] = *reinterpret_cast<const uint4 *>(sx + sw128_offset(i, wg * 4 + k));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t off = sw128_offset(i, wg * 4 + k);
+                const uint32_t vv[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const float a = bf_lo(vv[e2]) * w, bb = bf_hi(vv[e2]) * w;
+                    hi[e2] = pack_bf16x2(a, bb);
+                    lo[e2] = pack_bf16x2(a - bf_lo(hi[e2]), bb - bf_hi(hi[e2]));
+                }
+                if (build)
+                    *reinterpret_cast<uint4 *>(s_xh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                if (c.do_state)
+                    *reinterpret_cast<uint4 *>(s_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            fence_proxy_async_smem();
+            warp_arrive(&bar_xh);
+            return true;
+        };
+
+        // ---- H block k = bf16(hscale h) rows 128 k .. 128 k + 127, MN-major
+        // [s][p], into buffer (it kSBlk + k) & 1 once that buffer's previous
+        // C H^T is done; the chunk state emitted if asked for; the decay
+        // written back.  A non-first tile reads the state the previous tile's
+        // jumps left (the caller waited for them); an item's first tile loads
+        // its start state (a later segment waits until its predecessor has
+        // published it).
+        auto build_h = [&](const Tile &c, int k) -> bool {
+            const uint32_t gh = c.it * kSBlk + k;
+            const int buf = (int)(gh & 1);
+            if (gh >= 2 && !mbar_wait(&bar_hf[buf], ((gh >> 1) - 1) & 1))
+                return false;
+            const int64_t bh = c.bh;
+            const int seg = c.seg;
+            if (k == 0 && c.first && seg > 0 && !prm.prefilled) {
+                const unsigned int *cnt = prm.seg_count + bh * prm.n_seg + seg - 1;
+                bool ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
+                const uint64_t t_start = globaltimer_ns();
+                while (!ready) {
+                    if (globaltimer_ns() - t_start > 2000000000ull)
+                        break;
+                    __nanosleep(256);
+                    ready = ld_acquire_gpu(cnt) >= (unsigned)kComputeWarps;
+                }
+                if (!ready)
+                    return false;
+            }
+            tc_fence_after();
+            const float decay = ex2_approx(c.gL);
+            const float hscale = c.narrow ? decay : 1.f;
+            const int sidx = k * 128 + i;
+            const uint32_t acc = lane + Lay::t_st + k * P + c0w;
+            uint32_t r[kPHalf];
+            if (c.first) {
+                const float *src = nullptr;
+                if (seg > 0)  // later segment: the predecessor's state
+                    src = prm.seg_state + ((bh * prm.n_seg + seg - 1) * g.P) * g.S;
+                else if (prm.h_src)
+                    src = prm.h_src + bh * g.P * g.S;
+#pragma unroll
+                for (int j = 0; j < kPHalf; ++j)
+                    r[j] = __float_as_uint(src ? __ldcg(src + (int64_t)(c0w + j) * S + sidx) : 0.f);
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < kPHalf; cc += 16)
+                    tmem_ld16(acc + cc, *reinterpret_cast<uint32_t(*)[16]>(r + cc));
+                tmem_ld_wait();
+            }
+            float *emit_dst = (prm.states_out && (c.t & tpc_mask) == 0)
+                                  ? prm.states_out + ((bh * g.nc + (c.t >> prm.tpc_shift)) * g.P) * g.S
+                                  : nullptr;
+            uint32_t hp[kPHalf / 2];
+#pragma unroll
+            for (int j = 0; j < kPHalf; j += 2) {
+                const float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
+                if (emit_dst) {
+                    emit_dst[(int64_t)(c0w + j) * S + sidx] = v0;
+                    emit_dst[(int64_t)(c0w + j + 1) * S + sidx] = v1;
+                }
+                hp[j / 2] = pack_bf16x2(v0 * hscale, v1 * hscale);
+                r[j] = __float_as_uint(v0 * decay);
+                r[j + 1] = __float_as_uint(v1 * decay);
+            }
+            uint8_t *s_h = smem + Lay::off_h + buf * Lay::kH;
+#pragma unroll
+            for (int k4 = 0; k4 < kPHalf / 8; ++k4)
+                *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, c0w / 8 + k4)) =
+                    make_uint4(hp[4 * k4], hp[4 * k4 + 1], hp[4 * k4 + 2], hp[4 * k4 + 3]);
+            if (c.do_state) {
+#pragma unroll
+                for (int cc = 0; cc < kPHalf; cc += 16)
+                    tmem_st16(acc + cc, *reinterpret_cast<uint32_t(*)[16]>(r + cc));
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bar_hr[buf]);
+            return true;
+        };
+
+        // ---- scores: CB (f32, complete after the block loop) -> masked,
+        // decayed bf16 A operand in TMEM; warpgroup wg converts keys
+        // [64 wg, 64 wg + 64).  X_hat's barrier also publishes the g / dt table.
+        auto build_scores = [&](const Tile &c) -> bool {
+            const uint32_t par = c.it & 1;
+            if (!mbar_wait(&bar_blk, par) || !mbar_wait(&bar_xh, par))
+                return false;
+            tc_fence_after();
+            const bool full = c.n == kTile;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t cbv[2][16];
+#pragma unroll
+                for (int gq = 0; gq < 2; ++gq) {
+                    const int j0 = wg * 64 + half * 32 + gq * 16;
+                    if (j0 <= row_hi)  // warp-uniform: keys above the diagonal stay zero
+                        tmem_ld16(lane + Lay::t_cb + j0, cbv[gq]);
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int gq = 0; gq < 2; ++gq) {
+                    const int j0 = wg * 64 + half * 32 + gq * 16;
+                    uint32_t pk[8];
+                    if (j0 > row_hi) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pk[e] = 0u;
+                    } else if (c.narrow) {
+                        if (full && j0 + 15 < row_lo) {  // whole group below the diagonal
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                pk[e] = pack_bf16x2(__uint_as_float(cbv[gq][2 * e]),
+                                                    __uint_as_float(cbv[gq][2 * e + 1]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int j = j0 + 2 * e;
+                                const float a = (j <= i && j < c.n) ? __uint_as_float(cbv[gq][2 * e]) : 0.f;
+                                const float bb =
+                                    (j + 1 <= i && j + 1 < c.n) ? __uint_as_float(cbv[gq][2 * e + 1]) : 0.f;
+                                pk[e] = pack_bf16x2(a, bb);
+                            }
+                        }
+                    } else {
+                        const float4 *g4 = reinterpret_cast<const float4 *>(gtab + j0);
+                        const float4 *d4 = reinterpret_cast<const float4 *>(gtab + 128 + j0);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const float4 gg = g4[v4], dd = d4[v4];
+                            const float gj[4] = {gg.x, gg.y, gg.z, gg.w};
+                            const float dj[4] = {dd.x, dd.y, dd.z, dd.w};
+                            float val[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = j0 + 4 * v4 + e;
+                                val[e] = (j <= i && j < c.n) ? __uint_as_float(cbv[gq][4 * v4 + e]) *
+                                                                   ex2_approx(c.gi - gj[e]) * dj[e]
+                                                             : 0.f;
+                            }
+                            pk[2 * v4] = pack_bf16x2(val[0], val[1]);
+                            pk[2 * v4 + 1] = pack_bf16x2(val[2], val[3]);
+                        }
+                    }
+                    tmem_st8(lane + Lay::t_sc + j0 / 2, pk);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            warp_arrive(&bar_sc);
+            return true;
+        };
+
+        // ---- the state leaving an item: the next segment's start, or the
+        // final state (the caller waited for the item's last jumps)
+        auto leave_state = [&](const Tile &c) {
+            const int64_t bh = c.bh;
+            float *dst = nullptr;
+            const bool handoff = !c.last_seq && !prm.prefilled;
+            if (handoff)
+                dst = prm.seg_state + ((bh * prm.n_seg + c.seg) * g.P) * g.S;
+            else if (c.last_seq && want_final)
+                dst = prm.final_state + bh * g.P * g.S;
+            if (dst) {
+#pragma unroll 1
+                for (int k = 0; k < kSBlk; ++k) {
+                    const int sidx = k * 128 + i;
+                    uint32_t r[kPHalf];
+#pragma unroll
+                    for (int cc = 0; cc < kPHalf; cc += 16)
+                        tmem_ld16(lane + Lay::t_st + k * P + c0w + cc, *reinterpret_cast<uint32_t(*)[16]>(r + cc));
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < kPHalf; ++j)
+                        __stcg(dst + (int64_t)(c0w + j) * S + sidx, __uint_as_float(r[j]));
+                }
+            }
+            if (handoff) {
+                __threadfence();
+                __syncwarp();
+                if ((tid & 31) == 0)
+                    atomicAdd(prm.seg_count + bh * prm.n_seg + c.seg, 1u);
+            }
+        };
+
+        // ---- epilogue (the caller waited for Y): factorized y = r1 Y + D x
+        // with r1 = exp2(g_i - g_L); exact y = exp2(g_i) Y + Y1 + D x with Y1
+        // in the CB columns.  y goes over the tile's x in its slot.
+        auto epilogue = [&](const Tile &c) -> bool {
+            tc_fence_after();
+            const float r = c.narrow ? ex2_approx(c.gi - c.gL) : ex2_approx(c.gi);
+            uint8_t *sx = smem + Lay::off_x + c.sx * Lay::kX;
+#pragma unroll
+            for (int c16 = 0; c16 < kPHalf; c16 += 16) {
+                uint32_t ya[16], yb[16];
+                tmem_ld16(lane + Lay::t_y + c0w + c16, ya);
+                if (!c.narrow)
+                    tmem_ld16(lane + Lay::t_cb + c0w + c16, yb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const uint32_t off = sw128_offset(i, (c0w + c16) / 8 + k2);
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(sx + off);
+                    const uint32_t vv[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int cc = 8 * k2 + 2 * e;
+                        float y0 = fmaf(r, __uint_as_float(ya[cc]), c.Dh * bf_lo(vv[e]));
+                        float y1 = fmaf(r, __uint_as_float(ya[cc + 1]), c.Dh * bf_hi(vv[e]));
+                        if (!c.narrow) {
+                            y0 += __uint_as_float(yb[cc]);
+                            y1 += __uint_as_float(yb[cc + 1]);
+                        }
+                        o[e] = pack_bf16x2(y0, y1);
+                    }
+                    *reinterpret_cast<uint4 *>(sx + off) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            // Y (and the CB columns) read: the next tile's MMAs may overwrite them
+            tc_fence_before();
+            warp_arrive(&bar_ep);
+            fence_proxy_async_smem();
+            warp_arrive(&bar_ys[c.sx]);
+            return true;
+        };
+
+        bool ok = true;
+        Pos p1 = first_pos();
+        if (p1.valid) {
+            const Raw raw0 = load_raw(p1.w, p1.t);
+            Tile cur = make_tile(p1, 0, raw0);
+            p1 = next_pos(p1);
+            Raw raw1 = load_raw(p1.w, p1.t);
+            ok = build_xhat(cur);
+            for (int k = 0; k < kSBlk && ok; ++k)
+                ok = build_h(cur, k);
+            for (uint32_t it = 0; ok; ++it) {
+                if (!build_scores(cur)) {
+                    ok = false;
+                    break;
+                }
+                // the block loop of `it` is done: its jumps have left the state
+                if (cur.last_item && cur.do_state)
+                    leave_state(cur);
+                Tile nxt{};
+                if (p1.valid) {
+                    nxt = make_tile(p1, it + 1, raw1);
+                    for (int k = 0; k < 2 && ok; ++k)
+                        ok = build_h(nxt, k);
+                    if (!ok)
+                        break;
+                }
+                // Y1 done: X_hat hi, lo and the table are free, Y is complete
+                if (!mbar_wait(&bar_y, it & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (p1.valid && !build_xhat(nxt)) {
+                    ok = false;
+                    break;
+                }
+                if (!epilogue(cur)) {
+                    ok = false;
+                    break;
+                }
+                if (!p1.valid)
+                    break;
+                // the tile after the next one: its G / dt words are in flight
+                // for a whole tile before make_tile reads them
+                const Pos p2 = next_pos(p1);
+                const Raw raw2 = load_raw(p2.w, p2.t);
+                for (int k = 2; k < kSBlk && ok; ++k)
+                    ok = build_h(nxt, k);
+                cur = nxt;
+                p1 = p2;
+                raw1 = raw2;
+            }
+        }
+        if (!ok)
+            atomicOr(prm.status, 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
 int sm_count()
 {
     static int n = 0;
@@ -867,6 +1562,22 @@ cudaError_t launch_cfg(const CUtensorMap &tx, const CUtensorMap &tb, const CUten
     using Lay = CoLayout<P, S, STAGES>;
     const size_t smem = Lay::bytes + 1024;
     auto k = chunk_tc_kernel<P, S, STAGES, MODE>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int grid = prm.n_items < sm_count() ? prm.n_items : sm_count();
+    k<<<(unsigned)grid, kThreads, smem, st>>>(tx, tb, tcm, ty, prm);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <int P, int S>
+cudaError_t launch_big(const CUtensorMap &tx, const CUtensorMap &tb, const CUtensorMap &tcm,
+                       const CUtensorMap &ty, const Params &prm, cudaStream_t st)
+{
+    using Lay = BigLayout<P, S>;
+    const size_t smem = Lay::bytes + 1024;
+    auto k = chunk_big_kernel<P, S>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
@@ -960,7 +1671,7 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
                 float *final_state, void *y, const Geom &g, void *scratch, size_t scratch_bytes,
                 cudaStream_t st)
 {
-    if (!chunk_tc_supported(g))
+    if (mode == kModeOut ? !chunk_tc_supported(g) : !fused_tc_supported(g))
         return cudaErrorNotSupported;
     Params prm{};
     prm.dtT = dtT;
@@ -1009,19 +1720,34 @@ cudaError_t run(int mode, const void *x, const void *Bm, const void *Cm, const f
     if (!make_tmap_tokens_heads(&tx, x, g) || !make_tmap_tokens_groups(&tb, Bm, g) ||
         !make_tmap_tokens_groups(&tcm, Cm, g) || !make_tmap_tokens_heads(&ty, y, g))
         return cudaErrorInvalidValue;
+    if (mode == kModeFused && g.P == 64 && g.S == 384)
+        return launch_big<64, 384>(tx, tb, tcm, ty, prm, st);
+    if (mode == kModeFused && g.P == 64 && g.S == 512)
+        return launch_big<64, 512>(tx, tb, tcm, ty, prm, st);
     return mode == kModeOut ? dispatch<kModeOut>(tx, tb, tcm, ty, prm, st)
                             : dispatch<kModeFused>(tx, tb, tcm, ty, prm, st);
 }
 
 }  // namespace
 
+namespace {
+// work items and tile indices are 32-bit in the kernels
+bool tile_geometry_ok(const Geom &g)
+{
+    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
+    return (g.T == kTile || g.T == 2 * kTile) && g.L > 0 && g.L < (1LL << 31) && g.H <= 65535 &&
+           g.G <= 65535 && g.B <= 65535 && g.B * g.H * n_tiles < (1LL << 31);
+}
+}  // namespace
+
 bool chunk_tc_supported(const Geom &g)
 {
-    const bool shape = g.P == 64 && (g.S == 64 || g.S == 128 || g.S == 256);
-    // work items and tile indices are 32-bit in the kernel
-    const int64_t n_tiles = (g.L + kTile - 1) / kTile;
-    return shape && (g.T == kTile || g.T == 2 * kTile) && g.L > 0 && g.L < (1LL << 31) &&
-           g.H <= 65535 && g.G <= 65535 && g.B <= 65535 && g.B * g.H * n_tiles < (1LL << 31);
+    return g.P == 64 && (g.S == 64 || g.S == 128 || g.S == 256) && tile_geometry_ok(g);
+}
+
+bool fused_tc_supported(const Geom &g)
+{
+    return chunk_tc_supported(g) || (g.P == 64 && (g.S == 384 || g.S == 512) && tile_geometry_ok(g));
 }
 
 cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,

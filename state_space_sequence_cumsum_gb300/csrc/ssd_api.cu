@@ -126,12 +126,18 @@ cudaError_t run_chunk_out(const void *x, const void *Bm, const void *Cm, const f
 // default for the tensor-core shapes (a debugging / measurement switch).
 ssd_path_t choose_path(const Geom &g, ssd_dtype_t t, bool want_states)
 {
-    (void)want_states;
-    if (t != SSD_BF16 || !chunk_tc_supported(g))
+    if (t != SSD_BF16 || !fused_tc_supported(g))
         return (t == SSD_BF16 && state_pass_tc_supported(g)) ? SSD_PATH_STAGED_TENSOR_CORES
                                                              : SSD_PATH_STAGED_CUDA_CORES;
     const char *env = getenv("SSD_FWD_PATH");
     if (env && strcmp(env, "staged") == 0)
+        return SSD_PATH_STAGED_TENSOR_CORES;
+    // dstate 384 / 512 with every chunk state asked for: the staged path's
+    // state pass writes them as part of its work, and there it is the faster
+    // one (B 1, L 262144, H 32, S 512: 4.98 ms staged, 5.20 ms fused)
+    const bool force_fused = env && strcmp(env, "fused") == 0;
+    if (want_states && !force_fused && !chunk_tc_supported(g) && state_pass_tc_supported(g) &&
+        chunk_out_big_supported(g))
         return SSD_PATH_STAGED_TENSOR_CORES;
     return fused_pair_enabled(g) ? SSD_PATH_FUSED_PAIR_TENSOR_CORES : SSD_PATH_FUSED_TENSOR_CORES;
 }
@@ -432,7 +438,7 @@ size_t ssd_state_out_workspace_size(ssd_dims_t dims, ssd_dtype_t dtype, int chun
     Geom g;
     if (make_geom(dims, chunk_size, false, &g) != SSD_OK || (dtype != SSD_BF16 && dtype != SSD_F32))
         return 0;
-    const size_t b = (dtype == SSD_BF16 && chunk_tc_supported(g)) ? fused_tc_scratch_bytes(g) : 0;
+    const size_t b = (dtype == SSD_BF16 && fused_tc_supported(g)) ? fused_tc_scratch_bytes(g) : 0;
     return b ? b : 256;
 }
 
@@ -460,7 +466,7 @@ ssd_status_t ssd_state_out(const void *x, const void *Bm, const void *Cm, const 
     if (!ne)
         return ssd_state_pass(x, Bm, dt_t, G_cum, init_state, chunk_states, final_state, dims,
                               dtype, chunk_size, stream);
-    if (dtype != SSD_BF16 || !chunk_tc_supported(g))
+    if (dtype != SSD_BF16 || !fused_tc_supported(g))
         return SSD_ERR_UNSUPPORTED;
     const size_t need_ws = fused_tc_scratch_bytes(g);
     if (need_ws && (!workspace || workspace_bytes < need_ws ||

@@ -68,6 +68,9 @@ cudaError_t launch_state_pass_tc_segmented(const void *x, const void *Bm, const 
 
 // Tensor-core chunk output (stage 3) and fused single-pass forward (bf16).
 bool chunk_tc_supported(const Geom &g);
+// the fused one-head forward: chunk_tc_supported shapes, and dstate 384 / 512
+// (B / C streamed in 128-row dstate blocks)
+bool fused_tc_supported(const Geom &g);
 cudaError_t launch_chunk_out_tc(const void *x, const void *Bm, const void *Cm, const float *dtT,
                                 const float *Gc, const float *states, const float *D, void *y,
                                 const Geom &g, cudaStream_t st);

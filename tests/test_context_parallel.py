@@ -168,7 +168,7 @@ def _run_segments(inp, T, R, dtype):
     (2, 1024, 4, 64, 128, 1, 128, torch.bfloat16, 4),    # head-pair path
     (1, 1000, 6, 64, 64, 3, 128, torch.bfloat16, 3),     # ragged last segment
     (1, 2048, 4, 64, 256, 2, 256, torch.bfloat16, 2),    # one-head fused path
-    (1, 768, 2, 64, 512, 1, 128, torch.bfloat16, 3),     # staged, dstate 512
+    (1, 768, 2, 64, 512, 1, 128, torch.bfloat16, 3),     # staged, dstate 512 (chunk states)
     (2, 333, 3, 32, 48, 1, 64, torch.float32, 3),        # f32 CUDA cores
 ])
 def test_segments_in_sequence_equal_one_run(B, L, H, P, S, G, T, dtype, R):

@@ -13,8 +13,8 @@ scratch array, so a kernel that read scratch before writing it would show.
 The cases cover the head-pair path (one CTA per pair, prefilled segments,
 and the wrap plan whose sequences hand states from CTA to CTA), the one-head
 fused path at dstate 256 (prefilled segments, and hand-off segments when there
-are more sequences than SMs), the staged dstate-512 path with chunk states,
-and the f32 path.
+are more sequences than SMs), the staged dstate-512 path (taken when chunk
+states are asked for) and the f32 path.
 
 The file is named so pytest collects it last.
 """
