@@ -852,7 +852,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 // tile's B and C (128 KB each at S = 512) do not fit in shared memory next to
 // x, X_hat and H, so they stream through a two-slot ring in 128-row dstate
 // blocks and every contraction over S runs block by block: per block b,
-//   CB += C_b B_b^T,  state_b += B_b^T (X_hat hi + lo),  Y += C_b H_b^T,
+//   CB += C_b B_b^T,  Y += C_b H_b^T,  state_b += B_b^T (X_hat hi + lo),
 // where H_b = bf16 of the tile's start state rows of block b, built by the
 // compute warps into one of two 16 KB buffers just before the block's jump.
 // CB is complete only after the last block, so the score conversion and Y1
@@ -862,10 +862,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 // which stays in its slot until then; y is written over it and stored.
 //
 // Per tile `it`, compute warps: scores(it) -> [state leaving the item] ->
-// H blocks 0, 1 of it + 1 -> (Y1 done) X_hat(it + 1) -> epilogue(it) -> the
-// remaining H blocks of it + 1.  MMA thread, per block: C B^T, the jump (after
-// the block's H and, for block 0, X_hat), C H^T (block 0 after the previous
-// epilogue has read Y); then Y1 once the scores are converted.
+// H blocks 0, 1 of it + 1 -> (Y1 done) epilogue(it) -> X_hat(it + 1) -> the
+// remaining H blocks of it + 1.  MMA thread, per block: C B^T, C H^T (after
+// the block's H; block 0 after the previous epilogue has read Y), the jump
+// (block 0 after X_hat, which the compute warps build while that C H^T
+// runs); then Y1 once the scores are converted.
 //
 // Shared memory (P 64, S 512): B / C ring 2 x 64 KB, x ring 2 x 16 KB, X_hat
 // hi / lo 32 KB, H 2 x 16 KB, g / dt 1 KB = 225 KB.  TMEM: CB 128 columns,
@@ -1027,10 +1028,28 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                         for (int ks = 0; ks < 8; ++ks)
                             mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
                                    id_cb, (k > 0 || ks > 0) ? 1u : 0u);
-                        // the jump once the block's H has read the state (and
-                        // X_hat is built)
-                        if (!mbar_spin(&bar_hr[slot], (gb >> 1) & 1) ||
-                            (k == 0 && !mbar_spin(&bar_xh, par))) {
+                        // C H^T once the block's H is built (block 0: once the
+                        // previous epilogue has read Y), then the jump (block 0:
+                        // once X_hat is built, which the compute warps do after
+                        // that epilogue, while this C H^T runs)
+                        if (!mbar_spin(&bar_hr[slot], (gb >> 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!ep_done) {
+                            if (!mbar_spin(&bar_ep, (it - 1) & 1)) {
+                                ok = false;
+                                break;
+                            }
+                            ep_done = true;
+                        }
+                        tc_fence_after();
+                        const uint64_t d_h = desc_mn0(smem_u32(smem + Lay::off_h + slot * Lay::kH));
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2,
+                                   (k > 0 || ks > 0) ? 1u : 0u);
+                        if (k == 0 && !mbar_spin(&bar_xh, par)) {
                             ok = false;
                             break;
                         }
@@ -1043,19 +1062,6 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                                     mma_ss(tmem + Lay::t_st + k * P, desc_mn(d_bmn, ks),
                                            desc_mn(part ? d_lo : d_xh, ks), id_ds, 1u);
                         }
-                        if (!ep_done) {
-                            if (!mbar_spin(&bar_ep, (it - 1) & 1)) {
-                                ok = false;
-                                break;
-                            }
-                            ep_done = true;
-                            tc_fence_after();
-                        }
-                        const uint64_t d_h = desc_mn0(smem_u32(smem + Lay::off_h + slot * Lay::kH));
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)
-                            mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2,
-                                   (k > 0 || ks > 0) ? 1u : 0u);
                         mma_commit(&bar_hf[slot]);
                         mma_commit(&bar_empty[slot]);
                     }
@@ -1510,16 +1516,16 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                     ok = false;
                     break;
                 }
-                if (p1.valid && !build_xhat(nxt)) {
-                    ok = false;
-                    break;
-                }
                 if (!epilogue(cur)) {
                     ok = false;
                     break;
                 }
                 if (!p1.valid)
                     break;
+                if (!build_xhat(nxt)) {
+                    ok = false;
+                    break;
+                }
                 // the tile after the next one: its G / dt words are in flight
                 // for a whole tile before make_tile reads them
                 const Pos p2 = next_pos(p1);
