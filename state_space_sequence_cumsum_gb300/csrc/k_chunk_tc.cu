@@ -7,11 +7,13 @@
 // and section "Kernel 2: fwd_pass_state" for the state jump
 //     h <- exp2(G_last) h + X^T (B * dt * exp2(G_last - G)).
 //
-// One kernel, two modes:
+// chunk_tc_kernel, dstate 64 / 128 / 256, has two modes:
 //   OUT   -- a work item is (batch, chunk, head); h_c comes from chunk_states.
 //   FUSED -- a work item is (batch, head, segment of the sequence); the state
 //            is carried on chip from tile to tile, so chunk states never go
 //            through HBM unless the caller asks for them.
+// chunk_big_kernel is the FUSED mode for dstate 384 / 512, with B and C
+// streamed in 128-row dstate blocks (its own description is further down).
 // Tokens are processed in 128-token tiles (the tcgen05 M and K extent).  A
 // chunk of 256 tokens is two tiles: the second tile's starting state is the
 // first tile's state jump applied to h_c, and its G is taken relative to the
