@@ -51,9 +51,13 @@
  *   of 128: the state pass for P in {64, 128} and S % 64 == 0; the chunk
  *   output for P == 64 and S in {64, 128, 256}, and for S in {384, 512}
  *   with T == 128; the one-head fused pass for P == 64 and S in
- *   {64, 128, 256}; the head-pair fused pass for P == 64, S in {64, 128}
- *   and an even number of heads per group.  Other shapes and all f32 calls
- *   run f32-arithmetic CUDA-core kernels.
+ *   {64, 128, 256, 384, 512} (at 384 / 512 B and C stream through it in
+ *   128-row dstate blocks); the head-pair fused pass for P == 64, S in
+ *   {64, 128} and an even number of heads per group.  ssd_fwd takes a fused
+ *   pass wherever one serves the shape, except at S 384 / 512 when every
+ *   chunk state is asked for (the staged path writes them as part of its
+ *   work, and is faster there).  Other shapes and all f32 calls run
+ *   f32-arithmetic CUDA-core kernels.
  */
 #ifndef SSD_GB300_H
 #define SSD_GB300_H
