@@ -857,8 +857,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 //   CB += C_b B_b^T,  Y += C_b H_b^T,  state_b += B_b^T (X_hat hi + lo),
 // where H_b = bf16 of the tile's start state rows of block b, built by the
 // compute warps into one of two 16 KB buffers just before the block's jump.
-// CB is complete only after the last block, so the score conversion and Y1
-// follow the block loop.  Y holds C H^T and, for a factorized tile, Y1 on top
+// CB is complete with the last block's C B^T: the score conversion overlaps
+// that block's C H^T and jump, and Y1 follows the block loop.  Y holds C H^T and, for a factorized tile, Y1 on top
 // (y = exp2(g_i - g_L) Y + D x); an exact tile's Y1 goes to the CB columns
 // (y = exp2(g_i) Y + Y1 + D x).  D x is added in the epilogue from the x tile,
 // which stays in its slot until then; y is written over it and stored.
@@ -909,9 +909,10 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     __shared__ uint64_t bar_full_x[2], bar_empty_x[2], bar_ys[2];
     // H buffers: built (compute warps), free (the block's C H^T done)
     __shared__ uint64_t bar_hr[2], bar_hf[2];
-    // X_hat built; the block loop done (CB complete, state jumped); scores
-    // converted; Y complete (Y1 done); the epilogue has read Y; teardown
-    __shared__ uint64_t bar_xh, bar_blk, bar_sc, bar_y, bar_ep, bar_end;
+    // X_hat built; CB complete (the last block's C B^T done); the block loop
+    // done (state jumped); scores converted; Y complete (Y1 done); the
+    // epilogue has read Y; teardown
+    __shared__ uint64_t bar_xh, bar_cb, bar_blk, bar_sc, bar_y, bar_ep, bar_end;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_mode[2];  // per tile parity: 1 = factorized (narrow) decay
 
@@ -929,6 +930,7 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             mbar_init(&bar_hf[s], 1);
         }
         mbar_init(&bar_xh, kComputeWarps);
+        mbar_init(&bar_cb, 1);
         mbar_init(&bar_blk, 1);
         mbar_init(&bar_sc, kComputeWarps);
         mbar_init(&bar_y, 1);
@@ -1030,6 +1032,10 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                         for (int ks = 0; ks < 8; ++ks)
                             mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
                                    id_cb, (k > 0 || ks > 0) ? 1u : 0u);
+                        // CB is complete with the last block's C B^T: the score
+                        // conversion may overlap that block's C H^T and jump
+                        if (k == kSBlk - 1)
+                            mma_commit(&bar_cb);
                         // C H^T once the block's H is built (block 0: once the
                         // previous epilogue has read Y), then the jump (block 0:
                         // once X_hat is built, which the compute warps do after
@@ -1341,12 +1347,12 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             return true;
         };
 
-        // ---- scores: CB (f32, complete after the block loop) -> masked,
-        // decayed bf16 A operand in TMEM; warpgroup wg converts keys
+        // ---- scores: CB (f32, complete after the last block's C B^T) ->
+        // masked, decayed bf16 A operand in TMEM; warpgroup wg converts keys
         // [64 wg, 64 wg + 64).  X_hat's barrier also publishes the g / dt table.
         auto build_scores = [&](const Tile &c) -> bool {
             const uint32_t par = c.it & 1;
-            if (!mbar_wait(&bar_blk, par) || !mbar_wait(&bar_xh, par))
+            if (!mbar_wait(&bar_cb, par) || !mbar_wait(&bar_xh, par))
                 return false;
             tc_fence_after();
             const bool full = c.n == kTile;
@@ -1502,7 +1508,12 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                     ok = false;
                     break;
                 }
-                // the block loop of `it` is done: its jumps have left the state
+                // the block loop of `it` done: its jumps have left the state
+                if (!mbar_wait(&bar_blk, it & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 if (cur.last_item && cur.do_state)
                     leave_state(cur);
                 Tile nxt{};
