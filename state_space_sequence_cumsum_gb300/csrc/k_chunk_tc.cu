@@ -854,9 +854,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 // tile's B and C (128 KB each at S = 512) do not fit in shared memory next to
 // x, X_hat and H, so they stream through a two-slot ring in 128-row dstate
 // blocks and every contraction over S runs block by block: per block b,
-//   CB += C_b B_b^T,  Y += C_b H_b^T,  state_b += B_b^T (X_hat hi + lo),
-// where H_b = bf16 of the tile's start state rows of block b, built by the
-// compute warps into one of two 16 KB buffers just before the block's jump.
+//   [CB | Y] += C_b [B_b | H_b]^T (one N = 192 MMA per K step, so C_b is read
+//   once),  state_b += B_b^T (X_hat hi + lo),
+// where H_b = bf16 of the tile's start state rows of block b, written by the
+// compute warps transposed (K-major, [p][s]) into the block's ring slot, in
+// the 64 rows after each B region's 128 token rows, before the block's MMAs.
 // CB is complete with the last block's C B^T: the score conversion overlaps
 // that block's C H^T and jump, and Y1 follows the block loop.  Y holds C H^T and, for a factorized tile, Y1 on top
 // (y = exp2(g_i - g_L) Y + D x); an exact tile's Y1 goes to the CB columns
@@ -870,22 +872,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 // (block 0 after X_hat, which the compute warps build while that C H^T
 // runs); then Y1 once the scores are converted.
 //
-// Shared memory (P 64, S 512): B / C ring 2 x 64 KB, x ring 2 x 16 KB, X_hat
-// hi / lo 32 KB, H 2 x 16 KB, g / dt 1 KB = 225 KB.  TMEM: CB 128 columns,
-// scores 64, Y 64, state S / 128 blocks of 64.
+// Shared memory (P 64, S 512): B (+ H^T) / C ring 2 x 80 KB, x ring 2 x 16 KB,
+// X_hat hi / lo 32 KB, g / dt 1 KB = 225 KB.  TMEM: CB 128 columns and Y 64
+// (adjacent: one accumulator of the N = 192 MMA), scores 64, state S / 128
+// blocks of 64.
 template <int P, int S>
 struct BigLayout {
     static constexpr int kSBlk = S / 128;            // 128-row dstate blocks
-    static constexpr uint32_t kBlk = 2 * kRegion;    // one block of B or C: 128 tokens x 128 s
-    static constexpr uint32_t kSlot = 2 * kBlk;      // B block, then C block
+    // a B region: 128 token rows of 64 s (TMA), then 64 rows of H^T (p) over
+    // the same 64 s (compute warps), all K-major with the 128-byte swizzle
+    static constexpr uint32_t kRegB = kRegion + 64 * 128;
+    static constexpr uint32_t kBlkB = 2 * kRegB;     // one block of B and H^T
+    static constexpr uint32_t kBlkC = 2 * kRegion;   // one block of C: 128 tokens x 128 s
+    static constexpr uint32_t kSlot = kBlkB + kBlkC;
     static constexpr uint32_t kX = kRegion;          // x / y tile (P = 64)
-    static constexpr uint32_t kH = kRegion;          // H block: 128 rows s x 64 p bf16
     static constexpr uint32_t off_x = 2 * kSlot;     // two x slots (y is staged over x)
     static constexpr uint32_t off_xh = off_x + 2 * kX;  // X_hat hi, then lo
-    static constexpr uint32_t off_h = off_xh + 2 * kX;  // two H buffers, MN-major [s][p]
-    static constexpr uint32_t off_g = off_h + 2 * kH;   // [g 128 | dt 128] f32
+    static constexpr uint32_t off_g = off_xh + 2 * kX;  // [g 128 | dt 128] f32
     static constexpr uint32_t bytes = off_g + 256 * 4;
-    static constexpr uint32_t t_cb = 0, t_sc = 128, t_y = 192, t_st = 256;
+    static constexpr uint32_t t_cb = 0, t_y = 128, t_sc = 192, t_st = 256;
     static constexpr uint32_t kTmemCols = 512;
     static_assert(P == 64, "one 128-byte row of x / y / H per token or state index");
     static_assert(S % 128 == 0 && S >= 384 && t_st + kSBlk * P <= 512, "TMEM budget");
@@ -978,10 +983,10 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                             break;
                         }
                         uint8_t *sb = smem + slot * Lay::kSlot;
-                        mbar_arrive_expect_tx(&bar_full[slot], 2 * Lay::kBlk);
+                        mbar_arrive_expect_tx(&bar_full[slot], 4 * kRegion);
                         for (int r = 0; r < 2; ++r) {
-                            tma4(sb + r * kRegion, &tm_b, &bar_full[slot], (2 * k + r) * 64, grp, tok, w.b);
-                            tma4(sb + Lay::kBlk + r * kRegion, &tm_c, &bar_full[slot], (2 * k + r) * 64, grp,
+                            tma4(sb + r * Lay::kRegB, &tm_b, &bar_full[slot], (2 * k + r) * 64, grp, tok, w.b);
+                            tma4(sb + Lay::kBlkB + r * kRegion, &tm_c, &bar_full[slot], (2 * k + r) * 64, grp,
                                  tok, w.b);
                         }
                     }
@@ -993,9 +998,9 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     } else if (warp == 9) {
         // ---------------- MMA issuer (waits poll with test_wait)
         if ((tid & 31) == 0) {
-            const uint32_t id_cb = idesc_bf16(128, 128, false, false);
+            // [CB | Y] += C [B | H]^T: N = 128 tokens + P, both operands K-major
+            const uint32_t id_cby = idesc_bf16(128, 128 + P, false, false);
             const uint32_t id_y1 = idesc_bf16(128, P, false, true);  // A (scores) from TMEM
-            const uint32_t id_y2 = idesc_bf16(128, P, false, true);  // H is MN-major
             const uint32_t id_ds = idesc_bf16(128, P, true, true);
             const uint64_t d_xh = desc_mn0(smem_u32(smem + Lay::off_xh));
             const uint64_t d_lo = desc_mn0(smem_u32(smem + Lay::off_xh + Lay::kX));
@@ -1024,22 +1029,10 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
-                        const uint32_t sb = smem_u32(smem + slot * Lay::kSlot);
-                        const uint64_t d_bk = desc_k0(sb), d_ck = desc_k0(sb + Lay::kBlk);
-                        const uint64_t d_bmn = desc_mn0(sb);
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)
-                            mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, kRegion, ks),
-                                   id_cb, (k > 0 || ks > 0) ? 1u : 0u);
-                        // CB is complete with the last block's C B^T: the score
-                        // conversion may overlap that block's C H^T and jump
-                        if (k == kSBlk - 1)
-                            mma_commit(&bar_cb);
-                        // C H^T once the block's H is built (block 0: once the
-                        // previous epilogue has read Y), then the jump (block 0:
-                        // once X_hat is built, which the compute warps do after
-                        // that epilogue, while this C H^T runs)
+                        // C [B | H]^T once the block's H^T is in its slot (block
+                        // 0: once the previous epilogue has read Y), then the
+                        // jump (block 0: once X_hat is built, which the compute
+                        // warps do after that epilogue, while these MMAs run)
                         if (!mbar_spin(&bar_hr[slot], (gb >> 1) & 1)) {
                             ok = false;
                             break;
@@ -1052,11 +1045,17 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                             ep_done = true;
                         }
                         tc_fence_after();
-                        const uint64_t d_h = desc_mn0(smem_u32(smem + Lay::off_h + slot * Lay::kH));
+                        const uint32_t sb = smem_u32(smem + slot * Lay::kSlot);
+                        const uint64_t d_bk = desc_k0(sb), d_ck = desc_k0(sb + Lay::kBlkB);
+                        const uint64_t d_bmn = desc_mn0(sb, Lay::kRegB);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
-                            mma_ss(tmem + Lay::t_y, desc_k(d_ck, kRegion, ks), desc_mn(d_h, ks), id_y2,
-                                   (k > 0 || ks > 0) ? 1u : 0u);
+                            mma_ss(tmem + Lay::t_cb, desc_k(d_ck, kRegion, ks), desc_k(d_bk, Lay::kRegB, ks),
+                                   id_cby, (k > 0 || ks > 0) ? 1u : 0u);
+                        // CB is complete with the last block's MMAs above: the
+                        // score conversion may overlap that block's jump
+                        if (k == kSBlk - 1)
+                            mma_commit(&bar_cb);
                         if (k == 0 && !mbar_spin(&bar_xh, par)) {
                             ok = false;
                             break;
@@ -1267,10 +1266,10 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             return true;
         };
 
-        // ---- H block k = bf16(hscale h) rows 128 k .. 128 k + 127, MN-major
-        // [s][p], into buffer (it kSBlk + k) & 1 once that buffer's previous
-        // C H^T is done; the chunk state emitted if asked for; the decay
-        // written back.  A non-first tile reads the state the previous tile's
+        // ---- H block k = bf16(hscale h) rows 128 k .. 128 k + 127, stored
+        // transposed (K-major [p][s]) in the ring slot of block (it kSBlk + k)
+        // once that slot's previous block is done; the chunk state emitted if
+        // asked for; the decay written back.  A non-first tile reads the state the previous tile's
         // jumps left (the caller waited for them); an item's first tile loads
         // its start state (a later segment waits until its predecessor has
         // published it).
@@ -1318,7 +1317,15 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             float *emit_dst = (prm.states_out && (c.t & tpc_mask) == 0)
                                   ? prm.states_out + ((bh * g.nc + (c.t >> prm.tpc_shift)) * g.P) * g.S
                                   : nullptr;
-            uint32_t hp[kPHalf / 2];
+            // H^T, K-major: row 128 + p of this state row's 64-s region of the
+            // slot, element s % 64, 128-byte swizzle.  The swizzle XORs the
+            // 16-byte chunk index (address bits 4-6, zero in every other term
+            // here) with row & 7 == j & 7, so the address of row c0w + j is
+            // (h0 + 128 j) ^ ((j & 7) << 4).  Lanes of a warp cover 32
+            // consecutive s, so a row's 2-byte stores fall in 16 distinct banks.
+            const uint32_t h0 = smem_u32(smem + buf * Lay::kSlot + (i >> 6) * Lay::kRegB + (128 + c0w) * 128 +
+                                         (i & 7) * 2) +
+                                ((uint32_t)((i & 63) >> 3) << 4);
 #pragma unroll
             for (int j = 0; j < kPHalf; j += 2) {
                 const float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
@@ -1326,15 +1333,16 @@ chunk_big_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                     emit_dst[(int64_t)(c0w + j) * S + sidx] = v0;
                     emit_dst[(int64_t)(c0w + j + 1) * S + sidx] = v1;
                 }
-                hp[j / 2] = pack_bf16x2(v0 * hscale, v1 * hscale);
+                const uint32_t hv = pack_bf16x2(v0 * hscale, v1 * hscale);
+                asm volatile("st.shared.b16 [%0], %1;" ::"r"((h0 + j * 128) ^ (uint32_t)((j & 7) << 4)),
+                             "h"((unsigned short)(hv & 0xffffu))
+                             : "memory");
+                asm volatile("st.shared.b16 [%0], %1;" ::"r"((h0 + (j + 1) * 128) ^ (uint32_t)(((j + 1) & 7) << 4)),
+                             "h"((unsigned short)(hv >> 16))
+                             : "memory");
                 r[j] = __float_as_uint(v0 * decay);
                 r[j + 1] = __float_as_uint(v1 * decay);
             }
-            uint8_t *s_h = smem + Lay::off_h + buf * Lay::kH;
-#pragma unroll
-            for (int k4 = 0; k4 < kPHalf / 8; ++k4)
-                *reinterpret_cast<uint4 *>(s_h + sw128_offset(i, c0w / 8 + k4)) =
-                    make_uint4(hp[4 * k4], hp[4 * k4 + 1], hp[4 * k4 + 2], hp[4 * k4 + 3]);
             if (c.do_state) {
 #pragma unroll
                 for (int cc = 0; cc < kPHalf; cc += 16)
